@@ -1,0 +1,179 @@
+/*
+ * pcp.h -- C ABI of the GB300 (sm_103a) paged chunked-prefill attention library.
+ *
+ * The library implements the hot path of chunked prefill over a paged KV
+ * cache:
+ *
+ *   1. pcp_compute_out_cache_loc -- where each new token of a chunk goes in
+ *      the page pool, continuing inside the last partly filled page
+ *      (AReno PR #642 "chunked prefill must attend to cached prefix",
+ *      "What does this PR do?", third bullet; AstrAI "scalar paged prefill
+ *      fallback and decode causal fix", PagePool.bind_tasks, out_cache_loc).
+ *   2. pcp_kv_append -- the scatter of the chunk's K/V into the pool
+ *      (AstrAI CudaBackend.fwd_prefill, the k_buffer[layer, out_cache_loc]
+ *      write).
+ *   3. pcp_paged_extend_attn -- extend attention: every query row of a ragged
+ *      batch attends to its sequence's cached prefix plus its own chunk,
+ *      read through a page table, with bottom-right causal alignment
+ *      (AReno PR #642, "What does this PR do?"; AstrAI paged prefill kernels,
+ *      causal offset = KV length - query length), GQA, an optional sliding
+ *      window, and split-KV with a log-sum-exp combine for decode-shaped rows
+ *      (AstrAI paged decode split-KV kernel and its combine kernel).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All pointers named q, k, v, *_pool, out, lse, indptr/indices/lens,
+ *    out_cache_loc, workspace and dev_err are DEVICE pointers.  The caller
+ *    owns every buffer and the stream; the library allocates no device
+ *    memory and keeps no state except a per-device cache of the SM count and
+ *    of the driver's tensor-map encoder.
+ *  - bf16 tensors are passed as void* (IEEE bfloat16, 2 bytes, row major).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every call is asynchronous on that stream.
+ *  - Errors the host can see return a status before anything is launched.
+ *    Errors only the device can see (a page id outside the pool, a slot
+ *    outside the pool, a spin-wait that ran out) are recorded in *dev_err, a
+ *    caller-owned device int32 that the caller zeroes; the first error wins
+ *    and the offending access is skipped (its data read as zeros, its write
+ *    dropped).  No kernel traps.  Read it with pcp_read_error.
+ *
+ * Layouts
+ * -------
+ *  q         [total_q, n_q_heads, head_dim]        bf16
+ *  k, v      [n_tokens, n_kv_heads, head_dim]      bf16 (the chunk's new K/V)
+ *  k_pool,
+ *  v_pool    [num_pages * page_size, n_kv_heads, head_dim] bf16; slot
+ *            s = page * page_size + offset
+ *  qo_indptr [batch + 1] int32, prefix sums of chunk lengths (rows of q)
+ *  prefix_lens [batch] int32, cached tokens before each chunk; the KV length
+ *            of sequence b is L_b = prefix_lens[b] + chunk_len_b
+ *  kv_indptr [batch + 1] int32, CSR offsets into kv_indices, in PAGES
+ *  kv_indices int32 page ids; sequence b owns entries
+ *            [kv_indptr[b], kv_indptr[b+1]); at least ceil(L_b / page_size)
+ *            entries, all in [0, num_pages).  Entries after those may hold
+ *            anything (e.g. -1 padding of a dense page table) and are never
+ *            read.  Several sequences may list the same pages (successive
+ *            chunks of one prompt in one call).
+ *  out       [total_q, n_q_heads, head_dim] bf16 (round to nearest even)
+ *  lse       [total_q, n_q_heads] float32, natural log of the sum of
+ *            exp(sm_scale * q.k) over the visible keys; -inf for a row that
+ *            sees no key (impossible with a causal mask and window >= 1)
+ */
+#ifndef PCP_H_
+#define PCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pcp_status {
+    PCP_OK = 0,
+    PCP_ERR_INVALID_ARG = 1,  /* a null pointer, a negative or inconsistent size */
+    PCP_ERR_UNSUPPORTED = 2,  /* a shape this build has no kernel for */
+    PCP_ERR_BAD_INDEX = 3,    /* device: a page id or slot outside the pool */
+    PCP_ERR_WORKSPACE = 4,    /* workspace smaller than pcp_extend_workspace_size */
+    PCP_ERR_CUDA = 5,         /* a CUDA runtime or driver call failed */
+    PCP_ERR_TIMEOUT = 6       /* device: a bounded spin-wait gave up */
+} pcp_status;
+
+/* Static string naming a status code; never NULL. */
+const char* pcp_status_string(int status);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int pcp_abi_version(void);
+
+/*
+ * Slot mapping for the new tokens of every sequence (integer, bit-exact):
+ *   out_cache_loc[t] = kv_indices[kv_indptr[b] + p / page_size] * page_size
+ *                      + p % page_size,   p = prefix_lens[b] + (t - qo_indptr[b])
+ * for qo_indptr[b] <= t < qo_indptr[b+1].  Writes begin inside the last
+ * partly filled page when prefix_lens[b] % page_size != 0 (AReno PR #642,
+ * "What does this PR do?": continue prefill inside the last allocated KV
+ * page).  A page id outside [0, num_pages) sets *dev_err = PCP_ERR_BAD_INDEX
+ * and writes -1 for that token.
+ * out_cache_loc: device int64 [total_q], written.
+ */
+pcp_status pcp_compute_out_cache_loc(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                     const int32_t* kv_indices, const int32_t* prefix_lens,
+                                     int batch, int64_t total_q, int page_size,
+                                     int64_t num_pages, int64_t* out_cache_loc,
+                                     int32_t* dev_err, void* stream);
+
+/*
+ * KV append (a pure copy, bit-exact):
+ *   k_pool[out_cache_loc[t], :, :] = k[t, :, :],  v_pool[...] = v[t, :, :]
+ * for 0 <= t < n_tokens (AstrAI CudaBackend.fwd_prefill / fwd_decode, the
+ * write of the step's K/V at out_cache_loc before attention).  A location
+ * outside [0, pool_slots) sets *dev_err = PCP_ERR_BAD_INDEX and that token is
+ * skipped.  Slots not named in out_cache_loc are left untouched.
+ * head_dim * 2 bytes must be a multiple of 16; k, v and the pools must be
+ * 16-byte aligned.
+ */
+pcp_status pcp_kv_append(const void* k, const void* v, const int64_t* out_cache_loc,
+                         int64_t n_tokens, int n_kv_heads, int head_dim, void* k_pool,
+                         void* v_pool, int64_t pool_slots, int32_t* dev_err, void* stream);
+
+/*
+ * Bytes of device workspace pcp_paged_extend_attn needs for a call with at
+ * most `batch` sequences and `total_q` query rows (work lists, split-KV
+ * partials and counters).  Pure host arithmetic; 0 for an unsupported shape.
+ */
+size_t pcp_extend_workspace_size(int batch, int64_t total_q, int n_q_heads, int n_kv_heads,
+                                 int head_dim);
+
+/*
+ * Paged extend attention (AReno PR #642, "What does this PR do?": one
+ * paged varlen attention call for mixed prefix/chunk lengths with
+ * bottom-right causal alignment; AstrAI attn_paged_prefill / attn_paged_decode).
+ * For sequence b, query row i (position p = prefix_lens[b] + i) and query
+ * head h (KV head g = h / (n_q_heads / n_kv_heads)), the visible keys are
+ * j in [lo, p] with lo = max(0, p - window + 1) when window > 0, else 0:
+ *   s_j = sm_scale * q[row, h, :] . K[slot(b, j), g, :]
+ *   out[row, h, :] = sum_j softmax(s)_j * V[slot(b, j), g, :]
+ *   lse[row, h]    = log(sum_j exp(s_j))
+ * sm_scale <= 0 selects 1 / sqrt(head_dim) (AstrAI parameter packing).
+ * A chunk of length 0 is allowed (no rows); prefix_lens[b] == 0 is a plain
+ * prefill; a chunk of length 1 is a decode row.
+ *
+ * The K/V of the chunk itself must already be in the pool (pcp_kv_append
+ * first, as a serving step does).  Supported: head_dim in {64, 128},
+ * n_q_heads % n_kv_heads == 0, n_q_heads / n_kv_heads <= 128, page_size >= 1,
+ * window >= 0, num_pages * page_size < 2^31.  q, out, the pools and the
+ * workspace must be 16-byte aligned (256-byte aligned workspace).
+ * workspace: device memory of at least pcp_extend_workspace_size(...) bytes;
+ * its contents need no initialisation and are scratch between calls.  Calls
+ * that share one workspace must be ordered on the GPU (same stream).
+ * lse may be NULL.
+ */
+pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
+                                 const int32_t* kv_indptr, const int32_t* kv_indices,
+                                 const int32_t* prefix_lens, int batch, int64_t total_q,
+                                 const void* k_pool, const void* v_pool, int64_t num_pages,
+                                 int page_size, int n_q_heads, int n_kv_heads, int head_dim,
+                                 int window, float sm_scale, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                 void* stream);
+
+/*
+ * Synchronise `stream` and copy *dev_err to *host_err (host pointer).
+ * Returns PCP_ERR_CUDA if the synchronisation or copy fails.
+ */
+pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_err);
+
+/*
+ * Profiling hook.  When both events (cudaEvent_t passed as void*) are
+ * non-NULL, every later pcp_paged_extend_attn call records `before` on its
+ * stream right before the tensor-core extend kernel is launched and `after`
+ * right after it, so a caller can time that kernel alone.  Pass NULLs to
+ * turn it off.  Process-wide; not for concurrent use from several threads.
+ */
+pcp_status pcp_set_timing_events(void* before, void* after);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PCP_H_ */

@@ -1,0 +1,33 @@
+"""Paged chunked-prefill attention for NVIDIA GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libpcp.so`` (declared in
+``include/pcp.h``).  Every step of the path runs in the library's CUDA
+kernels; this module only checks tensors, allocates outputs and workspace
+with PyTorch, and passes raw pointers and the current CUDA stream.  There is
+no CPU or PyTorch fallback: if the library is missing, importing the compute
+functions raises.
+
+Functions (same names as the C entry points, without the ``pcp_`` prefix):
+
+* ``compute_out_cache_loc`` -- slots of a step's new tokens (int64)
+* ``kv_append``             -- scatter the chunk's K/V into the page pools
+* ``paged_extend_attn``     -- extend attention, returns ``(out, lse)``
+* ``workspace_size``        -- bytes of scratch a call needs
+"""
+from ._binding import (  # noqa: F401
+    PCPError,
+    Status,
+    compute_out_cache_loc,
+    kv_append,
+    lib,
+    library_path,
+    paged_extend_attn,
+    read_error,
+    set_timing_events,
+    workspace_size,
+)
+
+__all__ = [
+    "PCPError", "Status", "compute_out_cache_loc", "kv_append", "lib", "library_path",
+    "paged_extend_attn", "read_error", "set_timing_events", "workspace_size",
+]

@@ -1,0 +1,237 @@
+"""ctypes binding of libpcp.so: argument marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libpcp.so"
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, _LIB_NAME)
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    INVALID_ARG = 1
+    UNSUPPORTED = 2
+    BAD_INDEX = 3
+    WORKSPACE = 4
+    CUDA = 5
+    TIMEOUT = 6
+
+
+class PCPError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        msg = lib().pcp_status_string(int(status)).decode()
+        super().__init__(f"{where}: {msg}")
+
+
+def lib():
+    """The loaded library.  Raises if libpcp.so has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(
+                f"{path} is missing: build it with `python -m paged_chunked_prefill_gb300.build` "
+                "(there is no fallback implementation)")
+        L = ctypes.CDLL(path)
+        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                ctypes.c_size_t)
+        L.pcp_status_string.argtypes = [i32]
+        L.pcp_status_string.restype = ctypes.c_char_p
+        L.pcp_abi_version.argtypes = []
+        L.pcp_abi_version.restype = i32
+        L.pcp_compute_out_cache_loc.argtypes = [P, P, P, P, i32, i64, i32, i64, P, P, P]
+        L.pcp_compute_out_cache_loc.restype = i32
+        L.pcp_kv_append.argtypes = [P, P, P, i64, i32, i32, P, P, i64, P, P]
+        L.pcp_kv_append.restype = i32
+        L.pcp_extend_workspace_size.argtypes = [i32, i64, i32, i32, i32]
+        L.pcp_extend_workspace_size.restype = sz
+        L.pcp_paged_extend_attn.argtypes = [P, P, P, P, P, i32, i64, P, P, i64, i32, i32, i32,
+                                            i32, i32, f32, P, P, P, sz, P, P]
+        L.pcp_paged_extend_attn.restype = i32
+        L.pcp_read_error.argtypes = [P, P, P]
+        L.pcp_read_error.restype = i32
+        L.pcp_set_timing_events.argtypes = [P, P]
+        L.pcp_set_timing_events.restype = i32
+        _lib = L
+        return L
+
+
+def _check(status: int, where: str) -> None:
+    if status != Status.OK:
+        raise PCPError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, device) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_err_bufs = {}
+_ws_bufs = {}
+
+
+def _dev_err(device: torch.device) -> torch.Tensor:
+    key = (device.type, device.index)
+    t = _err_bufs.get(key)
+    if t is None:
+        t = torch.zeros(1, dtype=torch.int32, device=device)
+        _err_bufs[key] = t
+    return t
+
+
+def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    key = (device.type, device.index)
+    t = _ws_bufs.get(key)
+    if t is None or t.numel() < nbytes:
+        t = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_bufs[key] = t
+    return t
+
+
+def read_error(dev_err: torch.Tensor) -> int:
+    """Synchronise the current stream and return the device error word."""
+    host = ctypes.c_int32(0)
+    _check(lib().pcp_read_error(_ptr(dev_err), _stream(dev_err.device), ctypes.byref(host)),
+           "pcp_read_error")
+    return int(host.value)
+
+
+def _finish(dev_err: torch.Tensor, own: bool, check: bool, where: str) -> None:
+    if own and check:
+        code = read_error(dev_err)
+        if code != 0:
+            dev_err.zero_()
+            raise PCPError(code, where + " (device)")
+
+
+def workspace_size(batch: int, total_q: int, n_q_heads: int, n_kv_heads: int,
+                   head_dim: int) -> int:
+    return int(lib().pcp_extend_workspace_size(batch, total_q, n_q_heads, n_kv_heads, head_dim))
+
+
+def compute_out_cache_loc(qo_indptr: torch.Tensor, kv_indptr: torch.Tensor,
+                          kv_indices: torch.Tensor, prefix_lens: torch.Tensor, page_size: int,
+                          num_pages: int, total_q: Optional[int] = None,
+                          out: Optional[torch.Tensor] = None,
+                          dev_err: Optional[torch.Tensor] = None,
+                          check: bool = True) -> torch.Tensor:
+    """Slots (int64 [total_q]) where each new token of every chunk goes."""
+    dev = qo_indptr.device
+    for n, t in (("qo_indptr", qo_indptr), ("kv_indptr", kv_indptr),
+                 ("kv_indices", kv_indices), ("prefix_lens", prefix_lens)):
+        _need(t, n, torch.int32, dev)
+    batch = qo_indptr.numel() - 1
+    if total_q is None:
+        total_q = int(qo_indptr[-1].item()) if batch > 0 else 0
+    if out is None:
+        out = torch.empty(total_q, dtype=torch.int64, device=dev)
+    own = dev_err is None
+    if own:
+        dev_err = _dev_err(dev)
+    _check(lib().pcp_compute_out_cache_loc(_ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices),
+                                           _ptr(prefix_lens), batch, total_q, page_size,
+                                           num_pages, _ptr(out), _ptr(dev_err), _stream(dev)),
+           "pcp_compute_out_cache_loc")
+    _finish(dev_err, own, check, "pcp_compute_out_cache_loc")
+    return out
+
+
+def kv_append(k: torch.Tensor, v: torch.Tensor, out_cache_loc: torch.Tensor,
+              k_pool: torch.Tensor, v_pool: torch.Tensor,
+              dev_err: Optional[torch.Tensor] = None, check: bool = True) -> None:
+    """k_pool[out_cache_loc[t]] = k[t]; v_pool[...] = v[t]  (in place)."""
+    dev = k.device
+    for n, t in (("k", k), ("v", v), ("k_pool", k_pool), ("v_pool", v_pool)):
+        _need(t, n, torch.bfloat16, dev)
+    _need(out_cache_loc, "out_cache_loc", torch.int64, dev)
+    if k.dim() != 3 or v.shape != k.shape or k_pool.shape != v_pool.shape:
+        raise ValueError("k, v must be [n, Hkv, D] and the pools [slots, Hkv, D]")
+    if tuple(k_pool.shape[1:]) != tuple(k.shape[1:]):
+        raise ValueError("pool rows must match k rows")
+    own = dev_err is None
+    if own:
+        dev_err = _dev_err(dev)
+    _check(lib().pcp_kv_append(_ptr(k), _ptr(v), _ptr(out_cache_loc), k.shape[0], k.shape[1],
+                               k.shape[2], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
+                               _ptr(dev_err), _stream(dev)), "pcp_kv_append")
+    _finish(dev_err, own, check, "pcp_kv_append")
+
+
+def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch.Tensor,
+                      kv_indices: torch.Tensor, prefix_lens: torch.Tensor,
+                      k_pool: torch.Tensor, v_pool: torch.Tensor, page_size: int,
+                      n_q_heads: int, n_kv_heads: int, head_dim: int, window: int = 0,
+                      sm_scale: float = 0.0, *, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None,
+                      dev_err: Optional[torch.Tensor] = None,
+                      check: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Extend attention of every query row over its cached prefix and own
+    chunk (bottom-right causal, GQA, optional window).  Returns (out, lse):
+    out bf16 [total_q, Hq, D], lse float32 [total_q, Hq] (natural log)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k_pool, "k_pool", torch.bfloat16, dev)
+    _need(v_pool, "v_pool", torch.bfloat16, dev)
+    for n, t in (("qo_indptr", qo_indptr), ("kv_indptr", kv_indptr),
+                 ("kv_indices", kv_indices), ("prefix_lens", prefix_lens)):
+        _need(t, n, torch.int32, dev)
+    if q.dim() != 3 or q.shape[1] != n_q_heads or q.shape[2] != head_dim:
+        raise ValueError("q must be [total_q, n_q_heads, head_dim]")
+    if k_pool.shape[0] % page_size != 0:
+        raise ValueError("pool slots must be a multiple of page_size")
+    batch = qo_indptr.numel() - 1
+    total_q = q.shape[0]
+    num_pages = k_pool.shape[0] // page_size
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(total_q, n_q_heads, dtype=torch.float32, device=dev)
+    need = workspace_size(batch, total_q, n_q_heads, n_kv_heads, head_dim)
+    if workspace is None:
+        workspace = _workspace(dev, need)
+    own = dev_err is None
+    if own:
+        dev_err = _dev_err(dev)
+    _check(lib().pcp_paged_extend_attn(
+        _ptr(q), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(prefix_lens), batch,
+        total_q, _ptr(k_pool), _ptr(v_pool), num_pages, page_size, n_q_heads, n_kv_heads,
+        head_dim, window, float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel(), _ptr(dev_err), _stream(dev)), "pcp_paged_extend_attn")
+    _finish(dev_err, own, check, "pcp_paged_extend_attn")
+    return out, lse
+
+
+def set_timing_events(before, after) -> None:
+    """Record `before`/`after` (torch.cuda.Event, or None) around the
+    tensor-core kernel of every later paged_extend_attn call."""
+    b = ctypes.c_void_p(before.cuda_event) if before is not None else ctypes.c_void_p(0)
+    a = ctypes.c_void_p(after.cuda_event) if after is not None else ctypes.c_void_p(0)
+    _check(lib().pcp_set_timing_events(b, a), "pcp_set_timing_events")

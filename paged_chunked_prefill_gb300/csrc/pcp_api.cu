@@ -1,0 +1,321 @@
+// The C ABI: argument validation, workspace layout, tensor-map encoding and
+// the launches of the planner, tensor-core and row kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pcp.h"
+#include "pcp_internal.h"
+
+namespace pcp {
+
+cudaError_t launch_plan(cudaStream_t stream, const PlanParams& p);
+cudaError_t launch_extend_tc(int head_dim, int grid, cudaStream_t stream, const TcParams& p,
+                             const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv);
+cudaError_t launch_rows(int head_dim, int grid, cudaStream_t stream, const RowParams& p);
+cudaError_t launch_out_cache_loc(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                 const int32_t* kv_indices, const int32_t* prefix_lens,
+                                 int batch, int64_t total_q, int page_size, int64_t num_pages,
+                                 int64_t* loc, int32_t* dev_err, int sm_count,
+                                 cudaStream_t stream);
+cudaError_t launch_kv_append(const void* k, const void* v, const int64_t* loc, int64_t n_tokens,
+                             int chunks_per_token, void* k_pool, void* v_pool, int64_t pool_slots,
+                             int32_t* dev_err, int sm_count, cudaStream_t stream);
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sm_count[kMaxDevices] = {0};
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeFn g_encode = nullptr;
+cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+
+// SM count of the current device, cached per device.
+pcp_status sm_count(int* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PCP_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (dev < 0 || dev >= kMaxDevices) return PCP_ERR_UNSUPPORTED;
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PCP_ERR_CUDA;
+        g_sm_count[dev] = n;
+    }
+    *out = g_sm_count[dev];
+    return PCP_OK;
+}
+
+pcp_status get_encoder(EncodeFn* fn) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_encode == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || p == nullptr)
+            return PCP_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeFn>(p);
+    }
+    *fn = g_encode;
+    return PCP_OK;
+}
+
+// 3-D bf16 tensor map over [d2][d1][d0] with a 128-byte-swizzled box.
+pcp_status encode_3d(EncodeFn enc, CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
+                     uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2) {
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PCP_OK : PCP_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int gcd_int(int a, int b) {
+    while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+}  // namespace
+}  // namespace pcp
+
+using namespace pcp;
+
+extern "C" {
+
+const char* pcp_status_string(int status) {
+    switch (status) {
+        case PCP_OK: return "PCP_OK";
+        case PCP_ERR_INVALID_ARG: return "PCP_ERR_INVALID_ARG: invalid argument";
+        case PCP_ERR_UNSUPPORTED: return "PCP_ERR_UNSUPPORTED: unsupported shape";
+        case PCP_ERR_BAD_INDEX: return "PCP_ERR_BAD_INDEX: page id or slot outside the pool";
+        case PCP_ERR_WORKSPACE: return "PCP_ERR_WORKSPACE: workspace too small or misaligned";
+        case PCP_ERR_CUDA: return "PCP_ERR_CUDA: CUDA call failed";
+        case PCP_ERR_TIMEOUT: return "PCP_ERR_TIMEOUT: a bounded device wait ran out";
+        default: return "PCP_ERR_UNKNOWN";
+    }
+}
+
+int pcp_abi_version(void) { return 1; }
+
+pcp_status pcp_compute_out_cache_loc(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                     const int32_t* kv_indices, const int32_t* prefix_lens,
+                                     int batch, int64_t total_q, int page_size,
+                                     int64_t num_pages, int64_t* out_cache_loc,
+                                     int32_t* dev_err, void* stream) {
+    if (batch < 0 || total_q < 0 || page_size < 1 || num_pages < 0 || dev_err == nullptr)
+        return PCP_ERR_INVALID_ARG;
+    if (batch == 0 && total_q != 0) return PCP_ERR_INVALID_ARG;
+    if (total_q == 0) return PCP_OK;
+    if (!qo_indptr || !kv_indptr || !kv_indices || !prefix_lens || !out_cache_loc)
+        return PCP_ERR_INVALID_ARG;
+    int sms = 0;
+    pcp_status st = sm_count(&sms);
+    if (st != PCP_OK) return st;
+    cudaError_t e = launch_out_cache_loc(qo_indptr, kv_indptr, kv_indices, prefix_lens, batch,
+                                         total_q, page_size, num_pages, out_cache_loc, dev_err,
+                                         sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PCP_OK : PCP_ERR_CUDA;
+}
+
+pcp_status pcp_kv_append(const void* k, const void* v, const int64_t* out_cache_loc,
+                         int64_t n_tokens, int n_kv_heads, int head_dim, void* k_pool,
+                         void* v_pool, int64_t pool_slots, int32_t* dev_err, void* stream) {
+    if (n_tokens < 0 || n_kv_heads < 1 || head_dim < 1 || pool_slots < 0 || dev_err == nullptr)
+        return PCP_ERR_INVALID_ARG;
+    if ((head_dim * 2) % 16 != 0) return PCP_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return PCP_OK;
+    if (!k || !v || !out_cache_loc || !k_pool || !v_pool) return PCP_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16))
+        return PCP_ERR_INVALID_ARG;
+    int sms = 0;
+    pcp_status st = sm_count(&sms);
+    if (st != PCP_OK) return st;
+    const int chunks = n_kv_heads * head_dim * 2 / 16;
+    cudaError_t e = launch_kv_append(k, v, out_cache_loc, n_tokens, chunks, k_pool, v_pool,
+                                     pool_slots, dev_err, sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PCP_OK : PCP_ERR_CUDA;
+}
+
+size_t pcp_extend_workspace_size(int batch, int64_t total_q, int n_q_heads, int n_kv_heads,
+                                 int head_dim) {
+    if (head_dim != 64 && head_dim != 128) return 0;
+    WsLayout L;
+    if (!ws_layout(batch, total_q, n_q_heads, n_kv_heads, head_dim, &L)) return 0;
+    return L.total;
+}
+
+pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
+                                 const int32_t* kv_indptr, const int32_t* kv_indices,
+                                 const int32_t* prefix_lens, int batch, int64_t total_q,
+                                 const void* k_pool, const void* v_pool, int64_t num_pages,
+                                 int page_size, int n_q_heads, int n_kv_heads, int head_dim,
+                                 int window, float sm_scale, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                 void* stream) {
+    // ---- host-visible argument checks, before anything is launched
+    if (batch < 0 || total_q < 0 || total_q >= (int64_t(1) << 31) || n_q_heads < 1 ||
+        n_kv_heads < 1 || page_size < 1 || window < 0 || num_pages < 0 || dev_err == nullptr)
+        return PCP_ERR_INVALID_ARG;
+    if (batch == 0 && total_q != 0) return PCP_ERR_INVALID_ARG;
+    if (n_q_heads % n_kv_heads != 0) return PCP_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PCP_ERR_UNSUPPORTED;
+    const int group = n_q_heads / n_kv_heads;
+    if (group > kTileM) return PCP_ERR_UNSUPPORTED;
+    if (!std::isfinite(sm_scale)) return PCP_ERR_INVALID_ARG;
+    if (num_pages * (int64_t)page_size >= (int64_t(1) << 31)) return PCP_ERR_UNSUPPORTED;
+    WsLayout lay;
+    if (!ws_layout(batch, total_q, n_q_heads, n_kv_heads, head_dim, &lay))
+        return PCP_ERR_INVALID_ARG;
+    if (total_q == 0) return PCP_OK;
+    if (!q || !qo_indptr || !kv_indptr || !kv_indices || !prefix_lens || !k_pool || !v_pool ||
+        !out)
+        return PCP_ERR_INVALID_ARG;
+    if (num_pages < 1) return PCP_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16))
+        return PCP_ERR_INVALID_ARG;
+    if (workspace == nullptr || workspace_bytes < lay.total || !aligned(workspace, 256))
+        return PCP_ERR_WORKSPACE;
+
+    int sms = 0;
+    pcp_status st = sm_count(&sms);
+    if (st != PCP_OK) return st;
+    EncodeFn enc = nullptr;
+    st = get_encoder(&enc);
+    if (st != PCP_OK) return st;
+
+    const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)head_dim);
+    const float scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    const int qpos = q_positions_per_tile(group);
+    const int num_slots = (int)(num_pages * page_size);
+    const int g128 = gcd_int(page_size, kTileN);
+    const int box_rows = g128 >= 8 ? g128 : 0;
+
+    // ---- tensor maps: Q boxes of (64 dims, G heads, qpos positions); K/V
+    // boxes of (64 dims, one KV head, one page run)
+    CUtensorMap tq, tk, tv;
+    if ((st = encode_3d(enc, &tq, q, head_dim, n_q_heads, total_q, 64, group, qpos)) != PCP_OK)
+        return st;
+    const uint32_t kv_box = box_rows > 0 ? box_rows : 8;
+    if ((st = encode_3d(enc, &tk, k_pool, head_dim, n_kv_heads, num_slots, 64, 1, kv_box)) !=
+        PCP_OK)
+        return st;
+    if ((st = encode_3d(enc, &tv, v_pool, head_dim, n_kv_heads, num_slots, 64, 1, kv_box)) !=
+        PCP_OK)
+        return st;
+
+    // ---- 1. plan
+    PlanParams pp;
+    pp.qo_indptr = qo_indptr;
+    pp.kv_indptr = kv_indptr;
+    pp.prefix_lens = prefix_lens;
+    pp.batch = batch;
+    pp.total_q = total_q;
+    pp.n_kv_heads = n_kv_heads;
+    pp.group = group;
+    pp.page_size = page_size;
+    pp.window = window;
+    pp.sm_count = sms;
+    pp.ws = ws;
+    pp.lay = lay;
+    pp.dev_err = dev_err;
+    if (launch_plan(s, pp) != cudaSuccess) return PCP_ERR_CUDA;
+
+    // ---- 2. tensor-core extend kernel (persistent, one CTA per SM)
+    TcParams tp;
+    tp.qo_indptr = qo_indptr;
+    tp.kv_indptr = kv_indptr;
+    tp.kv_indices = kv_indices;
+    tp.prefix_lens = prefix_lens;
+    tp.ws = ws;
+    tp.lay = lay;
+    tp.k_pool = static_cast<const uint16_t*>(k_pool);
+    tp.v_pool = static_cast<const uint16_t*>(v_pool);
+    tp.out = static_cast<uint16_t*>(out);
+    tp.lse = lse;
+    tp.n_q_heads = n_q_heads;
+    tp.n_kv_heads = n_kv_heads;
+    tp.group = group;
+    tp.qpos = qpos;
+    tp.page_size = page_size;
+    tp.box_rows = box_rows;
+    tp.num_pages = num_pages;
+    tp.num_slots = num_slots;
+    tp.window = window;
+    tp.scale_log2 = scale_log2;
+    tp.dev_err = dev_err;
+    cudaEvent_t evb = nullptr, eva = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        evb = g_ev_before;
+        eva = g_ev_after;
+    }
+    if (evb && cudaEventRecord(evb, s) != cudaSuccess) return PCP_ERR_CUDA;
+    if (launch_extend_tc(head_dim, sms, s, tp, tq, tk, tv) != cudaSuccess) return PCP_ERR_CUDA;
+    if (eva && cudaEventRecord(eva, s) != cudaSuccess) return PCP_ERR_CUDA;
+
+    // ---- 3. decode-shaped rows (split-KV on CUDA cores)
+    if (row_path_max_chunk(group) > 0) {
+        RowParams rp;
+        rp.q = static_cast<const uint16_t*>(q);
+        rp.qo_indptr = qo_indptr;
+        rp.kv_indptr = kv_indptr;
+        rp.kv_indices = kv_indices;
+        rp.prefix_lens = prefix_lens;
+        rp.ws = ws;
+        rp.lay = lay;
+        rp.k_pool = static_cast<const uint16_t*>(k_pool);
+        rp.v_pool = static_cast<const uint16_t*>(v_pool);
+        rp.out = static_cast<uint16_t*>(out);
+        rp.lse = lse;
+        rp.n_q_heads = n_q_heads;
+        rp.n_kv_heads = n_kv_heads;
+        rp.group = group;
+        rp.page_size = page_size;
+        rp.num_pages = num_pages;
+        rp.window = window;
+        rp.scale_log2 = scale_log2;
+        rp.dev_err = dev_err;
+        if (launch_rows(head_dim, sms, s, rp) != cudaSuccess) return PCP_ERR_CUDA;
+    }
+    return PCP_OK;
+}
+
+pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_err) {
+    if (dev_err == nullptr || host_err == nullptr) return PCP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(host_err, dev_err, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess)
+        return PCP_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PCP_ERR_CUDA;
+    return PCP_OK;
+}
+
+pcp_status pcp_set_timing_events(void* before, void* after) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if ((before == nullptr) != (after == nullptr)) return PCP_ERR_INVALID_ARG;
+    g_ev_before = static_cast<cudaEvent_t>(before);
+    g_ev_after = static_cast<cudaEvent_t>(after);
+    return PCP_OK;
+}
+
+}  // extern "C"

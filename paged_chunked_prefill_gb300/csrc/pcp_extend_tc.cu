@@ -1,0 +1,572 @@
+// Tensor-core paged extend attention for sm_103a (tcgen05 + TMEM + TMA).
+//
+// Computes, for the tensor-core work items built by the planner, the extend
+// attention of AReno PR #642 ("What does this PR do?": later chunks attend to
+// the cached prefix plus their own chunk, bottom-right causal alignment) over
+// a paged KV pool, with GQA and an optional sliding window.  The AstrAI paged
+// prefill kernel (split-Q, mma.sync, one query head per CTA) is prior art for
+// the semantics only; this kernel is laid out for Blackwell:
+//
+//  * A work item is (sequence b, KV head g, 2 x 128 query rows).  The rows of
+//    one 128-row Q tile are (position, head) pairs of the G = Hq/Hkv query
+//    heads of KV head g, so every K/V tile fetched from HBM feeds 2 x G query
+//    heads (GQA head-group sharing) and 4 tcgen05 MMAs.
+//  * Warp roles (320 threads, persistent CTA per SM, dynamic item counter):
+//      warp 0      producer: Q by TMA; K/V pages gathered through the page
+//                  table into 128-byte-swizzled smem stages (one TMA box per
+//                  page run; cp.async for page sizes below 8 rows and for the
+//                  V rows past the sequence end, which are zero-filled);
+//      warp 1      one thread issues tcgen05.mma: S_u = Q_u K^T into TMEM,
+//                  then O_u += P_u V with P_u read from TMEM;
+//      warps 2-5   softmax for Q tile 0, warps 6-9 for Q tile 1: one thread
+//                  per row, tcgen05.ld of S, mask only on diagonal / window
+//                  edge tiles, online softmax in fp32 with exp2 and a lazy O
+//                  rescale (only when the running max grows by > 2^8), P
+//                  written back to TMEM as bf16, epilogue O / l -> bf16, lse.
+//  * Ping-pong: while one softmax group works on its S tile, the tensor core
+//    runs the other group's QK^T or PV.
+//  * Every wait is bounded; a wait that runs out records PCP_ERR_TIMEOUT,
+//    the CTA drains its copies and MMAs, frees TMEM and exits.
+#include "pcp_device.cuh"
+#include "pcp_internal.h"
+
+namespace pcp {
+
+namespace {
+
+template <int D>
+struct TcCfg {
+    static constexpr int kHalves = D / 64;                   // 128-byte column blocks
+    static constexpr int kStages = D == 128 ? 2 : 4;
+    static constexpr uint32_t kHalfBytes = kTileN * 128;     // one column block of a tile
+    static constexpr uint32_t kTileBytes = kTileN * D * 2;   // a K or V tile
+    static constexpr uint32_t kQBytes = kTileM * D * 2;      // a Q tile
+    static constexpr uint32_t kOffQ = 0;
+    // V stages sit before the K stages: the MN-major V operand is read with
+    // the largest descriptor strides, and this keeps every read of it inside
+    // the CTA's shared memory.
+    static constexpr uint32_t kOffV = kOffQ + kQTiles * kQBytes;
+    static constexpr uint32_t kOffK = kOffV + kStages * kTileBytes;
+    static constexpr uint32_t kOffBar = kOffK + kStages * kTileBytes;
+    static constexpr int kNumBars = 1 + 4 * kStages + 6 + 1;
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;
+    // barrier indices
+    static constexpr int bQFull = 0;
+    static constexpr int bKFull = 1;
+    static constexpr int bKEmpty = 1 + kStages;
+    static constexpr int bVFull = 1 + 2 * kStages;
+    static constexpr int bVEmpty = 1 + 3 * kStages;
+    static constexpr int bSFull = 1 + 4 * kStages;
+    static constexpr int bPFull = 3 + 4 * kStages;
+    static constexpr int bODone = 5 + 4 * kStages;
+    static constexpr int bDrain = 7 + 4 * kStages;
+};
+
+struct Geo {
+    int b, g, pos0, c, P, L, q_row0, nq;
+    int first[2], last[2];  // KV tile range of each Q tile (first > last: inactive)
+    int pl[2], ph[2];       // first / last valid absolute position of each Q tile
+    int t_begin, t_end;
+};
+
+__device__ __forceinline__ Geo make_geo(const TcParams& p, int4 it) {
+    Geo g;
+    g.b = it.x;
+    g.g = it.y;
+    g.pos0 = it.z;
+    const int q0 = p.qo_indptr[g.b];
+    g.c = p.qo_indptr[g.b + 1] - q0;
+    g.P = p.prefix_lens[g.b];
+    g.L = g.P + g.c;
+    g.q_row0 = q0 + g.pos0;
+    g.nq = (g.pos0 + p.qpos < g.c) ? 2 : 1;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int start = g.pos0 + u * p.qpos;
+        if (start < g.c) {
+            g.pl[u] = g.P + start;
+            g.ph[u] = g.P + min(start + p.qpos, g.c) - 1;
+            const int lo = p.window > 0 ? max(0, g.pl[u] - p.window + 1) : 0;
+            g.first[u] = lo / kTileN;
+            g.last[u] = g.ph[u] / kTileN;
+        } else {
+            g.pl[u] = g.ph[u] = 0;
+            g.first[u] = 1;
+            g.last[u] = 0;
+        }
+    }
+    g.t_begin = g.first[0];
+    g.t_end = g.nq == 2 ? g.last[1] : g.last[0];
+    return g;
+}
+
+__device__ __forceinline__ bool tile_active(const Geo& g, int u, int t) {
+    return g.first[u] <= t && t <= g.last[u];
+}
+
+// Load one K or V tile (keys [t*128, t*128+128) of sequence b, KV head g)
+// into a 128-byte-swizzled stage: column block h at h * 16 KB, row r at
+// r * 128 bytes, 16-byte chunk c of a row at position c ^ (r % 8).
+template <int D>
+__device__ __forceinline__ void load_kv_tile(const TcParams& p, const Geo& geo, int t,
+                                             const CUtensorMap* map, const uint16_t* pool,
+                                             uint32_t dst, uint32_t bar, bool zero_tail,
+                                             int lane) {
+    using C = TcCfg<D>;
+    const int key0 = t * kTileN;
+    const int32_t* pages = p.kv_indices + p.kv_indptr[geo.b];
+    const int ps = p.page_size;
+    if (p.box_rows > 0) {
+        const int br = p.box_rows;
+        const int nsub = kTileN / br;
+        const int nloads = nsub * C::kHalves;
+        int strad = -1;
+        if (zero_tail && geo.L > key0 && geo.L < key0 + kTileN && (geo.L - key0) % br != 0)
+            strad = (geo.L - key0) / br;
+        if (strad >= 0) {
+            // rows of this page run past the sequence end are zero-filled
+            const int ks = key0 + strad * br;
+            const int page = pages[ks / ps];
+            const bool bad = page < 0 || page >= p.num_pages;
+            if (bad && lane == 0) report_error(p.dev_err, PCP_ERR_BAD_INDEX);
+            const int64_t slot0 = (int64_t)page * ps + ks % ps;
+            for (int idx = lane; idx < br * C::kHalves * 8; idx += 32) {
+                const int row = idx / (C::kHalves * 8);
+                const int c = idx % (C::kHalves * 8);
+                const int rt = strad * br + row;
+                const bool ok = !bad && ks + row < geo.L;
+                const uint16_t* src =
+                    ok ? pool + ((slot0 + row) * p.n_kv_heads + geo.g) * D + c * 8 : pool;
+                cp_async_16(dst + (c >> 3) * C::kHalfBytes + rt * 128 + (((c & 7) ^ (rt & 7)) << 4),
+                            src, ok ? 16u : 0u);
+            }
+            cp_async_mbar_arrive(bar);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar,
+                                  (uint32_t)(nloads - (strad >= 0 ? C::kHalves : 0)) * br * 128);
+        __syncwarp();
+        if (lane < nloads) {
+            const int sb = lane % nsub;
+            const int h = lane / nsub;
+            if (sb != strad) {
+                const int key = key0 + sb * br;
+                int z = p.num_slots;  // fully out of range: TMA writes zeros
+                if (key < geo.L) {
+                    const int page = pages[key / ps];
+                    if (page >= 0 && page < p.num_pages)
+                        z = page * ps + key % ps;
+                    else
+                        report_error(p.dev_err, PCP_ERR_BAD_INDEX);
+                }
+                tma_load_3d(dst + h * C::kHalfBytes + sb * br * 128, map, bar, h * 64, geo.g, z);
+            }
+        }
+    } else {
+        // small pages: one 16-byte cp.async per row chunk, zero-filled past the end
+        for (int row = lane; row < kTileN; row += 32) {
+            const int key = key0 + row;
+            bool ok = key < geo.L;
+            int64_t slot = 0;
+            if (ok) {
+                const int page = pages[key / ps];
+                if (page >= 0 && page < p.num_pages) {
+                    slot = (int64_t)page * ps + key % ps;
+                } else {
+                    report_error(p.dev_err, PCP_ERR_BAD_INDEX);
+                    ok = false;
+                }
+            }
+            const uint16_t* src = ok ? pool + (slot * p.n_kv_heads + geo.g) * D : pool;
+#pragma unroll
+            for (int c = 0; c < C::kHalves * 8; ++c)
+                cp_async_16(dst + (c >> 3) * C::kHalfBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4),
+                            ok ? src + c * 8 : pool, ok ? 16u : 0u);
+        }
+        cp_async_mbar_arrive(bar);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
+    }
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    extend_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v) {
+    using C = TcCfg<D>;
+    constexpr int S = C::kStages;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t sQ = base + C::kOffQ;
+    const uint32_t sK = base + C::kOffK;
+    const uint32_t sV = base + C::kOffV;
+    const uint32_t sBar = base + C::kOffBar;
+    volatile int* misc = reinterpret_cast<volatile int*>(gbase + C::kOffMisc);
+    // misc[0] TMEM base, misc[1] current item, misc[2] abort flag
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::bQFull), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(C::bKFull + s), 1);
+            mbar_init(bar(C::bKEmpty + s), 1);
+            mbar_init(bar(C::bVFull + s), 1);
+            mbar_init(bar(C::bVEmpty + s), 1);
+        }
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(bar(C::bSFull + u), 1);
+            mbar_init(bar(C::bPFull + u), 128);
+            mbar_init(bar(C::bODone + u), 1);
+        }
+        mbar_init(bar(C::bDrain), 1);
+        fence_mbarrier_init();
+        misc[2] = 0;
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr((const void*)&misc[0]), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = (uint32_t)misc[0];
+
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(const_cast<unsigned char*>(p.ws) + p.lay.header);
+    const int n_items = hdr->n_tc_items;
+    const int4* items = reinterpret_cast<const int4*>(p.ws + p.lay.tc_items);
+    volatile int* abort_flag = &misc[2];
+    const int G = p.group;
+    const float sl2 = p.scale_log2;
+
+    uint32_t kv_iter = 0;          // KV tiles handled so far by this CTA
+    uint32_t act[2] = {0u, 0u};    // active (Q tile, KV tile) pairs so far, per Q tile
+    uint32_t n_done = 0;           // items finished (q_full phase)
+    int last_it[4] = {-1, -1, -1, -1};  // producer: last KV iteration per stage
+
+    for (;;) {
+        if (threadIdx.x == 0) misc[1] = atomicAdd(&hdr->tc_next, 1);
+        __syncthreads();
+        const int item = misc[1];
+        if (item >= n_items || *abort_flag) break;
+        const Geo geo = make_geo(p, items[item]);
+        const int ntiles = geo.t_end - geo.t_begin + 1;
+
+        if (warp == 0) {
+            // ------------------------------------------------ producer
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(C::bQFull),
+                                      (uint32_t)(geo.nq * C::kHalves * G * p.qpos * 128));
+                for (int u = 0; u < geo.nq; ++u)
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(sQ + u * C::kQBytes + h * (kTileM * 128), &tm_q,
+                                    bar(C::bQFull), h * 64, geo.g * G, geo.q_row0 + u * p.qpos);
+            }
+            for (int i = 0; i < ntiles; ++i) {
+                const int t = geo.t_begin + i;
+                const uint32_t cur = kv_iter + i;
+                const int st = cur % S;
+                const uint32_t ph = (cur / S) & 1u;
+                if (!mbar_wait(bar(C::bKEmpty + st), ph ^ 1u, abort_flag, p.dev_err, kSpinLimitNs))
+                    break;
+                load_kv_tile<D>(p, geo, t, &tm_k, p.k_pool, sK + st * C::kTileBytes,
+                                bar(C::bKFull + st), false, lane);
+                if (!mbar_wait(bar(C::bVEmpty + st), ph ^ 1u, abort_flag, p.dev_err, kSpinLimitNs))
+                    break;
+                load_kv_tile<D>(p, geo, t, &tm_v, p.v_pool, sV + st * C::kTileBytes,
+                                bar(C::bVFull + st), true, lane);
+                last_it[st] = (int)cur;
+            }
+        } else if (warp == 1) {
+            // ------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false);
+                constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, true);
+                auto issue_qk = [&](int u, int st) {
+                    const uint32_t qa = sQ + u * C::kQBytes;
+                    const uint32_t ka = sK + st * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * (kTileM * 128) + (kk & 3) * 32;
+                        umma_ss(tmem + u * 128, sdesc_sw128(qa + off, 16, 1024),
+                                sdesc_sw128(ka + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    }
+                };
+                auto issue_pv = [&](int u, int st, bool acc) {
+                    const uint32_t va = sV + st * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTileN / 16; ++kk)
+                        umma_ts(tmem + 256 + u * 128, tmem + u * 128 + kk * 8,
+                                sdesc_sw128(va + kk * 2048, C::kHalfBytes, 1024), idesc_pv,
+                                (acc || kk > 0) ? 1u : 0u);
+                };
+                bool ok = mbar_wait(bar(C::bQFull), n_done & 1u, abort_flag, p.dev_err,
+                                    kSpinLimitNs);
+                uint32_t aidx[2] = {act[0], act[1]};
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t c0 = kv_iter;
+                    ok = mbar_wait(bar(C::bKFull + c0 % S), (c0 / S) & 1u, abort_flag,
+                                   p.dev_err, kSpinLimitNs);
+                    if (ok) {
+                        fence_proxy_async_smem();
+                        tc_fence_after();
+                        for (int u = 0; u < 2; ++u)
+                            if (tile_active(geo, u, geo.t_begin)) {
+                                issue_qk(u, c0 % S);
+                                umma_commit(bar(C::bSFull + u));
+                            }
+                        umma_commit(bar(C::bKEmpty + c0 % S));
+                    }
+                }
+                for (int i = 0; ok && i < ntiles; ++i) {
+                    const int t = geo.t_begin + i;
+                    const uint32_t cur = kv_iter + i;
+                    const int st = cur % S;
+                    if (!mbar_wait(bar(C::bVFull + st), (cur / S) & 1u, abort_flag, p.dev_err,
+                                   kSpinLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_after();
+                    const bool has_next = i + 1 < ntiles;
+                    const int nst = (cur + 1) % S;
+                    bool k_next = false;
+                    for (int u = 0; u < 2 && ok; ++u) {
+                        if (tile_active(geo, u, t)) {
+                            if (!mbar_wait(bar(C::bPFull + u), aidx[u] & 1u, abort_flag,
+                                           p.dev_err, kSpinLimitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_pv(u, st, t != geo.first[u]);
+                            umma_commit(bar(C::bODone + u));
+                            ++aidx[u];
+                        }
+                        if (has_next && tile_active(geo, u, t + 1)) {
+                            if (!k_next) {
+                                if (!mbar_wait(bar(C::bKFull + nst), ((cur + 1) / S) & 1u,
+                                               abort_flag, p.dev_err, kSpinLimitNs)) {
+                                    ok = false;
+                                    break;
+                                }
+                                fence_proxy_async_smem();
+                                tc_fence_after();
+                                k_next = true;
+                            }
+                            issue_qk(u, nst);
+                            umma_commit(bar(C::bSFull + u));
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(bar(C::bVEmpty + st));
+                    if (k_next) umma_commit(bar(C::bKEmpty + nst));
+                }
+            }
+            __syncwarp();
+        } else {
+            // ------------------------------------------------ softmax + epilogue
+            const int u = (warp - 2) >> 2;
+            const int quarter = warp & 3;
+            const int r = quarter * 32 + lane;
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            const uint32_t tS = tmem + lane_off + (uint32_t)u * 128u;
+            const uint32_t tO = tmem + lane_off + 256u + (uint32_t)u * 128u;
+            if (u < geo.nq) {
+                const int pos_local = u * p.qpos + r / G;
+                const bool row_valid = r < p.qpos * G && geo.pos0 + pos_local < geo.c;
+                const int pabs = geo.P + geo.pos0 + pos_local;
+                const int head = geo.g * G + r % G;
+                float m_run = -INFINITY, l_run = 0.f;
+                bool ok = true;
+                for (int t = geo.first[u]; t <= geo.last[u]; ++t) {
+                    const uint32_t a = act[u] + (uint32_t)(t - geo.first[u]);
+                    if (!mbar_wait(bar(C::bSFull + u), a & 1u, abort_flag, p.dev_err,
+                                   kSpinLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t sr[4][32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) tmem_ld32(tS + 32u * i, sr[i]);
+                    tmem_ld_wait();
+                    const int key0 = t * kTileN;
+                    const bool need_mask =
+                        (key0 + kTileN - 1 > geo.pl[u]) ||
+                        (p.window > 0 && key0 < geo.ph[u] - p.window + 1);
+                    float mx = -INFINITY;
+                    if (need_mask) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int key = key0 + i * 32 + j;
+                                const bool vis =
+                                    key <= pabs && (p.window <= 0 || key > pabs - p.window);
+                                float s = __uint_as_float(sr[i][j]);
+                                s = vis ? s : -INFINITY;
+                                sr[i][j] = __float_as_uint(s);
+                                mx = fmaxf(mx, s);
+                            }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(sr[i][j]));
+                    }
+                    const float m_new = fmaxf(m_run, mx);
+                    float alpha = 1.f;
+                    bool resc = false;
+                    if (m_run == -INFINITY) {
+                        m_run = m_new;
+                    } else if ((m_new - m_run) * sl2 > 8.f) {
+                        alpha = fast_exp2((m_run - m_new) * sl2);
+                        m_run = m_new;
+                        resc = true;
+                    }
+                    const float nref = m_run == -INFINITY ? 0.f : -m_run * sl2;
+                    float sum = 0.f;
+                    uint32_t pk[2][32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            const float e0 = fast_exp2(fmaf(__uint_as_float(sr[i][j]), sl2, nref));
+                            const float e1 =
+                                fast_exp2(fmaf(__uint_as_float(sr[i][j + 1]), sl2, nref));
+                            sum += e0 + e1;
+                            pk[i >> 1][(i & 1) * 16 + (j >> 1)] = pack_bf16x2(e0, e1);
+                        }
+                    l_run = l_run * alpha + sum;
+                    if (t > geo.first[u]) {
+                        if (!mbar_wait(bar(C::bODone + u), (a - 1u) & 1u, abort_flag, p.dev_err,
+                                       kSpinLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+                            for (int i = 0; i < D / 32; ++i) {
+                                uint32_t o[32];
+                                tmem_ld32(tO + 32u * i, o);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                                tmem_st32(tO + 32u * i, o);
+                            }
+                        }
+                    }
+                    tmem_st32(tS, pk[0]);
+                    tmem_st32(tS + 32u, pk[1]);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(bar(C::bPFull + u));
+                }
+                if (ok) {
+                    const uint32_t a_last = act[u] + (uint32_t)(geo.last[u] - geo.first[u]);
+                    ok = mbar_wait(bar(C::bODone + u), a_last & 1u, abort_flag, p.dev_err,
+                                   kSpinLimitNs);
+                }
+                if (ok) {
+                    tc_fence_after();
+                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                    const int64_t orow = (int64_t)(geo.q_row0 + pos_local) * p.n_q_heads + head;
+                    uint16_t* op = p.out + orow * D;
+#pragma unroll
+                    for (int i = 0; i < D / 32; ++i) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + 32u * i, o);
+                        tmem_ld_wait();
+                        uint32_t w[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv,
+                                               __uint_as_float(o[2 * j + 1]) * inv);
+                        if (row_valid) {
+                            uint4* dst = reinterpret_cast<uint4*>(op + i * 32);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                                                    w[4 * j + 3]);
+                        }
+                    }
+                    if (row_valid && p.lse != nullptr)
+                        p.lse[orow] = l_run > 0.f ? (m_run * sl2 + __log2f(l_run)) * 0.69314718055994531f
+                                                  : -INFINITY;
+                }
+            }
+        }
+        kv_iter += (uint32_t)ntiles;
+        for (int u = 0; u < geo.nq; ++u) act[u] += (uint32_t)(geo.last[u] - geo.first[u] + 1);
+        ++n_done;
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+
+    // ---------------------------------------------------------- teardown
+    const bool aborted = *abort_flag != 0;
+    if (warp == 0) {
+        cp_async_wait_all();
+        if (aborted && lane == 0) {
+            // let every TMA load this CTA issued land before the CTA exits
+            volatile int dummy = 0;
+            for (int s = 0; s < S; ++s)
+                if (last_it[s] >= 0) {
+                    const uint32_t ph = ((uint32_t)last_it[s] / S) & 1u;
+                    mbar_wait(bar(C::bKFull + s), ph, &dummy, p.dev_err, kSpinLimitNs);
+                    mbar_wait(bar(C::bVFull + s), ph, &dummy, p.dev_err, kSpinLimitNs);
+                }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // every MMA (and its mbarrier arrivals) completes before TMEM is freed
+        volatile int dummy = 0;
+        umma_commit(bar(C::bDrain));
+        mbar_wait(bar(C::bDrain), 0u, &dummy, p.dev_err, kSpinLimitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+size_t tc_smem_bytes(int head_dim) {
+    return head_dim == 128 ? TcCfg<128>::kSmemBytes : TcCfg<64>::kSmemBytes;
+}
+
+cudaError_t launch_extend_tc(int head_dim, int grid, cudaStream_t stream, const TcParams& p,
+                             const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv) {
+    const size_t smem = tc_smem_bytes(head_dim);
+    cudaError_t e;
+    if (head_dim == 128) {
+        e = cudaFuncSetAttribute(extend_tc_kernel<128>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        extend_tc_kernel<128><<<grid, kTcThreads, smem, stream>>>(p, tq, tk, tv);
+    } else {
+        e = cudaFuncSetAttribute(extend_tc_kernel<64>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        extend_tc_kernel<64><<<grid, kTcThreads, smem, stream>>>(p, tq, tk, tv);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace pcp

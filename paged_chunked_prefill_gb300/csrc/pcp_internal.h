@@ -1,0 +1,156 @@
+// Shared host/device definitions: tile sizes, the workspace layout, work-item
+// formats and kernel parameter blocks.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pcp.h"
+
+namespace pcp {
+
+// ---- tensor-core extend kernel geometry
+constexpr int kTileM = 128;       // query rows per Q tile (tcgen05 M)
+constexpr int kTileN = 128;       // keys per KV tile
+constexpr int kQTiles = 2;        // Q tiles per work item (share each K/V tile)
+constexpr int kTcThreads = 320;   // producer warp, MMA warp, 2 x 4 softmax warps
+
+// ---- CUDA-core row kernel (decode-shaped rows, split-KV)
+constexpr int kRowMaxRows = 16;   // query rows (positions x heads) per row item
+constexpr int kRowTile = 128;     // keys per row-kernel tile
+constexpr int kRowThreads = 128;
+constexpr int kRowTargetItems = 1024;  // split lengths aim at about this many items
+
+// Spin-wait limit of every bounded wait (nanoseconds).
+constexpr uint64_t kSpinLimitNs = 2000000000ull;
+
+// A sequence's chunk goes to the row kernel when its rows (chunk_len * G)
+// fit one row item and G <= kRowMaxRows; everything else to the tensor cores.
+__host__ __device__ inline int row_path_max_chunk(int group) {
+    return group <= kRowMaxRows ? (kRowMaxRows / group) : 0;
+}
+
+__host__ __device__ inline int q_positions_per_tile(int group) { return kTileM / group; }
+
+// ---- workspace
+struct WsHeader {
+    int n_tc_items;
+    int n_row_items;
+    int tc_next;       // dynamic scheduler counters
+    int row_next;
+    int tiles_per_split;
+    int pad[59];       // 256 bytes
+};
+
+// Tensor-core work item: {b, kv head g, first chunk position, cost in KV tiles}
+// Row work item (two int4): {b, g, split, n_splits}, {kv_begin, kv_end, first item of group, 0}
+
+struct WsLayout {
+    size_t header;        // offset of WsHeader
+    size_t tc_items;      // int4 [cap_tc]
+    size_t row_items;     // int4 [2 * cap_row]
+    size_t group_cnt;     // int  [cap_groups]
+    size_t partial_o;     // float [cap_row * kRowMaxRows * head_dim]
+    size_t partial_ml;    // float2 [cap_row * kRowMaxRows]
+    size_t total;
+    int64_t cap_tc;
+    int64_t cap_row;
+    int64_t cap_groups;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline bool ws_layout(int batch, int64_t total_q, int n_q_heads, int n_kv_heads, int head_dim,
+                      WsLayout* L) {
+    if (batch < 0 || total_q < 0 || n_q_heads < 1 || n_kv_heads < 1 ||
+        n_q_heads % n_kv_heads != 0)
+        return false;
+    const int group = n_q_heads / n_kv_heads;
+    if (group > kTileM) return false;
+    const int64_t qpos = (int64_t)q_positions_per_tile(group) * kQTiles;
+    L->cap_tc = (int64_t)n_kv_heads * ((total_q + qpos - 1) / qpos + batch);
+    L->cap_groups = (int64_t)n_kv_heads * batch;
+    L->cap_row = L->cap_groups + kRowTargetItems;
+    size_t off = 0;
+    L->header = off;
+    off += sizeof(WsHeader);
+    L->tc_items = off = align_up(off, 256);
+    off += (size_t)(L->cap_tc > 0 ? L->cap_tc : 1) * 16;
+    L->row_items = off = align_up(off, 256);
+    off += (size_t)L->cap_row * 32;
+    L->group_cnt = off = align_up(off, 256);
+    off += (size_t)(L->cap_groups > 0 ? L->cap_groups : 1) * 4;
+    L->partial_o = off = align_up(off, 256);
+    off += (size_t)L->cap_row * kRowMaxRows * head_dim * 4;
+    L->partial_ml = off = align_up(off, 256);
+    off += (size_t)L->cap_row * kRowMaxRows * 8;
+    L->total = align_up(off, 256);
+    return true;
+}
+
+// ---- parameters of the planner kernel
+struct PlanParams {
+    const int32_t* qo_indptr;
+    const int32_t* kv_indptr;
+    const int32_t* prefix_lens;
+    int batch;
+    int64_t total_q;
+    int n_kv_heads;
+    int group;
+    int page_size;
+    int window;
+    int sm_count;
+    unsigned char* ws;
+    WsLayout lay;
+    int32_t* dev_err;
+};
+
+// ---- parameters of the tensor-core extend kernel
+struct TcParams {
+    const int32_t* qo_indptr;
+    const int32_t* kv_indptr;
+    const int32_t* kv_indices;
+    const int32_t* prefix_lens;
+    const unsigned char* ws;
+    WsLayout lay;
+    const uint16_t* k_pool;
+    const uint16_t* v_pool;
+    uint16_t* out;
+    float* lse;
+    int n_q_heads;
+    int n_kv_heads;
+    int group;
+    int qpos;          // positions per Q tile
+    int page_size;
+    int box_rows;      // rows per TMA page box; 0 selects cp.async gathers
+    int64_t num_pages;
+    int num_slots;
+    int window;
+    float scale_log2;  // sm_scale * log2(e)
+    int32_t* dev_err;
+};
+
+// ---- parameters of the row (split-KV) kernel
+struct RowParams {
+    const uint16_t* q;
+    const int32_t* qo_indptr;
+    const int32_t* kv_indptr;
+    const int32_t* kv_indices;
+    const int32_t* prefix_lens;
+    unsigned char* ws;
+    WsLayout lay;
+    const uint16_t* k_pool;
+    const uint16_t* v_pool;
+    uint16_t* out;
+    float* lse;
+    int n_q_heads;
+    int n_kv_heads;
+    int group;
+    int page_size;
+    int64_t num_pages;
+    int window;
+    float scale_log2;
+    int32_t* dev_err;
+};
+
+}  // namespace pcp

@@ -1,0 +1,178 @@
+// Work planning on the device (one CTA).
+//
+// From the device copies of qo_indptr / prefix_lens / kv_indptr it builds the
+// two work lists of one pcp_paged_extend_attn call, so the host needs no copy
+// of the metadata and no synchronisation:
+//
+//  * tensor-core items {b, kv head, first position, cost}: each covers
+//    kQTiles * (128 / G) positions of one chunk for one KV head (all G query
+//    heads of that KV head packed into the MMA rows).  Items are ordered by
+//    cost (number of KV tiles) descending -- longest-processing-time first
+//    for the persistent kernel's dynamic scheduler -- with a counting sort.
+//  * row items for decode-shaped chunks (chunk_len * G <= 16 rows): the KV
+//    range of each (sequence, KV head) is split into pieces of
+//    `tiles_per_split` 128-key tiles, chosen so the whole call has about
+//    kRowTargetItems items.  This is the split-KV idea of the AstrAI paged
+//    decode kernel (split count from the SM count, partials merged by a
+//    log-sum-exp combine), with a fixed item budget instead of a per-batch
+//    split count.
+#include "pcp_device.cuh"
+#include "pcp_internal.h"
+
+namespace pcp {
+
+namespace {
+
+struct SeqInfo {
+    int c, P, L;
+    bool ok;
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const PlanParams& p, int b) {
+    SeqInfo s;
+    const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
+    s.c = q1 - q0;
+    s.P = p.prefix_lens[b];
+    s.L = s.P + s.c;
+    const int pages = p.kv_indptr[b + 1] - p.kv_indptr[b];
+    s.ok = q0 >= 0 && s.c >= 0 && q1 <= p.total_q && s.P >= 0 && pages >= 0 &&
+           (int64_t)pages * p.page_size >= (int64_t)s.L;
+    return s;
+}
+
+// First visible key of absolute position `pos`.
+__device__ __forceinline__ int first_key(int pos, int window) {
+    return window > 0 ? max(0, pos - window + 1) : 0;
+}
+
+__device__ __forceinline__ int tc_cost(int P, int c, int k, int item_pos, int window) {
+    const int first = P + k * item_pos;
+    const int last = P + min((k + 1) * item_pos, c) - 1;
+    return last / kTileN - first_key(first, window) / kTileN + 1;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanParams p) {
+    __shared__ int hist[1024];
+    __shared__ int scan[1024];
+    __shared__ unsigned long long s_row_tiles;
+    __shared__ int s_rows;
+    __shared__ int s_tps;
+
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
+    int4* tc = reinterpret_cast<int4*>(p.ws + p.lay.tc_items);
+    int4* rows = reinterpret_cast<int4*>(p.ws + p.lay.row_items);
+    int* gcnt = reinterpret_cast<int*>(p.ws + p.lay.group_cnt);
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int item_pos = q_positions_per_tile(p.group) * kQTiles;
+    const int rmax = row_path_max_chunk(p.group);
+    const int H = p.n_kv_heads;
+
+    for (int i = tid; i < 1024; i += nt) hist[i] = 0;
+    for (int64_t i = tid; i < (int64_t)p.batch * H; i += nt) gcnt[i] = 0;
+    if (tid == 0) {
+        s_row_tiles = 0;
+        s_rows = 0;
+        if (p.batch > 0 && p.qo_indptr[p.batch] != p.total_q)
+            report_error(p.dev_err, PCP_ERR_INVALID_ARG);
+    }
+    __syncthreads();
+
+    // pass 1: validate, histogram of tensor-core costs, total row-path tiles
+    for (int b = tid; b < p.batch; b += nt) {
+        const SeqInfo s = seq_info(p, b);
+        if (!s.ok) {
+            report_error(p.dev_err, PCP_ERR_INVALID_ARG);
+            continue;
+        }
+        if (s.c == 0) continue;
+        if (s.c <= rmax) {
+            const int tiles = (s.L - 1) / kRowTile - first_key(s.P, p.window) / kRowTile + 1;
+            atomicAdd(&s_row_tiles, (unsigned long long)tiles * H);
+        } else {
+            const int n = (s.c + item_pos - 1) / item_pos;
+            for (int k = 0; k < n; ++k)
+                atomicAdd(&hist[min(tc_cost(s.P, s.c, k, item_pos, p.window), 1023)], H);
+        }
+    }
+    __syncthreads();
+
+    // descending exclusive scan of the cost histogram
+    scan[tid] = hist[1023 - tid];
+    __syncthreads();
+    for (int d = 1; d < 1024; d <<= 1) {
+        const int v = tid >= d ? scan[tid - d] : 0;
+        __syncthreads();
+        scan[tid] += v;
+        __syncthreads();
+    }
+    const int n_tc = scan[1023];
+    {
+        const int bucket = 1023 - tid;
+        const int incl = scan[tid];
+        __syncthreads();
+        hist[bucket] = incl - hist[bucket];  // becomes the bucket's first slot
+    }
+    if (tid == 0) {
+        const unsigned long long tot = s_row_tiles;
+        unsigned long long tps = (tot + kRowTargetItems - 1) / kRowTargetItems;
+        s_tps = (int)(tps < 1 ? 1 : tps);
+    }
+    __syncthreads();
+    const int tps = s_tps;
+
+    // pass 2: scatter tensor-core items, emit row items
+    for (int b = tid; b < p.batch; b += nt) {
+        const SeqInfo s = seq_info(p, b);
+        if (!s.ok || s.c == 0) continue;
+        if (s.c <= rmax) {
+            const int lo = first_key(s.P, p.window);
+            const int t0 = lo / kRowTile, t1 = (s.L - 1) / kRowTile;
+            const int tiles = t1 - t0 + 1;
+            const int ns = (tiles + tps - 1) / tps;
+            for (int g = 0; g < H; ++g) {
+                const int base = atomicAdd(&s_rows, ns);
+                for (int sp = 0; sp < ns; ++sp) {
+                    const int it = base + sp;
+                    if (it >= p.lay.cap_row) {
+                        report_error(p.dev_err, PCP_ERR_WORKSPACE);
+                        break;
+                    }
+                    const int kb = max(lo, (t0 + sp * tps) * kRowTile);
+                    const int ke = min(s.L, (t0 + (sp + 1) * tps) * kRowTile);
+                    rows[2 * it] = make_int4(b, g, sp, ns);
+                    rows[2 * it + 1] = make_int4(kb, ke, base, 0);
+                }
+            }
+        } else {
+            const int n = (s.c + item_pos - 1) / item_pos;
+            for (int k = 0; k < n; ++k) {
+                const int cost = tc_cost(s.P, s.c, k, item_pos, p.window);
+                const int slot = atomicAdd(&hist[min(cost, 1023)], H);
+                for (int g = 0; g < H; ++g) {
+                    if (slot + g >= p.lay.cap_tc) {
+                        report_error(p.dev_err, PCP_ERR_WORKSPACE);
+                        break;
+                    }
+                    tc[slot + g] = make_int4(b, g, k * item_pos, cost);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        hdr->n_tc_items = (int)min((int64_t)n_tc, p.lay.cap_tc);
+        hdr->n_row_items = (int)min((int64_t)s_rows, p.lay.cap_row);
+        hdr->tc_next = 0;
+        hdr->row_next = 0;
+        hdr->tiles_per_split = tps;
+    }
+}
+
+cudaError_t launch_plan(cudaStream_t stream, const PlanParams& p) {
+    plan_kernel<<<1, 1024, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pcp
