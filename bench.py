@@ -1,0 +1,418 @@
+"""Benchmark of the paged chunked-prefill hot path on GB300.
+
+One step = slot mapping + KV append + paged extend attention (device work
+planning, the tensor-core kernel and the split-KV row kernel) over one batch
+of the GQA chunked-prefill workload (Qwen3-8B-like attention: B=8, 32 query /
+8 KV heads, head_dim 128, page_size 16, chunk 512, prefix ~U[0, 8192],
+scattered pages), inputs resident in HBM.  The metric is effective TFLOP/s:
+4 * head_dim * n_q_heads * (visible query/key pairs per head) per step -- only
+unmasked QK^T and PV work counts.
+
+Prints one JSON line.  Extra keys: roofline of the tensor-core kernel, the
+oracle timed on the host cores (cpu_baseline), an end-to-end figure through
+the C ABI with host buffers, the decode-row and KV-append bandwidths, and
+the SM clocks sampled during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "extend-attn effective TFLOP/s"
+UNIT = "TFLOP/s"
+
+
+def visible_pairs(prefix_lens, chunk_lens, window: int) -> int:
+    """Query/key pairs one head attends to (closed form per sequence)."""
+    total = 0
+    for P, c in zip(np.asarray(prefix_lens, np.int64), np.asarray(chunk_lens, np.int64)):
+        p = P + np.arange(c, dtype=np.int64)
+        n = p + 1
+        if window > 0:
+            n = np.minimum(n, window)
+        total += int(n.sum())
+    return total
+
+
+def rows_pairs(batch, tok, head) -> int:
+    """Visible pairs of selected (row, head) samples."""
+    b_of = np.searchsorted(batch.qo_indptr, tok, side="right") - 1
+    p = batch.prefix_lens[b_of].astype(np.int64) + (tok - batch.qo_indptr[b_of])
+    n = p + 1
+    if batch.window > 0:
+        n = np.minimum(n, batch.window)
+    return int(n.sum())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(batch, seconds_target: float, seed: int = 0):
+    """Time the FP64 oracle on a bounded sample of rows of `batch` (appended
+    pools).  Returns (TFLOP/s of effective work, threads, sample text)."""
+    import oracle
+    loc = oracle.out_cache_loc(batch.qo_indptr, batch.kv_indptr, batch.kv_indices,
+                               batch.prefix_lens, batch.page_size, batch.num_pages)
+    kp, vp = batch.k_pool.copy(), batch.v_pool.copy()
+    oracle.kv_append(batch.k_new, batch.v_new, loc, kp, vp)
+    rng = np.random.default_rng(seed)
+    D, Hq = batch.head_dim, batch.n_q_heads
+    n = 64
+    elapsed, done_flops, rows = 0.0, 0, 0
+    while elapsed < seconds_target:
+        tok = rng.integers(0, batch.total_q, size=n)
+        head = rng.integers(0, Hq, size=n).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.paged_extend_attn(batch.q, batch.qo_indptr, batch.kv_indptr, batch.kv_indices,
+                                 batch.prefix_lens, kp, vp, batch.page_size, Hq,
+                                 batch.n_kv_heads, D, batch.window, batch.sm_scale,
+                                 rows=(tok, head))
+        elapsed += time.perf_counter() - t0
+        done_flops += 4 * D * rows_pairs(batch, tok, head)
+        rows += n
+        n = min(n * 2, 4096)
+    return (done_flops / elapsed / 1e12, oracle.num_threads(),
+            f"{rows} random (row, head) pairs of the workload, {elapsed:.1f} s")
+
+
+def run_reference(args):
+    """Reference arm: the FP64 oracle on the host cores, a bounded row sample
+    per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads as W
+    batch = W.gqa_prefill()
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, cores, sample = oracle_sample(batch, per_step, seed=i)
+        if i >= args.warmup:
+            vals.append(v)
+    value = float(np.mean(vals))
+    flops = 4 * batch.head_dim * batch.n_q_heads * visible_pairs(
+        batch.prefix_lens, batch.chunk_lens, batch.window)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": flops / (value * 1e12) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": batch.name, "global_batch": batch.batch,
+                   "tokens_per_step": batch.total_q},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {sample}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import paged_chunked_prefill_gb300 as pcp
+    import workloads as W
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    args.warmup = max(args.warmup, 3)
+
+    batch = W.gqa_prefill()
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from helpers import to_device
+    d = to_device(batch, dev)
+    flops = 4 * batch.head_dim * batch.n_q_heads * visible_pairs(
+        batch.prefix_lens, batch.chunk_lens, batch.window)
+    ws = torch.empty(pcp.workspace_size(batch.batch, batch.total_q, batch.n_q_heads,
+                                        batch.n_kv_heads, batch.head_dim),
+                     dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    loc = torch.empty(batch.total_q, dtype=torch.int64, device=dev)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(batch.total_q, batch.n_q_heads, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step(q=None):
+        pcp.compute_out_cache_loc(d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                                  d["prefix_lens"], batch.page_size, batch.num_pages,
+                                  total_q=batch.total_q, out=loc, dev_err=err)
+        pcp.kv_append(d["k_new"], d["v_new"], loc, d["k_pool"], d["v_pool"], dev_err=err)
+        pcp.paged_extend_attn(d["q"] if q is None else q, d["qo_indptr"], d["kv_indptr"],
+                              d["kv_indices"], d["prefix_lens"], d["k_pool"], d["v_pool"],
+                              batch.page_size, batch.n_q_heads, batch.n_kv_heads,
+                              batch.head_dim, batch.window, batch.sm_scale, out=out, lse=lse,
+                              workspace=ws, dev_err=err)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if pcp.read_error(err) != 0:
+        raise RuntimeError(f"device error {pcp.read_error(err)} during warm-up")
+
+    # ---- timed region: L2 flushed before every step, events around each step
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for e in ev:  # materialise the events before handing them to the library
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            pcp.set_timing_events(ev[i][2], ev[i][3])
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        pcp.set_timing_events(None, None)
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
+    tc_ms = [c.elapsed_time(e) for _, _, c, e in ev]
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        torch.distributed.barrier()
+    code = pcp.read_error(err)
+    if code != 0:
+        raise RuntimeError(f"device error {code} in the timed region")
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    peaks, peak_kind = load_peaks()
+    tc_avg = float(np.mean(tc_ms))
+    achieved = flops / (tc_avg * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": UNIT, "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "kernel": "extend_tc_kernel<128>", "kernel_ms": tc_avg,
+                "peak_source": f"{peak_kind} bf16 dense (burst)"}
+
+    # ---- end to end through the C ABI with pinned host buffers
+    h_q = d["q"].cpu().pin_memory()
+    h_k = d["k_new"].cpu().pin_memory()
+    h_v = d["v_new"].cpu().pin_memory()
+    h_meta = [d[n].cpu().pin_memory() for n in ("qo_indptr", "kv_indptr", "kv_indices",
+                                                 "prefix_lens")]
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq = torch.empty_like(d["q"])
+    h2d = sum(t.numel() * t.element_size() for t in [h_q, h_k, h_v] + h_meta)
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        dq.copy_(h_q, non_blocking=True)
+        d["k_new"].copy_(h_k, non_blocking=True)
+        d["v_new"].copy_(h_v, non_blocking=True)
+        for n, h in zip(("qo_indptr", "kv_indptr", "kv_indices", "prefix_lens"), h_meta):
+            d[n].copy_(h, non_blocking=True)
+        step(dq)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_value = world * flops / (float(np.mean(e2e_ms)) * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": batch.name, "global_batch": batch.batch * world,
+                   "tokens_per_step": batch.total_q * world,
+                   "visible_pairs_per_head": visible_pairs(batch.prefix_lens, batch.chunk_lens,
+                                                           batch.window),
+                   "l2": "flushed (256 MB write) before every timed step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": float(np.mean(e2e_ms))},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+    if not args.no_secondary and rank == 0:
+        line["secondary"] = secondary(pcp, torch, W, dev, peaks, peak_kind, flush)
+    if rank == 0 and world == 1:
+        v, cores, sample = oracle_sample(batch, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
+    """Decode-row KV bandwidth (the 31 decode rows of the mixed batch as a
+    decode-only call) and KV-append bandwidth, L2 flushed before each call."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from helpers import to_device
+    res = {}
+    db = W.decode_rows()
+    d = to_device(db, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(db.total_q, db.n_q_heads, dtype=torch.float32, device=dev)
+    ws = torch.empty(pcp.workspace_size(db.batch, db.total_q, db.n_q_heads, db.n_kv_heads,
+                                        db.head_dim), dtype=torch.uint8, device=dev)
+
+    def dec():
+        pcp.paged_extend_attn(d["q"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                              d["prefix_lens"], d["k_pool"], d["v_pool"], db.page_size,
+                              db.n_q_heads, db.n_kv_heads, db.head_dim, 0, 0.0, out=out,
+                              lse=lse, workspace=ws, dev_err=err)
+    ms = time_calls(torch, dec, flush)
+    kv_bytes = int(db.kv_lens.sum()) * db.n_kv_heads * db.head_dim * 2 * 2
+    io_bytes = (d["q"].numel() * 2 + out.numel() * 2 + lse.numel() * 4 +
+                int(db.kv_indptr[-1]) * 4)
+    gbs = (kv_bytes + io_bytes) / (ms * 1e-3) / 1e9
+    res["decode_rows"] = {"workload": db.name, "ms": ms, "GB/s": gbs,
+                          "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": kv_bytes + io_bytes,
+                          "peak_source": f"{peak_kind} HBM copy"}
+    gb = W.gqa_prefill()
+    g = to_device(gb, dev)
+    loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
+                                    g["prefix_lens"], gb.page_size, gb.num_pages)
+
+    def app():
+        pcp.kv_append(g["k_new"], g["v_new"], loc, g["k_pool"], g["v_pool"], dev_err=err)
+    ms = time_calls(torch, app, flush)
+    nbytes = 2 * 2 * gb.total_q * gb.n_kv_heads * gb.head_dim * 2 + 8 * gb.total_q
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res["kv_append"] = {"workload": f"{gb.total_q} tokens x {gb.n_kv_heads} KV heads x D "
+                                    f"{gb.head_dim}", "ms": ms, "GB/s": gbs,
+                        "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes}
+    if pcp.read_error(err) != 0:
+        raise RuntimeError("device error in secondary measurements")
+    return res
+
+
+def time_calls(torch, fn, flush, n=20, warm=5):
+    stream = torch.cuda.current_stream()
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(n):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    return float(np.median(ms))
+
+
+if __name__ == "__main__":
+    main()
