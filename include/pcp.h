@@ -158,6 +158,42 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
                                  void* stream);
 
 /*
+ * Size of the fixed device scratch array behind
+ * pcp_paged_extend_attn_noalloc (16 MiB).  Every GPU that loads the library
+ * keeps this much memory reserved until the process exits.
+ */
+#define PCP_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * pcp_paged_extend_attn without a caller-supplied workspace.  The pages this
+ * library follows have no counterpart: it exists for callers that cannot
+ * allocate device memory -- code inside a host framework that owns every
+ * allocation, a plugin ABI with no allocation hook, or a hot path that must
+ * not call cudaMalloc -- and so cannot pass a workspace.  Arguments, layouts,
+ * results and errors are those of pcp_paged_extend_attn; the work lists,
+ * split-KV partials and counters go to a file-scope device array of
+ * PCP_NOALLOC_SCRATCH_BYTES instead.  A call whose
+ * pcp_extend_workspace_size(...) exceeds that returns PCP_ERR_WORKSPACE
+ * before launching anything.  Nothing is allocated: no cudaMalloc, no
+ * cudaFree, no allocating library call.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  All calls on a device share the one array and it keeps the last
+ * call's contents; each call re-initialises what must start at zero, but
+ * calls whose GPU work overlaps (different streams, or several host threads)
+ * race on the array and must be ordered by the caller.
+ */
+pcp_status pcp_paged_extend_attn_noalloc(const void* q, const int32_t* qo_indptr,
+                                         const int32_t* kv_indptr, const int32_t* kv_indices,
+                                         const int32_t* prefix_lens, int batch, int64_t total_q,
+                                         const void* k_pool, const void* v_pool,
+                                         int64_t num_pages, int page_size, int n_q_heads,
+                                         int n_kv_heads, int head_dim, int window,
+                                         float sm_scale, void* out, float* lse,
+                                         int32_t* dev_err, void* stream);
+
+/*
  * Synchronise `stream` and copy *dev_err to *host_err (host pointer).
  * Returns PCP_ERR_CUDA if the synchronisation or copy fails.
  */
