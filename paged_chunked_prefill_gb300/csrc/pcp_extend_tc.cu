@@ -252,9 +252,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float sl2 = p.scale_log2;
 
     uint32_t kv_iter = 0;          // KV tiles handled so far by this CTA
-    uint32_t act[2] = {0u, 0u};    // active (Q tile, KV tile) pairs so far, per Q tile
-    uint32_t n_done = 0;           // items finished (q_full phase)
-    int last_it[4] = {-1, -1, -1, -1};  // producer: last KV iteration per stage
+    uint32_t act0 = 0u, act1 = 0u;  // active (Q tile, KV tile) pairs so far, per Q tile
+    uint32_t n_done = 0;            // items finished (q_full phase)
+    int last_issued = -1;           // producer: last KV iteration it issued loads for
 
     for (;;) {
         if (threadIdx.x == 0) misc[1] = atomicAdd(&hdr->tc_next, 1);
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     break;
                 load_kv_tile<D>(p, geo, t, &tm_v, p.v_pool, sV + st * C::kTileBytes,
                                 bar(C::bVFull + st), true, lane);
-                last_it[st] = (int)cur;
+                last_issued = (int)cur;
             }
         } else if (warp == 1) {
             // ------------------------------------------------ MMA issuer
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 };
                 bool ok = mbar_wait(bar(C::bQFull), n_done & 1u, abort_flag, p.dev_err,
                                     kSpinLimitNs);
-                uint32_t aidx[2] = {act[0], act[1]};
+                uint32_t aidx0 = act0, aidx1 = act1;
                 if (ok) {
                     tc_fence_after();
                     const uint32_t c0 = kv_iter;
@@ -323,11 +323,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (ok) {
                         fence_proxy_async_smem();
                         tc_fence_after();
-                        for (int u = 0; u < 2; ++u)
-                            if (tile_active(geo, u, geo.t_begin)) {
-                                issue_qk(u, c0 % S);
-                                umma_commit(bar(C::bSFull + u));
-                            }
+                        if (tile_active(geo, 0, geo.t_begin)) {
+                            issue_qk(0, c0 % S);
+                            umma_commit(bar(C::bSFull + 0));
+                        }
+                        if (tile_active(geo, 1, geo.t_begin)) {
+                            issue_qk(1, c0 % S);
+                            umma_commit(bar(C::bSFull + 1));
+                        }
                         umma_commit(bar(C::bKEmpty + c0 % S));
                     }
                 }
@@ -345,25 +348,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const bool has_next = i + 1 < ntiles;
                     const int nst = (cur + 1) % S;
                     bool k_next = false;
-                    for (int u = 0; u < 2 && ok; ++u) {
+                    // PV of Q tile u for this KV tile, then its QK^T for the next one
+                    auto step_u = [&](const int u, uint32_t& ai, const int first_u) -> bool {
                         if (tile_active(geo, u, t)) {
-                            if (!mbar_wait(bar(C::bPFull + u), aidx[u] & 1u, abort_flag,
-                                           p.dev_err, kSpinLimitNs)) {
-                                ok = false;
-                                break;
-                            }
+                            if (!mbar_wait(bar(C::bPFull + u), ai & 1u, abort_flag, p.dev_err,
+                                           kSpinLimitNs))
+                                return false;
                             tc_fence_after();
-                            issue_pv(u, st, t != geo.first[u]);
+                            issue_pv(u, st, t != first_u);
                             umma_commit(bar(C::bODone + u));
-                            ++aidx[u];
+                            ++ai;
                         }
                         if (has_next && tile_active(geo, u, t + 1)) {
                             if (!k_next) {
                                 if (!mbar_wait(bar(C::bKFull + nst), ((cur + 1) / S) & 1u,
-                                               abort_flag, p.dev_err, kSpinLimitNs)) {
-                                    ok = false;
-                                    break;
-                                }
+                                               abort_flag, p.dev_err, kSpinLimitNs))
+                                    return false;
                                 fence_proxy_async_smem();
                                 tc_fence_after();
                                 k_next = true;
@@ -371,8 +371,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             issue_qk(u, nst);
                             umma_commit(bar(C::bSFull + u));
                         }
+                        return true;
+                    };
+                    if (!step_u(0, aidx0, geo.first[0]) || !step_u(1, aidx1, geo.first[1])) {
+                        ok = false;
+                        break;
                     }
-                    if (!ok) break;
                     umma_commit(bar(C::bVEmpty + st));
                     if (k_next) umma_commit(bar(C::bKEmpty + nst));
                 }
@@ -387,47 +391,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t tS = tmem + lane_off + (uint32_t)u * 128u;
             const uint32_t tO = tmem + lane_off + 256u + (uint32_t)u * 128u;
             if (u < geo.nq) {
+                const int first_u = u == 0 ? geo.first[0] : geo.first[1];
+                const int last_u = u == 0 ? geo.last[0] : geo.last[1];
+                const int pl_u = u == 0 ? geo.pl[0] : geo.pl[1];
+                const int ph_u = u == 0 ? geo.ph[0] : geo.ph[1];
+                const uint32_t act_u = u == 0 ? act0 : act1;
                 const int pos_local = u * p.qpos + r / G;
                 const bool row_valid = r < p.qpos * G && geo.pos0 + pos_local < geo.c;
                 const int pabs = geo.P + geo.pos0 + pos_local;
                 const int head = geo.g * G + r % G;
                 float m_run = -INFINITY, l_run = 0.f;
                 bool ok = true;
-                for (int t = geo.first[u]; t <= geo.last[u]; ++t) {
-                    const uint32_t a = act[u] + (uint32_t)(t - geo.first[u]);
+                for (int t = first_u; t <= last_u; ++t) {
+                    const uint32_t a = act_u + (uint32_t)(t - first_u);
                     if (!mbar_wait(bar(C::bSFull + u), a & 1u, abort_flag, p.dev_err,
                                    kSpinLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    uint32_t sr[4][32];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) tmem_ld32(tS + 32u * i, sr[i]);
-                    tmem_ld_wait();
                     const int key0 = t * kTileN;
                     const bool need_mask =
-                        (key0 + kTileN - 1 > geo.pl[u]) ||
-                        (p.window > 0 && key0 < geo.ph[u] - p.window + 1);
-                    float mx = -INFINITY;
-                    if (need_mask) {
+                        (key0 + kTileN - 1 > pl_u) ||
+                        (p.window > 0 && key0 < ph_u - p.window + 1);
+                    // keys of this tile a row does not see become -inf (edge tiles only)
+                    auto mask64 = [&](uint32_t (&v)[2][32], int col0) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
+                        for (int i = 0; i < 2; ++i)
 #pragma unroll
                             for (int j = 0; j < 32; ++j) {
-                                const int key = key0 + i * 32 + j;
+                                const int key = key0 + col0 + i * 32 + j;
                                 const bool vis =
                                     key <= pabs && (p.window <= 0 || key > pabs - p.window);
-                                float s = __uint_as_float(sr[i][j]);
-                                s = vis ? s : -INFINITY;
-                                sr[i][j] = __float_as_uint(s);
-                                mx = fmaxf(mx, s);
+                                if (!vis) v[i][j] = __float_as_uint(-INFINITY);
                             }
-                    } else {
+                    };
+                    // pass 1: row maximum, 64 columns at a time
+                    float mx = -INFINITY;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t v[2][32];
+                        tmem_ld32(tS + 64u * h, v[0]);
+                        tmem_ld32(tS + 64u * h + 32u, v[1]);
+                        tmem_ld_wait();
+                        if (need_mask) mask64(v, 64 * h);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(sr[i][j]));
+                        for (int i = 0; i < 2; ++i)
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[i][j]));
                     }
                     const float m_new = fmaxf(m_run, mx);
                     float alpha = 1.f;
@@ -440,20 +451,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         resc = true;
                     }
                     const float nref = m_run == -INFINITY ? 0.f : -m_run * sl2;
+                    // pass 2: P = exp2(s * scale * log2e - m), packed to bf16 and written
+                    // over the S columns already consumed (P column c holds keys 2c, 2c+1)
                     float sum = 0.f;
-                    uint32_t pk[2][32];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t v[2][32];
+                        tmem_ld32(tS + 64u * h, v[0]);
+                        tmem_ld32(tS + 64u * h + 32u, v[1]);
+                        tmem_ld_wait();
+                        if (need_mask) mask64(v, 64 * h);
+                        uint32_t pk[32];
 #pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
-                            const float e0 = fast_exp2(fmaf(__uint_as_float(sr[i][j]), sl2, nref));
-                            const float e1 =
-                                fast_exp2(fmaf(__uint_as_float(sr[i][j + 1]), sl2, nref));
-                            sum += e0 + e1;
-                            pk[i >> 1][(i & 1) * 16 + (j >> 1)] = pack_bf16x2(e0, e1);
-                        }
+                        for (int i = 0; i < 2; ++i)
+#pragma unroll
+                            for (int j = 0; j < 32; j += 2) {
+                                const float e0 = fast_exp2(fmaf(__uint_as_float(v[i][j]), sl2, nref));
+                                const float e1 =
+                                    fast_exp2(fmaf(__uint_as_float(v[i][j + 1]), sl2, nref));
+                                sum += e0 + e1;
+                                pk[i * 16 + (j >> 1)] = pack_bf16x2(e0, e1);
+                            }
+                        tmem_st32(tS + 32u * h, pk);
+                    }
                     l_run = l_run * alpha + sum;
-                    if (t > geo.first[u]) {
+                    if (t > first_u) {
                         if (!mbar_wait(bar(C::bODone + u), (a - 1u) & 1u, abort_flag, p.dev_err,
                                        kSpinLimitNs)) {
                             ok = false;
@@ -473,14 +495,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             }
                         }
                     }
-                    tmem_st32(tS, pk[0]);
-                    tmem_st32(tS + 32u, pk[1]);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(bar(C::bPFull + u));
                 }
                 if (ok) {
-                    const uint32_t a_last = act[u] + (uint32_t)(geo.last[u] - geo.first[u]);
+                    const uint32_t a_last = act_u + (uint32_t)(last_u - first_u);
                     ok = mbar_wait(bar(C::bODone + u), a_last & 1u, abort_flag, p.dev_err,
                                    kSpinLimitNs);
                 }
@@ -514,7 +534,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
         kv_iter += (uint32_t)ntiles;
-        for (int u = 0; u < geo.nq; ++u) act[u] += (uint32_t)(geo.last[u] - geo.first[u] + 1);
+        act0 += (uint32_t)(geo.last[0] - geo.first[0] + 1);
+        if (geo.nq == 2) act1 += (uint32_t)(geo.last[1] - geo.first[1] + 1);
         ++n_done;
         tc_fence_before();
         __syncthreads();
@@ -528,11 +549,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (aborted && lane == 0) {
             // let every TMA load this CTA issued land before the CTA exits
             volatile int dummy = 0;
-            for (int s = 0; s < S; ++s)
-                if (last_it[s] >= 0) {
-                    const uint32_t ph = ((uint32_t)last_it[s] / S) & 1u;
-                    mbar_wait(bar(C::bKFull + s), ph, &dummy, p.dev_err, kSpinLimitNs);
-                    mbar_wait(bar(C::bVFull + s), ph, &dummy, p.dev_err, kSpinLimitNs);
+            for (int it = last_issued - S + 1; it <= last_issued; ++it)
+                if (it >= 0) {
+                    const uint32_t ph = ((uint32_t)it / S) & 1u;
+                    mbar_wait(bar(C::bKFull + it % S), ph, &dummy, p.dev_err, kSpinLimitNs);
+                    mbar_wait(bar(C::bVFull + it % S), ph, &dummy, p.dev_err, kSpinLimitNs);
                 }
         }
     } else if (warp == 1 && lane == 0) {
