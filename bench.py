@@ -196,6 +196,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--workload", default="gqa_prefill",
+                    help="workloads.CONFIGS name (the headline line uses gqa_prefill)")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -212,7 +215,7 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     args.warmup = max(args.warmup, 3)
 
-    batch = W.gqa_prefill()
+    batch = W.config_by_name(args.workload)
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from helpers import to_device
     d = to_device(batch, dev)
@@ -284,10 +287,46 @@ def main():
     achieved = flops / (tc_avg * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": UNIT, "frac": achieved / peaks["bf16_tflops"], "traffic": None,
-                "kernel": "extend_tc_kernel<128>", "kernel_ms": tc_avg,
+                "kernel": f"extend_tc_kernel<{batch.head_dim}>", "kernel_ms": tc_avg,
                 "peak_source": f"{peak_kind} bf16 dense (burst)"}
 
     # ---- end to end through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(args, torch, d, out, lse, step, flush, stream, flops, world)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": batch.name, "global_batch": batch.batch * world,
+                   "tokens_per_step": batch.total_q * world,
+                   "visible_pairs_per_head": visible_pairs(batch.prefix_lens, batch.chunk_lens,
+                                                           batch.window),
+                   "l2": "flushed (256 MB write) before every timed step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+    if not args.no_secondary and rank == 0:
+        line["secondary"] = secondary(pcp, torch, W, dev, peaks, peak_kind, flush)
+    if rank == 0 and world == 1:
+        v, cores, sample = oracle_sample(batch, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def end_to_end(args, torch, d, out, lse, step, flush, stream, flops, world):
+    """The same step through the public API with pinned host buffers: H2D of
+    the step's inputs (q, the chunk's K/V, the page-table metadata) and D2H of
+    out and lse inside the timed region."""
     h_q = d["q"].cpu().pin_memory()
     h_k = d["k_new"].cpu().pin_memory()
     h_v = d["v_new"].cpu().pin_memory()
@@ -323,33 +362,8 @@ def main():
         e2e_ms.append(a.elapsed_time(b))
     e2e_value = world * flops / (float(np.mean(e2e_ms)) * 1e-3) / 1e12
 
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": batch.name, "global_batch": batch.batch * world,
-                   "tokens_per_step": batch.total_q * world,
-                   "visible_pairs_per_head": visible_pairs(batch.prefix_lens, batch.chunk_lens,
-                                                           batch.window),
-                   "l2": "flushed (256 MB write) before every timed step",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roofline,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": float(np.mean(e2e_ms))},
-        "gpu_launches": 5 * args.steps,
-        "clocks": clocks.summary(),
-    }
-
-    if not args.no_secondary and rank == 0:
-        line["secondary"] = secondary(pcp, torch, W, dev, peaks, peak_kind, flush)
-    if rank == 0 and world == 1:
-        v, cores, sample = oracle_sample(batch, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": sample}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": float(np.mean(e2e_ms))}
 
 
 def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):

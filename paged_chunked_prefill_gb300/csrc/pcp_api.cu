@@ -10,6 +10,10 @@
 #include "pcp.h"
 #include "pcp_internal.h"
 
+#ifndef PCP_TMA_MIN_ROWS
+#define PCP_TMA_MIN_ROWS 8
+#endif
+
 namespace pcp {
 
 cudaError_t launch_plan(cudaStream_t stream, const PlanParams& p);
@@ -207,8 +211,11 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     const int qpos = q_positions_per_tile(group);
     const int num_slots = (int)(num_pages * page_size);
+    // TMA boxes for page runs of >= PCP_TMA_MIN_ROWS keys; smaller pages go to
+    // the cp.async gather warps (below 8 rows the TMA unit's per-box cost
+    // dominates; above, TMA out-runs two gather warps)
     const int g128 = gcd_int(page_size, kTileN);
-    const int box_rows = g128 >= 8 ? g128 : 0;
+    const int box_rows = g128 >= PCP_TMA_MIN_ROWS ? g128 : 0;
 
     // ---- tensor maps: Q boxes of (64 dims, G heads, qpos positions); K/V
     // boxes of (64 dims, one KV head, one page run)

@@ -11,18 +11,21 @@
 //    one 128-row Q tile are (position, head) pairs of the G = Hq/Hkv query
 //    heads of KV head g, so every K/V tile fetched from HBM feeds 2 x G query
 //    heads (GQA head-group sharing) and 4 tcgen05 MMAs.
-//  * Warp roles (320 threads, persistent CTA per SM, dynamic item counter):
-//      warp 0      producer: Q by TMA; K/V pages gathered through the page
-//                  table into 128-byte-swizzled smem stages (one TMA box per
-//                  page run; cp.async for page sizes below 8 rows and for the
-//                  V rows past the sequence end, which are zero-filled);
-//      warp 1      one thread issues tcgen05.mma: S_u = Q_u K^T into TMEM,
-//                  then O_u += P_u V with P_u read from TMEM;
-//      warps 2-5   softmax for Q tile 0, warps 6-9 for Q tile 1: one thread
+//  * Warp roles (384 threads, persistent CTA per SM, dynamic item counter):
+//      warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1: one thread
 //                  per row, tcgen05.ld of S, mask only on diagonal / window
 //                  edge tiles, online softmax in fp32 with exp2 and a lazy O
 //                  rescale (only when the running max grows by > 2^8), P
-//                  written back to TMEM as bf16, epilogue O / l -> bf16, lse.
+//                  written back to TMEM as bf16, epilogue O / l -> bf16, lse;
+//      warp 8      TMA: Q, and K/V when pages hold runs of >= 8 keys (one box
+//                  per page run and 64-column block);
+//      warp 9      one thread issues tcgen05.mma: S_u = Q_u K^T into TMEM,
+//                  then O_u += P_u V with P_u read from TMEM;
+//      warps 10-11 page gathers of K/V for pages below 8 keys: 16 lanes cover
+//                  one 256-byte row with 16-byte cp.async (fully coalesced),
+//                  rows past the sequence end zero-filled.  (The TMA unit takes
+//                  about one box per ~100 cycles, so one-key boxes are hopeless.)
+//    K and V land in 128-byte-swizzled shared-memory stages either way.
 //  * Ping-pong: while one softmax group works on its S tile, the tensor core
 //    runs the other group's QK^T or PV.
 //  * Every wait is bounded; a wait that runs out records PCP_ERR_TIMEOUT,
@@ -30,14 +33,25 @@
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
 
+// Of every 16 consecutive pairs of S columns, this many are exponentiated on
+// the FMA pipe (exp2_poly) and the rest on the MUFU unit, balancing the two.
+#ifndef PCP_EXP2_EMU_PAIRS
+#define PCP_EXP2_EMU_PAIRS 0
+#endif
+
 namespace pcp {
 
 namespace {
 
+constexpr int kExp2EmuPairs = PCP_EXP2_EMU_PAIRS;
+
 template <int D>
 struct TcCfg {
     static constexpr int kHalves = D / 64;                   // 128-byte column blocks
-    static constexpr int kStages = D == 128 ? 2 : 4;
+    // K gets one more stage than V when shared memory allows: K(t+1) is
+    // needed half a tile before V(t+1)
+    static constexpr int kStagesK = D == 128 ? 3 : 4;
+    static constexpr int kStagesV = D == 128 ? 2 : 4;
     static constexpr uint32_t kHalfBytes = kTileN * 128;     // one column block of a tile
     static constexpr uint32_t kTileBytes = kTileN * D * 2;   // a K or V tile
     static constexpr uint32_t kQBytes = kTileM * D * 2;      // a Q tile
@@ -46,21 +60,21 @@ struct TcCfg {
     // the largest descriptor strides, and this keeps every read of it inside
     // the CTA's shared memory.
     static constexpr uint32_t kOffV = kOffQ + kQTiles * kQBytes;
-    static constexpr uint32_t kOffK = kOffV + kStages * kTileBytes;
-    static constexpr uint32_t kOffBar = kOffK + kStages * kTileBytes;
-    static constexpr int kNumBars = 1 + 4 * kStages + 6 + 1;
+    static constexpr uint32_t kOffK = kOffV + kStagesV * kTileBytes;
+    static constexpr uint32_t kOffBar = kOffK + kStagesK * kTileBytes;
+    static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 6 + 1;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;
     // barrier indices
     static constexpr int bQFull = 0;
     static constexpr int bKFull = 1;
-    static constexpr int bKEmpty = 1 + kStages;
-    static constexpr int bVFull = 1 + 2 * kStages;
-    static constexpr int bVEmpty = 1 + 3 * kStages;
-    static constexpr int bSFull = 1 + 4 * kStages;
-    static constexpr int bPFull = 3 + 4 * kStages;
-    static constexpr int bODone = 5 + 4 * kStages;
-    static constexpr int bDrain = 7 + 4 * kStages;
+    static constexpr int bKEmpty = 1 + kStagesK;
+    static constexpr int bVFull = 1 + 2 * kStagesK;
+    static constexpr int bVEmpty = 1 + 2 * kStagesK + kStagesV;
+    static constexpr int bSFull = 1 + 2 * kStagesK + 2 * kStagesV;
+    static constexpr int bPFull = bSFull + 2;
+    static constexpr int bODone = bSFull + 4;
+    static constexpr int bDrain = bSFull + 6;
 };
 
 struct Geo {
@@ -105,89 +119,99 @@ __device__ __forceinline__ bool tile_active(const Geo& g, int u, int t) {
     return g.first[u] <= t && t <= g.last[u];
 }
 
-// Load one K or V tile (keys [t*128, t*128+128) of sequence b, KV head g)
-// into a 128-byte-swizzled stage: column block h at h * 16 KB, row r at
-// r * 128 bytes, 16-byte chunk c of a row at position c ^ (r % 8).
+// First slot of the page run one TMA lane loads for a KV tile (num_slots
+// when the run is past the sequence end or its page id is bad: the TMA then
+// writes zeros).  Read one tile ahead of the load that uses it.
 template <int D>
-__device__ __forceinline__ void load_kv_tile(const TcParams& p, const Geo& geo, int t,
-                                             const CUtensorMap* map, const uint16_t* pool,
-                                             uint32_t dst, uint32_t bar, bool zero_tail,
-                                             int lane) {
+__device__ __forceinline__ int fetch_box_slot(const TcParams& p, const Geo& geo,
+                                              const int32_t* pages, int t, int lane) {
+    using C = TcCfg<D>;
+    const int nsub = kTileN / p.box_rows;
+    const int key = t * kTileN + (lane % nsub) * p.box_rows;
+    int z = p.num_slots;
+    if (lane < nsub * C::kHalves && key < geo.L) {
+        const int page = pages[key / p.page_size];
+        if (page >= 0 && page < p.num_pages)
+            z = page * p.page_size + key % p.page_size;
+        else
+            report_error(p.dev_err, PCP_ERR_BAD_INDEX);
+    }
+    return z;
+}
+
+// Load one K or V tile (keys [t*128, t*128+128) of sequence b, KV head g)
+// by TMA into a 128-byte-swizzled stage: column block h at h * 16 KB, row r at
+// r * 128 bytes, 16-byte chunk c of a row at position c ^ (r % 8).  For V, the
+// page run holding the sequence end is copied with cp.async and zero-filled
+// past the end, so stale pool contents (possibly NaN) never meet P = 0.
+template <int D>
+__device__ __forceinline__ void tma_kv_tile(const TcParams& p, const Geo& geo, int t, int z,
+                                            const CUtensorMap* map, const uint16_t* pool,
+                                            uint32_t dst, uint32_t bar, bool zero_tail,
+                                            int lane) {
     using C = TcCfg<D>;
     const int key0 = t * kTileN;
-    const int32_t* pages = p.kv_indices + p.kv_indptr[geo.b];
-    const int ps = p.page_size;
-    if (p.box_rows > 0) {
-        const int br = p.box_rows;
-        const int nsub = kTileN / br;
-        const int nloads = nsub * C::kHalves;
-        int strad = -1;
-        if (zero_tail && geo.L > key0 && geo.L < key0 + kTileN && (geo.L - key0) % br != 0)
-            strad = (geo.L - key0) / br;
-        if (strad >= 0) {
-            // rows of this page run past the sequence end are zero-filled
-            const int ks = key0 + strad * br;
-            const int page = pages[ks / ps];
-            const bool bad = page < 0 || page >= p.num_pages;
-            if (bad && lane == 0) report_error(p.dev_err, PCP_ERR_BAD_INDEX);
-            const int64_t slot0 = (int64_t)page * ps + ks % ps;
-            for (int idx = lane; idx < br * C::kHalves * 8; idx += 32) {
-                const int row = idx / (C::kHalves * 8);
-                const int c = idx % (C::kHalves * 8);
-                const int rt = strad * br + row;
-                const bool ok = !bad && ks + row < geo.L;
-                const uint16_t* src =
-                    ok ? pool + ((slot0 + row) * p.n_kv_heads + geo.g) * D + c * 8 : pool;
-                cp_async_16(dst + (c >> 3) * C::kHalfBytes + rt * 128 + (((c & 7) ^ (rt & 7)) << 4),
-                            src, ok ? 16u : 0u);
-            }
-            cp_async_mbar_arrive(bar);
-        }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive_expect_tx(bar,
-                                  (uint32_t)(nloads - (strad >= 0 ? C::kHalves : 0)) * br * 128);
-        __syncwarp();
-        if (lane < nloads) {
-            const int sb = lane % nsub;
-            const int h = lane / nsub;
-            if (sb != strad) {
-                const int key = key0 + sb * br;
-                int z = p.num_slots;  // fully out of range: TMA writes zeros
-                if (key < geo.L) {
-                    const int page = pages[key / ps];
-                    if (page >= 0 && page < p.num_pages)
-                        z = page * ps + key % ps;
-                    else
-                        report_error(p.dev_err, PCP_ERR_BAD_INDEX);
-                }
-                tma_load_3d(dst + h * C::kHalfBytes + sb * br * 128, map, bar, h * 64, geo.g, z);
-            }
-        }
-    } else {
-        // small pages: one 16-byte cp.async per row chunk, zero-filled past the end
-        for (int row = lane; row < kTileN; row += 32) {
-            const int key = key0 + row;
-            bool ok = key < geo.L;
-            int64_t slot = 0;
-            if (ok) {
-                const int page = pages[key / ps];
-                if (page >= 0 && page < p.num_pages) {
-                    slot = (int64_t)page * ps + key % ps;
-                } else {
-                    report_error(p.dev_err, PCP_ERR_BAD_INDEX);
-                    ok = false;
-                }
-            }
-            const uint16_t* src = ok ? pool + (slot * p.n_kv_heads + geo.g) * D : pool;
-#pragma unroll
-            for (int c = 0; c < C::kHalves * 8; ++c)
-                cp_async_16(dst + (c >> 3) * C::kHalfBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4),
-                            ok ? src + c * 8 : pool, ok ? 16u : 0u);
+    const int br = p.box_rows;
+    const int nsub = kTileN / br;
+    const int nloads = nsub * C::kHalves;
+    int strad = -1;
+    if (zero_tail && geo.L > key0 && geo.L < key0 + kTileN && (geo.L - key0) % br != 0)
+        strad = (geo.L - key0) / br;
+    if (strad >= 0) {
+        const int ks = key0 + strad * br;
+        const int slot0 = __shfl_sync(0xffffffffu, z, strad);
+        const bool bad = slot0 >= p.num_slots;
+        for (int idx = lane; idx < br * C::kHalves * 8; idx += 32) {
+            const int row = idx / (C::kHalves * 8);
+            const int c = idx % (C::kHalves * 8);
+            const int rt = strad * br + row;
+            const bool ok = !bad && ks + row < geo.L;
+            const uint16_t* src =
+                ok ? pool + ((int64_t)(slot0 + row) * p.n_kv_heads + geo.g) * D + c * 8 : pool;
+            cp_async_16(dst + (c >> 3) * C::kHalfBytes + rt * 128 + (((c & 7) ^ (rt & 7)) << 4),
+                        src, ok ? 16u : 0u);
         }
         cp_async_mbar_arrive(bar);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar);
+    }
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive_expect_tx(bar, (uint32_t)(nloads - (strad >= 0 ? C::kHalves : 0)) * br * 128);
+    __syncwarp();
+    if (lane < nloads) {
+        const int sb = lane % nsub;
+        const int h = lane / nsub;
+        if (sb != strad)
+            tma_load_3d(dst + h * C::kHalfBytes + sb * br * 128, map, bar, h * 64, geo.g, z);
+    }
+}
+
+// One gather warp's share (rows gw*64 .. gw*64+63) of a K or V tile: lanes
+// split into groups covering one 256-byte (128-byte for D = 64) row each.
+template <int D>
+struct GatherShape {
+    static constexpr int kChunks = D / 8;                     // 16-byte chunks per row
+    static constexpr int kRowsPerInst = 32 / kChunks;         // rows per warp instruction
+    static constexpr int kRows = kTileN / kGatherWarps;       // rows per warp per tile
+    static constexpr int kInsts = kRows / kRowsPerInst;       // instructions per tile
+};
+
+template <int D>
+__device__ __forceinline__ void gather_kv_rows(const TcParams& p, const Geo& geo,
+                                               const int (&slot)[GatherShape<D>::kInsts],
+                                               const uint16_t* pool, uint32_t dst, int gw,
+                                               int lane) {
+    using C = TcCfg<D>;
+    using GS = GatherShape<D>;
+    const int c = lane % GS::kChunks;
+    const int rsub = lane / GS::kChunks;
+#pragma unroll
+    for (int j = 0; j < GS::kInsts; ++j) {
+        const int row = gw * GS::kRows + j * GS::kRowsPerInst + rsub;
+        const bool ok = slot[j] >= 0;
+        const uint16_t* src =
+            ok ? pool + ((int64_t)slot[j] * p.n_kv_heads + geo.g) * D + c * 8 : pool;
+        cp_async_16(dst + (c >> 3) * C::kHalfBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4),
+                    src, ok ? 16u : 0u);
     }
 }
 
@@ -199,7 +223,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v) {
     using C = TcCfg<D>;
-    constexpr int S = C::kStages;
+    constexpr int SK = C::kStagesK;
+    constexpr int SV = C::kStagesV;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -217,10 +242,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::bQFull), 1);
-        for (int s = 0; s < S; ++s) {
-            mbar_init(bar(C::bKFull + s), 1);
+        // TMA path: one arrive.expect_tx; gather path: one arrival per gather lane
+        const uint32_t full_count = p.box_rows > 0 ? 1u : 32u * kGatherWarps;
+        for (int s = 0; s < SK; ++s) {
+            mbar_init(bar(C::bKFull + s), full_count);
             mbar_init(bar(C::bKEmpty + s), 1);
-            mbar_init(bar(C::bVFull + s), 1);
+        }
+        for (int s = 0; s < SV; ++s) {
+            mbar_init(bar(C::bVFull + s), full_count);
             mbar_init(bar(C::bVEmpty + s), 1);
         }
         for (int u = 0; u < 2; ++u) {
@@ -235,7 +264,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
     }
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_addr((const void*)&misc[0]), 512);
         tmem_relinquish();
     }
@@ -254,7 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t kv_iter = 0;          // KV tiles handled so far by this CTA
     uint32_t act0 = 0u, act1 = 0u;  // active (Q tile, KV tile) pairs so far, per Q tile
     uint32_t n_done = 0;            // items finished (q_full phase)
-    int last_issued = -1;           // producer: last KV iteration it issued loads for
+    int last_issued = -1;           // TMA warp: last KV iteration it issued loads for
 
     for (;;) {
         if (threadIdx.x == 0) misc[1] = atomicAdd(&hdr->tc_next, 1);
@@ -264,8 +293,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const Geo geo = make_geo(p, items[item]);
         const int ntiles = geo.t_end - geo.t_begin + 1;
 
-        if (warp == 0) {
-            // ------------------------------------------------ producer
+        if (warp == kWarpTma) {
+            // ------------------------------------------------ TMA: Q (+ K/V)
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(C::bQFull),
                                       (uint32_t)(geo.nq * C::kHalves * G * p.qpos * 128));
@@ -274,42 +303,96 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tma_load_3d(sQ + u * C::kQBytes + h * (kTileM * 128), &tm_q,
                                     bar(C::bQFull), h * 64, geo.g * G, geo.q_row0 + u * p.qpos);
             }
-            for (int i = 0; i < ntiles; ++i) {
-                const int t = geo.t_begin + i;
-                const uint32_t cur = kv_iter + i;
-                const int st = cur % S;
-                const uint32_t ph = (cur / S) & 1u;
-                if (!mbar_wait(bar(C::bKEmpty + st), ph ^ 1u, abort_flag, p.dev_err, kSpinLimitNs))
-                    break;
-                load_kv_tile<D>(p, geo, t, &tm_k, p.k_pool, sK + st * C::kTileBytes,
-                                bar(C::bKFull + st), false, lane);
-                if (!mbar_wait(bar(C::bVEmpty + st), ph ^ 1u, abort_flag, p.dev_err, kSpinLimitNs))
-                    break;
-                load_kv_tile<D>(p, geo, t, &tm_v, p.v_pool, sV + st * C::kTileBytes,
-                                bar(C::bVFull + st), true, lane);
-                last_issued = (int)cur;
+            if (p.box_rows > 0) {
+                const int32_t* pages = p.kv_indices + p.kv_indptr[geo.b];
+                int z_cur = fetch_box_slot<D>(p, geo, pages, geo.t_begin, lane);
+                for (int i = 0; i < ntiles; ++i) {
+                    const int t = geo.t_begin + i;
+                    const uint32_t cur = kv_iter + i;
+                    const int sk = cur % SK, sv = cur % SV;
+                    // the next tile's page ids are in flight while this one waits
+                    const int z_next =
+                        i + 1 < ntiles ? fetch_box_slot<D>(p, geo, pages, t + 1, lane) : z_cur;
+                    if (!mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u, abort_flag,
+                                   p.dev_err, kSpinLimitNs))
+                        break;
+                    tma_kv_tile<D>(p, geo, t, z_cur, &tm_k, p.k_pool, sK + sk * C::kTileBytes,
+                                   bar(C::bKFull + sk), false, lane);
+                    if (!mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u, abort_flag,
+                                   p.dev_err, kSpinLimitNs))
+                        break;
+                    tma_kv_tile<D>(p, geo, t, z_cur, &tm_v, p.v_pool, sV + sv * C::kTileBytes,
+                                   bar(C::bVFull + sv), true, lane);
+                    last_issued = (int)cur;
+                    z_cur = z_next;
+                }
             }
-        } else if (warp == 1) {
+        } else if (warp >= kWarpGather0) {
+            // ------------------------------------------------ cp.async page gathers
+            if (p.box_rows == 0) {
+                using GS = GatherShape<D>;
+                const int gw = warp - kWarpGather0;
+                const int32_t* pages = p.kv_indices + p.kv_indptr[geo.b];
+                const int rsub = lane / GS::kChunks;
+                for (int i = 0; i < ntiles; ++i) {
+                    const int t = geo.t_begin + i;
+                    const uint32_t cur = kv_iter + i;
+                    const int sk = cur % SK, sv = cur % SV;
+                    // slots of this lane's rows (shared by K and V), read before
+                    // the wait so the page table's latency overlaps it
+                    int slot[GS::kInsts];
+#pragma unroll
+                    for (int j = 0; j < GS::kInsts; ++j) {
+                        const int key = t * kTileN + gw * GS::kRows + j * GS::kRowsPerInst + rsub;
+                        slot[j] = -1;
+                        if (key < geo.L) {
+                            const int page = pages[key / p.page_size];
+                            if (page >= 0 && page < p.num_pages)
+                                slot[j] = page * p.page_size + key % p.page_size;
+                            else
+                                report_error(p.dev_err, PCP_ERR_BAD_INDEX);
+                        }
+                    }
+                    if (!mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u, abort_flag,
+                                   p.dev_err, kSpinLimitNs))
+                        break;
+                    gather_kv_rows<D>(p, geo, slot, p.k_pool, sK + sk * C::kTileBytes, gw, lane);
+                    cp_async_mbar_arrive_noinc(bar(C::bKFull + sk));
+                    if (!mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u, abort_flag,
+                                   p.dev_err, kSpinLimitNs))
+                        break;
+                    gather_kv_rows<D>(p, geo, slot, p.v_pool, sV + sv * C::kTileBytes, gw, lane);
+                    cp_async_mbar_arrive_noinc(bar(C::bVFull + sv));
+                }
+            }
+        } else if (warp == kWarpMma) {
             // ------------------------------------------------ MMA issuer
             if (lane == 0) {
                 constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false);
                 constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, true);
+                // Descriptors are built once; a k-step, Q tile or stage only moves the
+                // start address, which sits in the low 14 bits in 16-byte units.
+                const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
+                const uint64_t dk = sdesc_sw128(sK, 16, 1024);
+                const uint64_t dv = sdesc_sw128(sV, C::kHalfBytes, 1024);
                 auto issue_qk = [&](int u, int st) {
-                    const uint32_t qa = sQ + u * C::kQBytes;
-                    const uint32_t ka = sK + st * C::kTileBytes;
+                    const uint64_t a0 = dq + ((uint32_t)u * C::kQBytes >> 4);
+                    const uint64_t b0 = dk + ((uint32_t)st * C::kTileBytes >> 4);
+                    const uint32_t d = tmem + (uint32_t)u * 128u;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * (kTileM * 128) + (kk & 3) * 32;
-                        umma_ss(tmem + u * 128, sdesc_sw128(qa + off, 16, 1024),
-                                sdesc_sw128(ka + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                        constexpr uint32_t kHalf16 = (kTileM * 128) >> 4;
+                        const uint32_t off = (uint32_t)(kk >> 2) * kHalf16 + (uint32_t)(kk & 3) * 2u;
+                        umma_ss(d, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                 };
                 auto issue_pv = [&](int u, int st, bool acc) {
-                    const uint32_t va = sV + st * C::kTileBytes;
+                    const uint64_t b0 = dv + ((uint32_t)st * C::kTileBytes >> 4);
+                    const uint32_t d = tmem + 256u + (uint32_t)u * 128u;
+                    const uint32_t a = tmem + (uint32_t)u * 128u;
 #pragma unroll
                     for (int kk = 0; kk < kTileN / 16; ++kk)
-                        umma_ts(tmem + 256 + u * 128, tmem + u * 128 + kk * 8,
-                                sdesc_sw128(va + kk * 2048, C::kHalfBytes, 1024), idesc_pv,
+                        umma_ts(d, a + kk * 8, b0 + (uint32_t)kk * (2048u >> 4), idesc_pv,
                                 (acc || kk > 0) ? 1u : 0u);
                 };
                 bool ok = mbar_wait(bar(C::bQFull), n_done & 1u, abort_flag, p.dev_err,
@@ -318,35 +401,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (ok) {
                     tc_fence_after();
                     const uint32_t c0 = kv_iter;
-                    ok = mbar_wait(bar(C::bKFull + c0 % S), (c0 / S) & 1u, abort_flag,
+                    ok = mbar_wait(bar(C::bKFull + c0 % SK), (c0 / SK) & 1u, abort_flag,
                                    p.dev_err, kSpinLimitNs);
                     if (ok) {
-                        fence_proxy_async_smem();
-                        tc_fence_after();
+                        if (p.box_rows == 0) fence_proxy_async_smem();
                         if (tile_active(geo, 0, geo.t_begin)) {
-                            issue_qk(0, c0 % S);
+                            issue_qk(0, c0 % SK);
                             umma_commit(bar(C::bSFull + 0));
                         }
                         if (tile_active(geo, 1, geo.t_begin)) {
-                            issue_qk(1, c0 % S);
+                            issue_qk(1, c0 % SK);
                             umma_commit(bar(C::bSFull + 1));
                         }
-                        umma_commit(bar(C::bKEmpty + c0 % S));
+                        umma_commit(bar(C::bKEmpty + c0 % SK));
                     }
                 }
                 for (int i = 0; ok && i < ntiles; ++i) {
                     const int t = geo.t_begin + i;
                     const uint32_t cur = kv_iter + i;
-                    const int st = cur % S;
-                    if (!mbar_wait(bar(C::bVFull + st), (cur / S) & 1u, abort_flag, p.dev_err,
+                    const int st = cur % SV;
+                    if (!mbar_wait(bar(C::bVFull + st), (cur / SV) & 1u, abort_flag, p.dev_err,
                                    kSpinLimitNs)) {
                         ok = false;
                         break;
                     }
-                    fence_proxy_async_smem();
-                    tc_fence_after();
+                    // cp.async wrote part of this V tile: small pages, or the page
+                    // run that holds the sequence end (zero-filled past it)
+                    if (p.box_rows == 0 ||
+                        (geo.L > t * kTileN && geo.L < t * kTileN + kTileN &&
+                         (geo.L - t * kTileN) % p.box_rows != 0))
+                        fence_proxy_async_smem();
                     const bool has_next = i + 1 < ntiles;
-                    const int nst = (cur + 1) % S;
+                    const int nst = (cur + 1) % SK;
                     bool k_next = false;
                     // PV of Q tile u for this KV tile, then its QK^T for the next one
                     auto step_u = [&](const int u, uint32_t& ai, const int first_u) -> bool {
@@ -361,11 +447,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         if (has_next && tile_active(geo, u, t + 1)) {
                             if (!k_next) {
-                                if (!mbar_wait(bar(C::bKFull + nst), ((cur + 1) / S) & 1u,
+                                if (!mbar_wait(bar(C::bKFull + nst), ((cur + 1) / SK) & 1u,
                                                abort_flag, p.dev_err, kSpinLimitNs))
                                     return false;
-                                fence_proxy_async_smem();
-                                tc_fence_after();
+                                if (p.box_rows == 0) fence_proxy_async_smem();
                                 k_next = true;
                             }
                             issue_qk(u, nst);
@@ -384,7 +469,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
         } else {
             // ------------------------------------------------ softmax + epilogue
-            const int u = (warp - 2) >> 2;
+            const int u = warp >> 2;
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -414,32 +499,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const bool need_mask =
                         (key0 + kTileN - 1 > pl_u) ||
                         (p.window > 0 && key0 < ph_u - p.window + 1);
-                    // keys of this tile a row does not see become -inf (edge tiles only)
-                    auto mask64 = [&](uint32_t (&v)[2][32], int col0) {
+                    // the whole S row of this thread: one TMEM load
+                    uint32_t v[128];
+                    tmem_ld128(tS, v);
+                    tmem_ld_wait();
+                    if (need_mask) {
+                        // keys this row does not see become -inf (edge tiles only)
 #pragma unroll
-                        for (int i = 0; i < 2; ++i)
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const int key = key0 + col0 + i * 32 + j;
-                                const bool vis =
-                                    key <= pabs && (p.window <= 0 || key > pabs - p.window);
-                                if (!vis) v[i][j] = __float_as_uint(-INFINITY);
-                            }
-                    };
-                    // pass 1: row maximum, 64 columns at a time
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t v[2][32];
-                        tmem_ld32(tS + 64u * h, v[0]);
-                        tmem_ld32(tS + 64u * h + 32u, v[1]);
-                        tmem_ld_wait();
-                        if (need_mask) mask64(v, 64 * h);
-#pragma unroll
-                        for (int i = 0; i < 2; ++i)
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[i][j]));
+                        for (int j = 0; j < 128; ++j) {
+                            const int key = key0 + j;
+                            const bool vis =
+                                key <= pabs && (p.window <= 0 || key > pabs - p.window);
+                            if (!vis) v[j] = __float_as_uint(-INFINITY);
+                        }
                     }
+                    // row maximum: eight independent chains of 3-input max
+                    float mx8[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 128; j += 2)
+                        mx8[(j >> 1) & 7] = max3f(mx8[(j >> 1) & 7], __uint_as_float(v[j]),
+                                                  __uint_as_float(v[j + 1]));
+                    const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]),
+                                           max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
                     const float m_new = fmaxf(m_run, mx);
                     float alpha = 1.f;
                     bool resc = false;
@@ -451,33 +534,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         resc = true;
                     }
                     const float nref = m_run == -INFINITY ? 0.f : -m_run * sl2;
-                    // pass 2: P = exp2(s * scale * log2e - m), packed to bf16 and written
-                    // over the S columns already consumed (P column c holds keys 2c, 2c+1)
-                    float sum = 0.f;
+                    // P = exp2(s * scale * log2e - m): packed scale-and-subtract, MUFU
+                    // ex2 for most pairs and the FMA-pipe polynomial for a few, packed
+                    // row sums, bf16 pairs (P column c holds keys 2c, 2c+1)
+                    const uint64_t sl2x2 = f2(sl2, sl2), nref2 = f2(nref, nref);
+                    uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+                    uint32_t pk[64];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t v[2][32];
-                        tmem_ld32(tS + 64u * h, v[0]);
-                        tmem_ld32(tS + 64u * h + 32u, v[1]);
-                        tmem_ld_wait();
-                        if (need_mask) mask64(v, 64 * h);
-                        uint32_t pk[32];
-#pragma unroll
-                        for (int i = 0; i < 2; ++i)
-#pragma unroll
-                            for (int j = 0; j < 32; j += 2) {
-                                const float e0 = fast_exp2(fmaf(__uint_as_float(v[i][j]), sl2, nref));
-                                const float e1 =
-                                    fast_exp2(fmaf(__uint_as_float(v[i][j + 1]), sl2, nref));
-                                sum += e0 + e1;
-                                pk[i * 16 + (j >> 1)] = pack_bf16x2(e0, e1);
-                            }
-                        tmem_st32(tS + 32u * h, pk);
+                    for (int c = 0; c < 64; ++c) {
+                        const uint64_t x = fma_f2(f2(__uint_as_float(v[2 * c]),
+                                                     __uint_as_float(v[2 * c + 1])),
+                                                  sl2x2, nref2);
+                        uint64_t e;
+                        if ((c & 15) < kExp2EmuPairs) {
+                            e = exp2_poly_f2(x);
+                        } else {
+                            e = f2(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
+                        }
+                        acc2[c & 3] = add_f2(acc2[c & 3], e);
+                        pk[c] = pack_bf16x2(f2_lo(e), f2_hi(e));
                     }
+                    tmem_st64(tS, pk);
+                    const uint64_t acc = add_f2(add_f2(acc2[0], acc2[1]), add_f2(acc2[2], acc2[3]));
+                    const float sum = f2_lo(acc) + f2_hi(acc);
                     l_run = l_run * alpha + sum;
                     if (t > first_u) {
                         if (!mbar_wait(bar(C::bODone + u), (a - 1u) & 1u, abort_flag, p.dev_err,
                                        kSpinLimitNs)) {
+                            tmem_st_wait();
                             ok = false;
                             break;
                         }
@@ -544,19 +628,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // ---------------------------------------------------------- teardown
     const bool aborted = *abort_flag != 0;
-    if (warp == 0) {
+    if (warp >= kWarpGather0) {
+        cp_async_wait_all();
+    } else if (warp == kWarpTma) {
         cp_async_wait_all();
         if (aborted && lane == 0) {
             // let every TMA load this CTA issued land before the CTA exits
             volatile int dummy = 0;
-            for (int it = last_issued - S + 1; it <= last_issued; ++it)
-                if (it >= 0) {
-                    const uint32_t ph = ((uint32_t)it / S) & 1u;
-                    mbar_wait(bar(C::bKFull + it % S), ph, &dummy, p.dev_err, kSpinLimitNs);
-                    mbar_wait(bar(C::bVFull + it % S), ph, &dummy, p.dev_err, kSpinLimitNs);
-                }
+            if (n_done > 0)
+                mbar_wait(bar(C::bQFull), (n_done - 1) & 1u, &dummy, p.dev_err, kSpinLimitNs);
+            for (int it = last_issued - SK + 1; it <= last_issued; ++it)
+                if (it >= 0)
+                    mbar_wait(bar(C::bKFull + it % SK), ((uint32_t)it / SK) & 1u, &dummy,
+                              p.dev_err, kSpinLimitNs);
+            for (int it = last_issued - SV + 1; it <= last_issued; ++it)
+                if (it >= 0)
+                    mbar_wait(bar(C::bVFull + it % SV), ((uint32_t)it / SV) & 1u, &dummy,
+                              p.dev_err, kSpinLimitNs);
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == kWarpMma && lane == 0) {
         // every MMA (and its mbarrier arrivals) completes before TMEM is freed
         volatile int dummy = 0;
         umma_commit(bar(C::bDrain));
@@ -565,7 +655,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, 512);
+    if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
 size_t tc_smem_bytes(int head_dim) {

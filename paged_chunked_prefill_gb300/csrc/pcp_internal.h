@@ -13,7 +13,11 @@ namespace pcp {
 constexpr int kTileM = 128;       // query rows per Q tile (tcgen05 M)
 constexpr int kTileN = 128;       // keys per KV tile
 constexpr int kQTiles = 2;        // Q tiles per work item (share each K/V tile)
-constexpr int kTcThreads = 320;   // producer warp, MMA warp, 2 x 4 softmax warps
+constexpr int kTcThreads = 384;   // 2 x 4 softmax warps, TMA warp, MMA warp, 2 gather warps
+constexpr int kWarpTma = 8;       // Q (and large page runs of K/V) by TMA
+constexpr int kWarpMma = 9;       // one thread issues tcgen05.mma
+constexpr int kWarpGather0 = 10;  // warps 10, 11: cp.async page gathers of K/V
+constexpr int kGatherWarps = 2;
 
 // ---- CUDA-core row kernel (decode-shaped rows, split-KV)
 constexpr int kRowMaxRows = 16;   // query rows (positions x heads) per row item
@@ -122,7 +126,7 @@ struct TcParams {
     int group;
     int qpos;          // positions per Q tile
     int page_size;
-    int box_rows;      // rows per TMA page box; 0 selects cp.async gathers
+    int box_rows;      // rows per TMA page box; 0 selects the cp.async gather warps
     int64_t num_pages;
     int num_slots;
     int window;
