@@ -19,7 +19,8 @@ namespace pcp {
 cudaError_t launch_plan(cudaStream_t stream, const PlanParams& p);
 cudaError_t launch_extend_tc(int head_dim, int grid, cudaStream_t stream, const TcParams& p,
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv);
-cudaError_t launch_rows(int head_dim, int grid, cudaStream_t stream, const RowParams& p);
+cudaError_t launch_rows(int head_dim, int grid, cudaStream_t stream, const RowParams& p,
+                        const CUtensorMap& tk, const CUtensorMap& tv);
 cudaError_t launch_out_cache_loc(const int32_t* qo_indptr, const int32_t* kv_indptr,
                                  const int32_t* kv_indices, const int32_t* prefix_lens,
                                  int batch, int64_t total_q, int page_size, int64_t num_pages,
@@ -298,11 +299,13 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
         rp.n_kv_heads = n_kv_heads;
         rp.group = group;
         rp.page_size = page_size;
+        rp.box_rows = box_rows;
         rp.num_pages = num_pages;
+        rp.num_slots = num_slots;
         rp.window = window;
         rp.scale_log2 = scale_log2;
         rp.dev_err = dev_err;
-        if (launch_rows(head_dim, sms, s, rp) != cudaSuccess) return PCP_ERR_CUDA;
+        if (launch_rows(head_dim, sms, s, rp, tk, tv) != cudaSuccess) return PCP_ERR_CUDA;
     }
     return PCP_OK;
 }

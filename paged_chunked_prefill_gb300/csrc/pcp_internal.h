@@ -22,7 +22,7 @@ constexpr int kGatherWarps = 2;
 // ---- CUDA-core row kernel (decode-shaped rows, split-KV)
 constexpr int kRowMaxRows = 16;   // query rows (positions x heads) per row item
 constexpr int kRowTile = 128;     // keys per row-kernel tile
-constexpr int kRowThreads = 128;
+constexpr int kRowThreads = 160;      // 4 consumer warps + 1 load warp
 constexpr int kRowTargetItems = 1024;  // split lengths aim at about this many items
 
 // Spin-wait limit of every bounded wait (nanoseconds).
@@ -151,7 +151,9 @@ struct RowParams {
     int n_kv_heads;
     int group;
     int page_size;
+    int box_rows;      // rows per TMA page box; 0 selects cp.async gathers
     int64_t num_pages;
+    int num_slots;
     int window;
     float scale_log2;
     int32_t* dev_err;

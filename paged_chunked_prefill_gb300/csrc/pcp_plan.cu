@@ -12,10 +12,11 @@
 //  * row items for decode-shaped chunks (chunk_len * G <= 16 rows): the KV
 //    range of each (sequence, KV head) is split into pieces of
 //    `tiles_per_split` 128-key tiles, chosen so the whole call has about
-//    kRowTargetItems items.  This is the split-KV idea of the AstrAI paged
-//    decode kernel (split count from the SM count, partials merged by a
-//    log-sum-exp combine), with a fixed item budget instead of a per-batch
-//    split count.
+//    three items per SM, and ordered longest first like the tensor-core
+//    items.  Each split owns a partial slot (the group's first slot + split
+//    index) for the log-sum-exp combine.  This is the split-KV idea of the
+//    AstrAI paged decode kernel (split count from the SM count, partials
+//    merged by a combine step).
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
 
@@ -55,6 +56,7 @@ __device__ __forceinline__ int tc_cost(int P, int c, int k, int item_pos, int wi
 
 __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanParams p) {
     __shared__ int hist[1024];
+    __shared__ int hist_r[1024];
     __shared__ int scan[1024];
     __shared__ unsigned long long s_row_tiles;
     __shared__ int s_rows;
@@ -69,7 +71,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     const int rmax = row_path_max_chunk(p.group);
     const int H = p.n_kv_heads;
 
-    for (int i = tid; i < 1024; i += nt) hist[i] = 0;
+    for (int i = tid; i < 1024; i += nt) hist[i] = hist_r[i] = 0;
     for (int64_t i = tid; i < (int64_t)p.batch * H; i += nt) gcnt[i] = 0;
     if (tid == 0) {
         s_row_tiles = 0;
@@ -116,11 +118,38 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     }
     if (tid == 0) {
         const unsigned long long tot = s_row_tiles;
-        unsigned long long tps = (tot + kRowTargetItems - 1) / kRowTargetItems;
+        const int target = min(3 * max(p.sm_count, 1), kRowTargetItems);
+        unsigned long long tps = (tot + target - 1) / target;
         s_tps = (int)(tps < 1 ? 1 : tps);
     }
     __syncthreads();
     const int tps = s_tps;
+
+    // histogram of row-item lengths (tiles), for longest-first order
+    for (int b = tid; b < p.batch; b += nt) {
+        const SeqInfo s = seq_info(p, b);
+        if (!s.ok || s.c == 0 || s.c > rmax) continue;
+        const int tiles = (s.L - 1) / kRowTile - first_key(s.P, p.window) / kRowTile + 1;
+        const int ns = (tiles + tps - 1) / tps;
+        if (ns > 1) atomicAdd(&hist_r[min(tps, 1023)], (ns - 1) * H);
+        atomicAdd(&hist_r[min(tiles - (ns - 1) * tps, 1023)], H);
+    }
+    __syncthreads();
+    scan[tid] = hist_r[1023 - tid];
+    __syncthreads();
+    for (int d = 1; d < 1024; d <<= 1) {
+        const int v = tid >= d ? scan[tid - d] : 0;
+        __syncthreads();
+        scan[tid] += v;
+        __syncthreads();
+    }
+    {
+        const int bucket = 1023 - tid;
+        const int incl = scan[tid];
+        __syncthreads();
+        hist_r[bucket] = incl - hist_r[bucket];
+    }
+    __syncthreads();
 
     // pass 2: scatter tensor-core items, emit row items
     for (int b = tid; b < p.batch; b += nt) {
@@ -132,10 +161,11 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
             const int tiles = t1 - t0 + 1;
             const int ns = (tiles + tps - 1) / tps;
             for (int g = 0; g < H; ++g) {
-                const int base = atomicAdd(&s_rows, ns);
+                const int base = atomicAdd(&s_rows, ns);  // the group's partial slots
                 for (int sp = 0; sp < ns; ++sp) {
-                    const int it = base + sp;
-                    if (it >= p.lay.cap_row) {
+                    const int len = min(tps, tiles - sp * tps);
+                    const int it = atomicAdd(&hist_r[min(len, 1023)], 1);
+                    if (it >= p.lay.cap_row || base + sp >= p.lay.cap_row) {
                         report_error(p.dev_err, PCP_ERR_WORKSPACE);
                         break;
                     }

@@ -1,21 +1,26 @@
-// Decode-shaped rows: split-KV attention on CUDA cores.
+// Decode-shaped rows: split-KV attention, HBM-bound.
 //
 // A chunk with chunk_len * G <= 16 query rows (a decode row is chunk_len 1)
-// is HBM-bound: each key is used by at most 16 rows, so this path streams the
-// K/V pages at full bandwidth instead of padding 128-row tensor-core tiles.
-// The KV range of each (sequence, KV head) is split across CTAs (AstrAI paged
-// decode "split-KV" kernel, prior art); each split writes an fp32 partial
-// (unnormalised O, running max, normaliser) to the workspace and the last
-// split to finish merges the partials with the log-sum-exp identity (the
-// AstrAI combine kernel's job, fused here so a mixed batch needs no extra
-// launch).  Masking is the same bottom-right causal / window rule as the
-// tensor-core path, per row.
+// uses each key for at most 16 rows, so this path is bound by reading the
+// K/V pages, not by arithmetic.  The KV range of each (sequence, KV head) is
+// split across CTAs (AstrAI paged decode "split-KV" kernel, prior art); each
+// split writes an fp32 partial (unnormalised O, running max, normaliser) to
+// the workspace and the last split to finish merges the partials with the
+// log-sum-exp identity (the AstrAI combine kernel's job, fused here so a
+// mixed batch needs no extra launch).  Masking is the same bottom-right
+// causal / window rule as the tensor-core path, per row.
 //
-// Layout: 4 warps; a 128-key tile is gathered through the page table with
-// 16-byte cp.async (any page size, zero-filled past the split end), double
-// buffered.  Warp w scores keys 32w..32w+31 of the tile (one key per lane),
-// keeps its own online-softmax state, and accumulates P V with lanes split
-// over head_dim.  The four warp states are merged at the end of the item.
+// Layout: one CTA per SM, 4 consumer warps and 1 load warp, a ring of
+// 128-key K+V stages with full/empty mbarriers.  The load warp fills a stage
+// by TMA (one box per page run of >= 8 keys and 64-column block; the V page
+// run holding the sequence end by zero-filling cp.async) or, for smaller
+// pages, by 16-byte cp.async gathers; both land in the 128-byte-swizzled
+// layout.  The up to 16 query rows (position x head) form the M = 16 side of
+// warp-level m16n8k16 bf16 MMAs: consumer warp w takes keys 32w..32w+31 of a
+// tile, computes S = Q K^T with K fragments from ldmatrix, keeps an online
+// softmax in fp32, reuses the S accumulators as the P operand, and adds P V
+// with V fragments from ldmatrix.trans.  The four warp states are merged at
+// the end of each item.
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
 
@@ -25,46 +30,66 @@ namespace {
 
 template <int D>
 struct RowCfg {
-    static constexpr int kRowStride = D * 2 + 16;           // padded smem row (bytes)
-    static constexpr int kTileBytes = kRowTile * kRowStride;
-    static constexpr int kOffQ = 0;                          // float [16][D]
-    static constexpr int kOffK = kOffQ + kRowMaxRows * D * 4;
-    static constexpr int kOffV = kOffK + 2 * kTileBytes;
-    static constexpr int kOffP = kOffV + 2 * kTileBytes;     // float [4][32][16]
-    static constexpr int kOffM = kOffP + 4 * 32 * kRowMaxRows * 4;  // float [4][16] m, l
-    static constexpr int kSmemBytes = kOffM + 2 * 4 * kRowMaxRows * 4 + 64;
-    static constexpr int kDPerLane = D / 32;
+    static constexpr int kHalves = D / 64;
+    static constexpr int kHalfBytes = kRowTile * 128;            // one 64-column block
+    static constexpr int kTileBytes = kRowTile * D * 2;          // a K or a V tile
+    static constexpr int kStages = D == 128 ? 3 : 6;
+    static constexpr int kOffStage = 0;                          // [stage][K | V]
+    static constexpr int kOffBar = kOffStage + kStages * 2 * kTileBytes;
+    static constexpr int kOffM = kOffBar + 2 * kStages * 8;      // float [4][16] m, then l
+    static constexpr int kSmemBytes = kOffM + 2 * 4 * kRowMaxRows * 4 + 64 + 1024;
 };
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// Byte offset of (row, dim) in a 128-byte-swizzled tile (16-byte granules).
+template <int D>
+__device__ __forceinline__ uint32_t swz(int row, int dim) {
+    return (uint32_t)((dim >> 6) * RowCfg<D>::kHalfBytes + row * 128 +
+                      ((((dim & 63) >> 3) ^ (row & 7)) << 4));
+}
 
 }  // namespace
 
 template <int D>
-__global__ void __launch_bounds__(kRowThreads) row_attn_kernel(const __grid_constant__ RowParams p) {
+__global__ void __launch_bounds__(kRowThreads, 1)
+    row_attn_kernel(const __grid_constant__ RowParams p, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v) {
     using C = RowCfg<D>;
-    extern __shared__ __align__(128) uint8_t sm[];
-    float* q_s = reinterpret_cast<float*>(sm + C::kOffQ);
-    float* p_s = reinterpret_cast<float*>(sm + C::kOffP);
+    constexpr int S = C::kStages;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
     float* m_s = reinterpret_cast<float*>(sm + C::kOffM);
     float* l_s = m_s + 4 * kRowMaxRows;
     __shared__ int s_item;
     __shared__ int s_last;
+    __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gid = lane >> 2, tig = lane & 3;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
     const int n_items = hdr->n_row_items;
     const int4* items = reinterpret_cast<const int4*>(p.ws + p.lay.row_items);
@@ -73,173 +98,293 @@ __global__ void __launch_bounds__(kRowThreads) row_attn_kernel(const __grid_cons
     int* gcnt = reinterpret_cast<int*>(p.ws + p.lay.group_cnt);
     const int G = p.group;
     const float sl2 = p.scale_log2;
+    const uint32_t sStage = base + C::kOffStage;
+    const uint32_t sBar = base + C::kOffBar;
+    auto full_bar = [&](int s) { return sBar + 8u * (uint32_t)s; };
+    auto empty_bar = [&](int s) { return sBar + 8u * (uint32_t)(S + s); };
+    volatile int* abort_flag = &s_abort;
 
+    if (tid == 0) {
+        const uint32_t full_count = p.box_rows > 0 ? 1u : 32u;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), full_count);
+            mbar_init(empty_bar(s), 4);
+        }
+        fence_mbarrier_init();
+        s_abort = 0;
+    }
+    __syncthreads();
+
+    uint32_t it_base = 0;  // tiles this CTA has run through the ring so far
+    int last_issued = -1;  // load warp: last ring position it filled
     for (;;) {
         if (tid == 0) s_item = atomicAdd(&hdr->row_next, 1);
         __syncthreads();
         const int item = s_item;
-        if (item >= n_items) break;
+        if (item >= n_items || *abort_flag) break;
         const int4 i0 = items[2 * item], i1 = items[2 * item + 1];
-        const int b = i0.x, g = i0.y, nsplit = i0.w;
+        const int b = i0.x, g = i0.y, split = i0.z, nsplit = i0.w;
         const int kb = i1.x, ke = i1.y, first_item = i1.z;
         const int q0 = p.qo_indptr[b];
         const int c = p.qo_indptr[b + 1] - q0;
         const int P = p.prefix_lens[b];
+        const int L = P + c;
         const int R = c * G;
-        const int32_t* pages = p.kv_indices + p.kv_indptr[b];
-
-        // query rows, pre-scaled into log2 units
-        for (int idx = tid; idx < R * D; idx += kRowThreads) {
-            const int r = idx / D, d = idx % D;
-            const uint16_t qb = p.q[((int64_t)(q0 + r / G) * p.n_q_heads + g * G + r % G) * D + d];
-            q_s[idx] = __uint_as_float((uint32_t)qb << 16) * sl2;
-        }
-
         const int t_first = kb / kRowTile, t_last = (ke - 1) / kRowTile;
-        auto issue_tile = [&](int t, int stage) {
-            uint8_t* kd = sm + C::kOffK + stage * C::kTileBytes;
-            uint8_t* vd = sm + C::kOffV + stage * C::kTileBytes;
-            constexpr int chunks = D * 2 / 16;
-            for (int idx = tid; idx < kRowTile * chunks; idx += kRowThreads) {
-                const int row = idx / chunks, ch = idx % chunks;
-                const int key = t * kRowTile + row;
-                bool ok = key >= kb && key < ke;
-                int64_t slot = 0;
-                if (ok) {
-                    const int page = pages[key / p.page_size];
-                    if (page >= 0 && page < p.num_pages) {
-                        slot = (int64_t)page * p.page_size + key % p.page_size;
-                    } else {
-                        ok = false;
-                        report_error(p.dev_err, PCP_ERR_BAD_INDEX);
-                    }
-                }
-                const int64_t off = (slot * p.n_kv_heads + g) * D + ch * 8;
-                cp_async_16(smem_addr(kd + row * C::kRowStride + ch * 16),
-                            ok ? (const void*)(p.k_pool + off) : (const void*)p.k_pool,
-                            ok ? 16u : 0u);
-                cp_async_16(smem_addr(vd + row * C::kRowStride + ch * 16),
-                            ok ? (const void*)(p.v_pool + off) : (const void*)p.v_pool,
-                            ok ? 16u : 0u);
-            }
-            cp_async_commit();
-        };
+        const int ntiles = t_last - t_first + 1;
 
-        // per-warp online softmax state (log2 units), replicated across lanes
-        float m_r[kRowMaxRows], l_r[kRowMaxRows];
-        float o_r[kRowMaxRows][C::kDPerLane];
+        // rows gid and gid + 8 of the 16-row MMA tile
+        const int row_lo = gid, row_hi = gid + 8;
+        float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+        float o[D / 8][4];
 #pragma unroll
-        for (int r = 0; r < kRowMaxRows; ++r) {
-            m_r[r] = -INFINITY;
-            l_r[r] = 0.f;
+        for (int dn = 0; dn < D / 8; ++dn)
 #pragma unroll
-            for (int i = 0; i < C::kDPerLane; ++i) o_r[r][i] = 0.f;
-        }
+            for (int j = 0; j < 4; ++j) o[dn][j] = 0.f;
 
-        issue_tile(t_first, 0);
-        for (int t = t_first; t <= t_last; ++t) {
-            const int stage = (t - t_first) & 1;
-            if (t < t_last) {
-                issue_tile(t + 1, stage ^ 1);
-                cp_async_wait_group<1>();
-            } else {
-                cp_async_wait_group<0>();
-            }
-            __syncthreads();
-            const uint8_t* kt = sm + C::kOffK + stage * C::kTileBytes;
-            const uint8_t* vt = sm + C::kOffV + stage * C::kTileBytes;
-            const int key = t * kRowTile + warp * 32 + lane;
-
-            // scores: one key per lane
-            float s[kRowMaxRows];
+        if (warp == 4) {
+            // ------------------------------------------------ load warp
+            const int32_t* pages = p.kv_indices + p.kv_indptr[b];
+            const int ps = p.page_size;
+            // slot (TMA: first slot of this lane's page run; gather: slots of
+            // rows lane + 32k) for a tile, read one tile ahead
+            auto fetch = [&](int t, int (&sl)[4]) {
 #pragma unroll
-            for (int r = 0; r < kRowMaxRows; ++r) s[r] = 0.f;
-            const uint8_t* krow = kt + (warp * 32 + lane) * C::kRowStride;
-#pragma unroll 2
-            for (int ch = 0; ch < D / 8; ++ch) {
-                const uint4 kv = *reinterpret_cast<const uint4*>(krow + ch * 16);
-                const float k8[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
-                                     bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
-#pragma unroll
-                for (int r = 0; r < kRowMaxRows; ++r) {
-                    if (r < R) {
-                        const float4 qa = *reinterpret_cast<const float4*>(q_s + r * D + ch * 8);
-                        const float4 qb = *reinterpret_cast<const float4*>(q_s + r * D + ch * 8 + 4);
-                        float acc = s[r];
-                        acc = fmaf(qa.x, k8[0], acc);
-                        acc = fmaf(qa.y, k8[1], acc);
-                        acc = fmaf(qa.z, k8[2], acc);
-                        acc = fmaf(qa.w, k8[3], acc);
-                        acc = fmaf(qb.x, k8[4], acc);
-                        acc = fmaf(qb.y, k8[5], acc);
-                        acc = fmaf(qb.z, k8[6], acc);
-                        acc = fmaf(qb.w, k8[7], acc);
-                        s[r] = acc;
+                for (int k = 0; k < 4; ++k) sl[k] = -1;
+                if (t > t_last) return;
+                if (p.box_rows > 0) {
+                    const int nsub = kRowTile / p.box_rows;
+                    const int key = t * kRowTile + (lane % nsub) * p.box_rows;
+                    sl[0] = p.num_slots;
+                    if (lane < nsub * C::kHalves && key < L) {
+                        const int page = pages[key / ps];
+                        if (page >= 0 && page < p.num_pages)
+                            sl[0] = page * ps + key % ps;
+                        else
+                            report_error(p.dev_err, PCP_ERR_BAD_INDEX);
                     }
-                }
-            }
-            // mask, online softmax, publish p to shared memory
-            const bool in_split = key >= kb && key < ke;
-#pragma unroll
-            for (int r = 0; r < kRowMaxRows; ++r) {
-                if (r < R) {
-                    const int pos = P + r / G;
-                    const bool vis = in_split && key <= pos && (p.window <= 0 || key > pos - p.window);
-                    const float sv = vis ? s[r] : -INFINITY;
-                    const float mx = warp_max(sv);
-                    const float m_new = fmaxf(m_r[r], mx);
-                    float pr = 0.f, alpha = 1.f;
-                    if (m_new != -INFINITY) {
-                        alpha = fast_exp2(m_r[r] - m_new);
-                        pr = fast_exp2(sv - m_new);
-                        m_r[r] = m_new;
-                    }
-                    l_r[r] = l_r[r] * alpha + pr;
-#pragma unroll
-                    for (int i = 0; i < C::kDPerLane; ++i) o_r[r][i] *= alpha;
-                    p_s[(warp * 32 + lane) * kRowMaxRows + r] = pr;
-                }
-            }
-            __syncwarp();
-            // O += P V over this warp's 32 keys; lanes split head_dim
-#pragma unroll 4
-            for (int tk = 0; tk < 32; ++tk) {
-                const uint8_t* vrow = vt + (warp * 32 + tk) * C::kRowStride + lane * C::kDPerLane * 2;
-                float vv[C::kDPerLane];
-                if constexpr (C::kDPerLane == 4) {
-                    const uint2 w = *reinterpret_cast<const uint2*>(vrow);
-                    vv[0] = bf16_lo(w.x); vv[1] = bf16_hi(w.x); vv[2] = bf16_lo(w.y); vv[3] = bf16_hi(w.y);
                 } else {
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(vrow);
-                    vv[0] = bf16_lo(w); vv[1] = bf16_hi(w);
-                }
-                const float* pp = p_s + (warp * 32 + tk) * kRowMaxRows;
 #pragma unroll
-                for (int r = 0; r < kRowMaxRows; ++r) {
-                    if (r < R) {
-                        const float pr = pp[r];
-#pragma unroll
-                        for (int i = 0; i < C::kDPerLane; ++i) o_r[r][i] = fmaf(pr, vv[i], o_r[r][i]);
+                    for (int k = 0; k < 4; ++k) {
+                        const int key = t * kRowTile + lane + 32 * k;
+                        if (key < L) {
+                            const int page = pages[key / ps];
+                            if (page >= 0 && page < p.num_pages)
+                                sl[k] = page * ps + key % ps;
+                            else
+                                report_error(p.dev_err, PCP_ERR_BAD_INDEX);
+                        }
                     }
                 }
-            }
-            __syncthreads();
-        }
-
-        // merge the four warps' states through shared memory (reusing the K stages)
-        float* wo = reinterpret_cast<float*>(sm + C::kOffK);  // [4][16][D]
+            };
+            int cur_sl[4], next_sl[4];
+            fetch(t_first, cur_sl);
+            for (int i = 0; i < ntiles; ++i) {
+                const int t = t_first + i;
+                const uint32_t it = it_base + i;
+                const int st = it % S;
+                fetch(t + 1, next_sl);
+                if (!mbar_wait(empty_bar(st), ((it / S) & 1u) ^ 1u, abort_flag, p.dev_err,
+                               kSpinLimitNs))
+                    break;
+                const uint32_t kd = sStage + st * 2 * C::kTileBytes;
+                const uint32_t vd = kd + C::kTileBytes;
+                if (p.box_rows > 0) {
+                    const int br = p.box_rows, nsub = kRowTile / br, nloads = nsub * C::kHalves;
+                    const int key0 = t * kRowTile;
+                    // the V page run holding the sequence end is zero-filled past it
+                    int strad = -1;
+                    if (L > key0 && L < key0 + kRowTile && (L - key0) % br != 0)
+                        strad = (L - key0) / br;
+                    if (strad >= 0) {
+                        const int slot0 = __shfl_sync(0xffffffffu, cur_sl[0], strad);
+                        const bool bad = slot0 >= p.num_slots;
+                        const int ks = key0 + strad * br;
+                        for (int idx = lane; idx < br * C::kHalves * 8; idx += 32) {
+                            const int row = idx / (C::kHalves * 8), cc = idx % (C::kHalves * 8);
+                            const int rt = strad * br + row;
+                            const bool ok = !bad && ks + row < L;
+                            const uint16_t* src =
+                                ok ? p.v_pool + ((int64_t)(slot0 + row) * p.n_kv_heads + g) * D + cc * 8
+                                   : p.v_pool;
+                            cp_async_16(vd + swz<D>(rt, cc * 8), src, ok ? 16u : 0u);
+                        }
+                        cp_async_mbar_arrive(full_bar(st));
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(
+                            full_bar(st), (uint32_t)(2 * nloads - (strad >= 0 ? C::kHalves : 0)) * br * 128);
+                    __syncwarp();
+                    if (lane < nloads) {
+                        const int sb = lane % nsub, h = lane / nsub;
+                        tma_load_3d(kd + h * C::kHalfBytes + sb * br * 128, &tm_k, full_bar(st),
+                                    h * 64, g, cur_sl[0]);
+                        if (sb != strad)
+                            tma_load_3d(vd + h * C::kHalfBytes + sb * br * 128, &tm_v, full_bar(st),
+                                        h * 64, g, cur_sl[0]);
+                    }
+                } else {
 #pragma unroll
-        for (int r = 0; r < kRowMaxRows; ++r) {
-            if (r < R) {
-                const float lsum = warp_sum(l_r[r]);
-                if (lane == 0) {
-                    m_s[warp * kRowMaxRows + r] = m_r[r];
-                    l_s[warp * kRowMaxRows + r] = lsum;
+                    for (int k = 0; k < 4; ++k) {
+                        const int row = lane + 32 * k;
+                        const bool ok = cur_sl[k] >= 0;
+                        const int64_t off = ((int64_t)(ok ? cur_sl[k] : 0) * p.n_kv_heads + g) * D;
+#pragma unroll
+                        for (int cc = 0; cc < C::kHalves * 8; ++cc) {
+                            cp_async_16(kd + swz<D>(row, cc * 8), p.k_pool + off + cc * 8, ok ? 16u : 0u);
+                            cp_async_16(vd + swz<D>(row, cc * 8), p.v_pool + off + cc * 8, ok ? 16u : 0u);
+                        }
+                    }
+                    cp_async_mbar_arrive_noinc(full_bar(st));
                 }
+                last_issued = (int)it;
 #pragma unroll
-                for (int i = 0; i < C::kDPerLane; ++i)
-                    wo[(warp * kRowMaxRows + r) * D + lane * C::kDPerLane + i] = o_r[r][i];
+                for (int k = 0; k < 4; ++k) cur_sl[k] = next_sl[k];
             }
+        } else {
+            // ------------------------------------------------ consumer warps
+            // Q as the A operand (rows gid and gid + 8, 16 dims per k-step); rows >= R are 0
+            uint32_t qa[D / 16][4];
+            {
+                const uint16_t* qlo = row_lo < R
+                    ? p.q + ((int64_t)(q0 + row_lo / G) * p.n_q_heads + g * G + row_lo % G) * D
+                    : nullptr;
+                const uint16_t* qhi = row_hi < R
+                    ? p.q + ((int64_t)(q0 + row_hi / G) * p.n_q_heads + g * G + row_hi % G) * D
+                    : nullptr;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int d0 = kk * 16 + tig * 2;
+                    qa[kk][0] = qlo ? *reinterpret_cast<const uint32_t*>(qlo + d0) : 0u;
+                    qa[kk][1] = qhi ? *reinterpret_cast<const uint32_t*>(qhi + d0) : 0u;
+                    qa[kk][2] = qlo ? *reinterpret_cast<const uint32_t*>(qlo + d0 + 8) : 0u;
+                    qa[kk][3] = qhi ? *reinterpret_cast<const uint32_t*>(qhi + d0 + 8) : 0u;
+                }
+            }
+            const int pos_lo = P + row_lo / G, pos_hi = P + row_hi / G;
+            for (int i = 0; i < ntiles; ++i) {
+                const int t = t_first + i;
+                const uint32_t it = it_base + i;
+                const int st = it % S;
+                if (!mbar_wait(full_bar(st), (it / S) & 1u, abort_flag, p.dev_err, kSpinLimitNs))
+                    break;
+                const uint32_t kbase = sStage + st * 2 * C::kTileBytes;
+                const uint32_t vbase = kbase + C::kTileBytes;
+                const int key_w = t * kRowTile + warp * 32;
+
+                // S = Q K^T for this warp's 32 keys: [block of 16 keys][n8 half][4]
+                float sc[2][2][4];
+#pragma unroll
+                for (int bl = 0; bl < 2; ++bl)
+#pragma unroll
+                    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) sc[bl][nb][j] = 0.f;
+#pragma unroll
+                for (int bl = 0; bl < 2; ++bl)
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int krow = warp * 32 + bl * 16 + (lane >> 4) * 8 + (lane & 7);
+                        const int dcol = kk * 16 + ((lane >> 3) & 1) * 8;
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(kbase + swz<D>(krow, dcol), b0, b1, b2, b3);
+                        mma_16816(sc[bl][0], qa[kk], b0, b1);
+                        mma_16816(sc[bl][1], qa[kk], b2, b3);
+                    }
+                // mask and scale; element j: row lo (j < 2) or hi, key = ... + 2 * tig + (j & 1)
+                float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+                for (int bl = 0; bl < 2; ++bl)
+#pragma unroll
+                    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int key = key_w + bl * 16 + nb * 8 + tig * 2 + (j & 1);
+                            const int pos = j < 2 ? pos_lo : pos_hi;
+                            const int row = j < 2 ? row_lo : row_hi;
+                            const bool vis = row < R && key >= kb && key < ke && key <= pos &&
+                                             (p.window <= 0 || key > pos - p.window);
+                            const float v = vis ? sc[bl][nb][j] * sl2 : -INFINITY;
+                            sc[bl][nb][j] = v;
+                            if (j < 2) mx_lo = fmaxf(mx_lo, v);
+                            else mx_hi = fmaxf(mx_hi, v);
+                        }
+                mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+                mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+                const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+                const float a_lo = mn_lo == -INFINITY ? 1.f : fast_exp2(m_lo - mn_lo);
+                const float a_hi = mn_hi == -INFINITY ? 1.f : fast_exp2(m_hi - mn_hi);
+                const float r_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+                const float r_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+                m_lo = mn_lo;
+                m_hi = mn_hi;
+                float s_lo = 0.f, s_hi = 0.f;
+                uint32_t pa[2][4];
+#pragma unroll
+                for (int bl = 0; bl < 2; ++bl)
+#pragma unroll
+                    for (int nb = 0; nb < 2; ++nb) {
+                        const float e0 = fast_exp2(sc[bl][nb][0] - r_lo);
+                        const float e1 = fast_exp2(sc[bl][nb][1] - r_lo);
+                        const float e2 = fast_exp2(sc[bl][nb][2] - r_hi);
+                        const float e3 = fast_exp2(sc[bl][nb][3] - r_hi);
+                        s_lo += e0 + e1;
+                        s_hi += e2 + e3;
+                        pa[bl][nb * 2 + 0] = pack_bf16x2(e0, e1);
+                        pa[bl][nb * 2 + 1] = pack_bf16x2(e2, e3);
+                    }
+                l_lo = l_lo * a_lo + s_lo;
+                l_hi = l_hi * a_hi + s_hi;
+#pragma unroll
+                for (int dn = 0; dn < D / 8; ++dn) {
+                    o[dn][0] *= a_lo;
+                    o[dn][1] *= a_lo;
+                    o[dn][2] *= a_hi;
+                    o[dn][3] *= a_hi;
+                }
+                // O += P V; V fragments for two 8-wide column chunks per ldmatrix.trans
+#pragma unroll
+                for (int bl = 0; bl < 2; ++bl)
+#pragma unroll
+                    for (int dn2 = 0; dn2 < D / 16; ++dn2) {
+                        const int vrow = warp * 32 + bl * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                        const int dcol = (dn2 * 2 + (lane >> 4)) * 8;
+                        uint32_t v0, v1, v2, v3;
+                        ldsm_x4_trans(vbase + swz<D>(vrow, dcol), v0, v1, v2, v3);
+                        mma_16816(o[2 * dn2], pa[bl], v0, v1);
+                        mma_16816(o[2 * dn2 + 1], pa[bl], v2, v3);
+                    }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(st));
+            }
+        }
+        it_base += (uint32_t)ntiles;
+
+        // merge the four warps' states through shared memory (reusing the stages)
+        __syncthreads();
+        float* wo = reinterpret_cast<float*>(sm + C::kOffStage);  // [4][16][D]
+        if (warp < 4) {
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+        if (tig == 0) {
+            m_s[warp * kRowMaxRows + row_lo] = m_lo;
+            m_s[warp * kRowMaxRows + row_hi] = m_hi;
+            l_s[warp * kRowMaxRows + row_lo] = l_lo;
+            l_s[warp * kRowMaxRows + row_hi] = l_hi;
+        }
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+            const int d = dn * 8 + tig * 2;
+            *reinterpret_cast<float2*>(&wo[(warp * kRowMaxRows + row_lo) * D + d]) =
+                make_float2(o[dn][0], o[dn][1]);
+            *reinterpret_cast<float2*>(&wo[(warp * kRowMaxRows + row_hi) * D + d]) =
+                make_float2(o[dn][2], o[dn][3]);
+        }
         }
         __syncthreads();
         for (int idx = tid; idx < R * D; idx += kRowThreads) {
@@ -263,8 +408,9 @@ __global__ void __launch_bounds__(kRowThreads) row_attn_kernel(const __grid_cons
                 if (d == 0 && p.lse != nullptr)
                     p.lse[orow] = lsum > 0.f ? (M + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
             } else {
-                part_o[((int64_t)item * kRowMaxRows + r) * D + d] = acc;
-                if (d == 0) part_ml[(int64_t)item * kRowMaxRows + r] = make_float2(M, lsum);
+                part_o[((int64_t)(first_item + split) * kRowMaxRows + r) * D + d] = acc;
+                if (d == 0)
+                    part_ml[(int64_t)(first_item + split) * kRowMaxRows + r] = make_float2(M, lsum);
             }
         }
         if (nsplit > 1) {
@@ -303,25 +449,37 @@ __global__ void __launch_bounds__(kRowThreads) row_attn_kernel(const __grid_cons
         }
         __syncthreads();
     }
+    // teardown: nothing may still be landing in shared memory when the CTA exits
+    if (warp == 4) {
+        cp_async_wait_all();
+        if (*abort_flag && lane == 0) {
+            volatile int dummy = 0;
+            for (int it = last_issued - S + 1; it <= last_issued; ++it)
+                if (it >= 0)
+                    mbar_wait(full_bar(it % S), ((uint32_t)it / S) & 1u, &dummy, p.dev_err,
+                              kSpinLimitNs);
+        }
+    }
 }
 
 size_t row_smem_bytes(int head_dim) {
     return head_dim == 128 ? RowCfg<128>::kSmemBytes : RowCfg<64>::kSmemBytes;
 }
 
-cudaError_t launch_rows(int head_dim, int grid, cudaStream_t stream, const RowParams& p) {
+cudaError_t launch_rows(int head_dim, int grid, cudaStream_t stream, const RowParams& p,
+                        const CUtensorMap& tk, const CUtensorMap& tv) {
     const size_t smem = row_smem_bytes(head_dim);
     cudaError_t e;
     if (head_dim == 128) {
         e = cudaFuncSetAttribute(row_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
-        row_attn_kernel<128><<<grid, kRowThreads, smem, stream>>>(p);
+        row_attn_kernel<128><<<grid, kRowThreads, smem, stream>>>(p, tk, tv);
     } else {
         e = cudaFuncSetAttribute(row_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
-        row_attn_kernel<64><<<grid, kRowThreads, smem, stream>>>(p);
+        row_attn_kernel<64><<<grid, kRowThreads, smem, stream>>>(p, tk, tv);
     }
     return cudaGetLastError();
 }
