@@ -278,14 +278,10 @@ __device__ __forceinline__ uint64_t f2(float lo, float hi) {
     return r;
 }
 __device__ __forceinline__ float f2_lo(uint64_t v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return lo;
+    return __uint_as_float(static_cast<uint32_t>(v));
 }
 __device__ __forceinline__ float f2_hi(uint64_t v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return hi;
+    return __uint_as_float(static_cast<uint32_t>(v >> 32));
 }
 __device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
     uint64_t d;

@@ -239,6 +239,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
+    // a call without tensor-core work (decode rows only) leaves at once
+    if (reinterpret_cast<const WsHeader*>(p.ws + p.lay.header)->n_tc_items == 0) return;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::bQFull), 1);

@@ -52,15 +52,47 @@ __device__ __forceinline__ int tc_cost(int P, int c, int k, int item_pos, int wi
     return last / kTileN - first_key(first, window) / kTileN + 1;
 }
 
+// Turn a 1024-bucket histogram into descending exclusive offsets (bucket
+// 1023 first) in place and return the total.  1024 threads; warp-shuffle
+// scans, three block barriers.
+__device__ __forceinline__ int desc_offsets(int* hist, int* warp_sums) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int own = hist[1023 - tid];
+    int v = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_sums[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        int x = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += n;
+        }
+        warp_sums[32 + lane] = x;  // inclusive prefix over warps
+    }
+    __syncthreads();
+    const int before = w > 0 ? warp_sums[32 + w - 1] : 0;
+    hist[1023 - tid] = before + v - own;
+    const int total = warp_sums[32 + 31];
+    __syncthreads();
+    return total;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanParams p) {
     __shared__ int hist[1024];
     __shared__ int hist_r[1024];
-    __shared__ int scan[1024];
+    __shared__ int warp_sums[64];
     __shared__ unsigned long long s_row_tiles;
     __shared__ int s_rows;
     __shared__ int s_tps;
+    __shared__ int4 s_seq[1024];  // {c, P, ok} of the first 1024 sequences
 
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
     int4* tc = reinterpret_cast<int4*>(p.ws + p.lay.tc_items);
@@ -72,6 +104,21 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     const int H = p.n_kv_heads;
 
     for (int i = tid; i < 1024; i += nt) hist[i] = hist_r[i] = 0;
+    // the metadata is read from global memory once; later passes use shared memory
+    for (int b = tid; b < min(p.batch, 1024); b += nt) {
+        const SeqInfo q = seq_info(p, b);
+        s_seq[b] = make_int4(q.c, q.P, q.ok ? 1 : 0, 0);
+    }
+    auto get_seq = [&](int b) {
+        if (b >= 1024) return seq_info(p, b);
+        const int4 v = s_seq[b];
+        SeqInfo q;
+        q.c = v.x;
+        q.P = v.y;
+        q.L = v.x + v.y;
+        q.ok = v.z != 0;
+        return q;
+    };
     for (int64_t i = tid; i < (int64_t)p.batch * H; i += nt) gcnt[i] = 0;
     if (tid == 0) {
         s_row_tiles = 0;
@@ -83,7 +130,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
 
     // pass 1: validate, histogram of tensor-core costs, total row-path tiles
     for (int b = tid; b < p.batch; b += nt) {
-        const SeqInfo s = seq_info(p, b);
+        const SeqInfo s = get_seq(b);
         if (!s.ok) {
             report_error(p.dev_err, PCP_ERR_INVALID_ARG);
             continue;
@@ -100,22 +147,8 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     }
     __syncthreads();
 
-    // descending exclusive scan of the cost histogram
-    scan[tid] = hist[1023 - tid];
-    __syncthreads();
-    for (int d = 1; d < 1024; d <<= 1) {
-        const int v = tid >= d ? scan[tid - d] : 0;
-        __syncthreads();
-        scan[tid] += v;
-        __syncthreads();
-    }
-    const int n_tc = scan[1023];
-    {
-        const int bucket = 1023 - tid;
-        const int incl = scan[tid];
-        __syncthreads();
-        hist[bucket] = incl - hist[bucket];  // becomes the bucket's first slot
-    }
+    // descending exclusive offsets of the cost histogram
+    const int n_tc = desc_offsets(hist, warp_sums);
     if (tid == 0) {
         const unsigned long long tot = s_row_tiles;
         const int target = min(3 * max(p.sm_count, 1), kRowTargetItems);
@@ -127,7 +160,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
 
     // histogram of row-item lengths (tiles), for longest-first order
     for (int b = tid; b < p.batch; b += nt) {
-        const SeqInfo s = seq_info(p, b);
+        const SeqInfo s = get_seq(b);
         if (!s.ok || s.c == 0 || s.c > rmax) continue;
         const int tiles = (s.L - 1) / kRowTile - first_key(s.P, p.window) / kRowTile + 1;
         const int ns = (tiles + tps - 1) / tps;
@@ -135,25 +168,11 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
         atomicAdd(&hist_r[min(tiles - (ns - 1) * tps, 1023)], H);
     }
     __syncthreads();
-    scan[tid] = hist_r[1023 - tid];
-    __syncthreads();
-    for (int d = 1; d < 1024; d <<= 1) {
-        const int v = tid >= d ? scan[tid - d] : 0;
-        __syncthreads();
-        scan[tid] += v;
-        __syncthreads();
-    }
-    {
-        const int bucket = 1023 - tid;
-        const int incl = scan[tid];
-        __syncthreads();
-        hist_r[bucket] = incl - hist_r[bucket];
-    }
-    __syncthreads();
+    desc_offsets(hist_r, warp_sums);
 
     // pass 2: scatter tensor-core items, emit row items
     for (int b = tid; b < p.batch; b += nt) {
-        const SeqInfo s = seq_info(p, b);
+        const SeqInfo s = get_seq(b);
         if (!s.ok || s.c == 0) continue;
         if (s.c <= rmax) {
             const int lo = first_key(s.P, p.window);

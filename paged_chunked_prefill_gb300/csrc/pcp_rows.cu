@@ -33,10 +33,11 @@ struct RowCfg {
     static constexpr int kHalves = D / 64;
     static constexpr int kHalfBytes = kRowTile * 128;            // one 64-column block
     static constexpr int kTileBytes = kRowTile * D * 2;          // a K or a V tile
-    static constexpr int kStages = D == 128 ? 3 : 6;
+    static constexpr int kStages = D == 128 ? 3 : 5;
     static constexpr int kOffStage = 0;                          // [stage][K | V]
-    static constexpr int kOffBar = kOffStage + kStages * 2 * kTileBytes;
-    static constexpr int kOffM = kOffBar + 2 * kStages * 8;      // float [4][16] m, then l
+    static constexpr int kOffMerge = kOffStage + kStages * 2 * kTileBytes;  // float [4][16][D]
+    static constexpr int kOffBar = kOffMerge + 4 * kRowMaxRows * D * 4;
+    static constexpr int kOffM = kOffBar + (2 * kStages + 4) * 8;  // float [4][16] m, then l
     static constexpr int kSmemBytes = kOffM + 2 * 4 * kRowMaxRows * 4 + 64 + 1024;
 };
 
@@ -78,13 +79,15 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v) {
     using C = RowCfg<D>;
     constexpr int S = C::kStages;
+    constexpr int NI = 2;                      // item hand-off slots
+    constexpr int kConsumerThreads = 128;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
     float* m_s = reinterpret_cast<float*>(sm + C::kOffM);
     float* l_s = m_s + 4 * kRowMaxRows;
-    __shared__ int s_item;
+    __shared__ volatile int s_item_q[NI];
     __shared__ int s_last;
     __shared__ int s_abort;
 
@@ -102,54 +105,64 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     const uint32_t sBar = base + C::kOffBar;
     auto full_bar = [&](int s) { return sBar + 8u * (uint32_t)s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (uint32_t)(S + s); };
+    auto item_full = [&](int s) { return sBar + 8u * (uint32_t)(2 * S + s); };
+    auto item_empty = [&](int s) { return sBar + 8u * (uint32_t)(2 * S + NI + s); };
     volatile int* abort_flag = &s_abort;
+    // the four consumer warps only (named barrier 1)
+    auto consumer_sync = [] { asm volatile("bar.sync 1, 128;" ::: "memory"); };
 
+    if (n_items == 0) return;
     if (tid == 0) {
         const uint32_t full_count = p.box_rows > 0 ? 1u : 32u;
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), full_count);
             mbar_init(empty_bar(s), 4);
         }
+        for (int s = 0; s < NI; ++s) {
+            mbar_init(item_full(s), 1);
+            mbar_init(item_empty(s), 4);
+        }
         fence_mbarrier_init();
         s_abort = 0;
     }
     __syncthreads();
 
-    uint32_t it_base = 0;  // tiles this CTA has run through the ring so far
-    int last_issued = -1;  // load warp: last ring position it filled
-    for (;;) {
-        if (tid == 0) s_item = atomicAdd(&hdr->row_next, 1);
-        __syncthreads();
-        const int item = s_item;
-        if (item >= n_items || *abort_flag) break;
-        const int4 i0 = items[2 * item], i1 = items[2 * item + 1];
-        const int b = i0.x, g = i0.y, split = i0.z, nsplit = i0.w;
-        const int kb = i1.x, ke = i1.y, first_item = i1.z;
-        const int q0 = p.qo_indptr[b];
-        const int c = p.qo_indptr[b + 1] - q0;
-        const int P = p.prefix_lens[b];
-        const int L = P + c;
-        const int R = c * G;
-        const int t_first = kb / kRowTile, t_last = (ke - 1) / kRowTile;
-        const int ntiles = t_last - t_first + 1;
-
-        // rows gid and gid + 8 of the 16-row MMA tile
-        const int row_lo = gid, row_hi = gid + 8;
-        float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-        float o[D / 8][4];
-#pragma unroll
-        for (int dn = 0; dn < D / 8; ++dn)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) o[dn][j] = 0.f;
-
-        if (warp == 4) {
-            // ------------------------------------------------ load warp
+    if (warp == 4) {
+        // ==================================================== load warp
+        // It takes items from the device counter, hands each to the consumer
+        // warps through the item queue, and streams its K/V tiles through the
+        // stage ring without waiting for the consumers to finish the previous
+        // item, so the next item's first tiles load during this one's merge.
+        uint32_t it = 0;       // ring position
+        int last_issued = -1;
+        for (int k = 0;; ++k) {
+            const int qs = k % NI;
+            int item = 0;
+            if (lane == 0) item = atomicAdd(&hdr->row_next, 1);
+            item = __shfl_sync(0xffffffffu, item, 0);
+            if (item >= n_items || *abort_flag) item = -1;
+            if (!mbar_wait(item_empty(qs), ((uint32_t)(k / NI) & 1u) ^ 1u, abort_flag, p.dev_err,
+                           kSpinLimitNs))
+                break;
+            if (lane == 0) {
+                s_item_q[qs] = item;
+                mbar_arrive(item_full(qs));
+            }
+            if (item < 0) break;
+            const int4 i0 = items[2 * item], i1 = items[2 * item + 1];
+            const int b = i0.x, g = i0.y;
+            const int kb = i1.x, ke = i1.y;
+            const int q0 = p.qo_indptr[b];
+            const int L = p.prefix_lens[b] + (p.qo_indptr[b + 1] - q0);
+            const int t_first = kb / kRowTile, t_last = (ke - 1) / kRowTile;
+            const int ntiles = t_last - t_first + 1;
+            const uint32_t it_base = it;
             const int32_t* pages = p.kv_indices + p.kv_indptr[b];
             const int ps = p.page_size;
             // slot (TMA: first slot of this lane's page run; gather: slots of
             // rows lane + 32k) for a tile, read one tile ahead
             auto fetch = [&](int t, int (&sl)[4]) {
-#pragma unroll
+    #pragma unroll
                 for (int k = 0; k < 4; ++k) sl[k] = -1;
                 if (t > t_last) return;
                 if (p.box_rows > 0) {
@@ -164,7 +177,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                             report_error(p.dev_err, PCP_ERR_BAD_INDEX);
                     }
                 } else {
-#pragma unroll
+    #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int key = t * kRowTile + lane + 32 * k;
                         if (key < L) {
@@ -225,12 +238,12 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                                         h * 64, g, cur_sl[0]);
                     }
                 } else {
-#pragma unroll
+    #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int row = lane + 32 * k;
                         const bool ok = cur_sl[k] >= 0;
                         const int64_t off = ((int64_t)(ok ? cur_sl[k] : 0) * p.n_kv_heads + g) * D;
-#pragma unroll
+    #pragma unroll
                         for (int cc = 0; cc < C::kHalves * 8; ++cc) {
                             cp_async_16(kd + swz<D>(row, cc * 8), p.k_pool + off + cc * 8, ok ? 16u : 0u);
                             cp_async_16(vd + swz<D>(row, cc * 8), p.v_pool + off + cc * 8, ok ? 16u : 0u);
@@ -239,11 +252,54 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                     cp_async_mbar_arrive_noinc(full_bar(st));
                 }
                 last_issued = (int)it;
-#pragma unroll
+    #pragma unroll
                 for (int k = 0; k < 4; ++k) cur_sl[k] = next_sl[k];
             }
-        } else {
-            // ------------------------------------------------ consumer warps
+            if (*abort_flag) break;
+            it = it_base + (uint32_t)ntiles;
+        }
+        // nothing may still be landing in shared memory when the CTA exits
+        cp_async_wait_all();
+        if (*abort_flag && lane == 0) {
+            volatile int dummy = 0;
+            for (int j = last_issued - S + 1; j <= last_issued; ++j)
+                if (j >= 0)
+                    mbar_wait(full_bar(j % S), ((uint32_t)j / S) & 1u, &dummy, p.dev_err,
+                              kSpinLimitNs);
+        }
+        return;
+    }
+
+    // ======================================================== consumer warps
+    uint32_t it = 0;
+    for (int k = 0;; ++k) {
+        const int qs = k % NI;
+        if (!mbar_wait(item_full(qs), (uint32_t)(k / NI) & 1u, abort_flag, p.dev_err, kSpinLimitNs))
+            break;
+        const int item = s_item_q[qs];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(item_empty(qs));
+        if (item < 0) break;
+        const int4 i0 = items[2 * item], i1 = items[2 * item + 1];
+        const int b = i0.x, g = i0.y, split = i0.z, nsplit = i0.w;
+        const int kb = i1.x, ke = i1.y, first_item = i1.z;
+        const int q0 = p.qo_indptr[b];
+        const int c = p.qo_indptr[b + 1] - q0;
+        const int P = p.prefix_lens[b];
+        const int R = c * G;
+        const int t_first = kb / kRowTile, t_last = (ke - 1) / kRowTile;
+        const int ntiles = t_last - t_first + 1;
+        const uint32_t it_base = it;
+
+        // rows gid and gid + 8 of the 16-row MMA tile
+        const int row_lo = gid, row_hi = gid + 8;
+        float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+        float o[D / 8][4];
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[dn][j] = 0.f;
+        {
             // Q as the A operand (rows gid and gid + 8, 16 dims per k-step); rows >= R are 0
             uint32_t qa[D / 16][4];
             {
@@ -360,13 +416,13 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(st));
             }
-        }
-        it_base += (uint32_t)ntiles;
+                }
+        if (*abort_flag) break;
+        it = it_base + (uint32_t)ntiles;
 
-        // merge the four warps' states through shared memory (reusing the stages)
-        __syncthreads();
-        float* wo = reinterpret_cast<float*>(sm + C::kOffStage);  // [4][16][D]
-        if (warp < 4) {
+        // merge the four warps' states through shared memory
+        float* wo = reinterpret_cast<float*>(sm + C::kOffMerge);  // [4][16][D]
+        {
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
         l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
@@ -386,8 +442,8 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 make_float2(o[dn][2], o[dn][3]);
         }
         }
-        __syncthreads();
-        for (int idx = tid; idx < R * D; idx += kRowThreads) {
+        consumer_sync();
+        for (int idx = tid; idx < R * D; idx += kConsumerThreads) {
             const int r = idx / D, d = idx % D;
             float M = -INFINITY;
 #pragma unroll
@@ -415,15 +471,15 @@ __global__ void __launch_bounds__(kRowThreads, 1)
         }
         if (nsplit > 1) {
             __threadfence();
-            __syncthreads();
+            consumer_sync();
             if (tid == 0) {
                 const int prev = atomicAdd(&gcnt[b * p.n_kv_heads + g], 1);
                 s_last = prev == nsplit - 1;
             }
-            __syncthreads();
+            consumer_sync();
             if (s_last) {
                 __threadfence();
-                for (int idx = tid; idx < R * D; idx += kRowThreads) {
+                for (int idx = tid; idx < R * D; idx += kConsumerThreads) {
                     const int r = idx / D, d = idx % D;
                     float M = -INFINITY;
                     for (int sp = 0; sp < nsplit; ++sp)
@@ -431,10 +487,10 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                     float acc = 0.f, lsum = 0.f;
                     if (M != -INFINITY) {
                         for (int sp = 0; sp < nsplit; ++sp) {
-                            const int64_t it = first_item + sp;
-                            const float2 ml = __ldcg(&part_ml[it * kRowMaxRows + r]);
+                            const int64_t ps_i = first_item + sp;
+                            const float2 ml = __ldcg(&part_ml[ps_i * kRowMaxRows + r]);
                             const float e = fast_exp2(ml.x - M);
-                            acc += e * __ldcg(&part_o[(it * kRowMaxRows + r) * D + d]);
+                            acc += e * __ldcg(&part_o[(ps_i * kRowMaxRows + r) * D + d]);
                             lsum += e * ml.y;
                         }
                     }
@@ -447,18 +503,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 if (tid == 0) gcnt[b * p.n_kv_heads + g] = 0;
             }
         }
-        __syncthreads();
-    }
-    // teardown: nothing may still be landing in shared memory when the CTA exits
-    if (warp == 4) {
-        cp_async_wait_all();
-        if (*abort_flag && lane == 0) {
-            volatile int dummy = 0;
-            for (int it = last_issued - S + 1; it <= last_issued; ++it)
-                if (it >= 0)
-                    mbar_wait(full_bar(it % S), ((uint32_t)it / S) & 1u, &dummy, p.dev_err,
-                              kSpinLimitNs);
-        }
+        consumer_sync();
     }
 }
 
