@@ -307,7 +307,7 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 6 * args.steps,
         "clocks": clocks.summary(),
     }
 

@@ -21,6 +21,7 @@ cudaError_t launch_extend_tc(int head_dim, int grid, cudaStream_t stream, const 
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv);
 cudaError_t launch_rows(int head_dim, int grid, cudaStream_t stream, const RowParams& p,
                         const CUtensorMap& tk, const CUtensorMap& tv);
+cudaError_t launch_combine(int head_dim, cudaStream_t stream, const CombineParams& p);
 cudaError_t launch_out_cache_loc(const int32_t* qo_indptr, const int32_t* kv_indptr,
                                  const int32_t* kv_indices, const int32_t* prefix_lens,
                                  int batch, int64_t total_q, int page_size, int64_t num_pages,
@@ -306,6 +307,17 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
         rp.scale_log2 = scale_log2;
         rp.dev_err = dev_err;
         if (launch_rows(head_dim, sms, s, rp, tk, tv) != cudaSuccess) return PCP_ERR_CUDA;
+        // ---- 4. merge split-KV partials (one CTA per split group)
+        CombineParams cp;
+        cp.ws = ws;
+        cp.lay = lay;
+        cp.out = static_cast<uint16_t*>(out);
+        cp.lse = lse;
+        cp.n_q_heads = n_q_heads;
+        cp.n_kv_heads = n_kv_heads;
+        cp.group = group;
+        cp.n_groups = batch * n_kv_heads;
+        if (launch_combine(head_dim, s, cp) != cudaSuccess) return PCP_ERR_CUDA;
     }
     return PCP_OK;
 }

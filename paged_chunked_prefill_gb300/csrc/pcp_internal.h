@@ -47,13 +47,15 @@ struct WsHeader {
 };
 
 // Tensor-core work item: {b, kv head g, first chunk position, cost in KV tiles}
-// Row work item (two int4): {b, g, split, n_splits}, {kv_begin, kv_end, first item of group, 0}
+// Row work item (three int4), fully resolved so the row kernel needs no
+// further metadata: {b, g, split, n_splits}, {kv_begin, kv_end, first partial
+// slot of the group, qo_indptr[b]}, {chunk_len, prefix_len, kv_indptr[b], kv_len}
 
 struct WsLayout {
     size_t header;        // offset of WsHeader
     size_t tc_items;      // int4 [cap_tc]
-    size_t row_items;     // int4 [2 * cap_row]
-    size_t group_cnt;     // int  [cap_groups]
+    size_t row_items;     // int4 [3 * cap_row]
+    size_t group_desc;    // int4 [cap_groups]: {first partial slot, n_splits, q0, chunk_len}
     size_t partial_o;     // float [cap_row * kRowMaxRows * head_dim]
     size_t partial_ml;    // float2 [cap_row * kRowMaxRows]
     size_t total;
@@ -81,9 +83,9 @@ inline bool ws_layout(int batch, int64_t total_q, int n_q_heads, int n_kv_heads,
     L->tc_items = off = align_up(off, 256);
     off += (size_t)(L->cap_tc > 0 ? L->cap_tc : 1) * 16;
     L->row_items = off = align_up(off, 256);
-    off += (size_t)L->cap_row * 32;
-    L->group_cnt = off = align_up(off, 256);
-    off += (size_t)(L->cap_groups > 0 ? L->cap_groups : 1) * 4;
+    off += (size_t)L->cap_row * 48;
+    L->group_desc = off = align_up(off, 256);
+    off += (size_t)(L->cap_groups > 0 ? L->cap_groups : 1) * 16;
     L->partial_o = off = align_up(off, 256);
     off += (size_t)L->cap_row * kRowMaxRows * head_dim * 4;
     L->partial_ml = off = align_up(off, 256);
@@ -132,6 +134,18 @@ struct TcParams {
     int window;
     float scale_log2;  // sm_scale * log2(e)
     int32_t* dev_err;
+};
+
+// ---- parameters of the split-KV combine kernel
+struct CombineParams {
+    const unsigned char* ws;
+    WsLayout lay;
+    uint16_t* out;
+    float* lse;
+    int n_q_heads;
+    int n_kv_heads;
+    int group;
+    int n_groups;      // batch * n_kv_heads
 };
 
 // ---- parameters of the row (split-KV) kernel

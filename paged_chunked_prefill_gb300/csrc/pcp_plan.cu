@@ -11,8 +11,9 @@
 //    for the persistent kernel's dynamic scheduler -- with a counting sort.
 //  * row items for decode-shaped chunks (chunk_len * G <= 16 rows): the KV
 //    range of each (sequence, KV head) is split into pieces of
-//    `tiles_per_split` 128-key tiles, chosen so the whole call has about
-//    three items per SM, and ordered longest first like the tensor-core
+//    about `tiles_per_split` 128-key tiles (nearly equal parts of the group),
+//    chosen so the whole call has about three items per SM, ordered longest
+//    first like the tensor-core
 //    items.  Each split owns a partial slot (the group's first slot + split
 //    index) for the log-sum-exp combine.  This is the split-KV idea of the
 //    AstrAI paged decode kernel (split count from the SM count, partials
@@ -44,6 +45,12 @@ __device__ __forceinline__ SeqInfo seq_info(const PlanParams& p, int b) {
 // First visible key of absolute position `pos`.
 __device__ __forceinline__ int first_key(int pos, int window) {
     return window > 0 ? max(0, pos - window + 1) : 0;
+}
+
+// Tiles [split_end(sp - 1), split_end(sp)) of a group's `tiles` form split sp:
+// ns nearly equal parts (lengths differ by at most one).
+__device__ __forceinline__ int split_end(int tiles, int ns, int sp) {
+    return (int)(((int64_t)(sp + 1) * tiles) / ns);
 }
 
 __device__ __forceinline__ int tc_cost(int P, int c, int k, int item_pos, int window) {
@@ -83,136 +90,220 @@ __device__ __forceinline__ int desc_offsets(int* hist, int* warp_sums) {
     return total;
 }
 
+// Exclusive prefix sum of a[0..1023] into a[0..1024] (a[1024] = total);
+// returns the total.  1024 threads.
+__device__ __forceinline__ int excl_scan(int* a, int* warp_sums) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int own = a[tid];
+    int v = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_sums[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        int x = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += n;
+        }
+        warp_sums[32 + lane] = x;
+    }
+    __syncthreads();
+    a[tid] = (w > 0 ? warp_sums[32 + w - 1] : 0) + v - own;
+    const int total = warp_sums[32 + 31];
+    if (tid == 0) a[1024] = total;
+    __syncthreads();
+    return total;
+}
+
+// Position of flattened index f among segments with exclusive starts a[0..n]:
+// the last s with a[s] <= f.
+__device__ __forceinline__ int segment_of(const int* a, int n, int f) {
+    int lo = 0, hi = n;  // answer in [lo, hi)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] <= f) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// atomicAdd(&base[key], inc) for every active lane, one atomic per distinct
+// key in the warp; returns this lane's old value (lanes with the same key
+// get consecutive ranges).
+__device__ __forceinline__ int warp_agg_add(int* base, int key, int inc) {
+    const unsigned act = __activemask();
+    const unsigned same = __match_any_sync(act, key);
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(same) - 1;
+    const int rank = __popc(same & ((1u << lane) - 1));
+    int old = 0;
+    if (lane == leader) old = atomicAdd(&base[key], inc * __popc(same));
+    old = __shfl_sync(same, old, leader);
+    return old + rank * inc;
+}
+
 }  // namespace
 
+// Sequences are processed in chunks of 1024 (one per thread); within a chunk
+// the per-sequence items and splits are flattened across all threads through
+// prefix sums, so a long chunk does not serialise on one thread.
 __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanParams p) {
     __shared__ int hist[1024];
     __shared__ int hist_r[1024];
     __shared__ int warp_sums[64];
+    __shared__ int s_a[1025];       // per-sequence counts, then their exclusive prefix
+    __shared__ int s_b[1025];
+    __shared__ int4 s_seq[1024];    // {c, P, ok, row tiles}
     __shared__ unsigned long long s_row_tiles;
-    __shared__ int s_rows;
     __shared__ int s_tps;
-    __shared__ int4 s_seq[1024];  // {c, P, ok} of the first 1024 sequences
 
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
     int4* tc = reinterpret_cast<int4*>(p.ws + p.lay.tc_items);
     int4* rows = reinterpret_cast<int4*>(p.ws + p.lay.row_items);
-    int* gcnt = reinterpret_cast<int*>(p.ws + p.lay.group_cnt);
-    const int tid = threadIdx.x, nt = blockDim.x;
+    int4* gdesc = reinterpret_cast<int4*>(p.ws + p.lay.group_desc);
+    const int tid = threadIdx.x, lane = tid & 31;
     const int item_pos = q_positions_per_tile(p.group) * kQTiles;
     const int rmax = row_path_max_chunk(p.group);
     const int H = p.n_kv_heads;
 
-    for (int i = tid; i < 1024; i += nt) hist[i] = hist_r[i] = 0;
-    // the metadata is read from global memory once; later passes use shared memory
-    for (int b = tid; b < min(p.batch, 1024); b += nt) {
-        const SeqInfo q = seq_info(p, b);
-        s_seq[b] = make_int4(q.c, q.P, q.ok ? 1 : 0, 0);
-    }
-    auto get_seq = [&](int b) {
-        if (b >= 1024) return seq_info(p, b);
-        const int4 v = s_seq[b];
-        SeqInfo q;
-        q.c = v.x;
-        q.P = v.y;
-        q.L = v.x + v.y;
-        q.ok = v.z != 0;
-        return q;
-    };
-    for (int64_t i = tid; i < (int64_t)p.batch * H; i += nt) gcnt[i] = 0;
+    hist[tid] = 0;
+    hist_r[tid] = 0;
+    for (int64_t i = tid; i < (int64_t)p.batch * H; i += 1024) gdesc[i] = make_int4(0, 0, 0, 0);
     if (tid == 0) {
         s_row_tiles = 0;
-        s_rows = 0;
         if (p.batch > 0 && p.qo_indptr[p.batch] != p.total_q)
             report_error(p.dev_err, PCP_ERR_INVALID_ARG);
     }
-    __syncthreads();
 
-    // pass 1: validate, histogram of tensor-core costs, total row-path tiles
-    for (int b = tid; b < p.batch; b += nt) {
-        const SeqInfo s = get_seq(b);
-        if (!s.ok) {
-            report_error(p.dev_err, PCP_ERR_INVALID_ARG);
-            continue;
+    // metadata of sequence chunk0 + tid (kept in s_seq); reports bad sequences once
+    auto load_chunk = [&](int chunk0, bool report) {
+        const int b = chunk0 + tid;
+        int4 v = make_int4(0, 0, 0, 0);
+        if (b < p.batch) {
+            const SeqInfo q = seq_info(p, b);
+            if (!q.ok && report) report_error(p.dev_err, PCP_ERR_INVALID_ARG);
+            const int tiles = (q.ok && q.c > 0 && q.c <= rmax)
+                                  ? (q.L - 1) / kRowTile - first_key(q.P, p.window) / kRowTile + 1
+                                  : 0;
+            v = make_int4(q.c, q.P, q.ok ? 1 : 0, tiles);
         }
-        if (s.c == 0) continue;
-        if (s.c <= rmax) {
-            const int tiles = (s.L - 1) / kRowTile - first_key(s.P, p.window) / kRowTile + 1;
-            atomicAdd(&s_row_tiles, (unsigned long long)tiles * H);
-        } else {
-            const int n = (s.c + item_pos - 1) / item_pos;
-            for (int k = 0; k < n; ++k)
-                atomicAdd(&hist[min(tc_cost(s.P, s.c, k, item_pos, p.window), 1023)], H);
+        s_seq[tid] = v;
+    };
+    auto n_tc_of = [&](int4 v) {  // tensor-core items of one KV head
+        return (v.z && v.x > rmax) ? (v.x + item_pos - 1) / item_pos : 0;
+    };
+    const bool one_chunk = p.batch <= 1024;
+
+    // ---- sweep 1: tensor-core cost histogram, row-path tile total
+    for (int chunk0 = 0; chunk0 < p.batch; chunk0 += 1024) {
+        __syncthreads();
+        load_chunk(chunk0, true);
+        s_a[tid] = n_tc_of(s_seq[tid]);
+        unsigned long long rt = (unsigned long long)s_seq[tid].w * H;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) rt += __shfl_xor_sync(0xffffffffu, rt, o);
+        if (lane == 0 && rt) atomicAdd(&s_row_tiles, rt);
+        __syncthreads();
+        const int total = excl_scan(s_a, warp_sums);
+        for (int f = tid; f < total; f += 1024) {
+            const int sl = segment_of(s_a, 1024, f);
+            const int4 v = s_seq[sl];
+            const int cost = tc_cost(v.y, v.x, f - s_a[sl], item_pos, p.window);
+            warp_agg_add(hist, min(cost, 1023), H);
         }
     }
     __syncthreads();
-
-    // descending exclusive offsets of the cost histogram
     const int n_tc = desc_offsets(hist, warp_sums);
     if (tid == 0) {
         const unsigned long long tot = s_row_tiles;
         const int target = min(3 * max(p.sm_count, 1), kRowTargetItems);
-        unsigned long long tps = (tot + target - 1) / target;
+        const unsigned long long tps = (tot + target - 1) / target;
         s_tps = (int)(tps < 1 ? 1 : tps);
     }
     __syncthreads();
     const int tps = s_tps;
+    auto ns_of = [&](int4 v) { return v.w > 0 ? (v.w + tps - 1) / tps : 0; };
 
-    // histogram of row-item lengths (tiles), for longest-first order
-    for (int b = tid; b < p.batch; b += nt) {
-        const SeqInfo s = get_seq(b);
-        if (!s.ok || s.c == 0 || s.c > rmax) continue;
-        const int tiles = (s.L - 1) / kRowTile - first_key(s.P, p.window) / kRowTile + 1;
-        const int ns = (tiles + tps - 1) / tps;
-        if (ns > 1) atomicAdd(&hist_r[min(tps, 1023)], (ns - 1) * H);
-        atomicAdd(&hist_r[min(tiles - (ns - 1) * tps, 1023)], H);
+    // ---- sweep 2: histogram of row-item lengths (for longest-first order)
+    for (int chunk0 = 0; chunk0 < p.batch; chunk0 += 1024) {
+        __syncthreads();
+        if (!one_chunk) load_chunk(chunk0, false);
+        s_b[tid] = ns_of(s_seq[tid]);
+        __syncthreads();
+        const int total = excl_scan(s_b, warp_sums);
+        for (int f = tid; f < total; f += 1024) {
+            const int sl = segment_of(s_b, 1024, f);
+            const int tiles = s_seq[sl].w, ns = s_b[sl + 1] - s_b[sl], sp = f - s_b[sl];
+            const int len = split_end(tiles, ns, sp) - split_end(tiles, ns, sp - 1);
+            warp_agg_add(hist_r, min(len, 1023), H);
+        }
     }
     __syncthreads();
-    desc_offsets(hist_r, warp_sums);
+    const int n_row = desc_offsets(hist_r, warp_sums);
 
-    // pass 2: scatter tensor-core items, emit row items
-    for (int b = tid; b < p.batch; b += nt) {
-        const SeqInfo s = get_seq(b);
-        if (!s.ok || s.c == 0) continue;
-        if (s.c <= rmax) {
-            const int lo = first_key(s.P, p.window);
-            const int t0 = lo / kRowTile, t1 = (s.L - 1) / kRowTile;
-            const int tiles = t1 - t0 + 1;
-            const int ns = (tiles + tps - 1) / tps;
+    // ---- sweep 3: scatter tensor-core items and row items
+    int slot_base = 0;  // partial slots used by earlier chunks
+    for (int chunk0 = 0; chunk0 < p.batch; chunk0 += 1024) {
+        __syncthreads();
+        if (!one_chunk) load_chunk(chunk0, false);
+        s_a[tid] = n_tc_of(s_seq[tid]);
+        s_b[tid] = ns_of(s_seq[tid]);
+        __syncthreads();
+        const int total_a = excl_scan(s_a, warp_sums);
+        const int total_b = excl_scan(s_b, warp_sums);
+        for (int f = tid; f < total_a; f += 1024) {
+            const int sl = segment_of(s_a, 1024, f);
+            const int4 v = s_seq[sl];
+            const int k = f - s_a[sl];
+            const int cost = tc_cost(v.y, v.x, k, item_pos, p.window);
+            const int slot = warp_agg_add(hist, min(cost, 1023), H);
             for (int g = 0; g < H; ++g) {
-                const int base = atomicAdd(&s_rows, ns);  // the group's partial slots
-                for (int sp = 0; sp < ns; ++sp) {
-                    const int len = min(tps, tiles - sp * tps);
-                    const int it = atomicAdd(&hist_r[min(len, 1023)], 1);
-                    if (it >= p.lay.cap_row || base + sp >= p.lay.cap_row) {
-                        report_error(p.dev_err, PCP_ERR_WORKSPACE);
-                        break;
-                    }
-                    const int kb = max(lo, (t0 + sp * tps) * kRowTile);
-                    const int ke = min(s.L, (t0 + (sp + 1) * tps) * kRowTile);
-                    rows[2 * it] = make_int4(b, g, sp, ns);
-                    rows[2 * it + 1] = make_int4(kb, ke, base, 0);
+                if (slot + g >= p.lay.cap_tc) {
+                    report_error(p.dev_err, PCP_ERR_WORKSPACE);
+                    break;
                 }
-            }
-        } else {
-            const int n = (s.c + item_pos - 1) / item_pos;
-            for (int k = 0; k < n; ++k) {
-                const int cost = tc_cost(s.P, s.c, k, item_pos, p.window);
-                const int slot = atomicAdd(&hist[min(cost, 1023)], H);
-                for (int g = 0; g < H; ++g) {
-                    if (slot + g >= p.lay.cap_tc) {
-                        report_error(p.dev_err, PCP_ERR_WORKSPACE);
-                        break;
-                    }
-                    tc[slot + g] = make_int4(b, g, k * item_pos, cost);
-                }
+                tc[slot + g] = make_int4(chunk0 + sl, g, k * item_pos, cost);
             }
         }
+        for (int f = tid; f < total_b; f += 1024) {
+            const int sl = segment_of(s_b, 1024, f);
+            const int b = chunk0 + sl;
+            const int4 v = s_seq[sl];
+            const int tiles = v.w, ns = s_b[sl + 1] - s_b[sl], sp = f - s_b[sl];
+            const int P = v.y, L = v.x + v.y;
+            const int lo = first_key(P, p.window);
+            const int t0 = lo / kRowTile;
+            const int tb = t0 + split_end(tiles, ns, sp - 1);
+            const int te = t0 + split_end(tiles, ns, sp);
+            const int kb = max(lo, tb * kRowTile);
+            const int ke = min(L, te * kRowTile);
+            const int q0 = p.qo_indptr[b];
+            const int kvb = p.kv_indptr[b];
+            const int it = warp_agg_add(hist_r, min(te - tb, 1023), H);
+            for (int g = 0; g < H; ++g) {
+                // the group's partial slots are consecutive: base + split
+                const int base = slot_base + s_b[sl] * H + g * ns;
+                if (it + g >= p.lay.cap_row || base + ns > p.lay.cap_row) {
+                    report_error(p.dev_err, PCP_ERR_WORKSPACE);
+                    break;
+                }
+                if (sp == 0) gdesc[(int64_t)b * H + g] = make_int4(base, ns, q0, v.x);
+                rows[3 * (it + g)] = make_int4(b, g, sp, ns);
+                rows[3 * (it + g) + 1] = make_int4(kb, ke, base, q0);
+                rows[3 * (it + g) + 2] = make_int4(v.x, P, kvb, L);
+            }
+        }
+        slot_base += total_b * H;
     }
     __syncthreads();
     if (tid == 0) {
         hdr->n_tc_items = (int)min((int64_t)n_tc, p.lay.cap_tc);
-        hdr->n_row_items = (int)min((int64_t)s_rows, p.lay.cap_row);
+        hdr->n_row_items = (int)min((int64_t)n_row, p.lay.cap_row);
         hdr->tc_next = 0;
         hdr->row_next = 0;
         hdr->tiles_per_split = tps;

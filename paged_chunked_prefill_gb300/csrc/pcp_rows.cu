@@ -5,9 +5,10 @@
 // K/V pages, not by arithmetic.  The KV range of each (sequence, KV head) is
 // split across CTAs (AstrAI paged decode "split-KV" kernel, prior art); each
 // split writes an fp32 partial (unnormalised O, running max, normaliser) to
-// the workspace and the last split to finish merges the partials with the
-// log-sum-exp identity (the AstrAI combine kernel's job, fused here so a
-// mixed batch needs no extra launch).  Masking is the same bottom-right
+// the workspace and combine_kernel merges the partials with the log-sum-exp
+// identity afterwards (the AstrAI combine kernel's job).  Merging inside the
+// last split to finish was tried: its dependent L2 reads stalled that SM's
+// load pipeline for ~10 us per group.  Masking is the same bottom-right
 // causal / window rule as the tensor-core path, per row.
 //
 // Layout: one CTA per SM, 4 consumer warps and 1 load warp, a ring of
@@ -34,10 +35,13 @@ struct RowCfg {
     static constexpr int kHalfBytes = kRowTile * 128;            // one 64-column block
     static constexpr int kTileBytes = kRowTile * D * 2;          // a K or a V tile
     static constexpr int kStages = D == 128 ? 3 : 5;
+    static constexpr int kItemSlots = 2;
+    static constexpr int kQStride = D * 2 + 16;                  // padded Q row (bytes)
     static constexpr int kOffStage = 0;                          // [stage][K | V]
-    static constexpr int kOffMerge = kOffStage + kStages * 2 * kTileBytes;  // float [4][16][D]
-    static constexpr int kOffBar = kOffMerge + 4 * kRowMaxRows * D * 4;
-    static constexpr int kOffM = kOffBar + (2 * kStages + 4) * 8;  // float [4][16] m, then l
+    static constexpr int kOffQ = kOffStage + kStages * 2 * kTileBytes;  // [slot][16][kQStride]
+    static constexpr int kOffDesc = kOffQ + kItemSlots * kRowMaxRows * kQStride;  // int4 [slot][3]
+    static constexpr int kOffBar = kOffDesc + kItemSlots * 48;
+    static constexpr int kOffM = kOffBar + (2 * kStages + 2 * kItemSlots) * 8;  // float [4][16] m, l
     static constexpr int kSmemBytes = kOffM + 2 * 4 * kRowMaxRows * 4 + 64 + 1024;
 };
 
@@ -79,7 +83,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v) {
     using C = RowCfg<D>;
     constexpr int S = C::kStages;
-    constexpr int NI = 2;                      // item hand-off slots
+    constexpr int NI = C::kItemSlots;
     constexpr int kConsumerThreads = 128;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -87,8 +91,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     uint8_t* sm = smem_raw + (base - raw);
     float* m_s = reinterpret_cast<float*>(sm + C::kOffM);
     float* l_s = m_s + 4 * kRowMaxRows;
-    __shared__ volatile int s_item_q[NI];
-    __shared__ int s_last;
+    int4* s_desc = reinterpret_cast<int4*>(sm + C::kOffDesc);  // published by mbarrier
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -98,10 +101,10 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     const int4* items = reinterpret_cast<const int4*>(p.ws + p.lay.row_items);
     float* part_o = reinterpret_cast<float*>(p.ws + p.lay.partial_o);
     float2* part_ml = reinterpret_cast<float2*>(p.ws + p.lay.partial_ml);
-    int* gcnt = reinterpret_cast<int*>(p.ws + p.lay.group_cnt);
     const int G = p.group;
     const float sl2 = p.scale_log2;
     const uint32_t sStage = base + C::kOffStage;
+    const uint32_t sQ = base + C::kOffQ;
     const uint32_t sBar = base + C::kOffBar;
     auto full_bar = [&](int s) { return sBar + 8u * (uint32_t)s; };
     auto empty_bar = [&](int s) { return sBar + 8u * (uint32_t)(S + s); };
@@ -111,7 +114,16 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     // the four consumer warps only (named barrier 1)
     auto consumer_sync = [] { asm volatile("bar.sync 1, 128;" ::: "memory"); };
 
-    if (n_items == 0) return;
+    // Items come from the longest-first list in snake order (round k takes
+    // position blockIdx.x of the k-th block of gridDim.x items, mirrored on odd
+    // rounds), which balances large and small items across CTAs; the load
+    // warp knows the next item in advance and reads its descriptor and first
+    // page ids during this one.
+    auto item_of = [&](int k) {
+        const int in_round = (k & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+        return k * (int)gridDim.x + in_round;
+    };
+    if ((int)blockIdx.x >= n_items) return;
     if (tid == 0) {
         const uint32_t full_count = p.box_rows > 0 ? 1u : 32u;
         for (int s = 0; s < S; ++s) {
@@ -119,7 +131,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
             mbar_init(empty_bar(s), 4);
         }
         for (int s = 0; s < NI; ++s) {
-            mbar_init(item_full(s), 1);
+            mbar_init(item_full(s), 33);  // 32 lanes' Q copies + the descriptor
             mbar_init(item_empty(s), 4);
         }
         fence_mbarrier_init();
@@ -129,75 +141,93 @@ __global__ void __launch_bounds__(kRowThreads, 1)
 
     if (warp == 4) {
         // ==================================================== load warp
-        // It takes items from the device counter, hands each to the consumer
-        // warps through the item queue, and streams its K/V tiles through the
-        // stage ring without waiting for the consumers to finish the previous
-        // item, so the next item's first tiles load during this one's merge.
-        uint32_t it = 0;       // ring position
-        int last_issued = -1;
-        for (int k = 0;; ++k) {
-            const int qs = k % NI;
-            int item = 0;
-            if (lane == 0) item = atomicAdd(&hdr->row_next, 1);
-            item = __shfl_sync(0xffffffffu, item, 0);
-            if (item >= n_items || *abort_flag) item = -1;
-            if (!mbar_wait(item_empty(qs), ((uint32_t)(k / NI) & 1u) ^ 1u, abort_flag, p.dev_err,
-                           kSpinLimitNs))
-                break;
-            if (lane == 0) {
-                s_item_q[qs] = item;
-                mbar_arrive(item_full(qs));
-            }
-            if (item < 0) break;
-            const int4 i0 = items[2 * item], i1 = items[2 * item + 1];
-            const int b = i0.x, g = i0.y;
-            const int kb = i1.x, ke = i1.y;
-            const int q0 = p.qo_indptr[b];
-            const int L = p.prefix_lens[b] + (p.qo_indptr[b + 1] - q0);
-            const int t_first = kb / kRowTile, t_last = (ke - 1) / kRowTile;
-            const int ntiles = t_last - t_first + 1;
-            const uint32_t it_base = it;
-            const int32_t* pages = p.kv_indices + p.kv_indptr[b];
-            const int ps = p.page_size;
-            // slot (TMA: first slot of this lane's page run; gather: slots of
-            // rows lane + 32k) for a tile, read one tile ahead
-            auto fetch = [&](int t, int (&sl)[4]) {
-    #pragma unroll
-                for (int k = 0; k < 4; ++k) sl[k] = -1;
-                if (t > t_last) return;
-                if (p.box_rows > 0) {
-                    const int nsub = kRowTile / p.box_rows;
-                    const int key = t * kRowTile + (lane % nsub) * p.box_rows;
-                    sl[0] = p.num_slots;
-                    if (lane < nsub * C::kHalves && key < L) {
+        const int ps = p.page_size;
+        // slot (TMA: first slot of this lane's page run; gather: slots of
+        // rows lane + 32k) of tile t of a sequence with page list `pages`
+        auto fetch = [&](const int32_t* pages, int L, int t, int (&sl)[4]) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sl[k] = -1;
+            if (p.box_rows > 0) {
+                const int nsub = kRowTile / p.box_rows;
+                const int key = t * kRowTile + (lane % nsub) * p.box_rows;
+                sl[0] = p.num_slots;
+                if (lane < nsub * C::kHalves && key < L) {
+                    const int page = pages[key / ps];
+                    if (page >= 0 && page < p.num_pages)
+                        sl[0] = page * ps + key % ps;
+                    else
+                        report_error(p.dev_err, PCP_ERR_BAD_INDEX);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int key = t * kRowTile + lane + 32 * k;
+                    if (key < L) {
                         const int page = pages[key / ps];
                         if (page >= 0 && page < p.num_pages)
-                            sl[0] = page * ps + key % ps;
+                            sl[k] = page * ps + key % ps;
                         else
                             report_error(p.dev_err, PCP_ERR_BAD_INDEX);
                     }
-                } else {
-    #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int key = t * kRowTile + lane + 32 * k;
-                        if (key < L) {
-                            const int page = pages[key / ps];
-                            if (page >= 0 && page < p.num_pages)
-                                sl[k] = page * ps + key % ps;
-                            else
-                                report_error(p.dev_err, PCP_ERR_BAD_INDEX);
-                        }
-                    }
                 }
-            };
-            int cur_sl[4], next_sl[4];
-            fetch(t_first, cur_sl);
+            }
+        };
+        uint32_t it = 0;  // ring position
+        int last_issued = -1;
+        int item = item_of(0);
+        int4 n0 = items[3 * item], n1 = items[3 * item + 1], n2 = items[3 * item + 2];
+        int next_sl[4];
+        fetch(p.kv_indices + n2.z, n2.w, n1.x / kRowTile, next_sl);
+        for (int k = 0;; ++k, item = item_of(k)) {
+            const int qs = k % NI;
+            const bool valid = item < n_items && !*abort_flag;
+            const int4 d0 = n0, d1 = n1, d2 = n2;
+            int cur_sl[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) cur_sl[j] = next_sl[j];
+            const int next_item = item_of(k + 1);
+            const bool next_valid = valid && next_item < n_items;
+            if (next_valid) {  // loads in flight during this item
+                n0 = items[3 * next_item];
+                n1 = items[3 * next_item + 1];
+                n2 = items[3 * next_item + 2];
+            }
+            // hand the item (or the end marker) and its Q rows to the consumers
+            if (!mbar_wait(item_empty(qs), ((uint32_t)(k / NI) & 1u) ^ 1u, abort_flag, p.dev_err,
+                           kSpinLimitNs))
+                break;
+            const int g = d0.y;
+            if (valid) {
+                const int R = d2.x * G;
+                const uint32_t qd = sQ + qs * kRowMaxRows * C::kQStride;
+                for (int idx = lane; idx < kRowMaxRows * (D / 8); idx += 32) {
+                    const int r = idx / (D / 8), cc = idx % (D / 8);
+                    const bool ok = r < R;
+                    const uint16_t* src =
+                        ok ? p.q + ((int64_t)(d1.w + r / G) * p.n_q_heads + g * G + r % G) * D + cc * 8
+                           : p.q;
+                    cp_async_16(qd + r * C::kQStride + cc * 16, src, ok ? 16u : 0u);
+                }
+            }
+            cp_async_mbar_arrive_noinc(item_full(qs));
+            if (lane == 0) {
+                s_desc[qs * 3 + 0] = valid ? d0 : make_int4(-1, 0, 0, 0);
+                s_desc[qs * 3 + 1] = d1;
+                s_desc[qs * 3 + 2] = d2;
+                mbar_arrive(item_full(qs));
+            }
+            if (!valid) break;
+            const int kb = d1.x, ke = d1.y, L = d2.w;
+            const int32_t* pages = p.kv_indices + d2.z;
+            const int t_first = kb / kRowTile, t_last = (ke - 1) / kRowTile;
+            const int ntiles = t_last - t_first + 1;
             for (int i = 0; i < ntiles; ++i) {
                 const int t = t_first + i;
-                const uint32_t it = it_base + i;
-                const int st = it % S;
-                fetch(t + 1, next_sl);
-                if (!mbar_wait(empty_bar(st), ((it / S) & 1u) ^ 1u, abort_flag, p.dev_err,
+                const uint32_t itp = it + i;
+                const int st = itp % S;
+                int nsl[4];
+                if (i + 1 < ntiles) fetch(pages, L, t + 1, nsl);
+                if (!mbar_wait(empty_bar(st), ((itp / S) & 1u) ^ 1u, abort_flag, p.dev_err,
                                kSpinLimitNs))
                     break;
                 const uint32_t kd = sStage + st * 2 * C::kTileBytes;
@@ -227,23 +257,24 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive_expect_tx(
-                            full_bar(st), (uint32_t)(2 * nloads - (strad >= 0 ? C::kHalves : 0)) * br * 128);
+                            full_bar(st),
+                            (uint32_t)(2 * nloads - (strad >= 0 ? C::kHalves : 0)) * br * 128);
                     __syncwarp();
                     if (lane < nloads) {
                         const int sb = lane % nsub, h = lane / nsub;
                         tma_load_3d(kd + h * C::kHalfBytes + sb * br * 128, &tm_k, full_bar(st),
                                     h * 64, g, cur_sl[0]);
                         if (sb != strad)
-                            tma_load_3d(vd + h * C::kHalfBytes + sb * br * 128, &tm_v, full_bar(st),
-                                        h * 64, g, cur_sl[0]);
+                            tma_load_3d(vd + h * C::kHalfBytes + sb * br * 128, &tm_v,
+                                        full_bar(st), h * 64, g, cur_sl[0]);
                     }
                 } else {
-    #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int row = lane + 32 * k;
-                        const bool ok = cur_sl[k] >= 0;
-                        const int64_t off = ((int64_t)(ok ? cur_sl[k] : 0) * p.n_kv_heads + g) * D;
-    #pragma unroll
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int row = lane + 32 * j;
+                        const bool ok = cur_sl[j] >= 0;
+                        const int64_t off = ((int64_t)(ok ? cur_sl[j] : 0) * p.n_kv_heads + g) * D;
+#pragma unroll
                         for (int cc = 0; cc < C::kHalves * 8; ++cc) {
                             cp_async_16(kd + swz<D>(row, cc * 8), p.k_pool + off + cc * 8, ok ? 16u : 0u);
                             cp_async_16(vd + swz<D>(row, cc * 8), p.v_pool + off + cc * 8, ok ? 16u : 0u);
@@ -251,12 +282,15 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                     }
                     cp_async_mbar_arrive_noinc(full_bar(st));
                 }
-                last_issued = (int)it;
-    #pragma unroll
-                for (int k = 0; k < 4; ++k) cur_sl[k] = next_sl[k];
+                last_issued = (int)itp;
+                if (i == 0 && next_valid)  // the next item's first page ids
+                    fetch(p.kv_indices + n2.z, n2.w, n1.x / kRowTile, next_sl);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (i + 1 < ntiles) cur_sl[j] = nsl[j];
             }
             if (*abort_flag) break;
-            it = it_base + (uint32_t)ntiles;
+            it += (uint32_t)ntiles;
         }
         // nothing may still be landing in shared memory when the CTA exits
         cp_async_wait_all();
@@ -276,55 +310,49 @@ __global__ void __launch_bounds__(kRowThreads, 1)
         const int qs = k % NI;
         if (!mbar_wait(item_full(qs), (uint32_t)(k / NI) & 1u, abort_flag, p.dev_err, kSpinLimitNs))
             break;
-        const int item = s_item_q[qs];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(item_empty(qs));
-        if (item < 0) break;
-        const int4 i0 = items[2 * item], i1 = items[2 * item + 1];
-        const int b = i0.x, g = i0.y, split = i0.z, nsplit = i0.w;
-        const int kb = i1.x, ke = i1.y, first_item = i1.z;
-        const int q0 = p.qo_indptr[b];
-        const int c = p.qo_indptr[b + 1] - q0;
-        const int P = p.prefix_lens[b];
-        const int R = c * G;
+        const int4 d0 = s_desc[qs * 3 + 0];
+        const int4 d1 = s_desc[qs * 3 + 1];
+        const int4 d2 = s_desc[qs * 3 + 2];
+        if (d0.x < 0) break;
+        const int g = d0.y, split = d0.z, nsplit = d0.w;
+        const int kb = d1.x, ke = d1.y, first_item = d1.z, q0 = d1.w;
+        const int P = d2.y;
+        const int R = d2.x * G;
         const int t_first = kb / kRowTile, t_last = (ke - 1) / kRowTile;
         const int ntiles = t_last - t_first + 1;
-        const uint32_t it_base = it;
 
-        // rows gid and gid + 8 of the 16-row MMA tile
+        // Q as the A operand (rows gid and gid + 8, 16 dims per k-step), from
+        // the item slot; rows >= R were zero-filled
         const int row_lo = gid, row_hi = gid + 8;
+        uint32_t qa[D / 16][4];
+        {
+            const uint32_t qb = sQ + qs * kRowMaxRows * C::kQStride;
+            const int qrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                ldsm_x4(qb + qrow * C::kQStride + (kk * 16 + (lane >> 4) * 8) * 2, qa[kk][0],
+                        qa[kk][1], qa[kk][2], qa[kk][3]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(item_empty(qs));
+        const int pos_lo = P + row_lo / G, pos_hi = P + row_hi / G;
         float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
         float o[D / 8][4];
 #pragma unroll
         for (int dn = 0; dn < D / 8; ++dn)
 #pragma unroll
             for (int j = 0; j < 4; ++j) o[dn][j] = 0.f;
-        {
-            // Q as the A operand (rows gid and gid + 8, 16 dims per k-step); rows >= R are 0
-            uint32_t qa[D / 16][4];
-            {
-                const uint16_t* qlo = row_lo < R
-                    ? p.q + ((int64_t)(q0 + row_lo / G) * p.n_q_heads + g * G + row_lo % G) * D
-                    : nullptr;
-                const uint16_t* qhi = row_hi < R
-                    ? p.q + ((int64_t)(q0 + row_hi / G) * p.n_q_heads + g * G + row_hi % G) * D
-                    : nullptr;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const int d0 = kk * 16 + tig * 2;
-                    qa[kk][0] = qlo ? *reinterpret_cast<const uint32_t*>(qlo + d0) : 0u;
-                    qa[kk][1] = qhi ? *reinterpret_cast<const uint32_t*>(qhi + d0) : 0u;
-                    qa[kk][2] = qlo ? *reinterpret_cast<const uint32_t*>(qlo + d0 + 8) : 0u;
-                    qa[kk][3] = qhi ? *reinterpret_cast<const uint32_t*>(qhi + d0 + 8) : 0u;
-                }
+
+        int last_st = 0;
+        bool ok = true;
+        for (int i = 0; i < ntiles; ++i) {
+            const int t = t_first + i;
+            const uint32_t itp = it + i;
+            const int st = itp % S;
+            if (!mbar_wait(full_bar(st), (itp / S) & 1u, abort_flag, p.dev_err, kSpinLimitNs)) {
+                ok = false;
+                break;
             }
-            const int pos_lo = P + row_lo / G, pos_hi = P + row_hi / G;
-            for (int i = 0; i < ntiles; ++i) {
-                const int t = t_first + i;
-                const uint32_t it = it_base + i;
-                const int st = it % S;
-                if (!mbar_wait(full_bar(st), (it / S) & 1u, abort_flag, p.dev_err, kSpinLimitNs))
-                    break;
                 const uint32_t kbase = sStage + st * 2 * C::kTileBytes;
                 const uint32_t vbase = kbase + C::kTileBytes;
                 const int key_w = t * kRowTile + warp * 32;
@@ -413,15 +441,20 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                         mma_16816(o[2 * dn2], pa[bl], v0, v1);
                         mma_16816(o[2 * dn2 + 1], pa[bl], v2, v3);
                     }
+            if (i + 1 < ntiles) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(st));
+            } else {
+                last_st = st;
             }
-                }
-        if (*abort_flag) break;
-        it = it_base + (uint32_t)ntiles;
+        }
+        if (!ok) break;
+        it += (uint32_t)ntiles;
 
-        // merge the four warps' states through shared memory
-        float* wo = reinterpret_cast<float*>(sm + C::kOffMerge);  // [4][16][D]
+        // merge the four warps' states through shared memory: the stage of
+        // this item's last tile, whose release waits until the merge is done
+        float* wo = reinterpret_cast<float*>(sm + C::kOffStage + last_st * 2 * C::kTileBytes);
+        consumer_sync();
         {
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
@@ -469,42 +502,86 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                     part_ml[(int64_t)(first_item + split) * kRowMaxRows + r] = make_float2(M, lsum);
             }
         }
-        if (nsplit > 1) {
-            __threadfence();
-            consumer_sync();
-            if (tid == 0) {
-                const int prev = atomicAdd(&gcnt[b * p.n_kv_heads + g], 1);
-                s_last = prev == nsplit - 1;
-            }
-            consumer_sync();
-            if (s_last) {
-                __threadfence();
-                for (int idx = tid; idx < R * D; idx += kConsumerThreads) {
-                    const int r = idx / D, d = idx % D;
-                    float M = -INFINITY;
-                    for (int sp = 0; sp < nsplit; ++sp)
-                        M = fmaxf(M, __ldcg(&part_ml[(int64_t)(first_item + sp) * kRowMaxRows + r]).x);
-                    float acc = 0.f, lsum = 0.f;
-                    if (M != -INFINITY) {
-                        for (int sp = 0; sp < nsplit; ++sp) {
-                            const int64_t ps_i = first_item + sp;
-                            const float2 ml = __ldcg(&part_ml[ps_i * kRowMaxRows + r]);
-                            const float e = fast_exp2(ml.x - M);
-                            acc += e * __ldcg(&part_o[(ps_i * kRowMaxRows + r) * D + d]);
-                            lsum += e * ml.y;
-                        }
-                    }
-                    const int64_t orow = (int64_t)(q0 + r / G) * p.n_q_heads + g * G + r % G;
-                    const float v = lsum > 0.f ? acc / lsum : 0.f;
-                    p.out[orow * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-                    if (d == 0 && p.lse != nullptr)
-                        p.lse[orow] = lsum > 0.f ? (M + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
-                }
-                if (tid == 0) gcnt[b * p.n_kv_heads + g] = 0;
-            }
-        }
         consumer_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(last_st));
     }
+}
+
+// Merge the split-KV partials of one (sequence, KV head) group: one CTA per
+// group, out[row, h, :] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s and
+// lse = (M + log2 L) ln 2, with M the largest split maximum (log2 units).
+// Every phase issues its loads independently (one (split, row) pair or one
+// output element per thread), so the kernel costs a few memory latencies.
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams p) {
+    constexpr int kMaxSplits = 64;  // more splits are folded over several passes
+    __shared__ float2 ml_s[kMaxSplits][kRowMaxRows];
+    __shared__ float M_s[kRowMaxRows], L_s[kRowMaxRows];
+    const int4 gd = reinterpret_cast<const int4*>(p.ws + p.lay.group_desc)[blockIdx.x];
+    const int base = gd.x, ns = gd.y, q0 = gd.z;
+    if (ns <= 1) return;
+    const int g = blockIdx.x % p.n_kv_heads;
+    const int G = p.group;
+    const int R = gd.w * G;
+    const float* part_o = reinterpret_cast<const float*>(p.ws + p.lay.partial_o);
+    const float2* part_ml = reinterpret_cast<const float2*>(p.ws + p.lay.partial_ml);
+    const int tid = threadIdx.x;
+    if (tid < kRowMaxRows) {
+        M_s[tid] = -INFINITY;
+        L_s[tid] = 0.f;
+    }
+    for (int s0 = 0; s0 < ns; s0 += kMaxSplits) {
+        const int nb = min(kMaxSplits, ns - s0);
+        __syncthreads();
+        for (int idx = tid; idx < nb * kRowMaxRows; idx += blockDim.x) {
+            const int sp = idx / kRowMaxRows, r = idx % kRowMaxRows;
+            ml_s[sp][r] = r < R ? part_ml[(int64_t)(base + s0 + sp) * kRowMaxRows + r]
+                                : make_float2(-INFINITY, 0.f);
+        }
+        __syncthreads();
+        if (tid < R) {  // running max and normaliser over the splits so far
+            float M = M_s[tid];
+            for (int sp = 0; sp < nb; ++sp) M = fmaxf(M, ml_s[sp][tid].x);
+            float L = M == -INFINITY ? 0.f : L_s[tid] * fast_exp2(M_s[tid] - M);
+            for (int sp = 0; sp < nb; ++sp)
+                if (M != -INFINITY) L += fast_exp2(ml_s[sp][tid].x - M) * ml_s[sp][tid].y;
+            M_s[tid] = M;
+            L_s[tid] = L;
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < R * D; idx += blockDim.x) {
+        const int r = idx / D, d = idx % D;
+        const float M = M_s[r];
+        float acc = 0.f;
+        for (int s0 = 0; s0 < ns; s0 += 8) {
+            float v[8], e[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int sp = s0 + j;
+                v[j] = sp < ns ? part_o[((int64_t)(base + sp) * kRowMaxRows + r) * D + d] : 0.f;
+                const float m = sp < ns ? part_ml[(int64_t)(base + sp) * kRowMaxRows + r].x : -INFINITY;
+                e[j] = (M == -INFINITY || m == -INFINITY) ? 0.f : fast_exp2(m - M);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc += e[j] * v[j];
+        }
+        const float L = L_s[r];
+        const int64_t orow = (int64_t)(q0 + r / G) * p.n_q_heads + g * G + r % G;
+        p.out[orow * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? acc / L : 0.f));
+        if (d == 0 && p.lse != nullptr)
+            p.lse[orow] = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+    }
+}
+
+cudaError_t launch_combine(int head_dim, cudaStream_t stream, const CombineParams& p) {
+    if (p.n_groups <= 0) return cudaSuccess;
+    if (head_dim == 128)
+        combine_kernel<128><<<p.n_groups, 256, 0, stream>>>(p);
+    else
+        combine_kernel<64><<<p.n_groups, 256, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 size_t row_smem_bytes(int head_dim) {
