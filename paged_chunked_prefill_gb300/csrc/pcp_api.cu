@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "pcp.h"
@@ -15,6 +16,11 @@
 #endif
 
 namespace pcp {
+
+bool pdl_enabled() {
+    static const bool on = std::getenv("PCP_DISABLE_PDL") == nullptr;
+    return on;
+}
 
 cudaError_t launch_plan(cudaStream_t stream, const PlanParams& p);
 cudaError_t launch_extend_tc(int head_dim, int grid, cudaStream_t stream, const TcParams& p,

@@ -7,6 +7,7 @@
 // k_buffer[layer, out_cache_loc] = k before attending; here both are kernels.
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
+#include "pcp_launch.h"
 
 namespace pcp {
 
@@ -16,6 +17,8 @@ __global__ void out_cache_loc_kernel(const int32_t* __restrict__ qo_indptr,
                                      const int32_t* __restrict__ prefix_lens, int batch,
                                      int64_t total_q, int page_size, int64_t num_pages,
                                      int64_t* __restrict__ loc, int32_t* dev_err) {
+    pdl_wait();
+    pdl_launch_dependents();
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total_q;
          t += (int64_t)gridDim.x * blockDim.x) {
         // sequence owning row t: the last b with qo_indptr[b] <= t
@@ -47,6 +50,8 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __res
                                  int chunks_per_token, uint4* __restrict__ k_pool,
                                  uint4* __restrict__ v_pool, int64_t pool_slots,
                                  int32_t* dev_err) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t total = n_tokens * chunks_per_token;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -72,10 +77,9 @@ cudaError_t launch_out_cache_loc(const int32_t* qo_indptr, const int32_t* kv_ind
     const int threads = 256;
     int64_t blocks = (total_q + threads - 1) / threads;
     if (blocks > (int64_t)sm_count * 8) blocks = (int64_t)sm_count * 8;
-    out_cache_loc_kernel<<<(int)blocks, threads, 0, stream>>>(qo_indptr, kv_indptr, kv_indices,
-                                                              prefix_lens, batch, total_q,
-                                                              page_size, num_pages, loc, dev_err);
-    return cudaGetLastError();
+    return launch_pdl(out_cache_loc_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                      qo_indptr, kv_indptr, kv_indices, prefix_lens, batch, total_q, page_size,
+                      num_pages, loc, dev_err);
 }
 
 cudaError_t launch_kv_append(const void* k, const void* v, const int64_t* loc, int64_t n_tokens,
@@ -85,11 +89,10 @@ cudaError_t launch_kv_append(const void* k, const void* v, const int64_t* loc, i
     const int64_t total = n_tokens * chunks_per_token;
     int64_t blocks = (total + threads - 1) / threads;
     if (blocks > (int64_t)sm_count * 16) blocks = (int64_t)sm_count * 16;
-    kv_append_kernel<<<(int)blocks, threads, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), loc, n_tokens,
-        chunks_per_token, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), pool_slots,
-        dev_err);
-    return cudaGetLastError();
+    return launch_pdl(kv_append_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                      static_cast<const uint4*>(k), static_cast<const uint4*>(v), loc, n_tokens,
+                      chunks_per_token, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool),
+                      pool_slots, dev_err);
 }
 
 }  // namespace pcp

@@ -27,6 +27,18 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched as a programmatic dependent of the
+// kernel before it on the stream, so its launch and prologue may overlap the
+// end of that kernel.  pdl_wait() returns once the previous kernel has
+// completed and its memory is visible; every kernel calls it on every path
+// before its first global memory access, which keeps the ordering transitive
+// along the whole stream.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // -------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -32,6 +32,7 @@
 //    the CTA drains its copies and MMAs, frees TMEM and exits.
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
+#include "pcp_launch.h"
 
 // Of every 16 consecutive pairs of S columns, this many are exponentiated on
 // the FMA pipe (exp2_poly) and the rest on the MUFU unit, balancing the two.
@@ -239,8 +240,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
-    // a call without tensor-core work (decode rows only) leaves at once
-    if (reinterpret_cast<const WsHeader*>(p.ws + p.lay.header)->n_tc_items == 0) return;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::bQFull), 1);
@@ -266,6 +265,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
     }
+    // the work list is the planner's output
+    pdl_wait();
+    // a call without tensor-core work (decode rows only) leaves at once
+    if (reinterpret_cast<const WsHeader*>(p.ws + p.lay.header)->n_tc_items == 0) return;
     if (warp == kWarpMma) {
         tmem_alloc(smem_addr((const void*)&misc[0]), 512);
         tmem_relinquish();
@@ -629,6 +632,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 
     // ---------------------------------------------------------- teardown
+    // no work left here: the next kernel on the stream may start launching
+    pdl_launch_dependents();
     const bool aborted = *abort_flag != 0;
     if (warp >= kWarpGather0) {
         cp_async_wait_all();
@@ -672,14 +677,16 @@ cudaError_t launch_extend_tc(int head_dim, int grid, cudaStream_t stream, const 
         e = cudaFuncSetAttribute(extend_tc_kernel<128>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        extend_tc_kernel<128><<<grid, kTcThreads, smem, stream>>>(p, tq, tk, tv);
+        e = launch_pdl(extend_tc_kernel<128>, dim3(grid), dim3(kTcThreads), smem, stream, p, tq,
+                       tk, tv);
     } else {
         e = cudaFuncSetAttribute(extend_tc_kernel<64>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        extend_tc_kernel<64><<<grid, kTcThreads, smem, stream>>>(p, tq, tk, tv);
+        e = launch_pdl(extend_tc_kernel<64>, dim3(grid), dim3(kTcThreads), smem, stream, p, tq,
+                       tk, tv);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace pcp

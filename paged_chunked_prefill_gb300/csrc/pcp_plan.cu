@@ -20,6 +20,7 @@
 //    merged by a combine step).
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
+#include "pcp_launch.h"
 
 namespace pcp {
 
@@ -171,6 +172,8 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     const int rmax = row_path_max_chunk(p.group);
     const int H = p.n_kv_heads;
 
+    pdl_wait();
+    pdl_launch_dependents();
     hist[tid] = 0;
     hist_r[tid] = 0;
     for (int64_t i = tid; i < (int64_t)p.batch * H; i += 1024) gdesc[i] = make_int4(0, 0, 0, 0);
@@ -311,8 +314,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
 }
 
 cudaError_t launch_plan(cudaStream_t stream, const PlanParams& p) {
-    plan_kernel<<<1, 1024, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, p);
 }
 
 }  // namespace pcp

@@ -24,6 +24,7 @@
 // the end of each item.
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
+#include "pcp_launch.h"
 
 namespace pcp {
 
@@ -96,6 +97,8 @@ __global__ void __launch_bounds__(kRowThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
+    pdl_wait();  // the work list is the planner's output
+    pdl_launch_dependents();
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
     const int n_items = hdr->n_row_items;
     const int4* items = reinterpret_cast<const int4*>(p.ws + p.lay.row_items);
@@ -518,6 +521,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
     constexpr int kMaxSplits = 64;  // more splits are folded over several passes
     __shared__ float2 ml_s[kMaxSplits][kRowMaxRows];
     __shared__ float M_s[kRowMaxRows], L_s[kRowMaxRows];
+    pdl_wait();
+    pdl_launch_dependents();
     const int4 gd = reinterpret_cast<const int4*>(p.ws + p.lay.group_desc)[blockIdx.x];
     const int base = gd.x, ns = gd.y, q0 = gd.z;
     if (ns <= 1) return;
@@ -578,10 +583,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
 cudaError_t launch_combine(int head_dim, cudaStream_t stream, const CombineParams& p) {
     if (p.n_groups <= 0) return cudaSuccess;
     if (head_dim == 128)
-        combine_kernel<128><<<p.n_groups, 256, 0, stream>>>(p);
-    else
-        combine_kernel<64><<<p.n_groups, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<128>, dim3(p.n_groups), dim3(256), 0, stream, p);
+    return launch_pdl(combine_kernel<64>, dim3(p.n_groups), dim3(256), 0, stream, p);
 }
 
 size_t row_smem_bytes(int head_dim) {
@@ -596,14 +599,16 @@ cudaError_t launch_rows(int head_dim, int grid, cudaStream_t stream, const RowPa
         e = cudaFuncSetAttribute(row_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
-        row_attn_kernel<128><<<grid, kRowThreads, smem, stream>>>(p, tk, tv);
+        e = launch_pdl(row_attn_kernel<128>, dim3(grid), dim3(kRowThreads), smem, stream, p, tk,
+                       tv);
     } else {
         e = cudaFuncSetAttribute(row_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
-        row_attn_kernel<64><<<grid, kRowThreads, smem, stream>>>(p, tk, tv);
+        e = launch_pdl(row_attn_kernel<64>, dim3(grid), dim3(kRowThreads), smem, stream, p, tk,
+                       tv);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace pcp
