@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t kv_iter = 0;          // KV tiles handled so far by this CTA
     uint32_t act0 = 0u, act1 = 0u;  // active (Q tile, KV tile) pairs so far, per Q tile
     uint32_t n_done = 0;            // items finished (q_full phase)
-    int last_issued = -1;           // TMA warp: last KV iteration it issued loads for
+    int last_issued = -1;           // TMA-issuing warps: last KV iteration they loaded
 
     for (;;) {
         if (threadIdx.x == 0) misc[1] = atomicAdd(&hdr->tc_next, 1);
@@ -298,9 +298,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const Geo geo = make_geo(p, items[item]);
         const int ntiles = geo.t_end - geo.t_begin + 1;
 
-        if (warp == kWarpTma) {
-            // ------------------------------------------------ TMA: Q (+ K/V)
-            if (lane == 0) {
+        // Page boxes: the TMA warp issues the K tiles and the first gather warp
+        // the V tiles.  The TMA unit accepts a warp's boxes one lane after the
+        // other (about 140 cycles per 2 KB box), so two issuing warps double
+        // the rate at which small pages arrive.
+        const bool kv_tma_warp =
+            warp == kWarpTma || (p.box_rows > 0 && warp == kWarpGather0);
+        if (kv_tma_warp) {
+            // ------------------------------------------------ TMA: Q, K / V
+            const bool is_k = warp == kWarpTma;
+            if (is_k && lane == 0) {
                 mbar_arrive_expect_tx(bar(C::bQFull),
                                       (uint32_t)(geo.nq * C::kHalves * G * p.qpos * 128));
                 for (int u = 0; u < geo.nq; ++u)
@@ -314,20 +321,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int i = 0; i < ntiles; ++i) {
                     const int t = geo.t_begin + i;
                     const uint32_t cur = kv_iter + i;
-                    const int sk = cur % SK, sv = cur % SV;
                     // the next tile's page ids are in flight while this one waits
                     const int z_next =
                         i + 1 < ntiles ? fetch_box_slot<D>(p, geo, pages, t + 1, lane) : z_cur;
-                    if (!mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u, abort_flag,
-                                   p.dev_err, kSpinLimitNs))
-                        break;
-                    tma_kv_tile<D>(p, geo, t, z_cur, &tm_k, p.k_pool, sK + sk * C::kTileBytes,
-                                   bar(C::bKFull + sk), false, lane);
-                    if (!mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u, abort_flag,
-                                   p.dev_err, kSpinLimitNs))
-                        break;
-                    tma_kv_tile<D>(p, geo, t, z_cur, &tm_v, p.v_pool, sV + sv * C::kTileBytes,
-                                   bar(C::bVFull + sv), true, lane);
+                    if (is_k) {
+                        const int sk = cur % SK;
+                        if (!mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u, abort_flag,
+                                       p.dev_err, kSpinLimitNs))
+                            break;
+                        tma_kv_tile<D>(p, geo, t, z_cur, &tm_k, p.k_pool,
+                                       sK + sk * C::kTileBytes, bar(C::bKFull + sk), false, lane);
+                    } else {
+                        const int sv = cur % SV;
+                        if (!mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u, abort_flag,
+                                       p.dev_err, kSpinLimitNs))
+                            break;
+                        tma_kv_tile<D>(p, geo, t, z_cur, &tm_v, p.v_pool,
+                                       sV + sv * C::kTileBytes, bar(C::bVFull + sv), true, lane);
+                    }
                     last_issued = (int)cur;
                     z_cur = z_next;
                 }
@@ -635,23 +646,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // no work left here: the next kernel on the stream may start launching
     pdl_launch_dependents();
     const bool aborted = *abort_flag != 0;
-    if (warp >= kWarpGather0) {
-        cp_async_wait_all();
-    } else if (warp == kWarpTma) {
+    if (warp == kWarpTma || warp >= kWarpGather0) {
         cp_async_wait_all();
         if (aborted && lane == 0) {
-            // let every TMA load this CTA issued land before the CTA exits
+            // let every TMA load this warp issued land before the CTA exits
             volatile int dummy = 0;
-            if (n_done > 0)
+            if (warp == kWarpTma && n_done > 0)
                 mbar_wait(bar(C::bQFull), (n_done - 1) & 1u, &dummy, p.dev_err, kSpinLimitNs);
-            for (int it = last_issued - SK + 1; it <= last_issued; ++it)
-                if (it >= 0)
-                    mbar_wait(bar(C::bKFull + it % SK), ((uint32_t)it / SK) & 1u, &dummy,
-                              p.dev_err, kSpinLimitNs);
-            for (int it = last_issued - SV + 1; it <= last_issued; ++it)
-                if (it >= 0)
-                    mbar_wait(bar(C::bVFull + it % SV), ((uint32_t)it / SV) & 1u, &dummy,
-                              p.dev_err, kSpinLimitNs);
+            if (warp == kWarpTma)
+                for (int it = last_issued - SK + 1; it <= last_issued; ++it)
+                    if (it >= 0)
+                        mbar_wait(bar(C::bKFull + it % SK), ((uint32_t)it / SK) & 1u, &dummy,
+                                  p.dev_err, kSpinLimitNs);
+            if (warp == kWarpGather0)
+                for (int it = last_issued - SV + 1; it <= last_issued; ++it)
+                    if (it >= 0)
+                        mbar_wait(bar(C::bVFull + it % SV), ((uint32_t)it / SV) & 1u, &dummy,
+                                  p.dev_err, kSpinLimitNs);
         }
     } else if (warp == kWarpMma && lane == 0) {
         // every MMA (and its mbarrier arrivals) completes before TMEM is freed
