@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int u = 0; u < 2; ++u) {
             mbar_init(bar(C::bSFull + u), 1);
-            mbar_init(bar(C::bPFull + u), 128);
+            mbar_init(bar(C::bPFull + u), 4);  // one arrival per softmax warp
             mbar_init(bar(C::bODone + u), 1);
         }
         mbar_init(bar(C::bDrain), 1);
@@ -505,8 +505,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 bool ok = true;
                 for (int t = first_u; t <= last_u; ++t) {
                     const uint32_t a = act_u + (uint32_t)(t - first_u);
-                    if (!mbar_wait(bar(C::bSFull + u), a & 1u, abort_flag, p.dev_err,
-                                   kSpinLimitNs)) {
+                    // waits decide per warp (tcgen05.ld/st and the P arrival are
+                    // warp-collective)
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar(C::bSFull + u), a & 1u, abort_flag,
+                                                           p.dev_err, kSpinLimitNs))) {
                         ok = false;
                         break;
                     }
@@ -569,14 +571,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         acc2[c & 3] = add_f2(acc2[c & 3], e);
                         pk[c] = pack_bf16x2(f2_lo(e), f2_hi(e));
+                        // P goes to TMEM in 16-column pieces while the rest is computed
+                        if ((c & 15) == 15) tmem_st16(tS + (uint32_t)(c - 15), &pk[c - 15]);
                     }
-                    tmem_st64(tS, pk);
-                    const uint64_t acc = add_f2(add_f2(acc2[0], acc2[1]), add_f2(acc2[2], acc2[3]));
-                    const float sum = f2_lo(acc) + f2_hi(acc);
-                    l_run = l_run * alpha + sum;
                     if (t > first_u) {
-                        if (!mbar_wait(bar(C::bODone + u), (a - 1u) & 1u, abort_flag, p.dev_err,
-                                       kSpinLimitNs)) {
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait(bar(C::bODone + u), (a - 1u) & 1u, abort_flag,
+                                                  p.dev_err, kSpinLimitNs))) {
                             tmem_st_wait();
                             ok = false;
                             break;
@@ -597,12 +598,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(bar(C::bPFull + u));
+                    // one arrival per warp once all its lanes' P is in TMEM
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::bPFull + u));
+                    // the row sum is off the MMA's critical path
+                    const uint64_t acc = add_f2(add_f2(acc2[0], acc2[1]), add_f2(acc2[2], acc2[3]));
+                    l_run = l_run * alpha + (f2_lo(acc) + f2_hi(acc));
                 }
                 if (ok) {
                     const uint32_t a_last = act_u + (uint32_t)(last_u - first_u);
-                    ok = mbar_wait(bar(C::bODone + u), a_last & 1u, abort_flag, p.dev_err,
-                                   kSpinLimitNs);
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bODone + u), a_last & 1u,
+                                                           abort_flag, p.dev_err, kSpinLimitNs));
                 }
                 if (ok) {
                     tc_fence_after();

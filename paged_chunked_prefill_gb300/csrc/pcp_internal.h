@@ -14,7 +14,7 @@ constexpr int kTileM = 128;       // query rows per Q tile (tcgen05 M)
 constexpr int kTileN = 128;       // keys per KV tile
 constexpr int kQTiles = 2;        // Q tiles per work item (share each K/V tile)
 constexpr int kTcThreads = 384;   // 2 x 4 softmax warps, TMA warp, MMA warp, 2 gather warps
-constexpr int kWarpTma = 8;       // Q (and large page runs of K/V) by TMA
+constexpr int kWarpTma = 8;       // Q (and the K page boxes) by TMA
 constexpr int kWarpMma = 9;       // one thread issues tcgen05.mma
 constexpr int kWarpGather0 = 10;  // warps 10, 11: cp.async page gathers of K/V
 constexpr int kGatherWarps = 2;
