@@ -57,6 +57,37 @@ def rows_pairs(batch, tok, head) -> int:
     return int(n.sum())
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the dominant kernel, from an ncu capture of this bench on the named workload
+# (profiles/extend_tc_gqa_prefill_ncu.md).  It is reported only while the
+# library sources hash to the value the capture ran with; after any change
+# the key reads null until the counters are taken again.
+NCU_TRAFFIC = {
+    ("gqa_prefill", "extend_tc_kernel<128>"): {
+        "bytes": 207.047936e6 + 18.555648e6,
+        "csrc_sha256": "647c09c2fcc50816ba3df9a5bfc0d3da",
+    },
+}
+
+
+def csrc_sha256() -> str:
+    import hashlib
+    d = os.path.join(ROOT, "paged_chunked_prefill_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        h.update(name.encode())
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:32]
+
+
+def ncu_traffic(workload: str, kernel: str):
+    rec = NCU_TRAFFIC.get((workload, kernel))
+    if rec is None or rec["csrc_sha256"] != csrc_sha256():
+        return None
+    return rec["bytes"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -294,7 +325,8 @@ def main():
     tc_avg = float(np.mean(tc_ms))
     achieved = flops / (tc_avg * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": UNIT, "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "unit": UNIT, "frac": achieved / peaks["bf16_tflops"],
+                "traffic": ncu_traffic(args.workload, f"extend_tc_kernel<{batch.head_dim}>"),
                 "kernel": f"extend_tc_kernel<{batch.head_dim}>", "kernel_ms": tc_avg,
                 "peak_source": f"{peak_kind} bf16 dense (burst)"}
 
