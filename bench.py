@@ -88,6 +88,14 @@ def ncu_traffic(workload: str, kernel: str):
     return rec["bytes"]
 
 
+def launches_per_step(batch) -> int:
+    """Library kernels one step launches."""
+    G = batch.n_q_heads // batch.n_kv_heads
+    rmax = 16 // G if G <= 16 else 0
+    c = np.diff(batch.qo_indptr)
+    return 3 + int((c > rmax).any()) + 2 * int(((c > 0) & (c <= rmax)).any())
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -151,6 +159,21 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class L2Flush:
+    """Flush of the 129 MB L2 before a timed step: write a 256 MB buffer, then
+    read it back, so nothing of the previous step stays in L2 and no dirty
+    line of the flush is left for the timed step to write back."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.buf.zero_()
+        self.torch.sum(self.buf, dim=0, out=self.out)
 
 
 def dist_env():
@@ -259,7 +282,7 @@ def main():
     loc = torch.empty(batch.total_q, dtype=torch.int64, device=dev)
     out = torch.empty_like(d["q"])
     lse = torch.empty(batch.total_q, batch.n_q_heads, dtype=torch.float32, device=dev)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
 
     def step(q=None):
         pcp.compute_out_cache_loc(d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
@@ -270,7 +293,7 @@ def main():
                               d["kv_indices"], d["prefix_lens"], d["k_pool"], d["v_pool"],
                               batch.page_size, batch.n_q_heads, batch.n_kv_heads,
                               batch.head_dim, batch.window, batch.sm_scale, out=out, lse=lse,
-                              workspace=ws, dev_err=err)
+                              workspace=ws, dev_err=err, qo_indptr_host=batch.qo_indptr)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -294,7 +317,7 @@ def main():
         # (1) whole steps: nothing between the library's launches, so each
         # kernel's launch overlaps the end of the one before it
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
@@ -302,10 +325,10 @@ def main():
         # (2) the same steps again with events around the tensor-core kernel
         # (they serialise its two neighbours, so they stay out of loop 1)
         for i in range(args.steps):
-            flush.zero_()
-            pcp.set_timing_events(ev[i][2], ev[i][3])
+            flush()
+            pcp.set_timing_events(ev[i][2], ev[i][3], pcp.TIMING_TC)
             step()
-        pcp.set_timing_events(None, None)
+        pcp.set_timing_events(None, None, pcp.TIMING_TC)
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
     tc_ms = [c.elapsed_time(e) for _, _, c, e in ev]
@@ -323,12 +346,17 @@ def main():
 
     peaks, peak_kind = load_peaks()
     tc_avg = float(np.mean(tc_ms))
-    achieved = flops / (tc_avg * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": UNIT, "frac": achieved / peaks["bf16_tflops"],
-                "traffic": ncu_traffic(args.workload, f"extend_tc_kernel<{batch.head_dim}>"),
-                "kernel": f"extend_tc_kernel<{batch.head_dim}>", "kernel_ms": tc_avg,
-                "peak_source": f"{peak_kind} bf16 dense (burst)"}
+    G = batch.n_q_heads // batch.n_kv_heads
+    row_max_chunk = 16 // G if G <= 16 else 0
+    if (np.diff(batch.qo_indptr) > row_max_chunk).any():
+        achieved = flops / (tc_avg * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                    "unit": UNIT, "frac": achieved / peaks["bf16_tflops"],
+                    "traffic": ncu_traffic(args.workload, f"extend_tc_kernel<{batch.head_dim}>"),
+                    "kernel": f"extend_tc_kernel<{batch.head_dim}>", "kernel_ms": tc_avg,
+                    "peak_source": f"{peak_kind} bf16 dense (burst)"}
+    else:  # decode-shaped rows only: no tensor-core launch to time
+        roofline = None
 
     # ---- end to end through the C ABI with pinned host buffers
     e2e = None
@@ -343,14 +371,14 @@ def main():
                    "tokens_per_step": batch.total_q * world,
                    "visible_pairs_per_head": visible_pairs(batch.prefix_lens, batch.chunk_lens,
                                                            batch.window),
-                   "l2": "flushed (256 MB write) before every timed step",
+                   "l2": "flushed before every timed step: 256 MB written, then read back",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
         "e2e": e2e,
-        # out_cache_loc, kv_append, plan, tensor-core kernel (+ row kernel and
-        # combine when the group fits a row item), in each of the two loops
-        "gpu_launches": 2 * args.steps * (
-            6 if batch.n_q_heads // batch.n_kv_heads <= 16 else 4),
+        # out_cache_loc, kv_append, plan, then the tensor-core kernel and/or the
+        # row kernel + combine (the host copy of qo_indptr skips a kernel
+        # without work), in each of the two timed loops
+        "gpu_launches": 2 * args.steps * launches_per_step(batch),
         "clocks": clocks.summary(),
     }
 
@@ -396,7 +424,7 @@ def end_to_end(args, torch, d, out, lse, step, flush, stream, flops, world):
     torch.cuda.synchronize()
     e2e_ms = []
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         e2e_step()
@@ -427,15 +455,25 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
         pcp.paged_extend_attn(d["q"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
                               d["prefix_lens"], d["k_pool"], d["v_pool"], db.page_size,
                               db.n_q_heads, db.n_kv_heads, db.head_dim, 0, 0.0, out=out,
-                              lse=lse, workspace=ws, dev_err=err)
+                              lse=lse, workspace=ws, dev_err=err, qo_indptr_host=db.qo_indptr)
     ms = time_calls(torch, dec, flush)
     kv_bytes = int(db.kv_lens.sum()) * db.n_kv_heads * db.head_dim * 2 * 2
     io_bytes = (d["q"].numel() * 2 + out.numel() * 2 + lse.numel() * 4 +
                 int(db.kv_indptr[-1]) * 4)
-    gbs = (kv_bytes + io_bytes) / (ms * 1e-3) / 1e9
+    nbytes = kv_bytes + io_bytes
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    # the row kernel alone, between CUDA events on the launching stream
+    kms = time_calls(torch, dec, flush, kernel=pcp.TIMING_ROWS, pcp=pcp)
+    kgbs = nbytes / (kms * 1e-3) / 1e9
     res["decode_rows"] = {"workload": db.name, "ms": ms, "GB/s": gbs,
-                          "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": kv_bytes + io_bytes,
-                          "peak_source": f"{peak_kind} HBM copy"}
+                          "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes,
+                          "peak_source": f"{peak_kind} HBM copy",
+                          "what": "whole call: planner, row kernel, split-KV combine"}
+    res["decode_rows_kernel"] = {"bound": "hbm", "kernel": f"row_attn_kernel<{db.head_dim}>",
+                                 "kernel_ms": kms, "achieved": kgbs, "peak": peaks["hbm_gbs"],
+                                 "unit": "GB/s", "frac": kgbs / peaks["hbm_gbs"],
+                                 "traffic": ncu_traffic("decode_rows",
+                                                        f"row_attn_kernel<{db.head_dim}>")}
     gb = W.gqa_prefill()
     g = to_device(gb, dev)
     loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
@@ -449,23 +487,91 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
     res["kv_append"] = {"workload": f"{gb.total_q} tokens x {gb.n_kv_heads} KV heads x D "
                                     f"{gb.head_dim}", "ms": ms, "GB/s": gbs,
                         "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes}
+    del g, loc
+
+    # the long-context batch: its 32768-token append and its attention call
+    lb = W.long_context()
+    g = to_device(lb, dev)
+    loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
+                                    g["prefix_lens"], lb.page_size, lb.num_pages)
+
+    def app_long():
+        pcp.kv_append(g["k_new"], g["v_new"], loc, g["k_pool"], g["v_pool"], dev_err=err)
+    ms = time_calls(torch, app_long, flush)
+    nbytes = 2 * 2 * lb.total_q * lb.n_kv_heads * lb.head_dim * 2 + 8 * lb.total_q
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res["kv_append_long"] = {"workload": f"{lb.total_q} tokens x {lb.n_kv_heads} KV heads x D "
+                                         f"{lb.head_dim}", "ms": ms, "GB/s": gbs,
+                             "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes}
+    lout = torch.empty_like(g["q"])
+    llse = torch.empty(lb.total_q, lb.n_q_heads, dtype=torch.float32, device=dev)
+    lws = torch.empty(pcp.workspace_size(lb.batch, lb.total_q, lb.n_q_heads, lb.n_kv_heads,
+                                         lb.head_dim), dtype=torch.uint8, device=dev)
+
+    def attn_long():
+        pcp.paged_extend_attn(g["q"], g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
+                              g["prefix_lens"], g["k_pool"], g["v_pool"], lb.page_size,
+                              lb.n_q_heads, lb.n_kv_heads, lb.head_dim, lb.window, lb.sm_scale,
+                              out=lout, lse=llse, workspace=lws, dev_err=err,
+                              qo_indptr_host=lb.qo_indptr)
+    ms = time_calls(torch, attn_long, flush, n=5, warm=2)
+    lflops = 4 * lb.head_dim * lb.n_q_heads * visible_pairs(lb.prefix_lens, lb.chunk_lens,
+                                                            lb.window)
+    tf = lflops / (ms * 1e-3) / 1e12
+    res["long_context_attn"] = {"workload": lb.name, "ms": ms, "TFLOP/s": tf,
+                                "frac_bf16": tf / peaks["bf16_tflops"]}
+    del g, loc, lout, llse, lws
+
+    # the mixed scheduler batch: prompt chunks (tensor cores) and decode rows
+    # (row kernel) in one call
+    mb = W.mixed_batch()
+    g = to_device(mb, dev)
+    loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
+                                    g["prefix_lens"], mb.page_size, mb.num_pages)
+    pcp.kv_append(g["k_new"], g["v_new"], loc, g["k_pool"], g["v_pool"], dev_err=err)
+    mout = torch.empty_like(g["q"])
+    mlse = torch.empty(mb.total_q, mb.n_q_heads, dtype=torch.float32, device=dev)
+    mws = torch.empty(pcp.workspace_size(mb.batch, mb.total_q, mb.n_q_heads, mb.n_kv_heads,
+                                         mb.head_dim), dtype=torch.uint8, device=dev)
+
+    def attn_mixed():
+        pcp.paged_extend_attn(g["q"], g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
+                              g["prefix_lens"], g["k_pool"], g["v_pool"], mb.page_size,
+                              mb.n_q_heads, mb.n_kv_heads, mb.head_dim, mb.window, mb.sm_scale,
+                              out=mout, lse=mlse, workspace=mws, dev_err=err,
+                              qo_indptr_host=mb.qo_indptr)
+    ms = time_calls(torch, attn_mixed, flush)
+    mflops = 4 * mb.head_dim * mb.n_q_heads * visible_pairs(mb.prefix_lens, mb.chunk_lens,
+                                                            mb.window)
+    tf = mflops / (ms * 1e-3) / 1e12
+    res["mixed_attn"] = {"workload": mb.name, "ms": ms, "TFLOP/s": tf,
+                         "frac_bf16": tf / peaks["bf16_tflops"]}
     if pcp.read_error(err) != 0:
         raise RuntimeError("device error in secondary measurements")
     return res
 
 
-def time_calls(torch, fn, flush, n=20, warm=5):
+def time_calls(torch, fn, flush, n=20, warm=5, kernel=None, pcp=None):
+    """Median ms of fn() between CUDA events, L2 flushed before each call; with
+    `kernel` (pcp.TIMING_*) the events bracket that library kernel only."""
     stream = torch.cuda.current_stream()
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
     ms = []
     for _ in range(n):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        fn()
-        b.record(stream)
+        if kernel is None:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        else:
+            a.record(stream)  # creates the events before the library records them
+            b.record(stream)
+            pcp.set_timing_events(a, b, kernel)
+            fn()
+            pcp.set_timing_events(None, None, kernel)
         b.synchronize()
         ms.append(a.elapsed_time(b))
     return float(np.median(ms))

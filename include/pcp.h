@@ -23,7 +23,8 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All pointers named q, k, v, *_pool, out, lse, indptr/indices/lens,
- *    out_cache_loc, workspace and dev_err are DEVICE pointers.  The caller
+ *    out_cache_loc, workspace and dev_err are DEVICE pointers; only the
+ *    optional *_host arguments are host pointers.  The caller
  *    owns every buffer and the stream; the library allocates no device
  *    memory and keeps no state except a per-device cache of the SM count and
  *    of the driver's tensor-map encoder.
@@ -138,6 +139,15 @@ size_t pcp_extend_workspace_size(int batch, int64_t total_q, int n_q_heads, int 
  * A chunk of length 0 is allowed (no rows); prefix_lens[b] == 0 is a plain
  * prefill; a chunk of length 1 is a decode row.
  *
+ * qo_indptr_host: NULL, or a HOST copy of qo_indptr ([batch + 1] int32, the
+ * same values as the device array; read during the call only, not kept).
+ * With it the call launches only the kernels that have work: chunks of at
+ * most 16 / (n_q_heads / n_kv_heads) rows go to the split-KV row kernel, the
+ * others to the tensor-core kernel, and a call whose chunks are all of one
+ * kind skips the other kernel's launch.  A host copy that does not start at
+ * 0, does not end at total_q or decreases returns PCP_ERR_INVALID_ARG before
+ * anything is launched.  Results are bit-identical with and without it.
+ *
  * The K/V of the chunk itself must already be in the pool (pcp_kv_append
  * first, as a serving step does).  Supported: head_dim in {64, 128},
  * n_q_heads % n_kv_heads == 0, n_q_heads / n_kv_heads <= 128, page_size >= 1,
@@ -150,7 +160,8 @@ size_t pcp_extend_workspace_size(int batch, int64_t total_q, int n_q_heads, int 
  */
 pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
                                  const int32_t* kv_indptr, const int32_t* kv_indices,
-                                 const int32_t* prefix_lens, int batch, int64_t total_q,
+                                 const int32_t* prefix_lens, const int32_t* qo_indptr_host,
+                                 int batch, int64_t total_q,
                                  const void* k_pool, const void* v_pool, int64_t num_pages,
                                  int page_size, int n_q_heads, int n_kv_heads, int head_dim,
                                  int window, float sm_scale, void* out, float* lse,
@@ -186,7 +197,9 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
  */
 pcp_status pcp_paged_extend_attn_noalloc(const void* q, const int32_t* qo_indptr,
                                          const int32_t* kv_indptr, const int32_t* kv_indices,
-                                         const int32_t* prefix_lens, int batch, int64_t total_q,
+                                         const int32_t* prefix_lens,
+                                         const int32_t* qo_indptr_host, int batch,
+                                         int64_t total_q,
                                          const void* k_pool, const void* v_pool,
                                          int64_t num_pages, int page_size, int n_q_heads,
                                          int n_kv_heads, int head_dim, int window,
@@ -199,14 +212,20 @@ pcp_status pcp_paged_extend_attn_noalloc(const void* q, const int32_t* qo_indptr
  */
 pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_err);
 
+/* Kernels pcp_set_timing_events can bracket. */
+#define PCP_TIMING_TC 0   /* the tensor-core extend kernel */
+#define PCP_TIMING_ROWS 1 /* the split-KV row kernel (decode-shaped rows) */
+
 /*
  * Profiling hook.  When both events (cudaEvent_t passed as void*) are
- * non-NULL, every later pcp_paged_extend_attn call records `before` on its
- * stream right before the tensor-core extend kernel is launched and `after`
- * right after it, so a caller can time that kernel alone.  Pass NULLs to
- * turn it off.  Process-wide; not for concurrent use from several threads.
+ * non-NULL, every later pcp_paged_extend_attn call that launches `kernel`
+ * (PCP_TIMING_TC or PCP_TIMING_ROWS) records `before` on its stream right
+ * before that kernel is launched and `after` right after it, so a caller can
+ * time that kernel alone.  Pass NULLs to turn it off.  Process-wide; not for
+ * concurrent use from several threads.  An unknown `kernel` or only one NULL
+ * event returns PCP_ERR_INVALID_ARG.
  */
-pcp_status pcp_set_timing_events(void* before, void* after);
+pcp_status pcp_set_timing_events(int kernel, void* before, void* after);
 
 #ifdef __cplusplus
 }

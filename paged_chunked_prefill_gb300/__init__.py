@@ -24,10 +24,13 @@ from ._binding import (  # noqa: F401
     paged_extend_attn,
     read_error,
     set_timing_events,
+    TIMING_ROWS,
+    TIMING_TC,
     workspace_size,
 )
 
 __all__ = [
     "PCPError", "Status", "compute_out_cache_loc", "kv_append", "lib", "library_path",
-    "paged_extend_attn", "read_error", "set_timing_events", "workspace_size",
+    "paged_extend_attn", "read_error", "set_timing_events", "TIMING_ROWS", "TIMING_TC",
+    "workspace_size",
 ]

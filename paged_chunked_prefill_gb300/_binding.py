@@ -7,6 +7,7 @@ import os
 import threading
 from typing import Optional, Tuple
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -60,12 +61,12 @@ def lib():
         L.pcp_kv_append.restype = i32
         L.pcp_extend_workspace_size.argtypes = [i32, i64, i32, i32, i32]
         L.pcp_extend_workspace_size.restype = sz
-        L.pcp_paged_extend_attn.argtypes = [P, P, P, P, P, i32, i64, P, P, i64, i32, i32, i32,
-                                            i32, i32, f32, P, P, P, sz, P, P]
+        L.pcp_paged_extend_attn.argtypes = [P, P, P, P, P, P, i32, i64, P, P, i64, i32, i32,
+                                            i32, i32, i32, f32, P, P, P, sz, P, P]
         L.pcp_paged_extend_attn.restype = i32
         L.pcp_read_error.argtypes = [P, P, P]
         L.pcp_read_error.restype = i32
-        L.pcp_set_timing_events.argtypes = [P, P]
+        L.pcp_set_timing_events.argtypes = [i32, P, P]
         L.pcp_set_timing_events.restype = i32
         _lib = L
         return L
@@ -78,6 +79,20 @@ def _check(status: int, where: str) -> None:
 
 def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _host_i32(a, n: int, name: str):
+    """(pointer, owner) of an optional host int32 array of n entries."""
+    if a is None:
+        return ctypes.c_void_p(0), None
+    if isinstance(a, torch.Tensor):
+        if a.device.type != "cpu":
+            raise ValueError(f"{name} must be a host (CPU) array")
+        a = a.numpy()
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    if a.ndim != 1 or a.shape[0] != n:
+        raise ValueError(f"{name} must hold {n} int32 entries")
+    return ctypes.c_void_p(a.ctypes.data), a
 
 
 def _stream(device: torch.device):
@@ -192,10 +207,15 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
                       lse: Optional[torch.Tensor] = None,
                       workspace: Optional[torch.Tensor] = None,
                       dev_err: Optional[torch.Tensor] = None,
+                      qo_indptr_host=None,
                       check: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
     """Extend attention of every query row over its cached prefix and own
     chunk (bottom-right causal, GQA, optional window).  Returns (out, lse):
-    out bf16 [total_q, Hq, D], lse float32 [total_q, Hq] (natural log)."""
+    out bf16 [total_q, Hq, D], lse float32 [total_q, Hq] (natural log).
+
+    qo_indptr_host: optional host copy of qo_indptr (numpy int32 array or CPU
+    int32 tensor); with it the call skips the launch of a kernel that would
+    have no work."""
     dev = q.device
     _need(q, "q", torch.bfloat16, dev)
     _need(k_pool, "k_pool", torch.bfloat16, dev)
@@ -220,18 +240,24 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
     own = dev_err is None
     if own:
         dev_err = _dev_err(dev)
+    host_ptr, host_keep = _host_i32(qo_indptr_host, batch + 1, "qo_indptr_host")
     _check(lib().pcp_paged_extend_attn(
-        _ptr(q), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(prefix_lens), batch,
-        total_q, _ptr(k_pool), _ptr(v_pool), num_pages, page_size, n_q_heads, n_kv_heads,
+        _ptr(q), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(prefix_lens), host_ptr,
+        batch, total_q, _ptr(k_pool), _ptr(v_pool), num_pages, page_size, n_q_heads, n_kv_heads,
         head_dim, window, float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel(), _ptr(dev_err), _stream(dev)), "pcp_paged_extend_attn")
+    del host_keep
     _finish(dev_err, own, check, "pcp_paged_extend_attn")
     return out, lse
 
 
-def set_timing_events(before, after) -> None:
-    """Record `before`/`after` (torch.cuda.Event, or None) around the
-    tensor-core kernel of every later paged_extend_attn call."""
+TIMING_TC = 0    # the tensor-core extend kernel
+TIMING_ROWS = 1  # the split-KV row kernel
+
+
+def set_timing_events(before, after, kernel: int = TIMING_TC) -> None:
+    """Record `before`/`after` (torch.cuda.Event, or None) around `kernel`
+    (TIMING_TC or TIMING_ROWS) in every later paged_extend_attn call."""
     b = ctypes.c_void_p(before.cuda_event) if before is not None else ctypes.c_void_p(0)
     a = ctypes.c_void_p(after.cuda_event) if after is not None else ctypes.c_void_p(0)
-    _check(lib().pcp_set_timing_events(b, a), "pcp_set_timing_events")
+    _check(lib().pcp_set_timing_events(kernel, b, a), "pcp_set_timing_events")

@@ -47,7 +47,8 @@ using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, voi
                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeFn g_encode = nullptr;
-cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+// profiling events per kernel kind (PCP_TIMING_TC, PCP_TIMING_ROWS)
+cudaEvent_t g_ev_before[2] = {nullptr, nullptr}, g_ev_after[2] = {nullptr, nullptr};
 
 // SM count of the current device, cached per device.
 pcp_status sm_count(int* out) {
@@ -125,7 +126,7 @@ const char* pcp_status_string(int status) {
     }
 }
 
-int pcp_abi_version(void) { return 1; }
+int pcp_abi_version(void) { return 2; }
 
 pcp_status pcp_compute_out_cache_loc(const int32_t* qo_indptr, const int32_t* kv_indptr,
                                      const int32_t* kv_indices, const int32_t* prefix_lens,
@@ -176,7 +177,8 @@ size_t pcp_extend_workspace_size(int batch, int64_t total_q, int n_q_heads, int 
 
 pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
                                  const int32_t* kv_indptr, const int32_t* kv_indices,
-                                 const int32_t* prefix_lens, int batch, int64_t total_q,
+                                 const int32_t* prefix_lens, const int32_t* qo_indptr_host,
+                                 int batch, int64_t total_q,
                                  const void* k_pool, const void* v_pool, int64_t num_pages,
                                  int page_size, int n_q_heads, int n_kv_heads, int head_dim,
                                  int window, float sm_scale, void* out, float* lse,
@@ -205,6 +207,24 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
         return PCP_ERR_INVALID_ARG;
     if (workspace == nullptr || workspace_bytes < lay.total || !aligned(workspace, 256))
         return PCP_ERR_WORKSPACE;
+    // With the host copy of qo_indptr the call launches only the kernels that
+    // have work: the tensor-core kernel for chunks of more than
+    // row_path_max_chunk(G) rows, the row kernel and combine for the others.
+    const int rmax = row_path_max_chunk(group);
+    bool run_tc = true, run_rows = rmax > 0;
+    if (qo_indptr_host != nullptr) {
+        if (qo_indptr_host[0] != 0 || qo_indptr_host[batch] != total_q)
+            return PCP_ERR_INVALID_ARG;
+        bool any_tc = false, any_row = false;
+        for (int b = 0; b < batch; ++b) {
+            const int64_t c = (int64_t)qo_indptr_host[b + 1] - qo_indptr_host[b];
+            if (c < 0) return PCP_ERR_INVALID_ARG;
+            if (c > rmax) any_tc = true;
+            else if (c > 0) any_row = true;
+        }
+        run_tc = any_tc;
+        run_rows = run_rows && any_row;
+    }
 
     int sms = 0;
     pcp_status st = sm_count(&sms);
@@ -278,18 +298,21 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
     tp.window = window;
     tp.scale_log2 = scale_log2;
     tp.dev_err = dev_err;
-    cudaEvent_t evb = nullptr, eva = nullptr;
+    cudaEvent_t evb = nullptr, eva = nullptr, evrb = nullptr, evra = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        evb = g_ev_before;
-        eva = g_ev_after;
+        evb = g_ev_before[PCP_TIMING_TC];
+        eva = g_ev_after[PCP_TIMING_TC];
+        evrb = g_ev_before[PCP_TIMING_ROWS];
+        evra = g_ev_after[PCP_TIMING_ROWS];
     }
     if (evb && cudaEventRecord(evb, s) != cudaSuccess) return PCP_ERR_CUDA;
-    if (launch_extend_tc(head_dim, sms, s, tp, tq, tk, tv) != cudaSuccess) return PCP_ERR_CUDA;
+    if (run_tc && launch_extend_tc(head_dim, sms, s, tp, tq, tk, tv) != cudaSuccess)
+        return PCP_ERR_CUDA;
     if (eva && cudaEventRecord(eva, s) != cudaSuccess) return PCP_ERR_CUDA;
 
-    // ---- 3. decode-shaped rows (split-KV on CUDA cores)
-    if (row_path_max_chunk(group) > 0) {
+    // ---- 3. decode-shaped rows (split-KV on CUDA cores, equal tiles per CTA)
+    if (run_rows) {
         RowParams rp;
         rp.q = static_cast<const uint16_t*>(q);
         rp.qo_indptr = qo_indptr;
@@ -312,7 +335,10 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
         rp.window = window;
         rp.scale_log2 = scale_log2;
         rp.dev_err = dev_err;
-        if (launch_rows(head_dim, sms, s, rp, tk, tv) != cudaSuccess) return PCP_ERR_CUDA;
+        if (evrb && cudaEventRecord(evrb, s) != cudaSuccess) return PCP_ERR_CUDA;
+        if (launch_rows(head_dim, row_grid(sms), s, rp, tk, tv) != cudaSuccess)
+            return PCP_ERR_CUDA;
+        if (evra && cudaEventRecord(evra, s) != cudaSuccess) return PCP_ERR_CUDA;
         // ---- 4. merge split-KV partials (one CTA per split group)
         CombineParams cp;
         cp.ws = ws;
@@ -338,11 +364,12 @@ pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_er
     return PCP_OK;
 }
 
-pcp_status pcp_set_timing_events(void* before, void* after) {
+pcp_status pcp_set_timing_events(int kernel, void* before, void* after) {
     std::lock_guard<std::mutex> lock(g_mu);
     if ((before == nullptr) != (after == nullptr)) return PCP_ERR_INVALID_ARG;
-    g_ev_before = static_cast<cudaEvent_t>(before);
-    g_ev_after = static_cast<cudaEvent_t>(after);
+    if (kernel != PCP_TIMING_TC && kernel != PCP_TIMING_ROWS) return PCP_ERR_INVALID_ARG;
+    g_ev_before[kernel] = static_cast<cudaEvent_t>(before);
+    g_ev_after[kernel] = static_cast<cudaEvent_t>(after);
     return PCP_OK;
 }
 

@@ -23,7 +23,7 @@ constexpr int kGatherWarps = 2;
 constexpr int kRowMaxRows = 16;   // query rows (positions x heads) per row item
 constexpr int kRowTile = 128;     // keys per row-kernel tile
 constexpr int kRowThreads = 160;      // 4 consumer warps + 1 load warp
-constexpr int kRowTargetItems = 1024;  // split lengths aim at about this many items
+constexpr int kRowMaxCtas = 512;       // row-kernel CTAs at most (one per SM below that)
 
 // Spin-wait limit of every bounded wait (nanoseconds).
 constexpr uint64_t kSpinLimitNs = 2000000000ull;
@@ -36,25 +36,51 @@ __host__ __device__ inline int row_path_max_chunk(int group) {
 
 __host__ __device__ inline int q_positions_per_tile(int group) { return kTileM / group; }
 
+// CTAs of the row kernel: one per SM.  The planner splits the row work for
+// exactly this many.
+__host__ __device__ inline int row_grid(int sm_count) {
+    return sm_count < 1 ? 1 : (sm_count > kRowMaxCtas ? kRowMaxCtas : sm_count);
+}
+
+// CTAs of a row grid of n that get row tiles: min(n, T), so each of them
+// gets at least one of the T tiles (the others exit at once).
+__host__ __device__ inline int row_ctas_used(int n, int T) { return T < n ? T : n; }
+
+// Row-kernel CTA `i` of the `n` used owns tiles [row_tile_begin(i),
+// row_tile_begin(i + 1)) of the T row tiles (all row groups' 128-key tiles
+// laid end to end).
+__host__ __device__ inline int row_tile_begin(int i, int n, int T) {
+    return (int)(((int64_t)i * T) / n);
+}
+
 // ---- workspace
 struct WsHeader {
     int n_tc_items;
-    int n_row_items;
-    int tc_next;       // dynamic scheduler counters
-    int row_next;
-    int tiles_per_split;
+    int n_row_groups;  // (sequence, KV head) groups on the row path
+    int tc_next;       // dynamic scheduler counter of the tensor-core kernel
+    int row_tiles;     // T: 128-key tiles of all row groups
+    int row_ctas;      // n: row-kernel CTAs the split was made for
     int pad[59];       // 256 bytes
 };
 
 // Tensor-core work item: {b, kv head g, first chunk position, cost in KV tiles}
-// Row work item (three int4), fully resolved so the row kernel needs no
-// further metadata: {b, g, split, n_splits}, {kv_begin, kv_end, first partial
-// slot of the group, qo_indptr[b]}, {chunk_len, prefix_len, kv_indptr[b], kv_len}
+//
+// Row path.  The row groups' tiles are laid end to end (group k covers tiles
+// [S_k, S_k + tiles_k)) and CTA i of n takes tiles [i*T/n, (i+1)*T/n), so
+// every CTA streams the same number of tiles (within one).  The piece of
+// group k that CTA i holds writes partial slot k + i: for two non-empty
+// pieces (k, i) != (k', i') with k + i = k' + i' the group and CTA orders
+// would have to cross, so the slots are distinct, and the pieces of one group
+// use consecutive slots.  A group held by one CTA writes out and lse directly.
+// Row group descriptor (three int4): {b, g, S_k, tiles_k},
+// {first key, qo_indptr[b], first partial slot, n_splits},
+// {chunk_len, prefix_len, kv_indptr[b], kv_len}.
 
 struct WsLayout {
     size_t header;        // offset of WsHeader
     size_t tc_items;      // int4 [cap_tc]
-    size_t row_items;     // int4 [3 * cap_row]
+    size_t row_groups;    // int4 [3 * cap_groups]: row group descriptors
+    size_t row_first;     // int [kRowMaxCtas]: first row group of each row-kernel CTA
     size_t group_desc;    // int4 [cap_groups]: {first partial slot, n_splits, q0, chunk_len}
     size_t partial_o;     // float [cap_row * kRowMaxRows * head_dim]
     size_t partial_ml;    // float2 [cap_row * kRowMaxRows]
@@ -76,14 +102,16 @@ inline bool ws_layout(int batch, int64_t total_q, int n_q_heads, int n_kv_heads,
     const int64_t qpos = (int64_t)q_positions_per_tile(group) * kQTiles;
     L->cap_tc = (int64_t)n_kv_heads * ((total_q + qpos - 1) / qpos + batch);
     L->cap_groups = (int64_t)n_kv_heads * batch;
-    L->cap_row = L->cap_groups + kRowTargetItems;
+    L->cap_row = L->cap_groups + kRowMaxCtas;  // partial slots: k + i < groups + CTAs
     size_t off = 0;
     L->header = off;
     off += sizeof(WsHeader);
     L->tc_items = off = align_up(off, 256);
     off += (size_t)(L->cap_tc > 0 ? L->cap_tc : 1) * 16;
-    L->row_items = off = align_up(off, 256);
-    off += (size_t)L->cap_row * 48;
+    L->row_groups = off = align_up(off, 256);
+    off += (size_t)(L->cap_groups > 0 ? L->cap_groups : 1) * 48;
+    L->row_first = off = align_up(off, 256);
+    off += (size_t)kRowMaxCtas * 4;
     L->group_desc = off = align_up(off, 256);
     off += (size_t)(L->cap_groups > 0 ? L->cap_groups : 1) * 16;
     L->partial_o = off = align_up(off, 256);

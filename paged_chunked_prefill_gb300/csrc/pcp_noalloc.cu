@@ -46,7 +46,8 @@ pcp_status scratch_for_current_device(void** out) {
 
 extern "C" pcp_status pcp_paged_extend_attn_noalloc(
     const void* q, const int32_t* qo_indptr, const int32_t* kv_indptr,
-    const int32_t* kv_indices, const int32_t* prefix_lens, int batch, int64_t total_q,
+    const int32_t* kv_indices, const int32_t* prefix_lens, const int32_t* qo_indptr_host,
+    int batch, int64_t total_q,
     const void* k_pool, const void* v_pool, int64_t num_pages, int page_size, int n_q_heads,
     int n_kv_heads, int head_dim, int window, float sm_scale, void* out, float* lse,
     int32_t* dev_err, void* stream) {
@@ -55,17 +56,18 @@ extern "C" pcp_status pcp_paged_extend_attn_noalloc(
     if (need == 0 || total_q == 0) {
         // an unsupported shape or an empty call: the regular entry point
         // gives the answer without touching any workspace
-        return pcp_paged_extend_attn(q, qo_indptr, kv_indptr, kv_indices, prefix_lens, batch,
-                                     total_q, k_pool, v_pool, num_pages, page_size, n_q_heads,
-                                     n_kv_heads, head_dim, window, sm_scale, out, lse, nullptr,
-                                     0, dev_err, stream);
+        return pcp_paged_extend_attn(q, qo_indptr, kv_indptr, kv_indices, prefix_lens,
+                                     qo_indptr_host, batch, total_q, k_pool, v_pool, num_pages,
+                                     page_size, n_q_heads, n_kv_heads, head_dim, window,
+                                     sm_scale, out, lse, nullptr, 0, dev_err, stream);
     }
     if (need > (size_t)PCP_NOALLOC_SCRATCH_BYTES) return PCP_ERR_WORKSPACE;
     void* scratch = nullptr;
     const pcp_status st = scratch_for_current_device(&scratch);
     if (st != PCP_OK) return st;
-    return pcp_paged_extend_attn(q, qo_indptr, kv_indptr, kv_indices, prefix_lens, batch,
-                                 total_q, k_pool, v_pool, num_pages, page_size, n_q_heads,
-                                 n_kv_heads, head_dim, window, sm_scale, out, lse, scratch,
-                                 (size_t)PCP_NOALLOC_SCRATCH_BYTES, dev_err, stream);
+    return pcp_paged_extend_attn(q, qo_indptr, kv_indptr, kv_indices, prefix_lens,
+                                 qo_indptr_host, batch, total_q, k_pool, v_pool, num_pages,
+                                 page_size, n_q_heads, n_kv_heads, head_dim, window, sm_scale,
+                                 out, lse, scratch, (size_t)PCP_NOALLOC_SCRATCH_BYTES, dev_err,
+                                 stream);
 }

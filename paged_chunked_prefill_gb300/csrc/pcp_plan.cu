@@ -9,15 +9,14 @@
 //    heads of that KV head packed into the MMA rows).  Items are ordered by
 //    cost (number of KV tiles) descending -- longest-processing-time first
 //    for the persistent kernel's dynamic scheduler -- with a counting sort.
-//  * row items for decode-shaped chunks (chunk_len * G <= 16 rows): the KV
-//    range of each (sequence, KV head) is split into pieces of
-//    about `tiles_per_split` 128-key tiles (nearly equal parts of the group),
-//    chosen so the whole call has about three items per SM, ordered longest
-//    first like the tensor-core
-//    items.  Each split owns a partial slot (the group's first slot + split
-//    index) for the log-sum-exp combine.  This is the split-KV idea of the
-//    AstrAI paged decode kernel (split count from the SM count, partials
-//    merged by a combine step).
+//  * row groups for decode-shaped chunks (chunk_len * G <= 16 rows), one per
+//    (sequence, KV head): their 128-key tiles are laid end to end and the
+//    row kernel's CTA i of n takes tiles [i*T/n, (i+1)*T/n), so every SM
+//    streams the same number of K/V bytes.  A group held by several CTAs is
+//    split at their boundaries; each piece owns a partial slot for the
+//    log-sum-exp combine.  This is the split-KV idea of the AstrAI paged
+//    decode kernel (splits from the SM count, partials merged by a combine
+//    step) with the split points chosen for equal work per SM.
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
 #include "pcp_launch.h"
@@ -46,12 +45,6 @@ __device__ __forceinline__ SeqInfo seq_info(const PlanParams& p, int b) {
 // First visible key of absolute position `pos`.
 __device__ __forceinline__ int first_key(int pos, int window) {
     return window > 0 ? max(0, pos - window + 1) : 0;
-}
-
-// Tiles [split_end(sp - 1), split_end(sp)) of a group's `tiles` form split sp:
-// ns nearly equal parts (lengths differ by at most one).
-__device__ __forceinline__ int split_end(int tiles, int ns, int sp) {
-    return (int)(((int64_t)(sp + 1) * tiles) / ns);
 }
 
 __device__ __forceinline__ int tc_cost(int P, int c, int k, int item_pos, int window) {
@@ -151,31 +144,31 @@ __device__ __forceinline__ int warp_agg_add(int* base, int key, int inc) {
 }  // namespace
 
 // Sequences are processed in chunks of 1024 (one per thread); within a chunk
-// the per-sequence items and splits are flattened across all threads through
-// prefix sums, so a long chunk does not serialise on one thread.
+// the per-sequence items and row groups are flattened across all threads
+// through prefix sums, so a long chunk does not serialise on one thread.
 __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanParams p) {
     __shared__ int hist[1024];
-    __shared__ int hist_r[1024];
     __shared__ int warp_sums[64];
     __shared__ int s_a[1025];       // per-sequence counts, then their exclusive prefix
     __shared__ int s_b[1025];
+    __shared__ int s_c[1025];
     __shared__ int4 s_seq[1024];    // {c, P, ok, row tiles}
     __shared__ unsigned long long s_row_tiles;
-    __shared__ int s_tps;
 
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
     int4* tc = reinterpret_cast<int4*>(p.ws + p.lay.tc_items);
-    int4* rows = reinterpret_cast<int4*>(p.ws + p.lay.row_items);
+    int4* rg = reinterpret_cast<int4*>(p.ws + p.lay.row_groups);
+    int* row_first = reinterpret_cast<int*>(p.ws + p.lay.row_first);
     int4* gdesc = reinterpret_cast<int4*>(p.ws + p.lay.group_desc);
     const int tid = threadIdx.x, lane = tid & 31;
     const int item_pos = q_positions_per_tile(p.group) * kQTiles;
     const int rmax = row_path_max_chunk(p.group);
     const int H = p.n_kv_heads;
+    const int n_ctas = row_grid(p.sm_count);
 
     pdl_wait();
     pdl_launch_dependents();
     hist[tid] = 0;
-    hist_r[tid] = 0;
     for (int64_t i = tid; i < (int64_t)p.batch * H; i += 1024) gdesc[i] = make_int4(0, 0, 0, 0);
     if (tid == 0) {
         s_row_tiles = 0;
@@ -202,7 +195,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     };
     const bool one_chunk = p.batch <= 1024;
 
-    // ---- sweep 1: tensor-core cost histogram, row-path tile total
+    // ---- sweep 1: tensor-core cost histogram, row tile total
     for (int chunk0 = 0; chunk0 < p.batch; chunk0 += 1024) {
         __syncthreads();
         load_chunk(chunk0, true);
@@ -222,43 +215,30 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     }
     __syncthreads();
     const int n_tc = desc_offsets(hist, warp_sums);
-    if (tid == 0) {
-        const unsigned long long tot = s_row_tiles;
-        const int target = min(3 * max(p.sm_count, 1), kRowTargetItems);
-        const unsigned long long tps = (tot + target - 1) / target;
-        s_tps = (int)(tps < 1 ? 1 : tps);
-    }
-    __syncthreads();
-    const int tps = s_tps;
-    auto ns_of = [&](int4 v) { return v.w > 0 ? (v.w + tps - 1) / tps : 0; };
+    const unsigned long long row_tiles_all = s_row_tiles;
+    if (tid == 0 && row_tiles_all >= (1ull << 31)) report_error(p.dev_err, PCP_ERR_UNSUPPORTED);
+    const int T = (int)min(row_tiles_all, (unsigned long long)INT32_MAX);
+    // the split uses min(n, T) CTAs, so every one of them holds at least one
+    // tile and every partial slot of a group is written
+    const int n_use = row_ctas_used(n_ctas, T);
+    // the row-kernel CTA holding tile x: the last i with i*T/n_use <= x
+    auto cta_of = [&](int x) {
+        return (int)((((int64_t)x + 1) * n_use + T - 1) / T) - 1;
+    };
 
-    // ---- sweep 2: histogram of row-item lengths (for longest-first order)
-    for (int chunk0 = 0; chunk0 < p.batch; chunk0 += 1024) {
-        __syncthreads();
-        if (!one_chunk) load_chunk(chunk0, false);
-        s_b[tid] = ns_of(s_seq[tid]);
-        __syncthreads();
-        const int total = excl_scan(s_b, warp_sums);
-        for (int f = tid; f < total; f += 1024) {
-            const int sl = segment_of(s_b, 1024, f);
-            const int tiles = s_seq[sl].w, ns = s_b[sl + 1] - s_b[sl], sp = f - s_b[sl];
-            const int len = split_end(tiles, ns, sp) - split_end(tiles, ns, sp - 1);
-            warp_agg_add(hist_r, min(len, 1023), H);
-        }
-    }
-    __syncthreads();
-    const int n_row = desc_offsets(hist_r, warp_sums);
-
-    // ---- sweep 3: scatter tensor-core items and row items
-    int slot_base = 0;  // partial slots used by earlier chunks
+    // ---- sweep 2: scatter tensor-core items and row groups
+    int grp_base = 0;   // row groups of earlier chunks
+    int tile_base = 0;  // row tiles of earlier chunks
     for (int chunk0 = 0; chunk0 < p.batch; chunk0 += 1024) {
         __syncthreads();
         if (!one_chunk) load_chunk(chunk0, false);
         s_a[tid] = n_tc_of(s_seq[tid]);
-        s_b[tid] = ns_of(s_seq[tid]);
+        s_b[tid] = s_seq[tid].w > 0 ? H : 0;
+        s_c[tid] = s_seq[tid].w;
         __syncthreads();
         const int total_a = excl_scan(s_a, warp_sums);
         const int total_b = excl_scan(s_b, warp_sums);
+        const int total_c = excl_scan(s_c, warp_sums);
         for (int f = tid; f < total_a; f += 1024) {
             const int sl = segment_of(s_a, 1024, f);
             const int4 v = s_seq[sl];
@@ -276,40 +256,38 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
         for (int f = tid; f < total_b; f += 1024) {
             const int sl = segment_of(s_b, 1024, f);
             const int b = chunk0 + sl;
+            const int g = f - s_b[sl];
+            const int k = grp_base + f;
             const int4 v = s_seq[sl];
-            const int tiles = v.w, ns = s_b[sl + 1] - s_b[sl], sp = f - s_b[sl];
-            const int P = v.y, L = v.x + v.y;
-            const int lo = first_key(P, p.window);
-            const int t0 = lo / kRowTile;
-            const int tb = t0 + split_end(tiles, ns, sp - 1);
-            const int te = t0 + split_end(tiles, ns, sp);
-            const int kb = max(lo, tb * kRowTile);
-            const int ke = min(L, te * kRowTile);
-            const int q0 = p.qo_indptr[b];
-            const int kvb = p.kv_indptr[b];
-            const int it = warp_agg_add(hist_r, min(te - tb, 1023), H);
-            for (int g = 0; g < H; ++g) {
-                // the group's partial slots are consecutive: base + split
-                const int base = slot_base + s_b[sl] * H + g * ns;
-                if (it + g >= p.lay.cap_row || base + ns > p.lay.cap_row) {
-                    report_error(p.dev_err, PCP_ERR_WORKSPACE);
-                    break;
-                }
-                if (sp == 0) gdesc[(int64_t)b * H + g] = make_int4(base, ns, q0, v.x);
-                rows[3 * (it + g)] = make_int4(b, g, sp, ns);
-                rows[3 * (it + g) + 1] = make_int4(kb, ke, base, q0);
-                rows[3 * (it + g) + 2] = make_int4(v.x, P, kvb, L);
+            const int tiles = v.w;
+            const int S = tile_base + s_c[sl] * H + g * tiles;
+            const int i_first = cta_of(S), i_last = cta_of(S + tiles - 1);
+            const int ns = i_last - i_first + 1;
+            const int base = k + i_first;
+            if (k >= p.lay.cap_groups || base + ns > p.lay.cap_row) {
+                report_error(p.dev_err, PCP_ERR_WORKSPACE);
+                continue;
             }
+            const int P = v.y, L = v.x + v.y;
+            const int q0 = p.qo_indptr[b];
+            rg[3 * k] = make_int4(b, g, S, tiles);
+            rg[3 * k + 1] = make_int4(first_key(P, p.window), q0, base, ns);
+            rg[3 * k + 2] = make_int4(v.x, P, p.kv_indptr[b], L);
+            gdesc[(int64_t)b * H + g] = make_int4(base, ns, q0, v.x);
+            // CTAs whose first tile lies in this group start with it
+            for (int i = i_first; i <= i_last; ++i)
+                if (row_tile_begin(i, n_use, T) >= S) row_first[i] = k;
         }
-        slot_base += total_b * H;
+        grp_base += total_b;
+        tile_base += total_c * H;
     }
     __syncthreads();
     if (tid == 0) {
         hdr->n_tc_items = (int)min((int64_t)n_tc, p.lay.cap_tc);
-        hdr->n_row_items = (int)min((int64_t)n_row, p.lay.cap_row);
+        hdr->n_row_groups = (int)min((int64_t)grp_base, p.lay.cap_groups);
         hdr->tc_next = 0;
-        hdr->row_next = 0;
-        hdr->tiles_per_split = tps;
+        hdr->row_tiles = T;
+        hdr->row_ctas = n_ctas;
     }
 }
 

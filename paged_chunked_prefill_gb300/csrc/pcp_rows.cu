@@ -99,9 +99,8 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     const int gid = lane >> 2, tig = lane & 3;
     pdl_wait();  // the work list is the planner's output
     pdl_launch_dependents();
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
-    const int n_items = hdr->n_row_items;
-    const int4* items = reinterpret_cast<const int4*>(p.ws + p.lay.row_items);
+    const WsHeader* hdr = reinterpret_cast<const WsHeader*>(p.ws + p.lay.header);
+    const int4* rg = reinterpret_cast<const int4*>(p.ws + p.lay.row_groups);
     float* part_o = reinterpret_cast<float*>(p.ws + p.lay.partial_o);
     float2* part_ml = reinterpret_cast<float2*>(p.ws + p.lay.partial_ml);
     const int G = p.group;
@@ -117,16 +116,19 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     // the four consumer warps only (named barrier 1)
     auto consumer_sync = [] { asm volatile("bar.sync 1, 128;" ::: "memory"); };
 
-    // Items come from the longest-first list in snake order (round k takes
-    // position blockIdx.x of the k-th block of gridDim.x items, mirrored on odd
-    // rounds), which balances large and small items across CTAs; the load
-    // warp knows the next item in advance and reads its descriptor and first
-    // page ids during this one.
-    auto item_of = [&](int k) {
-        const int in_round = (k & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
-        return k * (int)gridDim.x + in_round;
-    };
-    if ((int)blockIdx.x >= n_items) return;
+    // This CTA streams row tiles [x0, x1) of the T tiles of all row groups
+    // laid end to end: the same amount of K/V for every CTA.  Each row group
+    // it meets (from row_first[blockIdx.x] on) is one item; the load warp
+    // resolves the next item and reads its first page ids during this one.
+    const int T = hdr->row_tiles;
+    if (hdr->row_ctas != (int)gridDim.x) {  // the plan was made for another grid
+        if (tid == 0 && T > 0) report_error(p.dev_err, PCP_ERR_INVALID_ARG);
+        return;
+    }
+    const int n_use = row_ctas_used(gridDim.x, T);
+    if ((int)blockIdx.x >= n_use) return;
+    const int x0 = row_tile_begin(blockIdx.x, n_use, T);
+    const int x1 = row_tile_begin(blockIdx.x + 1, n_use, T);
     if (tid == 0) {
         const uint32_t full_count = p.box_rows > 0 ? 1u : 32u;
         for (int s = 0; s < S; ++s) {
@@ -175,25 +177,41 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 }
             }
         };
+        // the piece of row group kg = {A, B, C} that lies in [x0, x1) as a
+        // row item {b, g, split, n_splits}, {kv_begin, kv_end, first partial
+        // slot, q0}, {chunk_len, prefix_len, kv_indptr[b], kv_len}; its split
+        // index is blockIdx.x - (first CTA of the group) = blockIdx.x + kg - slot
+        auto resolve = [&](int kg, int4 A, int4 B, int4 Cg, int4& e0, int4& e1, int4& e2) {
+            const int a = max(x0, A.z) - A.z, e = min(x1, A.z + A.w) - A.z;
+            const int t0 = B.x / kRowTile;
+            e0 = make_int4(A.x, A.y, (int)blockIdx.x + kg - B.z, B.w);
+            e1 = make_int4(max(B.x, (t0 + a) * kRowTile), min(Cg.w, (t0 + e) * kRowTile), B.z,
+                           B.y);
+            e2 = Cg;
+        };
         uint32_t it = 0;  // ring position
         int last_issued = -1;
-        int item = item_of(0);
-        int4 n0 = items[3 * item], n1 = items[3 * item + 1], n2 = items[3 * item + 2];
+        int kg = reinterpret_cast<const int*>(p.ws + p.lay.row_first)[blockIdx.x];
+        int4 gA = rg[3 * kg], gB = rg[3 * kg + 1], gC = rg[3 * kg + 2];
+        int4 n0, n1, n2;
+        resolve(kg, gA, gB, gC, n0, n1, n2);
         int next_sl[4];
         fetch(p.kv_indices + n2.z, n2.w, n1.x / kRowTile, next_sl);
-        for (int k = 0;; ++k, item = item_of(k)) {
+        bool have = true;  // n0..n2 hold an item
+        for (int k = 0;; ++k) {
             const int qs = k % NI;
-            const bool valid = item < n_items && !*abort_flag;
+            const bool valid = have && !*abort_flag;
             const int4 d0 = n0, d1 = n1, d2 = n2;
             int cur_sl[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) cur_sl[j] = next_sl[j];
-            const int next_item = item_of(k + 1);
-            const bool next_valid = valid && next_item < n_items;
+            // the range goes on past this group: the next group follows
+            const bool next_valid = valid && gA.z + gA.w < x1;
             if (next_valid) {  // loads in flight during this item
-                n0 = items[3 * next_item];
-                n1 = items[3 * next_item + 1];
-                n2 = items[3 * next_item + 2];
+                ++kg;
+                gA = rg[3 * kg];
+                gB = rg[3 * kg + 1];
+                gC = rg[3 * kg + 2];
             }
             // hand the item (or the end marker) and its Q rows to the consumers
             if (!mbar_wait(item_empty(qs), ((uint32_t)(k / NI) & 1u) ^ 1u, abort_flag, p.dev_err,
@@ -286,14 +304,17 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                     cp_async_mbar_arrive_noinc(full_bar(st));
                 }
                 last_issued = (int)itp;
-                if (i == 0 && next_valid)  // the next item's first page ids
+                if (i == 0 && next_valid) {  // the next item and its first page ids
+                    resolve(kg, gA, gB, gC, n0, n1, n2);
                     fetch(p.kv_indices + n2.z, n2.w, n1.x / kRowTile, next_sl);
+                }
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     if (i + 1 < ntiles) cur_sl[j] = nsl[j];
             }
             if (*abort_flag) break;
             it += (uint32_t)ntiles;
+            have = next_valid;
         }
         // nothing may still be landing in shared memory when the CTA exits
         cp_async_wait_all();

@@ -43,8 +43,9 @@ def bf16_tensor_bits(t) -> np.ndarray:
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def run_gpu(batch, d=None, check=True):
-    """out_cache_loc -> kv_append -> paged_extend_attn on the GPU."""
+def run_gpu(batch, d=None, check=True, host_hint=True):
+    """out_cache_loc -> kv_append -> paged_extend_attn on the GPU (with the
+    host copy of qo_indptr unless host_hint is False)."""
     import paged_chunked_prefill_gb300 as pcp
     if d is None:
         d = to_device(batch)
@@ -55,7 +56,8 @@ def run_gpu(batch, d=None, check=True):
     out, lse = pcp.paged_extend_attn(d["q"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
                                      d["prefix_lens"], d["k_pool"], d["v_pool"],
                                      batch.page_size, batch.n_q_heads, batch.n_kv_heads,
-                                     batch.head_dim, batch.window, batch.sm_scale, check=check)
+                                     batch.head_dim, batch.window, batch.sm_scale, check=check,
+                                     qo_indptr_host=batch.qo_indptr if host_hint else None)
     return loc, d, out, lse
 
 

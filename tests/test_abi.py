@@ -41,7 +41,7 @@ def test_status_strings(lib):
         s = lib.pcp_status_string(code).decode()
         assert s.startswith("PCP_")
     assert lib.pcp_status_string(99).decode() == "PCP_ERR_UNKNOWN"
-    assert lib.pcp_abi_version() == 1
+    assert lib.pcp_abi_version() == 2
 
 
 def test_workspace_size(lib):
@@ -60,24 +60,35 @@ def test_host_validation_without_device(lib):
     dummy = ctypes.c_int32(0)
     err = ctypes.cast(ctypes.pointer(dummy), P)
     one = P(0x1000)
-    st = lib.pcp_paged_extend_attn(one, one, one, one, one, 1, 10, one, one, 4, 16, 30, 8, 128,
+    st = lib.pcp_paged_extend_attn(one, one, one, one, one, P(0), 1, 10, one, one, 4, 16, 30, 8, 128,
                                    0, 0.0, one, one, one, 1 << 20, err, P(0))
     assert st == 1   # INVALID_ARG: 30 % 8 != 0
-    st = lib.pcp_paged_extend_attn(one, one, one, one, one, 1, 10, one, one, 4, 16, 8, 8, 96,
+    st = lib.pcp_paged_extend_attn(one, one, one, one, one, P(0), 1, 10, one, one, 4, 16, 8, 8, 96,
                                    0, 0.0, one, one, one, 1 << 20, err, P(0))
     assert st == 2   # UNSUPPORTED head_dim
-    st = lib.pcp_paged_extend_attn(one, one, one, one, one, 1, 10, one, one, 4, 16, 8, 8, 128,
+    st = lib.pcp_paged_extend_attn(one, one, one, one, one, P(0), 1, 10, one, one, 4, 16, 8, 8, 128,
                                    -1, 0.0, one, one, one, 1 << 20, err, P(0))
     assert st == 1   # negative window
-    st = lib.pcp_paged_extend_attn(one, one, one, one, one, 1, 10, one, one, 4, 16, 8, 8, 128,
+    st = lib.pcp_paged_extend_attn(one, one, one, one, one, P(0), 1, 10, one, one, 4, 16, 8, 8, 128,
                                    0, 0.0, one, one, one, 16, err, P(0))
     assert st == 4   # workspace too small
+    # a host copy of qo_indptr that disagrees with total_q, or decreases
+    for host in ([0, 4, 9], [0, 6, 4, 10]):
+        h = (ctypes.c_int32 * len(host))(*host)
+        st = lib.pcp_paged_extend_attn(one, one, one, one, one, ctypes.cast(h, P),
+                                       len(host) - 1, 10, one, one, 4, 16, 8, 8, 128, 0, 0.0,
+                                       one, one, one, 1 << 30, err, P(0))
+        assert st == 1, host
     st = lib.pcp_kv_append(one, one, one, 5, 2, 128, one, one, 10, P(0), P(0))
     assert st == 1   # no error word
     st = lib.pcp_compute_out_cache_loc(one, one, one, one, 2, 10, 0, 4, one, err, P(0))
     assert st == 1   # page_size 0
+    # the profiling hook takes a known kernel and both events or neither
+    assert lib.pcp_set_timing_events(7, P(0), P(0)) == 1
+    assert lib.pcp_set_timing_events(0, one, P(0)) == 1
+    assert lib.pcp_set_timing_events(1, P(0), P(0)) == 0
     # empty work returns OK without touching the device
-    assert lib.pcp_paged_extend_attn(P(0), P(0), P(0), P(0), P(0), 0, 0, P(0), P(0), 0, 16, 8,
+    assert lib.pcp_paged_extend_attn(P(0), P(0), P(0), P(0), P(0), P(0), 0, 0, P(0), P(0), 0, 16, 8,
                                      8, 128, 0, 0.0, P(0), P(0), P(0), 0, err, P(0)) == 0
     assert lib.pcp_kv_append(P(0), P(0), P(0), 0, 2, 128, P(0), P(0), 0, err, P(0)) == 0
 

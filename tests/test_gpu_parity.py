@@ -121,8 +121,36 @@ def test_windows(window):
     full_parity(b, f"window {window}")
 
 
+@pytest.mark.parametrize("case", ["mixed", "decode", "prefill"])
+def test_host_hint_is_bit_identical(case):
+    """With and without the host copy of qo_indptr the same kernels do the
+    work (the hint only skips launches that have none): identical bits."""
+    if case == "mixed":
+        b = W.mixed_batch(prompt=700, chunk=300, n_decode=9, decode_max=1500)
+    elif case == "decode":
+        b = W.make_batch([5, 900, 3000, 40], [1, 1, 2, 1], 16, 4, 128, 64, seed=30)
+    else:
+        b = W.make_batch([0, 300], [200, 77], 16, 4, 128, 16, seed=31)
+    res = []
+    for hint in (True, False):
+        _, _, out, lse = run_gpu(b, host_hint=hint)
+        res.append((bf16_tensor_bits(out), lse.cpu().numpy()))
+    np.testing.assert_array_equal(res[0][0], res[1][0])
+    np.testing.assert_array_equal(res[0][1], res[1][1])
+    full_parity(b, f"hinted {case}")
+
+
+def test_decode_rows_many_splits():
+    """A few very long decode rows and many short ones: the long groups span
+    many row-kernel CTAs (many partial slots), the short ones share a CTA."""
+    rng = np.random.default_rng(12)
+    P = [60000, 45000] + list(rng.integers(1, 300, size=40))
+    b = W.make_batch(P, [1] * len(P), 8, 2, 128, 16, seed=32)
+    full_parity(b, "many splits")
+
+
 def test_decode_only_long():
-    """Many decode rows with long KV: split-KV items and the fused combine."""
+    """Many decode rows with long KV: split-KV items and the combine."""
     b = W.make_batch(list(np.random.default_rng(3).integers(1, 9000, size=12)), [1] * 12, 16, 4,
                      128, 64, seed=33)
     full_parity(b, "decode rows")

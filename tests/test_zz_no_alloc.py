@@ -29,7 +29,8 @@ def _noalloc_fn():
     import paged_chunked_prefill_gb300 as pcp
     f = pcp.lib().pcp_paged_extend_attn_noalloc
     P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
-    f.argtypes = [P, P, P, P, P, i32, i64, P, P, i64, i32, i32, i32, i32, i32, f32, P, P, P, P]
+    f.argtypes = [P, P, P, P, P, P, i32, i64, P, P, i64, i32, i32, i32, i32, i32, f32, P, P, P,
+                  P]
     f.restype = i32
     return f
 
@@ -53,7 +54,8 @@ def _run_both(batch):
     ptr = lambda t: ctypes.c_void_p(t.data_ptr())
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     st = _noalloc_fn()(ptr(d["q"]), ptr(d["qo_indptr"]), ptr(d["kv_indptr"]),
-                       ptr(d["kv_indices"]), ptr(d["prefix_lens"]), batch.batch, batch.total_q,
+                       ptr(d["kv_indices"]), ptr(d["prefix_lens"]), ctypes.c_void_p(0),
+                       batch.batch, batch.total_q,
                        ptr(d["k_pool"]), ptr(d["v_pool"]), batch.num_pages, batch.page_size,
                        batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.window,
                        float(batch.sm_scale), ptr(out), ptr(lse), ptr(err), stream)
@@ -78,6 +80,6 @@ def test_noalloc_refuses_oversized_calls():
     need = pcp.workspace_size(4096, 65536, 32, 8, 128)
     assert need > 16 * 1024 * 1024
     P = ctypes.c_void_p
-    st = _noalloc_fn()(P(0), P(0), P(0), P(0), P(0), 4096, 65536, P(0), P(0), 1, 16, 32, 8, 128,
-                       0, 0.0, P(0), P(0), P(0), P(0))
+    st = _noalloc_fn()(P(0), P(0), P(0), P(0), P(0), P(0), 4096, 65536, P(0), P(0), 1, 16, 32, 8,
+                       128, 0, 0.0, P(0), P(0), P(0), P(0))
     assert st == pcp.Status.WORKSPACE
