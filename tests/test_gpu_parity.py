@@ -150,7 +150,7 @@ def test_decode_rows_many_splits():
 
 
 def test_decode_only_long():
-    """Many decode rows with long KV: split-KV items and the combine."""
+    """Many decode rows with long KV: split-KV pieces and the combine."""
     b = W.make_batch(list(np.random.default_rng(3).integers(1, 9000, size=12)), [1] * 12, 16, 4,
                      128, 64, seed=33)
     full_parity(b, "decode rows")
