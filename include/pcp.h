@@ -87,6 +87,13 @@ const char* pcp_status_string(int status);
 int pcp_abi_version(void);
 
 /*
+ * Text of the CUDA error behind the last PCP_ERR_CUDA an entry point returned
+ * on the calling thread ("no error" if there was none).  Static string;
+ * never NULL.
+ */
+const char* pcp_last_cuda_error(void);
+
+/*
  * Slot mapping for the new tokens of every sequence (integer, bit-exact):
  *   out_cache_loc[t] = kv_indices[kv_indptr[b] + p / page_size] * page_size
  *                      + p % page_size,   p = prefix_lens[b] + (t - qo_indptr[b])

@@ -34,6 +34,8 @@ class PCPError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = int(status)
         msg = lib().pcp_status_string(int(status)).decode()
+        if self.status == Status.CUDA:
+            msg += f" ({lib().pcp_last_cuda_error().decode()})"
         super().__init__(f"{where}: {msg}")
 
 
@@ -55,6 +57,8 @@ def lib():
         L.pcp_status_string.restype = ctypes.c_char_p
         L.pcp_abi_version.argtypes = []
         L.pcp_abi_version.restype = i32
+        L.pcp_last_cuda_error.argtypes = []
+        L.pcp_last_cuda_error.restype = ctypes.c_char_p
         L.pcp_compute_out_cache_loc.argtypes = [P, P, P, P, i32, i64, i32, i64, P, P, P]
         L.pcp_compute_out_cache_loc.restype = i32
         L.pcp_kv_append.argtypes = [P, P, P, i64, i32, i32, P, P, i64, P, P]

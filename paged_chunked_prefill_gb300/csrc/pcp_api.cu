@@ -39,6 +39,15 @@ cudaError_t launch_kv_append(const void* k, const void* v, const int64_t* loc, i
 
 namespace {
 
+// The CUDA error behind the last PCP_ERR_CUDA returned on this thread.
+thread_local cudaError_t t_last_cuda = cudaSuccess;
+
+bool failed(cudaError_t e) {
+    if (e == cudaSuccess) return false;
+    t_last_cuda = e;
+    return true;
+}
+
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_sm_count[kMaxDevices] = {0};
@@ -53,12 +62,12 @@ cudaEvent_t g_ev_before[2] = {nullptr, nullptr}, g_ev_after[2] = {nullptr, nullp
 // SM count of the current device, cached per device.
 pcp_status sm_count(int* out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return PCP_ERR_CUDA;
+    if (failed(cudaGetDevice(&dev))) return PCP_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
     if (dev < 0 || dev >= kMaxDevices) return PCP_ERR_UNSUPPORTED;
     if (g_sm_count[dev] == 0) {
         int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        if (failed(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)))
             return PCP_ERR_CUDA;
         g_sm_count[dev] = n;
     }
@@ -71,8 +80,8 @@ pcp_status get_encoder(EncodeFn* fn) {
     if (g_encode == nullptr) {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
+        if (failed(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                    cudaEnableDefault, &q)) ||
             q != cudaDriverEntryPointSuccess || p == nullptr)
             return PCP_ERR_CUDA;
         g_encode = reinterpret_cast<EncodeFn>(p);
@@ -96,6 +105,7 @@ pcp_status encode_3d(EncodeFn enc, CUtensorMap* map, const void* base, uint64_t 
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
 
 int gcd_int(int a, int b) {
     while (b) {
@@ -128,6 +138,10 @@ const char* pcp_status_string(int status) {
 
 int pcp_abi_version(void) { return 2; }
 
+const char* pcp_last_cuda_error(void) {
+    return t_last_cuda == cudaSuccess ? "no error" : cudaGetErrorString(t_last_cuda);
+}
+
 pcp_status pcp_compute_out_cache_loc(const int32_t* qo_indptr, const int32_t* kv_indptr,
                                      const int32_t* kv_indices, const int32_t* prefix_lens,
                                      int batch, int64_t total_q, int page_size,
@@ -145,7 +159,7 @@ pcp_status pcp_compute_out_cache_loc(const int32_t* qo_indptr, const int32_t* kv
     cudaError_t e = launch_out_cache_loc(qo_indptr, kv_indptr, kv_indices, prefix_lens, batch,
                                          total_q, page_size, num_pages, out_cache_loc, dev_err,
                                          sms, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? PCP_OK : PCP_ERR_CUDA;
+    return failed(e) ? PCP_ERR_CUDA : PCP_OK;
 }
 
 pcp_status pcp_kv_append(const void* k, const void* v, const int64_t* out_cache_loc,
@@ -164,7 +178,7 @@ pcp_status pcp_kv_append(const void* k, const void* v, const int64_t* out_cache_
     const int chunks = n_kv_heads * head_dim * 2 / 16;
     cudaError_t e = launch_kv_append(k, v, out_cache_loc, n_tokens, chunks, k_pool, v_pool,
                                      pool_slots, dev_err, sms, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? PCP_OK : PCP_ERR_CUDA;
+    return failed(e) ? PCP_ERR_CUDA : PCP_OK;
 }
 
 size_t pcp_extend_workspace_size(int batch, int64_t total_q, int n_q_heads, int n_kv_heads,
@@ -273,7 +287,7 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
     pp.ws = ws;
     pp.lay = lay;
     pp.dev_err = dev_err;
-    if (launch_plan(s, pp) != cudaSuccess) return PCP_ERR_CUDA;
+    if (failed(launch_plan(s, pp))) return PCP_ERR_CUDA;
 
     // ---- 2. tensor-core extend kernel (persistent, one CTA per SM)
     TcParams tp;
@@ -306,10 +320,9 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
         evrb = g_ev_before[PCP_TIMING_ROWS];
         evra = g_ev_after[PCP_TIMING_ROWS];
     }
-    if (evb && cudaEventRecord(evb, s) != cudaSuccess) return PCP_ERR_CUDA;
-    if (run_tc && launch_extend_tc(head_dim, sms, s, tp, tq, tk, tv) != cudaSuccess)
-        return PCP_ERR_CUDA;
-    if (eva && cudaEventRecord(eva, s) != cudaSuccess) return PCP_ERR_CUDA;
+    if (evb && failed(cudaEventRecord(evb, s))) return PCP_ERR_CUDA;
+    if (run_tc && failed(launch_extend_tc(head_dim, sms, s, tp, tq, tk, tv))) return PCP_ERR_CUDA;
+    if (eva && failed(cudaEventRecord(eva, s))) return PCP_ERR_CUDA;
 
     // ---- 3. decode-shaped rows (split-KV on CUDA cores, equal tiles per CTA)
     if (run_rows) {
@@ -335,10 +348,9 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
         rp.window = window;
         rp.scale_log2 = scale_log2;
         rp.dev_err = dev_err;
-        if (evrb && cudaEventRecord(evrb, s) != cudaSuccess) return PCP_ERR_CUDA;
-        if (launch_rows(head_dim, row_grid(sms), s, rp, tk, tv) != cudaSuccess)
-            return PCP_ERR_CUDA;
-        if (evra && cudaEventRecord(evra, s) != cudaSuccess) return PCP_ERR_CUDA;
+        if (evrb && failed(cudaEventRecord(evrb, s))) return PCP_ERR_CUDA;
+        if (failed(launch_rows(head_dim, row_grid(sms), s, rp, tk, tv))) return PCP_ERR_CUDA;
+        if (evra && failed(cudaEventRecord(evra, s))) return PCP_ERR_CUDA;
         // ---- 4. merge split-KV partials (one CTA per split group)
         CombineParams cp;
         cp.ws = ws;
@@ -349,7 +361,7 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
         cp.n_kv_heads = n_kv_heads;
         cp.group = group;
         cp.n_groups = batch * n_kv_heads;
-        if (launch_combine(head_dim, s, cp) != cudaSuccess) return PCP_ERR_CUDA;
+        if (failed(launch_combine(head_dim, s, cp))) return PCP_ERR_CUDA;
     }
     return PCP_OK;
 }
@@ -357,10 +369,9 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
 pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_err) {
     if (dev_err == nullptr || host_err == nullptr) return PCP_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(host_err, dev_err, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
-        cudaSuccess)
+    if (failed(cudaMemcpyAsync(host_err, dev_err, sizeof(int32_t), cudaMemcpyDeviceToHost, s)))
         return PCP_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return PCP_ERR_CUDA;
+    if (failed(cudaStreamSynchronize(s))) return PCP_ERR_CUDA;
     return PCP_OK;
 }
 

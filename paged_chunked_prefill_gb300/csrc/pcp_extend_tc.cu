@@ -66,6 +66,9 @@ struct TcCfg {
     static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 6 + 1;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;
+    static_assert(kOffBar % 8 == 0 && kOffMisc % 4 == 0, "smem alignment");
+    static_assert(kOffQ % 1024 == 0 && kOffK % 1024 == 0 && kOffV % 1024 == 0,
+                  "128-byte-swizzled operands need 1024-byte alignment");
     // barrier indices
     static constexpr int bQFull = 0;
     static constexpr int bKFull = 1;

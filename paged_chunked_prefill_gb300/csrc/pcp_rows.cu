@@ -44,6 +44,8 @@ struct RowCfg {
     static constexpr int kOffBar = kOffDesc + kItemSlots * 48;
     static constexpr int kOffM = kOffBar + (2 * kStages + 2 * kItemSlots) * 8;  // float [4][16] m, l
     static constexpr int kSmemBytes = kOffM + 2 * 4 * kRowMaxRows * 4 + 64 + 1024;
+    static_assert(kOffDesc % 16 == 0 && kOffBar % 8 == 0 && kOffStage % 1024 == 0,
+                  "smem alignment");
 };
 
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,

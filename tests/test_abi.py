@@ -42,6 +42,8 @@ def test_status_strings(lib):
         assert s.startswith("PCP_")
     assert lib.pcp_status_string(99).decode() == "PCP_ERR_UNKNOWN"
     assert lib.pcp_abi_version() == 2
+    lib.pcp_last_cuda_error.restype = ctypes.c_char_p
+    assert lib.pcp_last_cuda_error().decode() == "no error"
 
 
 def test_workspace_size(lib):
