@@ -75,8 +75,15 @@ def _load():
                                               i32, dbl, i64, P, P, P, P]
         lib.oracle_attention.argtypes = [i32, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32,
                                          dbl, P, P]
+        mask_args = [i32, P, i64, i64, i64, i64, i64]
+        lib.oracle_attention_rows_masked.argtypes = (
+            [i32, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, dbl] + mask_args +
+            [i64, P, P, P, P])
+        lib.oracle_attention_masked.argtypes = (
+            [i32, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, dbl] + mask_args + [P, P])
         for f in (lib.oracle_out_cache_loc, lib.oracle_kv_append, lib.oracle_attention_rows,
-                  lib.oracle_attention, lib.oracle_num_threads, lib.oracle_version):
+                  lib.oracle_attention, lib.oracle_attention_rows_masked,
+                  lib.oracle_attention_masked, lib.oracle_num_threads, lib.oracle_version):
             f.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -134,15 +141,36 @@ def kv_append(k: np.ndarray, v: np.ndarray, loc: np.ndarray, k_pool: np.ndarray,
         raise OracleError(st, "kv_append")
 
 
+def mask_view(mask, batch: int, n_q_heads: int):
+    """A boolean mask as (uint8 array, b, h, q strides in elements, q extent,
+    kv extent): 2-D [batch, kv] (one key mask per sequence) or 4-D
+    [batch, 1 or Hq, 1 or q_len, kv]; size-1 head / query dimensions
+    broadcast (stride 0)."""
+    m = np.ascontiguousarray(np.asarray(mask, dtype=bool)).view(np.uint8)
+    if m.ndim == 2:
+        if m.shape[0] != batch:
+            raise ValueError("mask batch mismatch")
+        return m, m.shape[1], 0, 0, 1, m.shape[1]
+    if m.ndim != 4 or m.shape[0] != batch or m.shape[1] not in (1, n_q_heads):
+        raise ValueError("mask must be [B, kv] or [B, 1|Hq, 1|q, kv]")
+    sb = m.shape[1] * m.shape[2] * m.shape[3]
+    sh = 0 if m.shape[1] == 1 else m.shape[2] * m.shape[3]
+    sq = 0 if m.shape[2] == 1 else m.shape[3]
+    return m, sb, sh, sq, m.shape[2], m.shape[3]
+
+
 def paged_extend_attn(q, qo_indptr, kv_indptr, kv_indices, prefix_lens, k_pool, v_pool,
                       page_size: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
                       window: int = 0, sm_scale: float = 0.0,
-                      rows: Optional[Tuple[np.ndarray, np.ndarray]] = None):
+                      rows: Optional[Tuple[np.ndarray, np.ndarray]] = None,
+                      causal: bool = True, mask=None):
     """Extend attention in float64.
 
     Without ``rows``: returns out [total_q, Hq, D] and lse [total_q, Hq].
     With ``rows = (tokens, heads)``: returns out [n, D] and lse [n] for just
-    those (row of q, query head) pairs.
+    those (row of q, query head) pairs.  ``causal=False`` lets every row see
+    all of its sequence's keys; ``mask`` (see ``mask_view``) hides the keys
+    whose entry is False.
     """
     lib = _load()
     qo = _c(qo_indptr, np.int32)
@@ -157,11 +185,16 @@ def paged_extend_attn(q, qo_indptr, kv_indptr, kv_indices, prefix_lens, k_pool, 
     args = (B, _p(qo), _p(kvp), _p(kvi), _p(pl), _p(qb), _p(kp), _p(vp), num_pages,
             int(page_size), int(n_q_heads), int(n_kv_heads), int(head_dim), int(window),
             float(sm_scale))
+    if mask is None:
+        m, margs = None, (int(bool(causal)), None, 0, 0, 0, 0, 0)
+    else:
+        m, sb, sh, sq, ql, kl = mask_view(mask, B, n_q_heads)
+        margs = (int(bool(causal)), _p(m), sb, sh, sq, ql, kl)
     if rows is None:
         total_q = int(qo[-1])
         out = np.zeros((max(total_q, 1), n_q_heads, head_dim), dtype=np.float64)
         lse = np.zeros((max(total_q, 1), n_q_heads), dtype=np.float64)
-        st = lib.oracle_attention(*args, _p(out), _p(lse))
+        st = lib.oracle_attention_masked(*args, *margs, _p(out), _p(lse))
         if st != OK:
             raise OracleError(st, "attention")
         return out[:total_q], lse[:total_q]
@@ -170,13 +203,14 @@ def paged_extend_attn(q, qo_indptr, kv_indptr, kv_indices, prefix_lens, k_pool, 
     n = int(np.asarray(rows[0]).shape[0])
     out = np.zeros((max(n, 1), head_dim), dtype=np.float64)
     lse = np.zeros(max(n, 1), dtype=np.float64)
-    st = lib.oracle_attention_rows(*args, n, _p(tok), _p(head), _p(out), _p(lse))
+    st = lib.oracle_attention_rows_masked(*args, *margs, n, _p(tok), _p(head), _p(out),
+                                          _p(lse))
     if st != OK:
         raise OracleError(st, "attention_rows")
     return out[:n], lse[:n]
 
 
-def run_batch(batch, rows=None):
+def run_batch(batch, rows=None, causal=True, mask=None):
     """Append a workload's chunk into copies of its pools, then attend.
 
     Returns (out_cache_loc, k_pool_after, v_pool_after, out, lse)."""
@@ -188,5 +222,5 @@ def run_batch(batch, rows=None):
     out, lse = paged_extend_attn(batch.q, batch.qo_indptr, batch.kv_indptr, batch.kv_indices,
                                  batch.prefix_lens, kp, vp, batch.page_size, batch.n_q_heads,
                                  batch.n_kv_heads, batch.head_dim, batch.window,
-                                 batch.sm_scale, rows=rows)
+                                 batch.sm_scale, rows=rows, causal=causal, mask=mask)
     return loc, kp, vp, out, lse

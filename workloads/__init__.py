@@ -25,7 +25,7 @@ import numpy as np
 __all__ = [
     "Batch", "bf16_bits", "bf16_to_f32", "make_batch", "tiny_case",
     "zero_score_steps", "gqa_prefill", "mixed_batch", "stress_case",
-    "long_context", "CONFIGS", "config_by_name",
+    "long_context", "random_mask", "CONFIGS", "config_by_name",
 ]
 
 
@@ -324,6 +324,28 @@ def long_context(seed: int = 1005, batch: int = 4, prefix: int = 32768, chunk: i
                       page_size, seed=seed,
                       name=f"long context: B={batch}, prefix={prefix}, chunk={chunk}, "
                            f"{n_q_heads}q/{n_kv_heads}kv, D={head_dim}, ps={page_size}")
+
+
+def random_mask(batch: Batch, kind: str, seed: int, keep: float = 0.6) -> np.ndarray:
+    """A seeded boolean attention mask (True = keep) for ``batch``, laid out
+    as the attention call takes it:
+
+    * ``"2d"``       [B, kv]          one key mask per sequence
+    * ``"4d_bcast"`` [B, 1, q, kv]    per query row, shared by all heads
+    * ``"4d_heads"`` [B, Hq, q, kv]   per query row and head
+    * ``"4d_q1"``    [B, 1, 1, kv]    broadcast over rows and heads
+
+    q is the longest chunk, kv the longest KV length rounded up to a multiple
+    of 16 (entries past a sequence's end are never read).  Each entry is True
+    with probability ``keep``."""
+    rng = np.random.default_rng(seed)
+    B = batch.batch
+    qmax = int(batch.chunk_lens.max()) if B else 1
+    kv = int(-(-int(batch.kv_lens.max()) // 16) * 16) if B else 16
+    shape = {"2d": (B, kv), "4d_bcast": (B, 1, max(qmax, 1), kv),
+             "4d_heads": (B, batch.n_q_heads, max(qmax, 1), kv),
+             "4d_q1": (B, 1, 1, kv)}[kind]
+    return rng.random(shape) < keep
 
 
 CONFIGS = {
