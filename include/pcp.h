@@ -176,6 +176,39 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
                                  void* stream);
 
 /*
+ * Extend attention with a causal switch and an optional boolean mask (AstrAI
+ * attn_paged_prefill: `is_causal` and `mask`, True = keep, indexed by the
+ * request-local query row and key; its prefill-with-mask regression test runs
+ * a 4-D causal-pattern mask with causality off).  Arguments, layouts, results
+ * and errors are those of pcp_paged_extend_attn (which is this call with
+ * causal = 1 and no mask), plus:
+ *   causal    1: bottom-right causal (query row i sees keys j <= P_b + i, and
+ *                the window applies); 0: every row sees all keys j < L_b
+ *                (window must be 0).  Anything else is PCP_ERR_INVALID_ARG.
+ *   mask      NULL, or a DEVICE array of bytes (0 = masked, nonzero = keep).
+ *             Key j of query row i of sequence b, query head h is kept when
+ *             mask[b * mask_b_stride + h * mask_h_stride + i * mask_q_stride
+ *             + j] is nonzero, on top of the causal rule.  i is the row inside
+ *             the chunk (0 .. chunk_len_b - 1), j the key position
+ *             (0 .. L_b - 1).  A stride of 0 broadcasts that dimension (a 2-D
+ *             key mask [batch, kv] has h and q strides 0; a 4-D mask
+ *             [batch, 1, q, kv] has h stride 0).  Rows i >= mask_q_len (when
+ *             mask_q_stride != 0) and keys j >= mask_kv_len read as masked.
+ *             The mask must be 16-byte aligned and the three strides
+ *             non-negative multiples of 16 (bytes); otherwise
+ *             PCP_ERR_INVALID_ARG before anything is launched.
+ * A row whose visible set is empty gets out = 0 and lse = -inf.
+ */
+pcp_status pcp_paged_extend_attn_masked(
+    const void* q, const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+    const int32_t* prefix_lens, const int32_t* qo_indptr_host, int batch, int64_t total_q,
+    const void* k_pool, const void* v_pool, int64_t num_pages, int page_size, int n_q_heads,
+    int n_kv_heads, int head_dim, int window, float sm_scale, int causal, const uint8_t* mask,
+    int64_t mask_b_stride, int64_t mask_h_stride, int64_t mask_q_stride, int32_t mask_q_len,
+    int32_t mask_kv_len, void* out, float* lse, void* workspace, size_t workspace_bytes,
+    int32_t* dev_err, void* stream);
+
+/*
  * Size of the fixed device scratch array behind
  * pcp_paged_extend_attn_noalloc (16 MiB).  Every GPU that loads the library
  * keeps this much memory reserved until the process exits.

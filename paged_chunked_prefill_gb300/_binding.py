@@ -68,6 +68,10 @@ def lib():
         L.pcp_paged_extend_attn.argtypes = [P, P, P, P, P, P, i32, i64, P, P, i64, i32, i32,
                                             i32, i32, i32, f32, P, P, P, sz, P, P]
         L.pcp_paged_extend_attn.restype = i32
+        L.pcp_paged_extend_attn_masked.argtypes = [P, P, P, P, P, P, i32, i64, P, P, i64, i32,
+                                                   i32, i32, i32, i32, f32, i32, P, i64, i64,
+                                                   i64, i32, i32, P, P, P, sz, P, P]
+        L.pcp_paged_extend_attn_masked.restype = i32
         L.pcp_read_error.argtypes = [P, P, P]
         L.pcp_read_error.restype = i32
         L.pcp_set_timing_events.argtypes = [i32, P, P]
@@ -203,6 +207,29 @@ def kv_append(k: torch.Tensor, v: torch.Tensor, out_cache_loc: torch.Tensor,
     _finish(dev_err, own, check, "pcp_kv_append")
 
 
+def _mask_args(mask: Optional[torch.Tensor], batch: int, n_q_heads: int, device):
+    """(tensor kept alive, pointer, b/h/q strides, q extent, kv extent) of a
+    boolean mask: 2-D [batch, kv] or 4-D [batch, 1|Hq, 1|q, kv].  A mask whose
+    rows are not 16-byte aligned is copied into a padded one."""
+    if mask is None:
+        return None, ctypes.c_void_p(0), 0, 0, 0, 0, 0
+    if mask.dtype != torch.bool or mask.device != device:
+        raise TypeError(f"mask must be a bool tensor on {device}")
+    if mask.dim() == 2:
+        mask = mask.view(mask.shape[0], 1, 1, mask.shape[1])
+    if mask.dim() != 4 or mask.shape[0] != batch or mask.shape[1] not in (1, n_q_heads):
+        raise ValueError("mask must be [B, kv] or [B, 1|Hq, 1|q, kv]")
+    kv = mask.shape[3]
+    if kv % 16 != 0 or not mask.is_contiguous() or mask.data_ptr() % 16 != 0:
+        padded = torch.zeros(mask.shape[:3] + (-(-kv // 16) * 16,), dtype=torch.bool,
+                             device=device)
+        padded[..., :kv] = mask
+        mask = padded
+    sq = 0 if mask.shape[2] == 1 else mask.stride(2)
+    sh = 0 if mask.shape[1] == 1 else mask.stride(1)
+    return (mask, ctypes.c_void_p(mask.data_ptr()), mask.stride(0), sh, sq, mask.shape[2], kv)
+
+
 def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch.Tensor,
                       kv_indices: torch.Tensor, prefix_lens: torch.Tensor,
                       k_pool: torch.Tensor, v_pool: torch.Tensor, page_size: int,
@@ -211,7 +238,8 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
                       lse: Optional[torch.Tensor] = None,
                       workspace: Optional[torch.Tensor] = None,
                       dev_err: Optional[torch.Tensor] = None,
-                      qo_indptr_host=None,
+                      qo_indptr_host=None, causal: bool = True,
+                      mask: Optional[torch.Tensor] = None,
                       check: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
     """Extend attention of every query row over its cached prefix and own
     chunk (bottom-right causal, GQA, optional window).  Returns (out, lse):
@@ -219,7 +247,11 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
 
     qo_indptr_host: optional host copy of qo_indptr (numpy int32 array or CPU
     int32 tensor); with it the call skips the launch of a kernel that would
-    have no work."""
+    have no work.
+    causal=False: every row sees all keys of its sequence (no window).
+    mask: optional bool tensor (True = keep) of shape [B, kv] or
+    [B, 1|Hq, 1|q, kv], indexed by the row inside the chunk and the key
+    position, applied on top of the causal rule."""
     dev = q.device
     _need(q, "q", torch.bfloat16, dev)
     _need(k_pool, "k_pool", torch.bfloat16, dev)
@@ -245,11 +277,22 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
     if own:
         dev_err = _dev_err(dev)
     host_ptr, host_keep = _host_i32(qo_indptr_host, batch + 1, "qo_indptr_host")
-    _check(lib().pcp_paged_extend_attn(
-        _ptr(q), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(prefix_lens), host_ptr,
-        batch, total_q, _ptr(k_pool), _ptr(v_pool), num_pages, page_size, n_q_heads, n_kv_heads,
-        head_dim, window, float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
-        workspace.numel(), _ptr(dev_err), _stream(dev)), "pcp_paged_extend_attn")
+    if causal and mask is None:
+        _check(lib().pcp_paged_extend_attn(
+            _ptr(q), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(prefix_lens),
+            host_ptr, batch, total_q, _ptr(k_pool), _ptr(v_pool), num_pages, page_size,
+            n_q_heads, n_kv_heads, head_dim, window, float(sm_scale), _ptr(out), _ptr(lse),
+            _ptr(workspace), workspace.numel(), _ptr(dev_err), _stream(dev)),
+            "pcp_paged_extend_attn")
+    else:
+        mkeep, mptr, sb, sh, sq, mq, mkv = _mask_args(mask, batch, n_q_heads, dev)
+        _check(lib().pcp_paged_extend_attn_masked(
+            _ptr(q), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(prefix_lens),
+            host_ptr, batch, total_q, _ptr(k_pool), _ptr(v_pool), num_pages, page_size,
+            n_q_heads, n_kv_heads, head_dim, window, float(sm_scale), int(bool(causal)), mptr,
+            sb, sh, sq, mq, mkv, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+            _ptr(dev_err), _stream(dev)), "pcp_paged_extend_attn_masked")
+        del mkeep
     del host_keep
     _finish(dev_err, own, check, "pcp_paged_extend_attn")
     return out, lse

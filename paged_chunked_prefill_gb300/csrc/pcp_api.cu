@@ -189,18 +189,23 @@ size_t pcp_extend_workspace_size(int batch, int64_t total_q, int n_q_heads, int 
     return L.total;
 }
 
-pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
-                                 const int32_t* kv_indptr, const int32_t* kv_indices,
-                                 const int32_t* prefix_lens, const int32_t* qo_indptr_host,
-                                 int batch, int64_t total_q,
-                                 const void* k_pool, const void* v_pool, int64_t num_pages,
-                                 int page_size, int n_q_heads, int n_kv_heads, int head_dim,
-                                 int window, float sm_scale, void* out, float* lse,
-                                 void* workspace, size_t workspace_bytes, int32_t* dev_err,
-                                 void* stream) {
+pcp_status pcp_paged_extend_attn_masked(
+    const void* q, const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+    const int32_t* prefix_lens, const int32_t* qo_indptr_host, int batch, int64_t total_q,
+    const void* k_pool, const void* v_pool, int64_t num_pages, int page_size, int n_q_heads,
+    int n_kv_heads, int head_dim, int window, float sm_scale, int causal, const uint8_t* mask,
+    int64_t mask_b_stride, int64_t mask_h_stride, int64_t mask_q_stride, int32_t mask_q_len,
+    int32_t mask_kv_len, void* out, float* lse, void* workspace, size_t workspace_bytes,
+    int32_t* dev_err, void* stream) {
     // ---- host-visible argument checks, before anything is launched
     if (batch < 0 || total_q < 0 || total_q >= (int64_t(1) << 31) || n_q_heads < 1 ||
         n_kv_heads < 1 || page_size < 1 || window < 0 || num_pages < 0 || dev_err == nullptr)
+        return PCP_ERR_INVALID_ARG;
+    if ((causal != 0 && causal != 1) || (!causal && window > 0)) return PCP_ERR_INVALID_ARG;
+    if (mask != nullptr &&
+        (mask_b_stride < 0 || mask_h_stride < 0 || mask_q_stride < 0 || mask_q_len < 0 ||
+         mask_kv_len < 0 || !aligned(mask, 16) || mask_b_stride % 16 != 0 ||
+         mask_h_stride % 16 != 0 || mask_q_stride % 16 != 0))
         return PCP_ERR_INVALID_ARG;
     if (batch == 0 && total_q != 0) return PCP_ERR_INVALID_ARG;
     if (n_q_heads % n_kv_heads != 0) return PCP_ERR_INVALID_ARG;
@@ -283,6 +288,7 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
     pp.group = group;
     pp.page_size = page_size;
     pp.window = window;
+    pp.causal = causal;
     pp.sm_count = sms;
     pp.ws = ws;
     pp.lay = lay;
@@ -308,8 +314,17 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
     tp.page_size = page_size;
     tp.box_rows = box_rows;
     tp.num_pages = num_pages;
+    MaskParams mp;
+    mp.data = mask;
+    mp.b_stride = mask_b_stride;
+    mp.h_stride = mask_h_stride;
+    mp.q_stride = mask_q_stride;
+    mp.q_len = mask_q_len;
+    mp.kv_len = mask_kv_len;
     tp.num_slots = num_slots;
     tp.window = window;
+    tp.causal = causal;
+    tp.mask = mp;
     tp.scale_log2 = scale_log2;
     tp.dev_err = dev_err;
     cudaEvent_t evb = nullptr, eva = nullptr, evrb = nullptr, evra = nullptr;
@@ -346,6 +361,8 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
         rp.num_pages = num_pages;
         rp.num_slots = num_slots;
         rp.window = window;
+        rp.causal = causal;
+        rp.mask = mp;
         rp.scale_log2 = scale_log2;
         rp.dev_err = dev_err;
         if (evrb && failed(cudaEventRecord(evrb, s))) return PCP_ERR_CUDA;
@@ -364,6 +381,21 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
         if (failed(launch_combine(head_dim, s, cp))) return PCP_ERR_CUDA;
     }
     return PCP_OK;
+}
+
+pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
+                                 const int32_t* kv_indptr, const int32_t* kv_indices,
+                                 const int32_t* prefix_lens, const int32_t* qo_indptr_host,
+                                 int batch, int64_t total_q, const void* k_pool,
+                                 const void* v_pool, int64_t num_pages, int page_size,
+                                 int n_q_heads, int n_kv_heads, int head_dim, int window,
+                                 float sm_scale, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_err, void* stream) {
+    return pcp_paged_extend_attn_masked(q, qo_indptr, kv_indptr, kv_indices, prefix_lens,
+                                        qo_indptr_host, batch, total_q, k_pool, v_pool,
+                                        num_pages, page_size, n_q_heads, n_kv_heads, head_dim,
+                                        window, sm_scale, 1, nullptr, 0, 0, 0, 0, 0, out, lse,
+                                        workspace, workspace_bytes, dev_err, stream);
 }
 
 pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_err) {

@@ -107,7 +107,8 @@ __device__ __forceinline__ Geo make_geo(const TcParams& p, int4 it) {
             g.ph[u] = g.P + min(start + p.qpos, g.c) - 1;
             const int lo = p.window > 0 ? max(0, g.pl[u] - p.window + 1) : 0;
             g.first[u] = lo / kTileN;
-            g.last[u] = g.ph[u] / kTileN;
+            // causal: up to the tile's last row; otherwise every key of the sequence
+            g.last[u] = (p.causal ? g.ph[u] : g.L - 1) / kTileN;
         } else {
             g.pl[u] = g.ph[u] = 0;
             g.first[u] = 1;
@@ -189,6 +190,40 @@ __device__ __forceinline__ void tma_kv_tile(const TcParams& p, const Geo& geo, i
     }
 }
 
+// Nonzero bytes of a 32-bit word as 4 bits (bit e: byte e is nonzero).
+__device__ __forceinline__ uint32_t nonzero_bytes(uint32_t w) {
+    uint32_t t = w | (w >> 4);
+    t |= t >> 2;
+    t |= t >> 1;
+    t &= 0x01010101u;
+    return (t | (t >> 7) | (t >> 14) | (t >> 21)) & 0xFu;
+}
+
+// Keep-bits of keys [key0, key0 + 128) of one mask row: bit j of mb[j / 32]
+// is set when the mask keeps key key0 + j.  The row starts 16-byte aligned
+// (the host checks the base and the strides) and key0 is a multiple of 128;
+// keys at or past kv_len read as masked.  A null row is all masked.
+__device__ __forceinline__ void mask_bits_128(const uint8_t* mrow, int key0, int kv_len,
+                                              uint32_t (&mb)[4]) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) mb[w] = 0u;
+    if (mrow == nullptr) return;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const int k = key0 + c * 16;
+        uint32_t bits = 0u;
+        if (k + 16 <= kv_len) {
+            const uint4 x = __ldg(reinterpret_cast<const uint4*>(mrow + k));
+            bits = nonzero_bytes(x.x) | (nonzero_bytes(x.y) << 4) | (nonzero_bytes(x.z) << 8) |
+                   (nonzero_bytes(x.w) << 12);
+        } else {
+            for (int e = 0; e < 16 && k + e < kv_len; ++e)
+                if (mrow[k + e]) bits |= 1u << e;
+        }
+        mb[c >> 1] |= bits << ((c & 1) * 16);
+    }
+}
+
 // One gather warp's share (rows gw*64 .. gw*64+63) of a K or V tile: lanes
 // split into groups covering one 256-byte (128-byte for D = 64) row each.
 template <int D>
@@ -221,7 +256,9 @@ __device__ __forceinline__ void gather_kv_rows(const TcParams& p, const Geo& geo
 
 }  // namespace
 
-template <int D>
+// kMask: the call passes a boolean mask (a separate instantiation, so the
+// plain causal path carries none of its registers).
+template <int D, bool kMask>
 __global__ void __launch_bounds__(kTcThreads, 1)
     extend_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -517,20 +554,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc_fence_after();
                     const int key0 = t * kTileN;
+                    constexpr bool has_mask = kMask;
+                    // causal: the diagonal and window-edge tiles; otherwise the
+                    // tile holding the sequence end; with a mask, every tile
                     const bool need_mask =
-                        (key0 + kTileN - 1 > pl_u) ||
-                        (p.window > 0 && key0 < ph_u - p.window + 1);
+                        has_mask ||
+                        (p.causal ? (key0 + kTileN - 1 > pl_u) ||
+                                        (p.window > 0 && key0 < ph_u - p.window + 1)
+                                  : key0 + kTileN > geo.L);
+                    // the boolean mask's keep-bits of this row's keys in the tile
+                    uint32_t mb[4] = {~0u, ~0u, ~0u, ~0u};
+                    if constexpr (has_mask) {
+                        const int qi = geo.pos0 + pos_local;
+                        const bool in_mask =
+                            row_valid && (p.mask.q_stride == 0 || qi < p.mask.q_len);
+                        const uint8_t* mrow =
+                            in_mask ? p.mask.data + (int64_t)geo.b * p.mask.b_stride +
+                                          (int64_t)head * p.mask.h_stride +
+                                          (int64_t)qi * p.mask.q_stride
+                                    : nullptr;
+                        mask_bits_128(mrow, key0, p.mask.kv_len, mb);
+                    }
                     // the whole S row of this thread: one TMEM load
                     uint32_t v[128];
                     tmem_ld128(tS, v);
                     tmem_ld_wait();
                     if (need_mask) {
-                        // keys this row does not see become -inf (edge tiles only)
+                        // keys this row does not see become -inf
 #pragma unroll
                         for (int j = 0; j < 128; ++j) {
                             const int key = key0 + j;
                             const bool vis =
-                                key <= pabs && (p.window <= 0 || key > pabs - p.window);
+                                (p.causal ? key <= pabs && (p.window <= 0 || key > pabs - p.window)
+                                          : key < geo.L) &&
+                                ((mb[j >> 5] >> (j & 31)) & 1u);
                             if (!vis) v[j] = __float_as_uint(-INFINITY);
                         }
                     }
@@ -689,24 +746,26 @@ size_t tc_smem_bytes(int head_dim) {
     return head_dim == 128 ? TcCfg<128>::kSmemBytes : TcCfg<64>::kSmemBytes;
 }
 
+template <int D, bool kMask>
+cudaError_t launch_extend_tc_t(int grid, cudaStream_t stream, const TcParams& p,
+                               const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv) {
+    const size_t smem = TcCfg<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<D, kMask>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(extend_tc_kernel<D, kMask>, dim3(grid), dim3(kTcThreads), smem, stream, p,
+                      tq, tk, tv);
+}
+
 cudaError_t launch_extend_tc(int head_dim, int grid, cudaStream_t stream, const TcParams& p,
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv) {
-    const size_t smem = tc_smem_bytes(head_dim);
-    cudaError_t e;
-    if (head_dim == 128) {
-        e = cudaFuncSetAttribute(extend_tc_kernel<128>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = launch_pdl(extend_tc_kernel<128>, dim3(grid), dim3(kTcThreads), smem, stream, p, tq,
-                       tk, tv);
-    } else {
-        e = cudaFuncSetAttribute(extend_tc_kernel<64>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        e = launch_pdl(extend_tc_kernel<64>, dim3(grid), dim3(kTcThreads), smem, stream, p, tq,
-                       tk, tv);
-    }
-    return e;
+    const bool mask = p.mask.data != nullptr;
+    if (head_dim == 128)
+        return mask ? launch_extend_tc_t<128, true>(grid, stream, p, tq, tk, tv)
+                    : launch_extend_tc_t<128, false>(grid, stream, p, tq, tk, tv);
+    return mask ? launch_extend_tc_t<64, true>(grid, stream, p, tq, tk, tv)
+                : launch_extend_tc_t<64, false>(grid, stream, p, tq, tk, tv);
 }
 
 }  // namespace pcp

@@ -122,6 +122,19 @@ inline bool ws_layout(int batch, int64_t total_q, int n_q_heads, int n_kv_heads,
     return true;
 }
 
+// ---- visibility beyond the causal rule: causal flag and boolean mask
+// (True = keep) indexed [b * b_stride + h * h_stride + i * q_stride + j] with
+// i the row inside the chunk and j the key position; rows i >= q_len (when
+// q_stride != 0) and keys j >= kv_len read as masked.
+struct MaskParams {
+    const uint8_t* data;  // nullptr: no mask
+    int64_t b_stride;
+    int64_t h_stride;
+    int64_t q_stride;
+    int q_len;
+    int kv_len;
+};
+
 // ---- parameters of the planner kernel
 struct PlanParams {
     const int32_t* qo_indptr;
@@ -133,6 +146,7 @@ struct PlanParams {
     int group;
     int page_size;
     int window;
+    int causal;
     int sm_count;
     unsigned char* ws;
     WsLayout lay;
@@ -160,6 +174,8 @@ struct TcParams {
     int64_t num_pages;
     int num_slots;
     int window;
+    int causal;
+    MaskParams mask;
     float scale_log2;  // sm_scale * log2(e)
     int32_t* dev_err;
 };
@@ -197,6 +213,8 @@ struct RowParams {
     int64_t num_pages;
     int num_slots;
     int window;
+    int causal;
+    MaskParams mask;
     float scale_log2;
     int32_t* dev_err;
 };

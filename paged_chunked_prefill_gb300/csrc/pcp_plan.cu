@@ -47,9 +47,12 @@ __device__ __forceinline__ int first_key(int pos, int window) {
     return window > 0 ? max(0, pos - window + 1) : 0;
 }
 
-__device__ __forceinline__ int tc_cost(int P, int c, int k, int item_pos, int window) {
+// KV tiles of tensor-core item k of a chunk: up to the item's last row
+// (causal), or every key of the sequence (non-causal).
+__device__ __forceinline__ int tc_cost(int P, int c, int k, int item_pos, int window,
+                                       int causal) {
     const int first = P + k * item_pos;
-    const int last = P + min((k + 1) * item_pos, c) - 1;
+    const int last = causal ? P + min((k + 1) * item_pos, c) - 1 : P + c - 1;
     return last / kTileN - first_key(first, window) / kTileN + 1;
 }
 
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
         for (int f = tid; f < total; f += 1024) {
             const int sl = segment_of(s_a, 1024, f);
             const int4 v = s_seq[sl];
-            const int cost = tc_cost(v.y, v.x, f - s_a[sl], item_pos, p.window);
+            const int cost = tc_cost(v.y, v.x, f - s_a[sl], item_pos, p.window, p.causal);
             warp_agg_add(hist, min(cost, 1023), H);
         }
     }
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
             const int sl = segment_of(s_a, 1024, f);
             const int4 v = s_seq[sl];
             const int k = f - s_a[sl];
-            const int cost = tc_cost(v.y, v.x, k, item_pos, p.window);
+            const int cost = tc_cost(v.y, v.x, k, item_pos, p.window, p.causal);
             const int slot = warp_agg_add(hist, min(cost, 1023), H);
             for (int g = 0; g < H; ++g) {
                 if (slot + g >= p.lay.cap_tc) {

@@ -80,7 +80,8 @@ __device__ __forceinline__ uint32_t swz(int row, int dim) {
 
 }  // namespace
 
-template <int D>
+// kMask: the call passes a boolean mask (a separate instantiation).
+template <int D, bool kMask>
 __global__ void __launch_bounds__(kRowThreads, 1)
     row_attn_kernel(const __grid_constant__ RowParams p, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v) {
@@ -362,6 +363,23 @@ __global__ void __launch_bounds__(kRowThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(item_empty(qs));
         const int pos_lo = P + row_lo / G, pos_hi = P + row_hi / G;
+        const int L = d2.w;
+        // rows of the boolean mask for this lane's two query rows (null: the
+        // row is past the mask and sees nothing, or there is no such row)
+        const uint8_t* mrow_lo = nullptr;
+        const uint8_t* mrow_hi = nullptr;
+        if constexpr (kMask) {
+            const int b = d0.x;
+            auto mrow = [&](int row) -> const uint8_t* {
+                const int qi = row / G;
+                if (row >= R || (p.mask.q_stride != 0 && qi >= p.mask.q_len)) return nullptr;
+                return p.mask.data + (int64_t)b * p.mask.b_stride +
+                       (int64_t)(g * G + row % G) * p.mask.h_stride +
+                       (int64_t)qi * p.mask.q_stride;
+            };
+            mrow_lo = mrow(row_lo);
+            mrow_hi = mrow(row_hi);
+        }
         float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
         float o[D / 8][4];
 #pragma unroll
@@ -413,8 +431,14 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                             const int key = key_w + bl * 16 + nb * 8 + tig * 2 + (j & 1);
                             const int pos = j < 2 ? pos_lo : pos_hi;
                             const int row = j < 2 ? row_lo : row_hi;
-                            const bool vis = row < R && key >= kb && key < ke && key <= pos &&
-                                             (p.window <= 0 || key > pos - p.window);
+                            bool vis = row < R && key >= kb && key < ke &&
+                                       (p.causal ? key <= pos &&
+                                                       (p.window <= 0 || key > pos - p.window)
+                                                 : key < L);
+                            if constexpr (kMask) {
+                                const uint8_t* mr = j < 2 ? mrow_lo : mrow_hi;
+                                vis = vis && mr != nullptr && key < p.mask.kv_len && mr[key] != 0;
+                            }
                             const float v = vis ? sc[bl][nb][j] * sl2 : -INFINITY;
                             sc[bl][nb][j] = v;
                             if (j < 2) mx_lo = fmaxf(mx_lo, v);
@@ -614,24 +638,25 @@ size_t row_smem_bytes(int head_dim) {
     return head_dim == 128 ? RowCfg<128>::kSmemBytes : RowCfg<64>::kSmemBytes;
 }
 
+template <int D, bool kMask>
+cudaError_t launch_rows_t(int grid, cudaStream_t stream, const RowParams& p,
+                          const CUtensorMap& tk, const CUtensorMap& tv) {
+    const size_t smem = RowCfg<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(row_attn_kernel<D, kMask>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(row_attn_kernel<D, kMask>, dim3(grid), dim3(kRowThreads), smem, stream, p,
+                      tk, tv);
+}
+
 cudaError_t launch_rows(int head_dim, int grid, cudaStream_t stream, const RowParams& p,
                         const CUtensorMap& tk, const CUtensorMap& tv) {
-    const size_t smem = row_smem_bytes(head_dim);
-    cudaError_t e;
-    if (head_dim == 128) {
-        e = cudaFuncSetAttribute(row_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        e = launch_pdl(row_attn_kernel<128>, dim3(grid), dim3(kRowThreads), smem, stream, p, tk,
-                       tv);
-    } else {
-        e = cudaFuncSetAttribute(row_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        e = launch_pdl(row_attn_kernel<64>, dim3(grid), dim3(kRowThreads), smem, stream, p, tk,
-                       tv);
-    }
-    return e;
+    const bool mask = p.mask.data != nullptr;
+    if (head_dim == 128)
+        return mask ? launch_rows_t<128, true>(grid, stream, p, tk, tv)
+                    : launch_rows_t<128, false>(grid, stream, p, tk, tv);
+    return mask ? launch_rows_t<64, true>(grid, stream, p, tk, tv)
+                : launch_rows_t<64, false>(grid, stream, p, tk, tv);
 }
 
 }  // namespace pcp

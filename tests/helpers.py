@@ -43,9 +43,10 @@ def bf16_tensor_bits(t) -> np.ndarray:
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def run_gpu(batch, d=None, check=True, host_hint=True):
+def run_gpu(batch, d=None, check=True, host_hint=True, causal=True, mask=None):
     """out_cache_loc -> kv_append -> paged_extend_attn on the GPU (with the
-    host copy of qo_indptr unless host_hint is False)."""
+    host copy of qo_indptr unless host_hint is False; ``mask`` a numpy bool
+    array, moved to the device)."""
     import paged_chunked_prefill_gb300 as pcp
     if d is None:
         d = to_device(batch)
@@ -57,7 +58,11 @@ def run_gpu(batch, d=None, check=True, host_hint=True):
                                      d["prefix_lens"], d["k_pool"], d["v_pool"],
                                      batch.page_size, batch.n_q_heads, batch.n_kv_heads,
                                      batch.head_dim, batch.window, batch.sm_scale, check=check,
-                                     qo_indptr_host=batch.qo_indptr if host_hint else None)
+                                     qo_indptr_host=batch.qo_indptr if host_hint else None,
+                                     causal=causal,
+                                     mask=None if mask is None else
+                                     torch_mod().from_numpy(np.ascontiguousarray(mask)).to(
+                                         d["q"].device))
     return loc, d, out, lse
 
 

@@ -85,6 +85,16 @@ def test_host_validation_without_device(lib):
     assert st == 1   # no error word
     st = lib.pcp_compute_out_cache_loc(one, one, one, one, 2, 10, 0, 4, one, err, P(0))
     assert st == 1   # page_size 0
+    # causal flag and mask descriptor
+    f = lib.pcp_paged_extend_attn_masked
+    def masked(causal, window, mask, sb, sh, sq):
+        return f(one, one, one, one, one, P(0), 1, 10, one, one, 4, 16, 8, 8, 128, window, 0.0,
+                 causal, mask, sb, sh, sq, 4, 64, one, one, one, 1 << 30, err, P(0))
+    assert masked(2, 0, P(0), 0, 0, 0) == 1          # causal must be 0 or 1
+    assert masked(0, 8, P(0), 0, 0, 0) == 1          # a window needs causal attention
+    assert masked(1, 0, P(0x1008), 64, 0, 0) == 1    # mask not 16-byte aligned
+    assert masked(1, 0, one, 40, 0, 0) == 1          # stride not a multiple of 16
+    assert masked(1, 0, one, 64, 0, -16) == 1        # negative stride
     # the profiling hook takes a known kernel and both events or neither
     assert lib.pcp_set_timing_events(7, P(0), P(0)) == 1
     assert lib.pcp_set_timing_events(0, one, P(0)) == 1
