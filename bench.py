@@ -522,6 +522,10 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
                                 "frac_bf16": tf / peaks["bf16_tflops"]}
     del g, loc, lout, llse, lws
 
+    # non-causal attention and a 2-D key mask (keep 1/2) on the GQA workload:
+    # effective FLOPs count the visible pairs only
+    res.update(masked_secondary(pcp, torch, W, dev, peaks, flush, err))
+
     # the mixed scheduler batch: prompt chunks (tensor cores) and decode rows
     # (row kernel) in one call
     mb = W.mixed_batch()
@@ -548,6 +552,50 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
                          "frac_bf16": tf / peaks["bf16_tflops"]}
     if pcp.read_error(err) != 0:
         raise RuntimeError("device error in secondary measurements")
+    return res
+
+
+def masked_secondary(pcp, torch, W, dev, peaks, flush, err):
+    """Non-causal and 2-D-masked calls on the GQA chunked-prefill workload."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from helpers import to_device
+    gb = W.gqa_prefill()
+    g = to_device(gb, dev)
+    loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
+                                    g["prefix_lens"], gb.page_size, gb.num_pages)
+    pcp.kv_append(g["k_new"], g["v_new"], loc, g["k_pool"], g["v_pool"], dev_err=err)
+    out = torch.empty_like(g["q"])
+    lse = torch.empty(gb.total_q, gb.n_q_heads, dtype=torch.float32, device=dev)
+    ws = torch.empty(pcp.workspace_size(gb.batch, gb.total_q, gb.n_q_heads, gb.n_kv_heads,
+                                        gb.head_dim), dtype=torch.uint8, device=dev)
+    mask_np = W.random_mask(gb, "2d", seed=5, keep=0.5)
+    mask = torch.from_numpy(mask_np).to(dev)
+    res = {}
+    P = gb.prefix_lens.astype(np.int64)
+    C = gb.chunk_lens
+    L = P + C
+    for name, causal, m in (("non_causal_attn", False, None), ("masked_2d_attn", True, mask)):
+        def call():
+            pcp.paged_extend_attn(g["q"], g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
+                                  g["prefix_lens"], g["k_pool"], g["v_pool"], gb.page_size,
+                                  gb.n_q_heads, gb.n_kv_heads, gb.head_dim, 0, gb.sm_scale,
+                                  out=out, lse=lse, workspace=ws, dev_err=err,
+                                  qo_indptr_host=gb.qo_indptr, causal=causal, mask=m)
+        ms = time_calls(torch, call, flush, n=10, warm=3)
+        if m is None:
+            pairs = int((C * L).sum())
+        else:
+            keep = np.cumsum(mask_np, axis=1)   # kept keys among 0..j
+            pairs = 0
+            for b in range(gb.batch):
+                pos = P[b] + np.arange(C[b])
+                pairs += int(keep[b, pos].sum())
+        flops = 4 * gb.head_dim * gb.n_q_heads * pairs
+        tf = flops / (ms * 1e-3) / 1e12
+        res[name] = {"workload": gb.name + (", non-causal" if m is None else
+                                            ", causal + 2-D key mask keeping 1/2"),
+                     "ms": ms, "TFLOP/s": tf, "frac_bf16": tf / peaks["bf16_tflops"],
+                     "visible_pairs_per_head": pairs}
     return res
 
 
