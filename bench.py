@@ -526,6 +526,8 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
     # effective FLOPs count the visible pairs only
     res.update(masked_secondary(pcp, torch, W, dev, peaks, flush, err))
 
+    res["chunk_planner"] = planner_secondary(pcp)
+
     # the mixed scheduler batch: prompt chunks (tensor cores) and decode rows
     # (row kernel) in one call
     mb = W.mixed_batch()
@@ -553,6 +555,32 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
     if pcp.read_error(err) != 0:
         raise RuntimeError("device error in secondary measurements")
     return res
+
+
+def planner_secondary(pcp, n_decode=240, n_prompt=16, steps=200):
+    """Host time of one planned step (pcp_schedule_step through the binding)
+    in a serving loop of n_decode decoding requests and n_prompt incoming
+    2000-token prompts, token budget 8192, page size 16."""
+    rng = np.random.default_rng(11)
+    pg = pcp.Pager(200_000, 16)
+    ids = list(range(n_decode + n_prompt))
+    total = [int(x) for x in rng.integers(100, 4000, size=n_decode)] + [2000] * n_prompt
+    comp = [t - 1 for t in total[:n_decode]] + [0] * n_prompt
+    # the decoding requests already hold their pages
+    pg.schedule_step(ids[:n_decode], total[:n_decode], [0] * n_decode, 1 << 30)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        st = pg.schedule_step(ids, total, comp, 8192)
+        times.append(time.perf_counter() - t0)
+        qo = st["qo_indptr"]
+        for n, r in enumerate(st["row_req"]):
+            comp[r] += int(qo[n + 1] - qo[n])
+            if st["sample"][n]:
+                total[r] += 1
+    return {"workload": f"{n_decode} decoding + {n_prompt} prefilling requests, budget 8192, "
+                        f"page size 16", "us_per_step": float(np.median(times) * 1e6),
+            "what": "host time of pcp_schedule_step through the Python binding (median)"}
 
 
 def masked_secondary(pcp, torch, W, dev, peaks, flush, err):

@@ -246,6 +246,73 @@ pcp_status pcp_paged_extend_attn_noalloc(const void* q, const int32_t* qo_indptr
                                          float sm_scale, void* out, float* lse,
                                          int32_t* dev_err, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Host-side chunk planner and page pool.  Pure host code: every pointer
+ * below is a HOST pointer and nothing touches a GPU.  Not thread-safe: one
+ * pool is used from one thread at a time.
+ *
+ * The step upstream of the attention path (AReno PR #642: prompts longer
+ * than the scheduler's token budget are prefilled in chunks, decode rows run
+ * alongside, a request samples only once its final chunk has run, and prefill
+ * continues inside the last allocated KV page; vLLM PR #54076: with a
+ * recurrent-state grid of S tokens every chunk stops at the next grid point,
+ * also from an aligned start).
+ * ---------------------------------------------------------------------- */
+typedef struct pcp_pager pcp_pager;
+
+/* A pool of num_pages pages of page_size slots, all free.  NULL on a bad
+ * argument (num_pages < 0 or > INT32_MAX, page_size < 1) or out of memory.
+ * The caller owns it and frees it with pcp_pager_destroy. */
+pcp_pager* pcp_pager_create(int64_t num_pages, int page_size);
+void pcp_pager_destroy(pcp_pager* pager);
+
+/* Free pages in the pool (-1 for a NULL pool). */
+int64_t pcp_pager_num_free(const pcp_pager* pager);
+
+/* Entries of all requests' page lists together (-1 for a NULL pool): with the
+ * free pages, a bound on the kv_indices entries of any step. */
+int64_t pcp_pager_num_held(const pcp_pager* pager);
+
+/* The pages request req_id holds, in token order: writes up to `capacity`
+ * of them to `pages` (may be NULL) and returns how many it holds (0 for an
+ * unknown request, -1 for a NULL pool). */
+int64_t pcp_pager_request_pages(const pcp_pager* pager, int64_t req_id, int32_t* pages,
+                                int64_t capacity);
+
+/* Return request req_id's pages to the pool (a finished request). */
+pcp_status pcp_pager_release(pcp_pager* pager, int64_t req_id);
+
+/*
+ * Plan one serving step.  Request r (0 <= r < n_reqs, distinct req_ids[r])
+ * knows total_lens[r] tokens (prompt plus generated) of which num_computed[r]
+ * already have their K/V in the pool; its pending work is the difference.
+ *   1. Requests with exactly one pending token (decode-shaped) get it, in
+ *      order, while the budget lasts.
+ *   2. The others get chunks in order: as many pending tokens as the budget
+ *      left allows, stopping at the next multiple of state_block strictly
+ *      above num_computed[r] when state_block > 0.
+ *   Each chunk is cut to the tokens its request's pages plus the free pages
+ *   can hold (the pages are counted in the order the chunks are chosen).
+ *   3. Every request with a non-empty chunk, in request order, takes the
+ *      lowest-numbered free pages it needs, and becomes one row of the step.
+ * Outputs (host arrays the caller sizes; n_reqs + 1 entries bound the rows):
+ *   *n_rows; row_req[n] (index r of row n); qo_indptr[n + 1] (chunk
+ *   offsets); prefix_lens[n] (= num_computed of the row's request);
+ *   kv_indptr[n + 1] / kv_indices (each row's full page list, the CSR the
+ *   attention call takes, in pages); sample[n] (1 when the row's chunk ends
+ *   at total_lens, i.e. the step samples a token for it).
+ * The caller advances num_computed by the chunk lengths afterwards.
+ * Errors: PCP_ERR_INVALID_ARG for a NULL pool or array, a negative size,
+ * num_computed > total_lens, repeated req_ids, or a request holding fewer
+ * pages than its computed tokens need; PCP_ERR_WORKSPACE when kv_indices_cap
+ * is smaller than the page entries of the step (nothing is allocated then).
+ */
+pcp_status pcp_schedule_step(pcp_pager* pager, int n_reqs, const int64_t* req_ids,
+                             const int32_t* total_lens, const int32_t* num_computed, int budget,
+                             int state_block, int32_t* n_rows, int32_t* row_req,
+                             int32_t* qo_indptr, int32_t* prefix_lens, int32_t* kv_indptr,
+                             int32_t* kv_indices, int64_t kv_indices_cap, uint8_t* sample);
+
 /*
  * Synchronise `stream` and copy *dev_err to *host_err (host pointer).
  * Returns PCP_ERR_CUDA if the synchronisation or copy fails.

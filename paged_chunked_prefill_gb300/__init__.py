@@ -13,8 +13,10 @@ Functions (same names as the C entry points, without the ``pcp_`` prefix):
 * ``kv_append``             -- scatter the chunk's K/V into the page pools
 * ``paged_extend_attn``     -- extend attention, returns ``(out, lse)``
 * ``workspace_size``        -- bytes of scratch a call needs
+* ``Pager``                 -- host page pool and chunk planner of a serving step
 """
 from ._binding import (  # noqa: F401
+    Pager,
     PCPError,
     Status,
     compute_out_cache_loc,
@@ -30,7 +32,7 @@ from ._binding import (  # noqa: F401
 )
 
 __all__ = [
-    "PCPError", "Status", "compute_out_cache_loc", "kv_append", "lib", "library_path",
+    "Pager", "PCPError", "Status", "compute_out_cache_loc", "kv_append", "lib", "library_path",
     "paged_extend_attn", "read_error", "set_timing_events", "TIMING_ROWS", "TIMING_TC",
     "workspace_size",
 ]

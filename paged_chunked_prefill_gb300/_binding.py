@@ -72,6 +72,20 @@ def lib():
                                                    i32, i32, i32, i32, f32, i32, P, i64, i64,
                                                    i64, i32, i32, P, P, P, sz, P, P]
         L.pcp_paged_extend_attn_masked.restype = i32
+        L.pcp_pager_create.argtypes = [i64, i32]
+        L.pcp_pager_create.restype = P
+        L.pcp_pager_destroy.argtypes = [P]
+        L.pcp_pager_destroy.restype = None
+        L.pcp_pager_num_free.argtypes = [P]
+        L.pcp_pager_num_free.restype = i64
+        L.pcp_pager_num_held.argtypes = [P]
+        L.pcp_pager_num_held.restype = i64
+        L.pcp_pager_request_pages.argtypes = [P, i64, P, i64]
+        L.pcp_pager_request_pages.restype = i64
+        L.pcp_pager_release.argtypes = [P, i64]
+        L.pcp_pager_release.restype = i32
+        L.pcp_schedule_step.argtypes = [P, i32, P, P, P, i32, i32, P, P, P, P, P, P, i64, P]
+        L.pcp_schedule_step.restype = i32
         L.pcp_read_error.argtypes = [P, P, P]
         L.pcp_read_error.restype = i32
         L.pcp_set_timing_events.argtypes = [i32, P, P]
@@ -308,3 +322,66 @@ def set_timing_events(before, after, kernel: int = TIMING_TC) -> None:
     b = ctypes.c_void_p(before.cuda_event) if before is not None else ctypes.c_void_p(0)
     a = ctypes.c_void_p(after.cuda_event) if after is not None else ctypes.c_void_p(0)
     _check(lib().pcp_set_timing_events(kernel, b, a), "pcp_set_timing_events")
+
+
+class Pager:
+    """Host-side page pool and chunk planner (``pcp_pager_*``,
+    ``pcp_schedule_step``): argument marshalling only."""
+
+    def __init__(self, num_pages: int, page_size: int):
+        self._h = lib().pcp_pager_create(int(num_pages), int(page_size))
+        if not self._h:
+            raise ValueError("pcp_pager_create: bad arguments")
+        self.page_size = int(page_size)
+
+    def close(self) -> None:
+        if self._h:
+            lib().pcp_pager_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        return int(lib().pcp_pager_num_free(self._h))
+
+    def request_pages(self, req_id: int) -> np.ndarray:
+        n = int(lib().pcp_pager_request_pages(self._h, int(req_id), None, 0))
+        out = np.zeros(max(n, 1), np.int32)
+        lib().pcp_pager_request_pages(self._h, int(req_id), out.ctypes.data_as(ctypes.c_void_p),
+                                      n)
+        return out[:n]
+
+    def release(self, req_id: int) -> None:
+        _check(lib().pcp_pager_release(self._h, int(req_id)), "pcp_pager_release")
+
+    def schedule_step(self, req_ids, total_lens, num_computed, budget: int,
+                      state_block: int = 0) -> dict:
+        """Plan one step; returns numpy arrays row_req, qo_indptr,
+        prefix_lens, kv_indptr, kv_indices and sample (bool)."""
+        ids = np.ascontiguousarray(req_ids, dtype=np.int64)
+        tot = np.ascontiguousarray(total_lens, dtype=np.int32)
+        comp = np.ascontiguousarray(num_computed, dtype=np.int32)
+        n = int(ids.shape[0])
+        if tot.shape != (n,) or comp.shape != (n,):
+            raise ValueError("req_ids, total_lens and num_computed must have one entry each")
+        cap = int(lib().pcp_pager_num_held(self._h)) + self.num_free() + 1
+        nrows = ctypes.c_int32(0)
+        row_req = np.empty(n + 1, np.int32)
+        qo = np.empty(n + 1, np.int32)
+        pre = np.empty(n + 1, np.int32)
+        kvp = np.empty(n + 1, np.int32)
+        kvi = np.empty(cap, np.int32)
+        smp = np.empty(n + 1, np.uint8)
+        ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+        _check(lib().pcp_schedule_step(self._h, n, ptr(ids), ptr(tot), ptr(comp), int(budget),
+                                       int(state_block), ctypes.byref(nrows), ptr(row_req),
+                                       ptr(qo), ptr(pre), ptr(kvp), ptr(kvi), cap, ptr(smp)),
+               "pcp_schedule_step")
+        r = int(nrows.value)
+        return {"row_req": row_req[:r].copy(), "qo_indptr": qo[:r + 1].copy(),
+                "prefix_lens": pre[:r].copy(), "kv_indptr": kvp[:r + 1].copy(),
+                "kv_indices": kvi[:int(kvp[r])].copy(), "sample": smp[:r].astype(bool)}
