@@ -279,8 +279,48 @@ int64_t pcp_pager_num_held(const pcp_pager* pager);
 int64_t pcp_pager_request_pages(const pcp_pager* pager, int64_t req_id, int32_t* pages,
                                 int64_t capacity);
 
-/* Return request req_id's pages to the pool (a finished request). */
+/* Drop request req_id's hold on its pages (a finished request); a page
+ * nobody holds any more (no request, not the prefix index) is free again. */
 pcp_status pcp_pager_release(pcp_pager* pager, int64_t req_id);
+
+/*
+ * Shared pages (vLLM PR #54076, "E2E": an immediate re-ask of a prompt
+ * reuses its cached blocks, and the hit is quantised to whole blocks: at
+ * most floor((P - 1) / page_size) * page_size tokens of a P-token prompt,
+ * so the prompt's last token is always computed).  Pages carry reference
+ * counts; a shared page is read-only.
+ *
+ * pcp_pager_share: request dst_req (holding no pages) takes read-only
+ * references to the first ceil(n_tokens / page_size) pages of src_req, e.g.
+ * for several continuations of one prompt; the caller then treats dst_req as
+ * having n_tokens computed.  PCP_ERR_INVALID_ARG if src_req holds fewer
+ * pages, dst_req already holds pages, or the ids are equal.
+ *
+ * pcp_pager_cache_prompt: enter request req_id's full pages into the prefix
+ * index, keyed by tokens[0 .. (i + 1) * page_size) for page i (a chained
+ * 64-bit hash, with the page's tokens kept and compared on lookup).  Call it
+ * once those tokens' K/V are computed.  Only whole pages are entered; a key
+ * that is already present keeps its page.  The index holds a reference to
+ * each page it names.  Returns the pages newly entered (-1 on a bad
+ * argument).
+ *
+ * pcp_pager_match_prefix: request req_id (holding no pages) takes read-only
+ * references to the longest run of indexed pages that matches tokens[0 ..
+ * n_tokens), at most floor((n_tokens - 1) / page_size) of them, and
+ * *n_hit = their tokens; the caller starts it with that many computed.
+ *
+ * pcp_pager_clear_cache: empty the prefix index (pages only it held are
+ * freed).  There is no other eviction.
+ *
+ * A step whose chunk starts inside a shared, partly filled page copies that
+ * page first (copy-on-write, see pcp_schedule_step).
+ */
+pcp_status pcp_pager_share(pcp_pager* pager, int64_t src_req, int64_t dst_req, int64_t n_tokens);
+int64_t pcp_pager_cache_prompt(pcp_pager* pager, int64_t req_id, const int32_t* tokens,
+                               int64_t n_tokens);
+pcp_status pcp_pager_match_prefix(pcp_pager* pager, int64_t req_id, const int32_t* tokens,
+                                  int64_t n_tokens, int64_t* n_hit);
+pcp_status pcp_pager_clear_cache(pcp_pager* pager);
 
 /*
  * Plan one serving step.  Request r (0 <= r < n_reqs, distinct req_ids[r])
@@ -292,15 +332,23 @@ pcp_status pcp_pager_release(pcp_pager* pager, int64_t req_id);
  *      left allows, stopping at the next multiple of state_block strictly
  *      above num_computed[r] when state_block > 0.
  *   Each chunk is cut to the tokens its request's pages plus the free pages
- *   can hold (the pages are counted in the order the chunks are chosen).
- *   3. Every request with a non-empty chunk, in request order, takes the
- *      lowest-numbered free pages it needs, and becomes one row of the step.
+ *   can hold (the pages are counted in the order the chunks are chosen); a
+ *   chunk that starts inside a page other holders share also counts one
+ *   page for its copy, and gets no tokens when no page is free for it.
+ *   3. Every request with a non-empty chunk, in request order, becomes one
+ *      row of the step: if its chunk starts inside a page whose reference
+ *      count (as the rows before left it) is above one, it takes the lowest
+ *      free page, which replaces the shared one in its list, and the step
+ *      reports the copy (copy_src[c] -> copy_dst[c], the first copy_slots[c]
+ *      slots, to run with pcp_copy_page_slots before the step's KV append);
+ *      then it takes the lowest free pages its new tokens need.
  * Outputs (host arrays the caller sizes; n_reqs + 1 entries bound the rows):
  *   *n_rows; row_req[n] (index r of row n); qo_indptr[n + 1] (chunk
  *   offsets); prefix_lens[n] (= num_computed of the row's request);
  *   kv_indptr[n + 1] / kv_indices (each row's full page list, the CSR the
  *   attention call takes, in pages); sample[n] (1 when the row's chunk ends
- *   at total_lens, i.e. the step samples a token for it).
+ *   at total_lens, i.e. the step samples a token for it); *n_copies and
+ *   copy_src / copy_dst / copy_slots (n_reqs entries bound them).
  * The caller advances num_computed by the chunk lengths afterwards.
  * Errors: PCP_ERR_INVALID_ARG for a NULL pool or array, a negative size,
  * num_computed > total_lens, repeated req_ids, or a request holding fewer
@@ -311,7 +359,24 @@ pcp_status pcp_schedule_step(pcp_pager* pager, int n_reqs, const int64_t* req_id
                              const int32_t* total_lens, const int32_t* num_computed, int budget,
                              int state_block, int32_t* n_rows, int32_t* row_req,
                              int32_t* qo_indptr, int32_t* prefix_lens, int32_t* kv_indptr,
-                             int32_t* kv_indices, int64_t kv_indices_cap, uint8_t* sample);
+                             int32_t* kv_indices, int64_t kv_indices_cap, uint8_t* sample,
+                             int32_t* n_copies, int32_t* copy_src, int32_t* copy_dst,
+                             int32_t* copy_slots);
+
+/*
+ * Copy-on-write of shared pages on the device (integer copy, bit-exact): for
+ * each c < n_copies, slots [0, n_slots[c]) of page src_pages[c] of k_pool
+ * and v_pool ([num_pages * page_size, n_kv_heads, head_dim] bf16) are
+ * copied to the same slots of page dst_pages[c].  src_pages, dst_pages and
+ * n_slots are DEVICE int32 arrays.  A page id outside [0, num_pages) or a
+ * slot count outside [0, page_size] sets *dev_err = PCP_ERR_BAD_INDEX and
+ * that copy is skipped.  The destinations must not overlap the sources.
+ * n_copies <= 65535.
+ */
+pcp_status pcp_copy_page_slots(void* k_pool, void* v_pool, int64_t num_pages, int page_size,
+                               int n_kv_heads, int head_dim, const int32_t* src_pages,
+                               const int32_t* dst_pages, const int32_t* n_slots, int n_copies,
+                               int32_t* dev_err, void* stream);
 
 /*
  * Synchronise `stream` and copy *dev_err to *host_err (host pointer).

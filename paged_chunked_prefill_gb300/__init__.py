@@ -11,6 +11,7 @@ Functions (same names as the C entry points, without the ``pcp_`` prefix):
 
 * ``compute_out_cache_loc`` -- slots of a step's new tokens (int64)
 * ``kv_append``             -- scatter the chunk's K/V into the page pools
+* ``copy_page_slots``       -- copy-on-write of shared pages
 * ``paged_extend_attn``     -- extend attention, returns ``(out, lse)``
 * ``workspace_size``        -- bytes of scratch a call needs
 * ``Pager``                 -- host page pool and chunk planner of a serving step
@@ -20,6 +21,7 @@ from ._binding import (  # noqa: F401
     PCPError,
     Status,
     compute_out_cache_loc,
+    copy_page_slots,
     kv_append,
     lib,
     library_path,
@@ -32,7 +34,7 @@ from ._binding import (  # noqa: F401
 )
 
 __all__ = [
-    "Pager", "PCPError", "Status", "compute_out_cache_loc", "kv_append", "lib", "library_path",
-    "paged_extend_attn", "read_error", "set_timing_events", "TIMING_ROWS", "TIMING_TC",
+    "Pager", "PCPError", "Status", "compute_out_cache_loc", "copy_page_slots", "kv_append",
+    "lib", "library_path", "paged_extend_attn", "read_error", "set_timing_events", "TIMING_ROWS", "TIMING_TC",
     "workspace_size",
 ]

@@ -84,8 +84,19 @@ def lib():
         L.pcp_pager_request_pages.restype = i64
         L.pcp_pager_release.argtypes = [P, i64]
         L.pcp_pager_release.restype = i32
-        L.pcp_schedule_step.argtypes = [P, i32, P, P, P, i32, i32, P, P, P, P, P, P, i64, P]
+        L.pcp_schedule_step.argtypes = [P, i32, P, P, P, i32, i32, P, P, P, P, P, P, i64, P,
+                                        P, P, P, P]
         L.pcp_schedule_step.restype = i32
+        L.pcp_pager_share.argtypes = [P, i64, i64, i64]
+        L.pcp_pager_share.restype = i32
+        L.pcp_pager_cache_prompt.argtypes = [P, i64, P, i64]
+        L.pcp_pager_cache_prompt.restype = i64
+        L.pcp_pager_match_prefix.argtypes = [P, i64, P, i64, P]
+        L.pcp_pager_match_prefix.restype = i32
+        L.pcp_pager_clear_cache.argtypes = [P]
+        L.pcp_pager_clear_cache.restype = i32
+        L.pcp_copy_page_slots.argtypes = [P, P, i64, i32, i32, i32, P, P, P, i32, P, P]
+        L.pcp_copy_page_slots.restype = i32
         L.pcp_read_error.argtypes = [P, P, P]
         L.pcp_read_error.restype = i32
         L.pcp_set_timing_events.argtypes = [i32, P, P]
@@ -316,6 +327,29 @@ TIMING_TC = 0    # the tensor-core extend kernel
 TIMING_ROWS = 1  # the split-KV row kernel
 
 
+def copy_page_slots(k_pool: torch.Tensor, v_pool: torch.Tensor, page_size: int,
+                    src_pages: torch.Tensor, dst_pages: torch.Tensor, n_slots: torch.Tensor,
+                    dev_err: Optional[torch.Tensor] = None, check: bool = True) -> None:
+    """Copy-on-write on the device: slots [0, n_slots[c]) of page
+    src_pages[c] -> page dst_pages[c], K and V (int32 device tensors)."""
+    dev = k_pool.device
+    _need(k_pool, "k_pool", torch.bfloat16, dev)
+    _need(v_pool, "v_pool", torch.bfloat16, dev)
+    for n, t in (("src_pages", src_pages), ("dst_pages", dst_pages), ("n_slots", n_slots)):
+        _need(t, n, torch.int32, dev)
+    if k_pool.shape != v_pool.shape or k_pool.dim() != 3 or k_pool.shape[0] % page_size:
+        raise ValueError("pools must be [num_pages * page_size, Hkv, D]")
+    own = dev_err is None
+    if own:
+        dev_err = _dev_err(dev)
+    _check(lib().pcp_copy_page_slots(_ptr(k_pool), _ptr(v_pool), k_pool.shape[0] // page_size,
+                                     page_size, k_pool.shape[1], k_pool.shape[2],
+                                     _ptr(src_pages), _ptr(dst_pages), _ptr(n_slots),
+                                     src_pages.numel(), _ptr(dev_err), _stream(dev)),
+           "pcp_copy_page_slots")
+    _finish(dev_err, own, check, "pcp_copy_page_slots")
+
+
 def set_timing_events(before, after, kernel: int = TIMING_TC) -> None:
     """Record `before`/`after` (torch.cuda.Event, or None) around `kernel`
     (TIMING_TC or TIMING_ROWS) in every later paged_extend_attn call."""
@@ -358,6 +392,35 @@ class Pager:
     def release(self, req_id: int) -> None:
         _check(lib().pcp_pager_release(self._h, int(req_id)), "pcp_pager_release")
 
+    def share(self, src_req: int, dst_req: int, n_tokens: int) -> None:
+        """dst_req takes read-only references to src_req's pages holding its
+        first n_tokens tokens."""
+        _check(lib().pcp_pager_share(self._h, int(src_req), int(dst_req), int(n_tokens)),
+               "pcp_pager_share")
+
+    def cache_prompt(self, req_id: int, tokens) -> int:
+        """Enter the request's full pages into the prefix index; returns the
+        pages newly entered."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = int(lib().pcp_pager_cache_prompt(self._h, int(req_id),
+                                             t.ctypes.data_as(ctypes.c_void_p), t.shape[0]))
+        if n < 0:
+            raise ValueError("pcp_pager_cache_prompt: bad arguments")
+        return n
+
+    def match_prefix(self, req_id: int, tokens) -> int:
+        """Attach the longest cached run of whole pages matching the prompt
+        (leaving at least its last token); returns the tokens covered."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        hit = ctypes.c_int64(0)
+        _check(lib().pcp_pager_match_prefix(self._h, int(req_id),
+                                            t.ctypes.data_as(ctypes.c_void_p), t.shape[0],
+                                            ctypes.byref(hit)), "pcp_pager_match_prefix")
+        return int(hit.value)
+
+    def clear_cache(self) -> None:
+        _check(lib().pcp_pager_clear_cache(self._h), "pcp_pager_clear_cache")
+
     def schedule_step(self, req_ids, total_lens, num_computed, budget: int,
                       state_block: int = 0) -> dict:
         """Plan one step; returns numpy arrays row_req, qo_indptr,
@@ -376,12 +439,20 @@ class Pager:
         kvp = np.empty(n + 1, np.int32)
         kvi = np.empty(cap, np.int32)
         smp = np.empty(n + 1, np.uint8)
+        ncp = ctypes.c_int32(0)
+        csrc = np.empty(n + 1, np.int32)
+        cdst = np.empty(n + 1, np.int32)
+        cslots = np.empty(n + 1, np.int32)
         ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
         _check(lib().pcp_schedule_step(self._h, n, ptr(ids), ptr(tot), ptr(comp), int(budget),
                                        int(state_block), ctypes.byref(nrows), ptr(row_req),
-                                       ptr(qo), ptr(pre), ptr(kvp), ptr(kvi), cap, ptr(smp)),
+                                       ptr(qo), ptr(pre), ptr(kvp), ptr(kvi), cap, ptr(smp),
+                                       ctypes.byref(ncp), ptr(csrc), ptr(cdst), ptr(cslots)),
                "pcp_schedule_step")
         r = int(nrows.value)
+        c = int(ncp.value)
         return {"row_req": row_req[:r].copy(), "qo_indptr": qo[:r + 1].copy(),
                 "prefix_lens": pre[:r].copy(), "kv_indptr": kvp[:r + 1].copy(),
-                "kv_indices": kvi[:int(kvp[r])].copy(), "sample": smp[:r].astype(bool)}
+                "kv_indices": kvi[:int(kvp[r])].copy(), "sample": smp[:r].astype(bool),
+                "copy_src": csrc[:c].copy(), "copy_dst": cdst[:c].copy(),
+                "copy_slots": cslots[:c].copy()}

@@ -33,6 +33,10 @@ cudaError_t launch_out_cache_loc(const int32_t* qo_indptr, const int32_t* kv_ind
                                  int batch, int64_t total_q, int page_size, int64_t num_pages,
                                  int64_t* loc, int32_t* dev_err, int sm_count,
                                  cudaStream_t stream);
+cudaError_t launch_copy_page_slots(const int32_t* src, const int32_t* dst,
+                                   const int32_t* n_slots, int n_copies, int64_t num_pages,
+                                   int page_size, int chunks_per_slot, void* k_pool,
+                                   void* v_pool, int32_t* dev_err, cudaStream_t stream);
 cudaError_t launch_kv_append(const void* k, const void* v, const int64_t* loc, int64_t n_tokens,
                              int chunks_per_token, void* k_pool, void* v_pool, int64_t pool_slots,
                              int32_t* dev_err, int sm_count, cudaStream_t stream);
@@ -179,6 +183,25 @@ pcp_status pcp_kv_append(const void* k, const void* v, const int64_t* out_cache_
     cudaError_t e = launch_kv_append(k, v, out_cache_loc, n_tokens, chunks, k_pool, v_pool,
                                      pool_slots, dev_err, sms, static_cast<cudaStream_t>(stream));
     return failed(e) ? PCP_ERR_CUDA : PCP_OK;
+}
+
+pcp_status pcp_copy_page_slots(void* k_pool, void* v_pool, int64_t num_pages, int page_size,
+                               int n_kv_heads, int head_dim, const int32_t* src_pages,
+                               const int32_t* dst_pages, const int32_t* n_slots, int n_copies,
+                               int32_t* dev_err, void* stream) {
+    if (num_pages < 0 || page_size < 1 || n_kv_heads < 1 || head_dim < 1 || n_copies < 0 ||
+        n_copies > 65535 || dev_err == nullptr)
+        return PCP_ERR_INVALID_ARG;
+    if ((head_dim * 2) % 16 != 0) return PCP_ERR_UNSUPPORTED;
+    if (n_copies == 0) return PCP_OK;
+    if (!k_pool || !v_pool || !src_pages || !dst_pages || !n_slots) return PCP_ERR_INVALID_ARG;
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16)) return PCP_ERR_INVALID_ARG;
+    const int chunks = n_kv_heads * head_dim * 2 / 16;
+    return failed(launch_copy_page_slots(src_pages, dst_pages, n_slots, n_copies, num_pages,
+                                         page_size, chunks, k_pool, v_pool, dev_err,
+                                         static_cast<cudaStream_t>(stream)))
+               ? PCP_ERR_CUDA
+               : PCP_OK;
 }
 
 size_t pcp_extend_workspace_size(int batch, int64_t total_q, int n_q_heads, int n_kv_heads,

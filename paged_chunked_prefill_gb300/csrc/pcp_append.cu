@@ -5,6 +5,8 @@
 // prefix is not a multiple of the page size lands mid-page.  AstrAI's
 // PagePool.bind_tasks builds out_cache_loc once per step and the backend writes
 // k_buffer[layer, out_cache_loc] = k before attending; here both are kernels.
+#include <algorithm>
+
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
 #include "pcp_launch.h"
@@ -67,6 +69,48 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __res
         __stcs(k_pool + s * chunks_per_token + ch, kv);
         __stcs(v_pool + s * chunks_per_token + ch, vv);
     }
+}
+
+// Copy-on-write of shared pages: for copy c, slots [0, n_slots[c]) of page
+// src[c] go to the same slots of page dst[c], K and V.  One CTA row per copy;
+// a thread moves one 16-byte chunk.
+__global__ void copy_page_slots_kernel(const int32_t* __restrict__ src,
+                                       const int32_t* __restrict__ dst,
+                                       const int32_t* __restrict__ n_slots, int64_t num_pages,
+                                       int page_size, int chunks_per_slot,
+                                       uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                                       int32_t* dev_err) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int c = blockIdx.y;
+    const int64_t s = src[c], d = dst[c];
+    const int n = n_slots[c];
+    if (s < 0 || s >= num_pages || d < 0 || d >= num_pages || n < 0 || n > page_size) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) report_error(dev_err, PCP_ERR_BAD_INDEX);
+        return;
+    }
+    const int64_t total = (int64_t)n * chunks_per_slot;
+    const int64_t s0 = s * page_size * chunks_per_slot, d0 = d * page_size * chunks_per_slot;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 kv = k_pool[s0 + i];
+        const uint4 vv = v_pool[s0 + i];
+        k_pool[d0 + i] = kv;
+        v_pool[d0 + i] = vv;
+    }
+}
+
+cudaError_t launch_copy_page_slots(const int32_t* src, const int32_t* dst,
+                                   const int32_t* n_slots, int n_copies, int64_t num_pages,
+                                   int page_size, int chunks_per_slot, void* k_pool,
+                                   void* v_pool, int32_t* dev_err, cudaStream_t stream) {
+    const int threads = 256;
+    const int64_t per_copy = (int64_t)page_size * chunks_per_slot;
+    const int64_t bx = std::min<int64_t>((per_copy + threads - 1) / threads, 64);
+    return launch_pdl(copy_page_slots_kernel, dim3((unsigned)bx, (unsigned)n_copies),
+                      dim3(threads), 0, stream, src, dst, n_slots, num_pages, page_size,
+                      chunks_per_slot, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool),
+                      dev_err);
 }
 
 cudaError_t launch_out_cache_loc(const int32_t* qo_indptr, const int32_t* kv_indptr,

@@ -89,6 +89,8 @@ def test_library_hand_worked_step():
     pg.schedule_step([5, 9], [8, 2], [0, 0], 16)
     free_before = pg.num_free()
     st = pg.schedule_step([5, 8, 9], [9, 13, 6], [8, 0, 2], 8)
+    for k in ("copy_src", "copy_dst", "copy_slots"):
+        assert st.pop(k).size == 0
     model_free = list(range(3, 10))
     model_pages = {5: [0, 1], 9: [2]}
     want = chunk_plan.plan_step(model_free, model_pages, [5, 8, 9], [9, 13, 6], [8, 0, 2], 8, 0,
@@ -146,12 +148,8 @@ def lib_factory(num_pages, ps):
 
 
 def model_factory(num_pages, ps):
-    st = {"free": list(range(num_pages)), "pages": {}, "ps": ps}
-    def release(rid):
-        st["free"].extend(st["pages"].pop(rid, []))
-        st["free"].sort()
-    st["release"] = release
-    return st
+    pool = chunk_plan.PagePool(num_pages, ps)
+    return {"pool": pool, "release": pool.release}
 
 
 def lib_plan(state, ids, tot, comp, budget, sb):
@@ -160,8 +158,7 @@ def lib_plan(state, ids, tot, comp, budget, sb):
 
 
 def model_plan(state, ids, tot, comp, budget, sb):
-    return chunk_plan.plan_step(state["free"], state["pages"], ids, tot, comp, budget, sb,
-                                state["ps"])
+    return state["pool"].plan_step(ids, tot, comp, budget, sb)
 
 
 @pytest.mark.parametrize("seed", range(12))
@@ -218,6 +215,8 @@ def test_errors():
     z = np.zeros(4, np.int32)
     smp = np.zeros(4, np.uint8)
     ptr = lambda a: a.ctypes.data_as(P)
+    nc = ctypes.c_int32(0)
     st = L.pcp_schedule_step(pg._h, 1, ptr(ids), ptr(tot), ptr(comp), 64, 0, ctypes.byref(n),
-                             ptr(z), ptr(z), ptr(z), ptr(z), ptr(z), 1, ptr(smp))
+                             ptr(z), ptr(z), ptr(z), ptr(z), ptr(z), 1, ptr(smp),
+                             ctypes.byref(nc), ptr(z), ptr(z), ptr(z))
     assert st == pcp.Status.WORKSPACE and pg.num_free() == 4   # nothing taken
