@@ -527,6 +527,7 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
     res.update(masked_secondary(pcp, torch, W, dev, peaks, flush, err))
 
     res["chunk_planner"] = planner_secondary(pcp)
+    res["cow_page_copy"] = cow_secondary(pcp, torch, dev, peaks, flush)
 
     # the mixed scheduler batch: prompt chunks (tensor cores) and decode rows
     # (row kernel) in one call
@@ -581,6 +582,24 @@ def planner_secondary(pcp, n_decode=240, n_prompt=16, steps=200):
     return {"workload": f"{n_decode} decoding + {n_prompt} prefilling requests, budget 8192, "
                         f"page size 16", "us_per_step": float(np.median(times) * 1e6),
             "what": "host time of pcp_schedule_step through the Python binding (median)"}
+
+
+def cow_secondary(pcp, torch, dev, peaks, flush, n_copies=2048, page_size=16, hkv=8, d=128):
+    """pcp_copy_page_slots on 2048 whole pages (K and V) of a pool of 8192."""
+    num_pages = 4 * n_copies
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    kp = torch.randn(num_pages * page_size, hkv, d, device=dev, generator=g).to(torch.bfloat16)
+    vp = torch.randn(num_pages * page_size, hkv, d, device=dev, generator=g).to(torch.bfloat16)
+    perm = torch.randperm(num_pages, device=dev, generator=g).to(torch.int32)
+    src, dst = perm[:n_copies].contiguous(), perm[n_copies:2 * n_copies].contiguous()
+    nsl = torch.full((n_copies,), page_size, dtype=torch.int32, device=dev)
+    ms = time_calls(torch, lambda: pcp.copy_page_slots(kp, vp, page_size, src, dst, nsl,
+                                                        check=False), flush)
+    nbytes = 2 * 2 * n_copies * page_size * hkv * d * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"{n_copies} whole pages of {page_size} slots x {hkv} KV heads x D {d}",
+            "ms": ms, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes}
 
 
 def masked_secondary(pcp, torch, W, dev, peaks, flush, err):
