@@ -59,13 +59,17 @@ def rows_pairs(batch, tok, head) -> int:
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the dominant kernel, from an ncu capture of this bench on the named workload
-# (profiles/extend_tc_gqa_prefill_ncu.md).  It is reported only while the
+# (profiles/extend_tc_gqa_prefill_ncu.md, profiles/row_attn_decode_rows_ncu.md).  It is reported only while the
 # library sources hash to the value the capture ran with; after any change
 # the key reads null until the counters are taken again.
 NCU_TRAFFIC = {
     ("gqa_prefill", "extend_tc_kernel<128>"): {
-        "bytes": 207.047936e6 + 18.555648e6,
-        "csrc_sha256": "647c09c2fcc50816ba3df9a5bfc0d3da",
+        "bytes": 203.641600e6 + 18.675456e6,
+        "csrc_sha256": "ad5cc7033dc159f84fe66565cfead63d",
+    },
+    ("decode_rows", "row_attn_kernel<128>"): {
+        "bytes": 275.739136e6 + 3.936512e6,
+        "csrc_sha256": "ad5cc7033dc159f84fe66565cfead63d",
     },
 }
 
