@@ -88,6 +88,7 @@ struct Geo {
     int t_begin, t_end;
 };
 
+template <bool kCausal>
 __device__ __forceinline__ Geo make_geo(const TcParams& p, int4 it) {
     Geo g;
     g.b = it.x;
@@ -108,7 +109,7 @@ __device__ __forceinline__ Geo make_geo(const TcParams& p, int4 it) {
             const int lo = p.window > 0 ? max(0, g.pl[u] - p.window + 1) : 0;
             g.first[u] = lo / kTileN;
             // causal: up to the tile's last row; otherwise every key of the sequence
-            g.last[u] = (p.causal ? g.ph[u] : g.L - 1) / kTileN;
+            g.last[u] = (kCausal ? g.ph[u] : g.L - 1) / kTileN;
         } else {
             g.pl[u] = g.ph[u] = 0;
             g.first[u] = 1;
@@ -256,9 +257,10 @@ __device__ __forceinline__ void gather_kv_rows(const TcParams& p, const Geo& geo
 
 }  // namespace
 
-// kMask: the call passes a boolean mask (a separate instantiation, so the
-// plain causal path carries none of its registers).
-template <int D, bool kMask>
+// kMask: the call passes a boolean mask; kCausal: bottom-right causal (else
+// every row sees all keys).  Separate instantiations, so the plain causal
+// path carries none of the other paths' instructions or registers.
+template <int D, bool kMask, bool kCausal>
 __global__ void __launch_bounds__(kTcThreads, 1)
     extend_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncthreads();
         const int item = misc[1];
         if (item >= n_items || *abort_flag) break;
-        const Geo geo = make_geo(p, items[item]);
+        const Geo geo = make_geo<kCausal>(p, items[item]);
         const int ntiles = geo.t_end - geo.t_begin + 1;
 
         // Page boxes: the TMA warp issues the K tiles and the first gather warp
@@ -559,7 +561,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // tile holding the sequence end; with a mask, every tile
                     const bool need_mask =
                         has_mask ||
-                        (p.causal ? (key0 + kTileN - 1 > pl_u) ||
+                        (kCausal ? (key0 + kTileN - 1 > pl_u) ||
                                         (p.window > 0 && key0 < ph_u - p.window + 1)
                                   : key0 + kTileN > geo.L);
                     // the boolean mask's keep-bits of this row's keys in the tile
@@ -585,7 +587,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         for (int j = 0; j < 128; ++j) {
                             const int key = key0 + j;
                             const bool vis =
-                                (p.causal ? key <= pabs && (p.window <= 0 || key > pabs - p.window)
+                                (kCausal ? key <= pabs && (p.window <= 0 || key > pabs - p.window)
                                           : key < geo.L) &&
                                 ((mb[j >> 5] >> (j & 31)) & 1u);
                             if (!vis) v[j] = __float_as_uint(-INFINITY);
@@ -746,26 +748,34 @@ size_t tc_smem_bytes(int head_dim) {
     return head_dim == 128 ? TcCfg<128>::kSmemBytes : TcCfg<64>::kSmemBytes;
 }
 
-template <int D, bool kMask>
+template <int D, bool kMask, bool kCausal>
 cudaError_t launch_extend_tc_t(int grid, cudaStream_t stream, const TcParams& p,
                                const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv) {
     const size_t smem = TcCfg<D>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<D, kMask>,
+    cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<D, kMask, kCausal>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(extend_tc_kernel<D, kMask>, dim3(grid), dim3(kTcThreads), smem, stream, p,
-                      tq, tk, tv);
+    return launch_pdl(extend_tc_kernel<D, kMask, kCausal>, dim3(grid), dim3(kTcThreads), smem,
+                      stream, p, tq, tk, tv);
+}
+
+template <int D>
+cudaError_t launch_extend_tc_d(int grid, cudaStream_t stream, const TcParams& p,
+                               const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv) {
+    const bool mask = p.mask.data != nullptr;
+    if (p.causal)
+        return mask ? launch_extend_tc_t<D, true, true>(grid, stream, p, tq, tk, tv)
+                    : launch_extend_tc_t<D, false, true>(grid, stream, p, tq, tk, tv);
+    return mask ? launch_extend_tc_t<D, true, false>(grid, stream, p, tq, tk, tv)
+                : launch_extend_tc_t<D, false, false>(grid, stream, p, tq, tk, tv);
 }
 
 cudaError_t launch_extend_tc(int head_dim, int grid, cudaStream_t stream, const TcParams& p,
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv) {
-    const bool mask = p.mask.data != nullptr;
-    if (head_dim == 128)
-        return mask ? launch_extend_tc_t<128, true>(grid, stream, p, tq, tk, tv)
-                    : launch_extend_tc_t<128, false>(grid, stream, p, tq, tk, tv);
-    return mask ? launch_extend_tc_t<64, true>(grid, stream, p, tq, tk, tv)
-                : launch_extend_tc_t<64, false>(grid, stream, p, tq, tk, tv);
+    return head_dim == 128 ? launch_extend_tc_d<128>(grid, stream, p, tq, tk, tv)
+                           : launch_extend_tc_d<64>(grid, stream, p, tq, tk, tv);
 }
 
 }  // namespace pcp
