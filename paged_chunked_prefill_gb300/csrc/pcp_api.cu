@@ -336,6 +336,7 @@ pcp_status pcp_paged_extend_attn_masked(
     tp.qpos = qpos;
     tp.page_size = page_size;
     tp.box_rows = box_rows;
+    tp.page_shift = (page_size & (page_size - 1)) == 0 ? __builtin_ctz((unsigned)page_size) : -1;
     tp.num_pages = num_pages;
     MaskParams mp;
     mp.data = mask;

@@ -387,29 +387,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         } else if (warp >= kWarpGather0) {
             // ------------------------------------------------ cp.async page gathers
+            // each gather warp copies rows gw*64 .. gw*64+63 of every K and V
+            // tile (two warps issuing cp.async in parallel)
             if (p.box_rows == 0) {
                 using GS = GatherShape<D>;
                 const int gw = warp - kWarpGather0;
                 const int32_t* pages = p.kv_indices + p.kv_indptr[geo.b];
                 const int rsub = lane / GS::kChunks;
-                for (int i = 0; i < ntiles; ++i) {
-                    const int t = geo.t_begin + i;
-                    const uint32_t cur = kv_iter + i;
-                    const int sk = cur % SK, sv = cur % SV;
-                    // slots of this lane's rows (shared by K and V), read before
-                    // the wait so the page table's latency overlaps it
-                    int slot[GS::kInsts];
+                // slots of this lane's rows of tile t (shared by K and V)
+                auto fetch_slots = [&](int t, int (&slot)[GS::kInsts]) {
 #pragma unroll
                     for (int j = 0; j < GS::kInsts; ++j) {
                         const int key = t * kTileN + gw * GS::kRows + j * GS::kRowsPerInst + rsub;
                         slot[j] = -1;
                         if (key < geo.L) {
-                            const int page = pages[key / p.page_size];
+                            const int entry =
+                                p.page_shift >= 0 ? key >> p.page_shift : key / p.page_size;
+                            const int page = pages[entry];
                             if (page >= 0 && page < p.num_pages)
-                                slot[j] = page * p.page_size + key % p.page_size;
+                                slot[j] = page * p.page_size + (key - entry * p.page_size);
                             else
                                 report_error(p.dev_err, PCP_ERR_BAD_INDEX);
                         }
+                    }
+                };
+                for (int i = 0; i < ntiles; ++i) {
+                    const int t = geo.t_begin + i;
+                    const uint32_t cur = kv_iter + i;
+                    const int sk = cur % SK, sv = cur % SV;
+                    int slot[GS::kInsts];
+                    fetch_slots(t, slot);
+                    // the next tile's page-table lines go to L1 while this one
+                    // is waited for and issued
+                    if (i + 1 < ntiles) {
+                        const int key = (t + 1) * kTileN + gw * GS::kRows + 2 * lane;
+                        if (key < geo.L)
+                            prefetch_l1(pages + (p.page_shift >= 0 ? key >> p.page_shift
+                                                                   : key / p.page_size));
                     }
                     if (!mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u, abort_flag,
                                    p.dev_err, kSpinLimitNs))

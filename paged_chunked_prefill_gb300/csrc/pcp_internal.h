@@ -171,6 +171,7 @@ struct TcParams {
     int qpos;          // positions per Q tile
     int page_size;
     int box_rows;      // rows per TMA page box; 0 selects the cp.async gather warps
+    int page_shift;    // log2(page_size) for a power of two, else -1
     int64_t num_pages;
     int num_slots;
     int window;
