@@ -225,6 +225,36 @@ __device__ __forceinline__ void mask_bits_128(const uint8_t* mrow, int key0, int
     }
 }
 
+// The same 128 keep-bits when every lane of the warp reads one mask row: lane
+// l reads keys key0 + 4l .. key0 + 4l + 3 and the warp assembles the words
+// with shuffles.
+__device__ __forceinline__ void mask_bits_128_warp(const uint8_t* mrow, int key0, int kv_len,
+                                                   int lane, uint32_t (&mb)[4]) {
+    const int k = key0 + 4 * lane;
+    uint32_t nib = 0u;
+    if (k + 4 <= kv_len) {
+        nib = nonzero_bytes(__ldg(reinterpret_cast<const uint32_t*>(mrow + k)));
+    } else {
+        for (int e = 0; e < 4 && k + e < kv_len; ++e)
+            if (mrow[k + e]) nib |= 1u << e;
+    }
+    uint32_t part = nib << (4 * (lane & 7));
+    part |= __shfl_xor_sync(0xffffffffu, part, 1);
+    part |= __shfl_xor_sync(0xffffffffu, part, 2);
+    part |= __shfl_xor_sync(0xffffffffu, part, 4);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) mb[w] = __shfl_sync(0xffffffffu, part, 8 * w);
+}
+
+// Bits j of [0, 32) with lo <= j < hi.
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
+    lo = max(0, min(lo, 32));
+    hi = max(0, min(hi, 32));
+    const uint32_t below_hi = hi >= 32 ? ~0u : (1u << hi) - 1u;
+    const uint32_t below_lo = lo >= 32 ? ~0u : (1u << lo) - 1u;
+    return below_hi & ~below_lo;
+}
+
 // One gather warp's share (rows gw*64 .. gw*64+63) of a K or V tile: lanes
 // split into groups covering one 256-byte (128-byte for D = 64) row each.
 template <int D>
@@ -578,18 +608,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         (kCausal ? (key0 + kTileN - 1 > pl_u) ||
                                         (p.window > 0 && key0 < ph_u - p.window + 1)
                                   : key0 + kTileN > geo.L);
-                    // the boolean mask's keep-bits of this row's keys in the tile
+                    // keep-bits of this row's keys in the tile (bit j of mb[j / 32]):
+                    // the boolean mask's entries, and'ed with the causal / length
+                    // range, so each key costs one bit test
                     uint32_t mb[4] = {~0u, ~0u, ~0u, ~0u};
                     if constexpr (has_mask) {
-                        const int qi = geo.pos0 + pos_local;
-                        const bool in_mask =
-                            row_valid && (p.mask.q_stride == 0 || qi < p.mask.q_len);
-                        const uint8_t* mrow =
-                            in_mask ? p.mask.data + (int64_t)geo.b * p.mask.b_stride +
-                                          (int64_t)head * p.mask.h_stride +
-                                          (int64_t)qi * p.mask.q_stride
-                                    : nullptr;
-                        mask_bits_128(mrow, key0, p.mask.kv_len, mb);
+                        if (p.mask.h_stride == 0 && p.mask.q_stride == 0) {
+                            // one mask row for the whole tile: the warp builds it
+                            const uint8_t* mrow =
+                                p.mask.data + (int64_t)geo.b * p.mask.b_stride;
+                            mask_bits_128_warp(mrow, key0, p.mask.kv_len, lane, mb);
+                        } else {
+                            const int qi = geo.pos0 + pos_local;
+                            const bool in_mask =
+                                row_valid && (p.mask.q_stride == 0 || qi < p.mask.q_len);
+                            const uint8_t* mrow =
+                                in_mask ? p.mask.data + (int64_t)geo.b * p.mask.b_stride +
+                                              (int64_t)head * p.mask.h_stride +
+                                              (int64_t)qi * p.mask.q_stride
+                                        : nullptr;
+                            mask_bits_128(mrow, key0, p.mask.kv_len, mb);
+                        }
+                        // visible key range of the row in tile coordinates
+                        const int hi = kCausal ? pabs - key0 + 1 : geo.L - key0;
+                        const int lo = kCausal && p.window > 0 ? pabs - p.window + 1 - key0 : 0;
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) mb[w] &= range_bits(lo - 32 * w, hi - 32 * w);
                     }
                     // the whole S row of this thread: one TMEM load
                     uint32_t v[128];
@@ -599,11 +643,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         // keys this row does not see become -inf
 #pragma unroll
                         for (int j = 0; j < 128; ++j) {
-                            const int key = key0 + j;
-                            const bool vis =
-                                (kCausal ? key <= pabs && (p.window <= 0 || key > pabs - p.window)
-                                          : key < geo.L) &&
-                                ((mb[j >> 5] >> (j & 31)) & 1u);
+                            bool vis;
+                            if constexpr (has_mask) {
+                                vis = (mb[j >> 5] >> (j & 31)) & 1u;
+                            } else {
+                                const int key = key0 + j;
+                                vis = kCausal ? key <= pabs &&
+                                                    (p.window <= 0 || key > pabs - p.window)
+                                              : key < geo.L;
+                            }
                             if (!vis) v[j] = __float_as_uint(-INFINITY);
                         }
                     }
