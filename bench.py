@@ -180,6 +180,23 @@ class L2Flush:
         self.torch.sum(self.buf, dim=0, out=self.out)
 
 
+def max_over_ranks(torch, value: float, world: int, device) -> float:
+    """The largest of every rank's value (all_reduce MAX; the value itself on
+    one rank).  Used for step times: the whole job is as slow as its slowest
+    rank."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Units per second of the whole job: every rank processes its own
+    replica's units (weak scaling) in at most `ms` milliseconds."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -337,16 +354,14 @@ def main():
     step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
     tc_ms = [c.elapsed_time(e) for _, _, c, e in ev]
     total_ms = float(sum(step_ms))
+    total_ms = max_over_ranks(torch, total_ms, world, dev)
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
         torch.distributed.barrier()
     code = pcp.read_error(err)
     if code != 0:
         raise RuntimeError(f"device error {code} in the timed region")
     ms_per_step = total_ms / args.steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_rate(flops, world, ms_per_step) / 1e12
 
     peaks, peak_kind = load_peaks()
     tc_avg = float(np.mean(tc_ms))
@@ -435,10 +450,12 @@ def end_to_end(args, torch, d, out, lse, step, flush, stream, flops, world):
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    e2e_value = world * flops / (float(np.mean(e2e_ms)) * 1e-3) / 1e12
+    e2e_mean = max_over_ranks(torch, float(np.mean(e2e_ms)), world, torch.device(
+        "cuda", torch.cuda.current_device()))
+    e2e_value = whole_job_rate(flops, world, e2e_mean) / 1e12
 
     return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": float(np.mean(e2e_ms))}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_mean}
 
 
 def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
