@@ -312,6 +312,7 @@ pcp_status pcp_paged_extend_attn_masked(
     pp.page_size = page_size;
     pp.window = window;
     pp.causal = causal;
+    pp.tc_work = run_tc ? 1 : 0;
     pp.sm_count = sms;
     pp.ws = ws;
     pp.lay = lay;

@@ -147,6 +147,7 @@ struct PlanParams {
     int page_size;
     int window;
     int causal;
+    int tc_work;       // 0: the host knows no chunk goes to the tensor cores
     int sm_count;
     unsigned char* ws;
     WsLayout lay;

@@ -26,17 +26,19 @@ namespace pcp {
 namespace {
 
 struct SeqInfo {
-    int c, P, L;
+    int c, P, L, q0, kvb;
     bool ok;
 };
 
 __device__ __forceinline__ SeqInfo seq_info(const PlanParams& p, int b) {
     SeqInfo s;
     const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
+    s.q0 = q0;
+    s.kvb = p.kv_indptr[b];
     s.c = q1 - q0;
     s.P = p.prefix_lens[b];
     s.L = s.P + s.c;
-    const int pages = p.kv_indptr[b + 1] - p.kv_indptr[b];
+    const int pages = p.kv_indptr[b + 1] - s.kvb;
     s.ok = q0 >= 0 && s.c >= 0 && q1 <= p.total_q && s.P >= 0 && pages >= 0 &&
            (int64_t)pages * p.page_size >= (int64_t)s.L;
     return s;
@@ -156,6 +158,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     __shared__ int s_b[1025];
     __shared__ int s_c[1025];
     __shared__ int4 s_seq[1024];    // {c, P, ok, row tiles}
+    __shared__ int2 s_off[1024];    // {qo_indptr[b], kv_indptr[b]}
     __shared__ unsigned long long s_row_tiles;
 
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
@@ -183,8 +186,10 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     auto load_chunk = [&](int chunk0, bool report) {
         const int b = chunk0 + tid;
         int4 v = make_int4(0, 0, 0, 0);
+        int2 off = make_int2(0, 0);
         if (b < p.batch) {
             const SeqInfo q = seq_info(p, b);
+            off = make_int2(q.q0, q.kvb);
             if (!q.ok && report) report_error(p.dev_err, PCP_ERR_INVALID_ARG);
             const int tiles = (q.ok && q.c > 0 && q.c <= rmax)
                                   ? (q.L - 1) / kRowTile - first_key(q.P, p.window) / kRowTile + 1
@@ -192,6 +197,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
             v = make_int4(q.c, q.P, q.ok ? 1 : 0, tiles);
         }
         s_seq[tid] = v;
+        s_off[tid] = off;
     };
     auto n_tc_of = [&](int4 v) {  // tensor-core items of one KV head
         return (v.z && v.x > rmax) ? (v.x + item_pos - 1) / item_pos : 0;
@@ -208,16 +214,18 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
         for (int o = 16; o > 0; o >>= 1) rt += __shfl_xor_sync(0xffffffffu, rt, o);
         if (lane == 0 && rt) atomicAdd(&s_row_tiles, rt);
         __syncthreads();
-        const int total = excl_scan(s_a, warp_sums);
-        for (int f = tid; f < total; f += 1024) {
-            const int sl = segment_of(s_a, 1024, f);
-            const int4 v = s_seq[sl];
-            const int cost = tc_cost(v.y, v.x, f - s_a[sl], item_pos, p.window, p.causal);
-            warp_agg_add(hist, min(cost, 1023), H);
+        if (p.tc_work) {
+            const int total = excl_scan(s_a, warp_sums);
+            for (int f = tid; f < total; f += 1024) {
+                const int sl = segment_of(s_a, 1024, f);
+                const int4 v = s_seq[sl];
+                const int cost = tc_cost(v.y, v.x, f - s_a[sl], item_pos, p.window, p.causal);
+                warp_agg_add(hist, min(cost, 1023), H);
+            }
         }
     }
     __syncthreads();
-    const int n_tc = desc_offsets(hist, warp_sums);
+    const int n_tc = p.tc_work ? desc_offsets(hist, warp_sums) : 0;
     const unsigned long long row_tiles_all = s_row_tiles;
     if (tid == 0 && row_tiles_all >= (1ull << 31)) report_error(p.dev_err, PCP_ERR_UNSUPPORTED);
     const int T = (int)min(row_tiles_all, (unsigned long long)INT32_MAX);
@@ -239,7 +247,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
         s_b[tid] = s_seq[tid].w > 0 ? H : 0;
         s_c[tid] = s_seq[tid].w;
         __syncthreads();
-        const int total_a = excl_scan(s_a, warp_sums);
+        const int total_a = p.tc_work ? excl_scan(s_a, warp_sums) : 0;
         const int total_b = excl_scan(s_b, warp_sums);
         const int total_c = excl_scan(s_c, warp_sums);
         for (int f = tid; f < total_a; f += 1024) {
@@ -272,10 +280,10 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
                 continue;
             }
             const int P = v.y, L = v.x + v.y;
-            const int q0 = p.qo_indptr[b];
+            const int q0 = s_off[sl].x;
             rg[3 * k] = make_int4(b, g, S, tiles);
             rg[3 * k + 1] = make_int4(first_key(P, p.window), q0, base, ns);
-            rg[3 * k + 2] = make_int4(v.x, P, p.kv_indptr[b], L);
+            rg[3 * k + 2] = make_int4(v.x, P, s_off[sl].y, L);
             gdesc[(int64_t)b * H + g] = make_int4(base, ns, q0, v.x);
             // CTAs whose first tile lies in this group start with it
             for (int i = i_first; i <= i_last; ++i)
