@@ -19,21 +19,31 @@ __global__ void out_cache_loc_kernel(const int32_t* __restrict__ qo_indptr,
                                      const int32_t* __restrict__ prefix_lens, int batch,
                                      int64_t total_q, int page_size, int64_t num_pages,
                                      int64_t* __restrict__ loc, int32_t* dev_err) {
+    // qo_indptr in shared memory (one coalesced read per CTA) when it fits,
+    // so the search below costs no global round trips
+    constexpr int kStagedSeqs = 2048;
+    __shared__ int s_qo[kStagedSeqs + 1];
     pdl_wait();
     pdl_launch_dependents();
+    const bool staged = batch <= kStagedSeqs;
+    if (staged) {
+        for (int i = threadIdx.x; i <= batch; i += blockDim.x) s_qo[i] = qo_indptr[i];
+        __syncthreads();
+    }
+    const int32_t* qo = staged ? s_qo : qo_indptr;
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total_q;
          t += (int64_t)gridDim.x * blockDim.x) {
         // sequence owning row t: the last b with qo_indptr[b] <= t
         int lo = 0, hi = batch;  // answer in [lo, hi)
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (qo_indptr[mid] <= t) lo = mid;
+            if (qo[mid] <= t) lo = mid;
             else hi = mid;
         }
         const int b = lo;
         int64_t out = -1;
-        if (t >= qo_indptr[b] && t < qo_indptr[b + 1]) {
-            const int64_t pos = (int64_t)prefix_lens[b] + (t - qo_indptr[b]);
+        if (t >= qo[b] && t < qo[b + 1]) {
+            const int64_t pos = (int64_t)prefix_lens[b] + (t - qo[b]);
             const int64_t entry = pos / page_size;
             if (pos >= 0 && entry < (int64_t)kv_indptr[b + 1] - kv_indptr[b]) {
                 const int64_t page = kv_indices[kv_indptr[b] + entry];

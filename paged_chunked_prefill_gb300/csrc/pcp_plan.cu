@@ -176,11 +176,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     pdl_launch_dependents();
     hist[tid] = 0;
     for (int64_t i = tid; i < (int64_t)p.batch * H; i += 1024) gdesc[i] = make_int4(0, 0, 0, 0);
-    if (tid == 0) {
-        s_row_tiles = 0;
-        if (p.batch > 0 && p.qo_indptr[p.batch] != p.total_q)
-            report_error(p.dev_err, PCP_ERR_INVALID_ARG);
-    }
+    if (tid == 0) s_row_tiles = 0;
 
     // metadata of sequence chunk0 + tid (kept in s_seq); reports bad sequences once
     auto load_chunk = [&](int chunk0, bool report) {
@@ -190,7 +186,9 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
         if (b < p.batch) {
             const SeqInfo q = seq_info(p, b);
             off = make_int2(q.q0, q.kvb);
-            if (!q.ok && report) report_error(p.dev_err, PCP_ERR_INVALID_ARG);
+            // qo_indptr[batch] must be total_q (the last sequence's end)
+            if (report && (!q.ok || (b == p.batch - 1 && q.q0 + q.c != p.total_q)))
+                report_error(p.dev_err, PCP_ERR_INVALID_ARG);
             const int tiles = (q.ok && q.c > 0 && q.c <= rmax)
                                   ? (q.L - 1) / kRowTile - first_key(q.P, p.window) / kRowTile + 1
                                   : 0;

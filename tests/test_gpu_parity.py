@@ -278,6 +278,22 @@ def test_bad_chunk_page_reported_by_slot_mapping():
     assert e.value.status == pcp.Status.BAD_INDEX
 
 
+@pytest.mark.parametrize("last", [45, 55])
+def test_device_qo_indptr_end_must_be_total_q(last):
+    """Without the host copy, the planner checks on the device that
+    qo_indptr[batch] equals total_q (the rows of q); a sequence that would
+    run past total_q is skipped, so nothing is read or written out of range."""
+    import paged_chunked_prefill_gb300 as pcp
+    import torch
+    b = W.make_batch([10, 60], [20, 30], 8, 2, 64, 16, seed=43)
+    d = to_device(b)
+    qo = torch.tensor([0, 20, last], dtype=torch.int32, device="cuda")
+    with pytest.raises(pcp.PCPError) as e:
+        pcp.paged_extend_attn(d["q"], qo, d["kv_indptr"], d["kv_indices"], d["prefix_lens"],
+                              d["k_pool"], d["v_pool"], 16, 8, 2, 64)
+    assert e.value.status == pcp.Status.INVALID_ARG
+
+
 def test_host_errors_before_launch():
     import paged_chunked_prefill_gb300 as pcp
     import torch
