@@ -383,6 +383,8 @@ pcp_status pcp_paged_extend_attn_masked(
         rp.group = group;
         rp.page_size = page_size;
         rp.box_rows = box_rows;
+        rp.box_shift = box_rows > 0 ? __builtin_ctz((unsigned)box_rows) : 0;
+        rp.page_shift = tp.page_shift;
         rp.num_pages = num_pages;
         rp.num_slots = num_slots;
         rp.window = window;

@@ -212,6 +212,8 @@ struct RowParams {
     int group;
     int page_size;
     int box_rows;      // rows per TMA page box; 0 selects cp.async gathers
+    int box_shift;     // log2(box_rows) (a power of two), when box_rows > 0
+    int page_shift;    // log2(page_size) when it is a power of two, else -1
     int64_t num_pages;
     int num_slots;
     int window;

@@ -150,19 +150,24 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     if (warp == 4) {
         // ==================================================== load warp
         const int ps = p.page_size;
+        // box geometry: nsub page runs of br = 2^box_shift rows per tile
+        const int nsub_shift = 7 - p.box_shift;  // kRowTile = 128 = 2^7
+        const int nsub = 1 << nsub_shift;
+        // page-table entry of key (a shift for power-of-two page sizes)
+        auto entry_of = [&](int key) { return p.page_shift >= 0 ? key >> p.page_shift : key / ps; };
         // slot (TMA: first slot of this lane's page run; gather: slots of
         // rows lane + 32k) of tile t of a sequence with page list `pages`
         auto fetch = [&](const int32_t* pages, int L, int t, int (&sl)[4]) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) sl[k] = -1;
             if (p.box_rows > 0) {
-                const int nsub = kRowTile / p.box_rows;
-                const int key = t * kRowTile + (lane % nsub) * p.box_rows;
+                const int key = t * kRowTile + ((lane & (nsub - 1)) << p.box_shift);
                 sl[0] = p.num_slots;
                 if (lane < nsub * C::kHalves && key < L) {
-                    const int page = pages[key / ps];
+                    const int e = entry_of(key);
+                    const int page = pages[e];
                     if (page >= 0 && page < p.num_pages)
-                        sl[0] = page * ps + key % ps;
+                        sl[0] = page * ps + (key - e * ps);
                     else
                         report_error(p.dev_err, PCP_ERR_BAD_INDEX);
                 }
@@ -171,9 +176,10 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 for (int k = 0; k < 4; ++k) {
                     const int key = t * kRowTile + lane + 32 * k;
                     if (key < L) {
-                        const int page = pages[key / ps];
+                        const int e = entry_of(key);
+                        const int page = pages[e];
                         if (page >= 0 && page < p.num_pages)
-                            sl[k] = page * ps + key % ps;
+                            sl[k] = page * ps + (key - e * ps);
                         else
                             report_error(p.dev_err, PCP_ERR_BAD_INDEX);
                     }
@@ -257,12 +263,12 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 const uint32_t kd = sStage + st * 2 * C::kTileBytes;
                 const uint32_t vd = kd + C::kTileBytes;
                 if (p.box_rows > 0) {
-                    const int br = p.box_rows, nsub = kRowTile / br, nloads = nsub * C::kHalves;
+                    const int br = p.box_rows, nloads = nsub * C::kHalves;
                     const int key0 = t * kRowTile;
                     // the V page run holding the sequence end is zero-filled past it
                     int strad = -1;
-                    if (L > key0 && L < key0 + kRowTile && (L - key0) % br != 0)
-                        strad = (L - key0) / br;
+                    if (L > key0 && L < key0 + kRowTile && ((L - key0) & (br - 1)) != 0)
+                        strad = (L - key0) >> p.box_shift;
                     if (strad >= 0) {
                         const int slot0 = __shfl_sync(0xffffffffu, cur_sl[0], strad);
                         const bool bad = slot0 >= p.num_slots;
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                             (uint32_t)(2 * nloads - (strad >= 0 ? C::kHalves : 0)) * br * 128);
                     __syncwarp();
                     if (lane < nloads) {
-                        const int sb = lane % nsub, h = lane / nsub;
+                        const int sb = lane & (nsub - 1), h = lane >> nsub_shift;
                         tma_load_3d(kd + h * C::kHalfBytes + sb * br * 128, &tm_k, full_bar(st),
                                     h * 64, g, cur_sl[0]);
                         if (sb != strad)
@@ -422,6 +428,28 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                     }
                 // mask and scale; element j: row lo (j < 2) or hi, key = ... + 2 * tig + (j & 1)
                 float mx_lo = -INFINITY, mx_hi = -INFINITY;
+                // every row of the item sees all 32 keys of this warp (the
+                // interior of a long KV range): scale only.  Rows past R hold
+                // zero queries; their results are never read.
+                bool all_vis = !kMask && key_w >= kb && key_w + 32 <= ke;
+                if (p.causal)
+                    all_vis = all_vis && key_w + 31 <= P &&
+                              (p.window <= 0 || key_w > P + d2.x - 1 - p.window);
+                else
+                    all_vis = all_vis && key_w + 32 <= L;
+                if (all_vis) {
+#pragma unroll
+                    for (int bl = 0; bl < 2; ++bl)
+#pragma unroll
+                        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float v = sc[bl][nb][j] * sl2;
+                                sc[bl][nb][j] = v;
+                                if (j < 2) mx_lo = fmaxf(mx_lo, v);
+                                else mx_hi = fmaxf(mx_hi, v);
+                            }
+                } else {
 #pragma unroll
                 for (int bl = 0; bl < 2; ++bl)
 #pragma unroll
@@ -444,6 +472,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                             if (j < 2) mx_lo = fmaxf(mx_lo, v);
                             else mx_hi = fmaxf(mx_hi, v);
                         }
+                }
                 mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
                 mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
                 mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
@@ -472,12 +501,15 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                     }
                 l_lo = l_lo * a_lo + s_lo;
                 l_hi = l_hi * a_hi + s_hi;
+                // O is rescaled only when some row's running max moved
+                if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
 #pragma unroll
-                for (int dn = 0; dn < D / 8; ++dn) {
-                    o[dn][0] *= a_lo;
-                    o[dn][1] *= a_lo;
-                    o[dn][2] *= a_hi;
-                    o[dn][3] *= a_hi;
+                    for (int dn = 0; dn < D / 8; ++dn) {
+                        o[dn][0] *= a_lo;
+                        o[dn][1] *= a_lo;
+                        o[dn][2] *= a_hi;
+                        o[dn][3] *= a_hi;
+                    }
                 }
                 // O += P V; V fragments for two 8-wide column chunks per ldmatrix.trans
 #pragma unroll

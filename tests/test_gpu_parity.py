@@ -149,6 +149,19 @@ def test_decode_rows_many_splits():
     full_parity(b, "many splits")
 
 
+@pytest.mark.parametrize("ps", [8, 24, 48, 112])
+def test_decode_rows_page_windows(ps):
+    """Long decode rows over small and odd page sizes: the row kernel reads
+    page ids through a moving window of page-table entries, with tiles that
+    straddle its halves when the page size does not divide 128; some rows
+    start past key 0 (sliding window) and some are split across CTAs."""
+    rng = np.random.default_rng(ps)
+    P = [9000, 7001, 3000] + list(rng.integers(1, 2500, size=9))
+    for window in (0, 2000):
+        b = W.make_batch(P, [1] * len(P), 16, 4, 128, ps, seed=50 + ps, window=window)
+        full_parity(b, f"decode rows, page_size {ps}, window {window}")
+
+
 def test_decode_only_long():
     """Many decode rows with long KV: split-KV pieces and the combine."""
     b = W.make_batch(list(np.random.default_rng(3).integers(1, 9000, size=12)), [1] * 12, 16, 4,
