@@ -426,39 +426,57 @@ def end_to_end(args, torch, pcp, batch, d, out_ref, flush, stream, flops, world)
     read-back of its previous step has finished; with three sets that wait
     does not chain one step's copies, kernels and read-back to the next's.
 
+    The inputs travel as one pinned buffer and out / lse come back as one, so
+    a step makes one copy each way.
+
     Also reported: the same step run alone (copies, kernels, read-back one
     after the other, L2 flushed before it)."""
-    h_q = d["q"].cpu().pin_memory()
-    h_k = d["k_new"].cpu().pin_memory()
-    h_v = d["v_new"].cpu().pin_memory()
-    meta = ("qo_indptr", "kv_indptr", "kv_indices", "prefix_lens")
-    h_meta = [d[n].cpu().pin_memory() for n in meta]
-    h2d = sum(t.numel() * t.element_size() for t in [h_q, h_k, h_v] + h_meta)
+    # one pinned input buffer (q, the chunk's K/V, the metadata) and one
+    # output buffer (out, lse) per step, each moved by one copy: the copy
+    # engines pay a fixed cost per copy
+    inputs = ("q", "k_new", "v_new", "qo_indptr", "kv_indptr", "kv_indices", "prefix_lens")
+    dev = d["q"].device
+
+    def layout(tensors):
+        offs, off = [], 0
+        for t in tensors:
+            offs.append(off)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, off
+
+    def views(buf, offs, likes):
+        return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                for o, t in zip(offs, likes)]
+
+    in_offs, in_bytes = layout([d[n] for n in inputs])
+    h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    for hv, n in zip(views(h_in, in_offs, [d[n] for n in inputs]), inputs):
+        hv.copy_(d[n].cpu())
+    h2d = in_bytes
+    out_like = [torch.empty_like(d["q"]),
+                torch.empty(batch.total_q, batch.n_q_heads, dtype=torch.float32, device=dev)]
+    out_offs, out_bytes = layout(out_like)
     ws_bytes = pcp.workspace_size(batch.batch, batch.total_q, batch.n_q_heads, batch.n_kv_heads,
                                   batch.head_dim)
-    dev = d["q"].device
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     n_sets = 3
     sets = []
     for _ in range(n_sets):
-        S = {n: torch.empty_like(d[n]) for n in ("q", "k_new", "v_new") + meta}
+        S = {"in": torch.empty(in_bytes, dtype=torch.uint8, device=dev),
+             "res": torch.empty(out_bytes, dtype=torch.uint8, device=dev),
+             "h_res": torch.empty(out_bytes, dtype=torch.uint8).pin_memory()}
+        S.update(zip(inputs, views(S["in"], in_offs, [d[n] for n in inputs])))
+        S["out"], S["lse"] = views(S["res"], out_offs, out_like)
+        S["h_out"], S["h_lse"] = views(S["h_res"], out_offs, out_like)
         S["k_pool"] = d["k_pool"].clone()
         S["v_pool"] = d["v_pool"].clone()
-        S["out"] = torch.empty_like(d["q"])
-        S["lse"] = torch.empty(batch.total_q, batch.n_q_heads, dtype=torch.float32, device=dev)
         S["loc"] = torch.empty(batch.total_q, dtype=torch.int64, device=dev)
         S["ws"] = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-        S["h_out"] = torch.empty(S["out"].shape, dtype=S["out"].dtype).pin_memory()
-        S["h_lse"] = torch.empty(S["lse"].shape, dtype=S["lse"].dtype).pin_memory()
         sets.append(S)
-    d2h = sum(sets[0][n].numel() * sets[0][n].element_size() for n in ("h_out", "h_lse"))
+    d2h = out_bytes
 
     def h2d_copies(S):
-        S["q"].copy_(h_q, non_blocking=True)
-        S["k_new"].copy_(h_k, non_blocking=True)
-        S["v_new"].copy_(h_v, non_blocking=True)
-        for n, h in zip(meta, h_meta):
-            S[n].copy_(h, non_blocking=True)
+        S["in"].copy_(h_in, non_blocking=True)
 
     def kernels(S):
         pcp.compute_out_cache_loc(S["qo_indptr"], S["kv_indptr"], S["kv_indices"],
@@ -472,8 +490,7 @@ def end_to_end(args, torch, pcp, batch, d, out_ref, flush, stream, flops, world)
                               dev_err=err, qo_indptr_host=batch.qo_indptr)
 
     def d2h_copies(S):
-        S["h_out"].copy_(S["out"], non_blocking=True)
-        S["h_lse"].copy_(S["lse"], non_blocking=True)
+        S["h_res"].copy_(S["res"], non_blocking=True)
 
     s_in, s_back = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
