@@ -27,18 +27,6 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Named barrier `id` over `count` threads (a multiple of 32) that also ANDs
-// `pred` across them: every participant gets the same answer.
-__device__ __forceinline__ bool wg_barrier_all(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
-        "barrier.cta.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
 
 // ------------------------------------------- programmatic dependent launch
 // Every kernel of the library is launched as a programmatic dependent of the
@@ -154,18 +142,11 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
 
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 // Order this thread's generic-proxy view of shared memory before later
 // async-proxy accesses (tensor-core operand reads).
@@ -301,12 +282,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};"
-        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
-        : "memory");
-}
 
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -346,53 +321,13 @@ __device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
-__device__ __forceinline__ uint64_t sub_f2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
 
-// exp2_poly on a packed pair: the same reduction and polynomial, with the
-// fp32 steps as packed instructions and 2^n inserted by one integer
-// multiply-add per element (t's low mantissa bits hold n; the bias of the
-// shifter constant vanishes when shifted by 23).
-__device__ __forceinline__ uint64_t exp2_poly_f2(uint64_t x) {
-    const float x0 = fmaxf(f2_lo(x), -125.0f), x1 = fmaxf(f2_hi(x), -125.0f);
-    const uint64_t xc = f2(x0, x1);
-    const uint64_t magic = f2(12582912.0f, 12582912.0f);
-    const uint64_t t = add_f2(xc, magic);
-    const uint64_t n = sub_f2(t, magic);
-    const uint64_t f = sub_f2(xc, n);
-    uint64_t p = fma_f2(f2(0.0551716685f, 0.0551716685f), f, f2(0.2426111251f, 0.2426111251f));
-    p = fma_f2(p, f, f2(0.6932609677f, 0.6932609677f));
-    p = fma_f2(p, f, f2(0.9999280572f, 0.9999280572f));
-    const uint32_t r0 = __float_as_uint(f2_lo(t)) * 8388608u + __float_as_uint(f2_lo(p));
-    const uint32_t r1 = __float_as_uint(f2_hi(t)) * 8388608u + __float_as_uint(f2_hi(p));
-    return f2(__uint_as_float(r0), __uint_as_float(r1));
-}
 
-// 2^x on the FMA pipe, for use beside the MUFU ex2 when the latter is the
-// bottleneck.  Cody-Waite reduction x = n + f with n = round(x) (by the
-// 1.5 * 2^23 shifter) and |f| <= 1/2, then a degree-3 polynomial for 2^f whose
-// coefficients are a relative-error minimax (Remez) fit on [-1/2, 1/2]
-// (max relative error 7.5e-5), and 2^n added into the exponent field.
-// x is clamped to >= -125 so the result stays a normal number; inputs below
-// that (masked keys, x = -inf) give about 2^-125 instead of 0.
-__device__ __forceinline__ float exp2_poly(float x) {
-    x = fmaxf(x, -125.0f);
-    const float t = x + 12582912.0f;
-    const float n = t - 12582912.0f;
-    const float f = x - n;
-    const float p = fmaf(fmaf(fmaf(0.0551716685f, f, 0.2426111251f), f, 0.6932609677f), f,
-                         0.9999280572f);
-    const uint32_t ni = (uint32_t)(__float_as_int(t) - 0x4B400000);
-    return __uint_as_float(__float_as_uint(p) + (ni << 23));
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -34,17 +34,9 @@
 #include "pcp_internal.h"
 #include "pcp_launch.h"
 
-// Of every 16 consecutive pairs of S columns, this many are exponentiated on
-// the FMA pipe (exp2_poly) and the rest on the MUFU unit, balancing the two.
-#ifndef PCP_EXP2_EMU_PAIRS
-#define PCP_EXP2_EMU_PAIRS 0
-#endif
-
 namespace pcp {
 
 namespace {
-
-constexpr int kExp2EmuPairs = PCP_EXP2_EMU_PAIRS;
 
 template <int D>
 struct TcCfg {
@@ -677,8 +669,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     const float nref = m_run == -INFINITY ? 0.f : -m_run * sl2;
                     // P = exp2(s * scale * log2e - m): packed scale-and-subtract, MUFU
-                    // ex2 for most pairs and the FMA-pipe polynomial for a few, packed
-                    // row sums, bf16 pairs (P column c holds keys 2c, 2c+1)
+                    // ex2 (MUFU), packed row sums, bf16 pairs (P column c holds keys
+                    // 2c, 2c+1)
                     const uint64_t sl2x2 = f2(sl2, sl2), nref2 = f2(nref, nref);
                     uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
                     uint32_t pk[64];
@@ -687,12 +679,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const uint64_t x = fma_f2(f2(__uint_as_float(v[2 * c]),
                                                      __uint_as_float(v[2 * c + 1])),
                                                   sl2x2, nref2);
-                        uint64_t e;
-                        if ((c & 15) < kExp2EmuPairs) {
-                            e = exp2_poly_f2(x);
-                        } else {
-                            e = f2(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
-                        }
+                        const uint64_t e = f2(fast_exp2(f2_lo(x)), fast_exp2(f2_hi(x)));
                         acc2[c & 3] = add_f2(acc2[c & 3], e);
                         pk[c] = pack_bf16x2(f2_lo(e), f2_hi(e));
                         // P goes to TMEM in 16-column pieces while the rest is computed
