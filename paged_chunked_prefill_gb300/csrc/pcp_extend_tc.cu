@@ -632,17 +632,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_ld128(tS, v);
                     tmem_ld_wait();
                     if (need_mask) {
-                        // keys this row does not see become -inf
+                        // keys this row does not see become -inf: tile columns
+                        // [lo, hi) are visible
+                        const int hi = kCausal ? pabs - key0 + 1 : geo.L - key0;
+                        const int lo = kCausal && p.window > 0 ? pabs - p.window + 1 - key0 : 0;
 #pragma unroll
                         for (int j = 0; j < 128; ++j) {
                             bool vis;
                             if constexpr (has_mask) {
                                 vis = (mb[j >> 5] >> (j & 31)) & 1u;
                             } else {
-                                const int key = key0 + j;
-                                vis = kCausal ? key <= pabs &&
-                                                    (p.window <= 0 || key > pabs - p.window)
-                                              : key < geo.L;
+                                vis = j < hi && j >= lo;
                             }
                             if (!vis) v[j] = __float_as_uint(-INFINITY);
                         }
