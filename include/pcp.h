@@ -32,11 +32,15 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Every call is asynchronous on that stream.
  *  - Errors the host can see return a status before anything is launched.
- *    Errors only the device can see (a page id outside the pool, a slot
- *    outside the pool, a spin-wait that ran out) are recorded in *dev_err, a
- *    caller-owned device int32 that the caller zeroes; the first error wins
- *    and the offending access is skipped (its data read as zeros, its write
- *    dropped).  No kernel traps.  Read it with pcp_read_error.
+ *    Errors only the device can see are recorded in *dev_err, a
+ *    caller-owned device int32 that the caller zeroes; the first error wins.
+ *    A page id or slot outside the pool (PCP_ERR_BAD_INDEX) skips the
+ *    offending access (its data read as zeros, its write dropped); device
+ *    metadata that contradicts itself (a chunk ending past total_q,
+ *    qo_indptr[batch] != total_q, fewer page entries than ceil(L_b /
+ *    page_size); PCP_ERR_INVALID_ARG) skips that sequence; a spin-wait that
+ *    ran out (PCP_ERR_TIMEOUT) ends the CTA after its copies have landed.
+ *    No kernel traps.  Read the word with pcp_read_error.
  *
  * Layouts
  * -------
