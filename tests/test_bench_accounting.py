@@ -1,0 +1,51 @@
+"""The benchmark's FLOP accounting: the number of visible (query, key) pairs
+per head that the effective-TFLOP/s metric counts (4 * head_dim * n_q_heads
+flops per pair: QK^T and PV, masked pairs excluded).
+
+Pinned against a brute-force count of the bottom-right causal rule (query
+row i of a chunk with prefix P sees keys j with j <= P + i, and with a window
+W also j > P + i - W), and against the pair counts of two configurations
+that follow from it in closed form: the tiny case (prefixes 0 and 37, chunks
+5 and 40: 15 + 2300 = 2315 pairs) and the mixed batch's prompt rows (one
+4097-token prompt as chunks 2048 / 2048 / 1: 2,098,176 + 6,292,480 + 4097 =
+8,394,753 pairs).
+"""
+import numpy as np
+import pytest
+
+import bench
+import workloads as W
+
+
+def brute_pairs(prefix_lens, chunk_lens, window):
+    n = 0
+    for P, c in zip(prefix_lens, chunk_lens):
+        for i in range(c):
+            p = P + i
+            for j in range(p + 1):
+                if window <= 0 or j > p - window:
+                    n += 1
+    return n
+
+
+def test_tiny_case_pairs():
+    assert bench.visible_pairs([0, 37], [5, 40], 0) == 2315
+
+
+def test_mixed_prompt_rows_pairs():
+    assert bench.visible_pairs([0, 2048, 4096], [2048, 2048, 1], 0) == 8_394_753
+
+
+@pytest.mark.parametrize("window", [0, 1, 7, 64])
+def test_visible_pairs_matches_brute_force(window):
+    rng = np.random.default_rng(window)
+    P = rng.integers(0, 150, size=9).tolist()
+    C = rng.integers(0, 40, size=9).tolist()
+    assert bench.visible_pairs(P, C, window) == brute_pairs(P, C, window)
+
+
+def test_row_samples_sum_to_the_whole():
+    b = W.make_batch([0, 37, 300, 5], [5, 40, 1, 64], 4, 2, 64, 16, seed=7, window=100)
+    tok = np.arange(b.total_q)
+    assert bench.rows_pairs(b, tok, np.zeros_like(tok)) == \
+        bench.visible_pairs(b.prefix_lens, b.chunk_lens, b.window)
