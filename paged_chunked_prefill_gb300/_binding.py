@@ -367,6 +367,9 @@ class Pager:
         if not self._h:
             raise ValueError("pcp_pager_create: bad arguments")
         self.page_size = int(page_size)
+        self._bufs = None
+        self._nrows, self._ncp = ctypes.c_int32(0), ctypes.c_int32(0)
+        self._nrows_ref, self._ncp_ref = ctypes.byref(self._nrows), ctypes.byref(self._ncp)
 
     def close(self) -> None:
         if self._h:
@@ -431,28 +434,32 @@ class Pager:
         n = int(ids.shape[0])
         if tot.shape != (n,) or comp.shape != (n,):
             raise ValueError("req_ids, total_lens and num_computed must have one entry each")
-        cap = int(lib().pcp_pager_num_held(self._h)) + self.num_free() + 1
-        nrows = ctypes.c_int32(0)
-        row_req = np.empty(n + 1, np.int32)
-        qo = np.empty(n + 1, np.int32)
-        pre = np.empty(n + 1, np.int32)
-        kvp = np.empty(n + 1, np.int32)
-        kvi = np.empty(cap, np.int32)
-        smp = np.empty(n + 1, np.uint8)
-        ncp = ctypes.c_int32(0)
-        csrc = np.empty(n + 1, np.int32)
-        cdst = np.empty(n + 1, np.int32)
-        cslots = np.empty(n + 1, np.int32)
-        ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
-        _check(lib().pcp_schedule_step(self._h, n, ptr(ids), ptr(tot), ptr(comp), int(budget),
-                                       int(state_block), ctypes.byref(nrows), ptr(row_req),
-                                       ptr(qo), ptr(pre), ptr(kvp), ptr(kvi), cap, ptr(smp),
-                                       ctypes.byref(ncp), ptr(csrc), ptr(cdst), ptr(cslots)),
+        L = lib()
+        cap = int(L.pcp_pager_num_held(self._h)) + int(L.pcp_pager_num_free(self._h)) + 1
+        # output buffers are kept between steps and grown when too small; the
+        # results handed back are copies
+        b = self._bufs
+        if b is None or b["n"] < n + 1 or b["cap"] < cap:
+            m = max(n + 1, 2 * b["n"] if b else 0)
+            k = max(cap, 2 * b["cap"] if b else 0)
+            b = self._bufs = {"n": m, "cap": k, "kvi": np.empty(k, np.int32),
+                              "smp": np.empty(m, np.uint8),
+                              **{x: np.empty(m, np.int32) for x in (
+                                  "row_req", "qo", "pre", "kvp", "csrc", "cdst", "cslots")}}
+        kvi = b["kvi"]
+        _check(L.pcp_schedule_step(self._h, n, ids.ctypes.data, tot.ctypes.data,
+                                   comp.ctypes.data, int(budget), int(state_block),
+                                   self._nrows_ref, b["row_req"].ctypes.data, b["qo"].ctypes.data,
+                                   b["pre"].ctypes.data, b["kvp"].ctypes.data, kvi.ctypes.data,
+                                   int(b["cap"]), b["smp"].ctypes.data, self._ncp_ref,
+                                   b["csrc"].ctypes.data, b["cdst"].ctypes.data,
+                                   b["cslots"].ctypes.data),
                "pcp_schedule_step")
-        r = int(nrows.value)
-        c = int(ncp.value)
-        return {"row_req": row_req[:r].copy(), "qo_indptr": qo[:r + 1].copy(),
-                "prefix_lens": pre[:r].copy(), "kv_indptr": kvp[:r + 1].copy(),
-                "kv_indices": kvi[:int(kvp[r])].copy(), "sample": smp[:r].astype(bool),
-                "copy_src": csrc[:c].copy(), "copy_dst": cdst[:c].copy(),
-                "copy_slots": cslots[:c].copy()}
+        r = int(self._nrows.value)
+        c = int(self._ncp.value)
+        kvp = b["kvp"]
+        return {"row_req": b["row_req"][:r].copy(), "qo_indptr": b["qo"][:r + 1].copy(),
+                "prefix_lens": b["pre"][:r].copy(), "kv_indptr": kvp[:r + 1].copy(),
+                "kv_indices": kvi[:int(kvp[r])].copy(), "sample": b["smp"][:r].astype(bool),
+                "copy_src": b["csrc"][:c].copy(), "copy_dst": b["cdst"][:c].copy(),
+                "copy_slots": b["cslots"][:c].copy()}
