@@ -236,18 +236,26 @@ pcp_status pcp_schedule_step(pcp_pager* p, int n_reqs, const int64_t* req_ids,
                        row_req == nullptr || qo_indptr == nullptr || prefix_lens == nullptr ||
                        kv_indptr == nullptr || sample == nullptr))
         return PCP_ERR_INVALID_ARG;
+    // each request's page list, looked up once (null: it holds no pages yet;
+    // the map keeps element addresses stable while others are inserted)
+    std::vector<std::vector<int32_t>*> held_pages(n_reqs, nullptr);
     {
-        std::set<int64_t> seen;
+        std::vector<int64_t> ids(req_ids, req_ids + n_reqs);
+        std::sort(ids.begin(), ids.end());
+        if (std::adjacent_find(ids.begin(), ids.end()) != ids.end()) return PCP_ERR_INVALID_ARG;
         for (int r = 0; r < n_reqs; ++r) {
-            if (total_lens[r] < 0 || num_computed[r] < 0 || num_computed[r] > total_lens[r] ||
-                !seen.insert(req_ids[r]).second)
+            if (total_lens[r] < 0 || num_computed[r] < 0 || num_computed[r] > total_lens[r])
                 return PCP_ERR_INVALID_ARG;
-            // the pages a request holds must cover its computed tokens
             auto it = p->req_pages.find(req_ids[r]);
-            const int64_t held = it == p->req_pages.end() ? 0 : (int64_t)it->second.size();
+            if (it != p->req_pages.end()) held_pages[r] = &it->second;
+            // the pages a request holds must cover its computed tokens
+            const int64_t held = held_pages[r] ? (int64_t)held_pages[r]->size() : 0;
             if (held < pages_for(num_computed[r], p->page_size)) return PCP_ERR_INVALID_ARG;
         }
     }
+    auto n_held = [&](int r) -> int64_t {
+        return held_pages[r] ? (int64_t)held_pages[r]->size() : 0;
+    };
     // ---- choose the chunk of every request
     std::vector<int32_t> chunk(n_reqs, 0);
     int64_t left = budget;
@@ -257,15 +265,12 @@ pcp_status pcp_schedule_step(pcp_pager* p, int n_reqs, const int64_t* req_ids,
     auto needs_copy = [&](int r) {
         const int64_t start = num_computed[r];
         if (start % p->page_size == 0) return false;
-        auto it = p->req_pages.find(req_ids[r]);
         const int64_t idx = start / p->page_size;
-        return it != p->req_pages.end() && idx < (int64_t)it->second.size() &&
-               p->refs[it->second[idx]] > 1;
+        return idx < n_held(r) && p->refs[(*held_pages[r])[idx]] > 1;
     };
     auto grant = [&](int r, int64_t want) {
         const int64_t start = num_computed[r];
-        auto it = p->req_pages.find(req_ids[r]);
-        const int64_t held = it == p->req_pages.end() ? 0 : (int64_t)it->second.size();
+        const int64_t held = n_held(r);
         int64_t avail = free_pages;
         if (needs_copy(r)) {
             if (avail == 0) return;  // no page to copy the shared one into
@@ -300,9 +305,7 @@ pcp_status pcp_schedule_step(pcp_pager* p, int n_reqs, const int64_t* req_ids,
     for (int r = 0; r < n_reqs; ++r) {
         if (chunk[r] == 0) continue;
         const int64_t end = (int64_t)num_computed[r] + chunk[r];
-        auto it = p->req_pages.find(req_ids[r]);
-        const int64_t held = it == p->req_pages.end() ? 0 : (int64_t)it->second.size();
-        entries += std::max<int64_t>(held, pages_for(end, p->page_size));  // the row's page list
+        entries += std::max<int64_t>(n_held(r), pages_for(end, p->page_size));  // the row's page list
         ++rows;
     }
     if (kv_indices_cap < entries || (entries > 0 && kv_indices == nullptr))
@@ -315,7 +318,8 @@ pcp_status pcp_schedule_step(pcp_pager* p, int n_reqs, const int64_t* req_ids,
     for (int r = 0; r < n_reqs; ++r) {
         if (chunk[r] == 0) continue;
         const bool copy = needs_copy(r);
-        std::vector<int32_t>& pages = p->req_pages[req_ids[r]];
+        if (held_pages[r] == nullptr) held_pages[r] = &p->req_pages[req_ids[r]];
+        std::vector<int32_t>& pages = *held_pages[r];
         const int64_t end = (int64_t)num_computed[r] + chunk[r];
         if (copy) {  // copy-on-write of the shared page the chunk continues in
             const int64_t idx = num_computed[r] / p->page_size;
