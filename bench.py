@@ -691,21 +691,21 @@ def planner_secondary(pcp, n_decode=240, n_prompt=16, steps=200):
     2000-token prompts, token budget 8192, page size 16."""
     rng = np.random.default_rng(11)
     pg = pcp.Pager(200_000, 16)
-    ids = list(range(n_decode + n_prompt))
-    total = [int(x) for x in rng.integers(100, 4000, size=n_decode)] + [2000] * n_prompt
-    comp = [t - 1 for t in total[:n_decode]] + [0] * n_prompt
+    # the loop's state lives in int arrays, as a serving loop keeps it
+    ids = np.arange(n_decode + n_prompt, dtype=np.int64)
+    total = np.concatenate([rng.integers(100, 4000, size=n_decode),
+                            np.full(n_prompt, 2000)]).astype(np.int32)
+    comp = np.concatenate([total[:n_decode] - 1, np.zeros(n_prompt, np.int32)]).astype(np.int32)
     # the decoding requests already hold their pages
-    pg.schedule_step(ids[:n_decode], total[:n_decode], [0] * n_decode, 1 << 30)
+    pg.schedule_step(ids[:n_decode], total[:n_decode], np.zeros(n_decode, np.int32), 1 << 30)
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
         st = pg.schedule_step(ids, total, comp, 8192)
         times.append(time.perf_counter() - t0)
-        qo = st["qo_indptr"]
-        for n, r in enumerate(st["row_req"]):
-            comp[r] += int(qo[n + 1] - qo[n])
-            if st["sample"][n]:
-                total[r] += 1
+        rows = st["row_req"]
+        comp[rows] += np.diff(st["qo_indptr"]).astype(np.int32)
+        total[rows[st["sample"]]] += 1
     return {"workload": f"{n_decode} decoding + {n_prompt} prefilling requests, budget 8192, "
                         f"page size 16", "us_per_step": float(np.median(times) * 1e6),
             "what": "host time of pcp_schedule_step through the Python binding (median)"}
