@@ -58,10 +58,10 @@ def rows_pairs(batch, tok, head) -> int:
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
-# the dominant kernel, from an ncu capture of this bench on the named workload
-# (profiles/extend_tc_gqa_prefill_ncu.md, profiles/row_attn_decode_rows_ncu.md).  It is reported only while the
-# library sources hash to the value the capture ran with; after any change
-# the key reads null until the counters are taken again.
+# the dominant kernel, from an ncu capture of this bench on the named workload.
+# It is reported only while the library sources hash to the value the capture
+# ran with; after any change the key reads null until the counters are taken
+# again.
 NCU_TRAFFIC = {
     ("gqa_prefill", "extend_tc_kernel<128>"): {
         "bytes": 203.634176e6 + 17.143808e6,
@@ -98,6 +98,47 @@ def ncu_traffic(workload: str, kernel: str):
     if rec is None or rec["csrc_sha256"] != csrc_sha256():
         return None
     return rec["bytes"]
+
+
+def to_device(batch, dev):
+    """The workload's arrays as device tensors (bf16 bit patterns and int32)."""
+    import torch
+    t16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    nonempty = lambda a: a if len(a) else np.zeros(1, np.int32)
+    return dict(q=t16(batch.q), k_new=t16(batch.k_new), v_new=t16(batch.v_new),
+                k_pool=t16(batch.k_pool), v_pool=t16(batch.v_pool),
+                qo_indptr=i32(batch.qo_indptr), kv_indptr=i32(batch.kv_indptr),
+                kv_indices=i32(nonempty(batch.kv_indices)),
+                prefix_lens=i32(nonempty(batch.prefix_lens)))
+
+
+def row_max_chunk(batch) -> int:
+    """Longest chunk the split-KV row kernel takes (decode-shaped rows)."""
+    G = batch.n_q_heads // batch.n_kv_heads
+    return 16 // G if G <= 16 else 0
+
+
+def split_work(batch):
+    """(visible pairs per head of the chunks the tensor-core kernel takes,
+    algorithmic bytes of the decode-shaped rows the row kernel takes: the K/V
+    of every visible key once per KV head, q, out, lse and page ids)."""
+    c = batch.chunk_lens.astype(np.int64)
+    P = batch.prefix_lens.astype(np.int64)
+    rmax = row_max_chunk(batch)
+    tc = c > rmax
+    tc_pairs = visible_pairs(P[tc], c[tc], batch.window)
+    rows = (c > 0) & ~tc
+    D, Hkv, Hq = batch.head_dim, batch.n_kv_heads, batch.n_q_heads
+    first = np.maximum(0, P[rows] - batch.window + 1) if batch.window > 0 else 0 * P[rows]
+    keys = (P[rows] + c[rows] - first).sum()
+    pages = 0
+    for b in np.nonzero(rows)[0]:
+        pages += -(-(int(P[b] + c[b])) // batch.page_size)
+    n_rows = int(c[rows].sum())
+    row_bytes = int(keys) * Hkv * D * 2 * 2 + n_rows * Hq * (D * 2 * 2 + 4) + 4 * pages
+    return tc_pairs, row_bytes
 
 
 def launches_per_step(batch) -> int:
@@ -212,9 +253,10 @@ def dist_env():
     return world, rank, local
 
 
-def oracle_sample(batch, seconds_target: float, seed: int = 0):
+def oracle_sample(batch, seconds_target: float, seed: int = 0, detail: bool = False):
     """Time the FP64 oracle on a bounded sample of rows of `batch` (appended
-    pools).  Returns (TFLOP/s of effective work, threads, sample text)."""
+    pools).  Returns (TFLOP/s of effective work, threads, sample text), plus
+    the seconds spent and the (row, head) pairs done with detail=True."""
     import oracle
     loc = oracle.out_cache_loc(batch.qo_indptr, batch.kv_indptr, batch.kv_indices,
                                batch.prefix_lens, batch.page_size, batch.num_pages)
@@ -236,36 +278,59 @@ def oracle_sample(batch, seconds_target: float, seed: int = 0):
         done_flops += 4 * D * rows_pairs(batch, tok, head)
         rows += n
         n = min(n * 2, 4096)
-    return (done_flops / elapsed / 1e12, oracle.num_threads(),
-            f"{rows} random (row, head) pairs of the workload, {elapsed:.1f} s")
+    res = (done_flops / elapsed / 1e12, oracle.num_threads(),
+           f"{rows} random (row, head) pairs of the workload, {elapsed:.1f} s")
+    return res + (elapsed, rows) if detail else res
+
+
+def config_dict(batch, world: int) -> dict:
+    """The workload description both arms print."""
+    return {"workload": batch.name, "global_batch": batch.batch * world,
+            "tokens_per_step": batch.total_q * world,
+            "visible_pairs_per_head": visible_pairs(batch.prefix_lens, batch.chunk_lens,
+                                                    batch.window),
+            "l2": "flushed before every timed step: 256 MB written, then read back",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def run_reference(args):
-    """Reference arm: the FP64 oracle on the host cores, a bounded row sample
-    per step."""
+    """Reference arm: the FP64 oracle on the host cores.  Each step runs the
+    oracle on a bounded random sample of (row, head) pairs of the workload
+    (about 60 s of oracle time over the whole run); the value is the
+    effective TFLOP/s of that sample, ms_per_step the oracle time actually
+    spent per step, and ms_per_step_extrapolated the time a whole step of the
+    workload would take at that rate."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
     import workloads as W
-    batch = W.gqa_prefill()
+    batch = W.config_by_name(args.workload)
     per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
-    vals = []
+    vals, secs, rows = [], [], []
     for i in range(args.warmup + args.steps):
-        v, cores, sample = oracle_sample(batch, per_step, seed=i)
+        v, cores, sample, spent, n = oracle_sample(batch, per_step, seed=i, detail=True)
         if i >= args.warmup:
             vals.append(v)
+            secs.append(spent)
+            rows.append(n)
     value = float(np.mean(vals))
     flops = 4 * batch.head_dim * batch.n_q_heads * visible_pairs(
         batch.prefix_lens, batch.chunk_lens, batch.window)
+    ms = float(np.mean(secs)) * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": flops / (value * 1e12) * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": batch.name, "global_batch": batch.batch,
-                   "tokens_per_step": batch.total_q},
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms,
+        "ms_per_step_extrapolated": flops / (value * 1e12) * 1e3,
+        "ms_per_step_note": "ms_per_step is the oracle time spent per step on its sample; "
+                            "ms_per_step_extrapolated is a whole step of the workload at the "
+                            "sample's rate (extrapolated, not measured)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": config_dict(batch, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"per step: {sample}"},
+                         "sample": f"per step: {int(np.mean(rows))} random (row, head) pairs "
+                                   f"of the workload, {ms / 1e3:.2f} s of oracle time"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -299,8 +364,6 @@ def main():
     args.warmup = max(args.warmup, 3)
 
     batch = W.config_by_name(args.workload)
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from helpers import to_device
     d = to_device(batch, dev)
     flops = 4 * batch.head_dim * batch.n_q_heads * visible_pairs(
         batch.prefix_lens, batch.chunk_lens, batch.window)
@@ -313,16 +376,17 @@ def main():
     lse = torch.empty(batch.total_q, batch.n_q_heads, dtype=torch.float32, device=dev)
     flush = L2Flush(torch, dev)
 
-    def step(q=None):
+    def step(tc_events=None):
         pcp.compute_out_cache_loc(d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
                                   d["prefix_lens"], batch.page_size, batch.num_pages,
                                   total_q=batch.total_q, out=loc, dev_err=err)
         pcp.kv_append(d["k_new"], d["v_new"], loc, d["k_pool"], d["v_pool"], dev_err=err)
-        pcp.paged_extend_attn(d["q"] if q is None else q, d["qo_indptr"], d["kv_indptr"],
+        pcp.paged_extend_attn(d["q"], d["qo_indptr"], d["kv_indptr"],
                               d["kv_indices"], d["prefix_lens"], d["k_pool"], d["v_pool"],
                               batch.page_size, batch.n_q_heads, batch.n_kv_heads,
                               batch.head_dim, batch.window, batch.sm_scale, out=out, lse=lse,
-                              workspace=ws, dev_err=err, qo_indptr_host=batch.qo_indptr)
+                              workspace=ws, dev_err=err, qo_indptr_host=batch.qo_indptr,
+                              tc_events=tc_events)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -355,9 +419,7 @@ def main():
         # (they serialise its two neighbours, so they stay out of loop 1)
         for i in range(args.steps):
             flush()
-            pcp.set_timing_events(ev[i][2], ev[i][3], pcp.TIMING_TC)
-            step()
-        pcp.set_timing_events(None, None, pcp.TIMING_TC)
+            step(tc_events=(ev[i][2], ev[i][3]))
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
     tc_ms = [c.elapsed_time(e) for _, _, c, e in ev]
@@ -373,10 +435,9 @@ def main():
 
     peaks, peak_kind = load_peaks()
     tc_avg = float(np.mean(tc_ms))
-    G = batch.n_q_heads // batch.n_kv_heads
-    row_max_chunk = 16 // G if G <= 16 else 0
-    if (np.diff(batch.qo_indptr) > row_max_chunk).any():
-        achieved = flops / (tc_avg * 1e-3) / 1e12
+    if (np.diff(batch.qo_indptr) > row_max_chunk(batch)).any():
+        tc_flops = 4 * batch.head_dim * batch.n_q_heads * split_work(batch)[0]
+        achieved = tc_flops / (tc_avg * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                     "unit": UNIT, "frac": achieved / peaks["bf16_tflops"],
                     "traffic": ncu_traffic(args.workload, f"extend_tc_kernel<{batch.head_dim}>"),
@@ -394,12 +455,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": batch.name, "global_batch": batch.batch * world,
-                   "tokens_per_step": batch.total_q * world,
-                   "visible_pairs_per_head": visible_pairs(batch.prefix_lens, batch.chunk_lens,
-                                                           batch.window),
-                   "l2": "flushed before every timed step: 256 MB written, then read back",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": config_dict(batch, world),
         "roofline": roofline,
         "e2e": e2e,
         # out_cache_loc, kv_append, plan, then the tensor-core kernel and/or the
@@ -564,122 +620,108 @@ def end_to_end(args, torch, pcp, batch, d, out_ref, flush, stream, flops, world)
             "alone_ms_per_step": alone_ms}
 
 
-def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
-    """Decode-row KV bandwidth (the 31 decode rows of the mixed batch as a
-    decode-only call) and KV-append bandwidth, L2 flushed before each call."""
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from helpers import to_device
-    res = {}
-    db = W.decode_rows()
-    d = to_device(db, dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
+def attn_figures(pcp, torch, batch, dev, peaks, flush, err, n=20, warm=5, causal=True,
+                 mask=None, pairs=None):
+    """One attention call on `batch` (its chunk's K/V appended first), L2
+    flushed before each timed call: the whole call, and the tensor-core and
+    row kernels alone between per-call events.  Effective FLOPs count the
+    visible pairs only (`pairs` per head when a mask hides more keys)."""
+    d = to_device(batch, dev)
+    loc = pcp.compute_out_cache_loc(d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                                    d["prefix_lens"], batch.page_size, batch.num_pages)
+    pcp.kv_append(d["k_new"], d["v_new"], loc, d["k_pool"], d["v_pool"], dev_err=err)
     out = torch.empty_like(d["q"])
-    lse = torch.empty(db.total_q, db.n_q_heads, dtype=torch.float32, device=dev)
-    ws = torch.empty(pcp.workspace_size(db.batch, db.total_q, db.n_q_heads, db.n_kv_heads,
-                                        db.head_dim), dtype=torch.uint8, device=dev)
+    lse = torch.empty(batch.total_q, batch.n_q_heads, dtype=torch.float32, device=dev)
+    ws = torch.empty(pcp.workspace_size(batch.batch, batch.total_q, batch.n_q_heads,
+                                        batch.n_kv_heads, batch.head_dim),
+                     dtype=torch.uint8, device=dev)
+    mask_t = None if mask is None else torch.from_numpy(mask).to(dev)
 
-    def dec():
+    def call(tc_ev=None, row_ev=None):
         pcp.paged_extend_attn(d["q"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
-                              d["prefix_lens"], d["k_pool"], d["v_pool"], db.page_size,
-                              db.n_q_heads, db.n_kv_heads, db.head_dim, 0, 0.0, out=out,
-                              lse=lse, workspace=ws, dev_err=err, qo_indptr_host=db.qo_indptr)
-    ms = time_calls(torch, dec, flush)
-    kv_bytes = int(db.kv_lens.sum()) * db.n_kv_heads * db.head_dim * 2 * 2
-    io_bytes = (d["q"].numel() * 2 + out.numel() * 2 + lse.numel() * 4 +
-                int(db.kv_indptr[-1]) * 4)
-    nbytes = kv_bytes + io_bytes
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    # the row kernel alone, between CUDA events on the launching stream
-    kms = time_calls(torch, dec, flush, kernel=pcp.TIMING_ROWS, pcp=pcp)
-    kgbs = nbytes / (kms * 1e-3) / 1e9
-    res["decode_rows"] = {"workload": db.name, "ms": ms, "GB/s": gbs,
+                              d["prefix_lens"], d["k_pool"], d["v_pool"], batch.page_size,
+                              batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.window,
+                              batch.sm_scale, out=out, lse=lse, workspace=ws, dev_err=err,
+                              qo_indptr_host=batch.qo_indptr, causal=causal, mask=mask_t,
+                              tc_events=tc_ev, rows_events=row_ev)
+    tc_pairs, row_bytes = split_work(batch)
+    all_pairs = visible_pairs(batch.prefix_lens, batch.chunk_lens, batch.window)
+    if pairs is not None:  # a mask or non-causal call: all its work is on the tensor cores
+        all_pairs = tc_pairs = pairs
+    D, Hq = batch.head_dim, batch.n_q_heads
+    ms = time_calls(torch, lambda ev: call(), flush, n=n, warm=warm)
+    r = {"workload": batch.name, "ms": ms,
+         "TFLOP/s": 4 * D * Hq * all_pairs / (ms * 1e-3) / 1e12,
+         "what": "whole call (planner, kernels, combine), effective FLOPs of visible pairs"}
+    r["frac_bf16"] = r["TFLOP/s"] / peaks["bf16_tflops"]
+    if tc_pairs > 0:
+        kms = time_calls(torch, lambda ev: call(tc_ev=ev), flush, n=n, warm=warm, events=True)
+        tf = 4 * D * Hq * tc_pairs / (kms * 1e-3) / 1e12
+        r["tc_kernel"] = {"bound": "tensor", "kernel": f"extend_tc_kernel<{D}>",
+                          "kernel_ms": kms, "achieved": tf, "peak": peaks["bf16_tflops"],
+                          "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                          "visible_pairs_per_head": int(tc_pairs)}
+    if row_bytes > 0 and pairs is None:
+        kms = time_calls(torch, lambda ev: call(row_ev=ev), flush, n=n, warm=warm, events=True)
+        gbs = row_bytes / (kms * 1e-3) / 1e9
+        r["row_kernel"] = {"bound": "hbm", "kernel": f"row_attn_kernel<{D}>", "kernel_ms": kms,
+                           "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": gbs / peaks["hbm_gbs"], "bytes": int(row_bytes)}
+    return r
+
+
+def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
+    """Per-kernel figures on every workload the benchmark does not time as
+    its headline, L2 flushed before each call."""
+    res = {"peak_source": f"{peak_kind} (MEASURED_PEAKS.json when present): bf16 dense "
+                          f"burst {peaks['bf16_tflops']} TFLOP/s, HBM copy {peaks['hbm_gbs']} GB/s"}
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    # decode rows: the 31 decode rows of the mixed batch as a decode-only call
+    db = W.decode_rows()
+    r = attn_figures(pcp, torch, db, dev, peaks, flush, err)
+    _, nbytes = split_work(db)
+    gbs = nbytes / (r["ms"] * 1e-3) / 1e9
+    res["decode_rows"] = {"workload": db.name, "ms": r["ms"], "GB/s": gbs,
                           "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes,
-                          "peak_source": f"{peak_kind} HBM copy",
                           "what": "whole call: planner, row kernel, split-KV combine"}
-    res["decode_rows_kernel"] = {"bound": "hbm", "kernel": f"row_attn_kernel<{db.head_dim}>",
-                                 "kernel_ms": kms, "achieved": kgbs, "peak": peaks["hbm_gbs"],
-                                 "unit": "GB/s", "frac": kgbs / peaks["hbm_gbs"],
-                                 "traffic": ncu_traffic("decode_rows",
-                                                        f"row_attn_kernel<{db.head_dim}>")}
-    gb = W.gqa_prefill()
-    g = to_device(gb, dev)
-    loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
-                                    g["prefix_lens"], gb.page_size, gb.num_pages)
+    res["decode_rows_kernel"] = dict(r["row_kernel"],
+                                     traffic=ncu_traffic("decode_rows",
+                                                         f"row_attn_kernel<{db.head_dim}>"))
 
-    def app():
-        pcp.kv_append(g["k_new"], g["v_new"], loc, g["k_pool"], g["v_pool"], dev_err=err)
-    ms = time_calls(torch, app, flush)
-    nbytes = 2 * 2 * gb.total_q * gb.n_kv_heads * gb.head_dim * 2 + 8 * gb.total_q
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    res["kv_append"] = {"workload": f"{gb.total_q} tokens x {gb.n_kv_heads} KV heads x D "
-                                    f"{gb.head_dim}", "ms": ms, "GB/s": gbs,
-                        "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes}
-    del g, loc
+    # the KV append of the GQA chunk (4096 tokens) and of the long-context chunk
+    for key, b in (("kv_append", W.gqa_prefill()), ("kv_append_long", W.long_context())):
+        g = to_device(b, dev)
+        loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
+                                        g["prefix_lens"], b.page_size, b.num_pages)
+        ms = time_calls(torch, lambda ev: pcp.kv_append(g["k_new"], g["v_new"], loc,
+                                                        g["k_pool"], g["v_pool"], dev_err=err),
+                        flush)
+        nbytes = 2 * 2 * b.total_q * b.n_kv_heads * b.head_dim * 2 + 8 * b.total_q
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[key] = {"workload": f"{b.total_q} tokens x {b.n_kv_heads} KV heads x D "
+                                f"{b.head_dim}", "ms": ms, "GB/s": gbs,
+                    "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes}
+        del g, loc
 
-    # the long-context batch: its 32768-token append and its attention call
-    lb = W.long_context()
-    g = to_device(lb, dev)
-    loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
-                                    g["prefix_lens"], lb.page_size, lb.num_pages)
+    # the long-context batch, the mixed scheduler batch (prompt chunks on the
+    # tensor cores beside decode rows in one call), the GQA workload over the
+    # flat one-slot-per-token pool (page size 1), and the page-boundary and
+    # window stress batches
+    res["long_context_attn"] = attn_figures(pcp, torch, W.long_context(), dev, peaks, flush,
+                                            err, n=5, warm=2)
+    res["mixed_attn"] = attn_figures(pcp, torch, W.mixed_batch(), dev, peaks, flush, err)
+    res["gqa_prefill_ps1"] = attn_figures(pcp, torch, W.gqa_prefill(page_size=1), dev, peaks,
+                                          flush, err, n=10, warm=3)
+    for name in ("stress_ps1_w4096", "stress_ps1_w0", "stress_ps16_w4096", "stress_ps16_w0"):
+        res[name] = attn_figures(pcp, torch, W.config_by_name(name), dev, peaks, flush, err,
+                                 n=10, warm=3)
 
-    def app_long():
-        pcp.kv_append(g["k_new"], g["v_new"], loc, g["k_pool"], g["v_pool"], dev_err=err)
-    ms = time_calls(torch, app_long, flush)
-    nbytes = 2 * 2 * lb.total_q * lb.n_kv_heads * lb.head_dim * 2 + 8 * lb.total_q
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    res["kv_append_long"] = {"workload": f"{lb.total_q} tokens x {lb.n_kv_heads} KV heads x D "
-                                         f"{lb.head_dim}", "ms": ms, "GB/s": gbs,
-                             "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes}
-    lout = torch.empty_like(g["q"])
-    llse = torch.empty(lb.total_q, lb.n_q_heads, dtype=torch.float32, device=dev)
-    lws = torch.empty(pcp.workspace_size(lb.batch, lb.total_q, lb.n_q_heads, lb.n_kv_heads,
-                                         lb.head_dim), dtype=torch.uint8, device=dev)
-
-    def attn_long():
-        pcp.paged_extend_attn(g["q"], g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
-                              g["prefix_lens"], g["k_pool"], g["v_pool"], lb.page_size,
-                              lb.n_q_heads, lb.n_kv_heads, lb.head_dim, lb.window, lb.sm_scale,
-                              out=lout, lse=llse, workspace=lws, dev_err=err,
-                              qo_indptr_host=lb.qo_indptr)
-    ms = time_calls(torch, attn_long, flush, n=5, warm=2)
-    lflops = 4 * lb.head_dim * lb.n_q_heads * visible_pairs(lb.prefix_lens, lb.chunk_lens,
-                                                            lb.window)
-    tf = lflops / (ms * 1e-3) / 1e12
-    res["long_context_attn"] = {"workload": lb.name, "ms": ms, "TFLOP/s": tf,
-                                "frac_bf16": tf / peaks["bf16_tflops"]}
-    del g, loc, lout, llse, lws
-
-    # non-causal attention and a 2-D key mask (keep 1/2) on the GQA workload:
-    # effective FLOPs count the visible pairs only
+    # non-causal attention and a 2-D key mask (keep 1/2) on the GQA workload
     res.update(masked_secondary(pcp, torch, W, dev, peaks, flush, err))
 
     res["chunk_planner"] = planner_secondary(pcp)
     res["cow_page_copy"] = cow_secondary(pcp, torch, dev, peaks, flush)
-
-    # the mixed scheduler batch: prompt chunks (tensor cores) and decode rows
-    # (row kernel) in one call
-    mb = W.mixed_batch()
-    g = to_device(mb, dev)
-    loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
-                                    g["prefix_lens"], mb.page_size, mb.num_pages)
-    pcp.kv_append(g["k_new"], g["v_new"], loc, g["k_pool"], g["v_pool"], dev_err=err)
-    mout = torch.empty_like(g["q"])
-    mlse = torch.empty(mb.total_q, mb.n_q_heads, dtype=torch.float32, device=dev)
-    mws = torch.empty(pcp.workspace_size(mb.batch, mb.total_q, mb.n_q_heads, mb.n_kv_heads,
-                                         mb.head_dim), dtype=torch.uint8, device=dev)
-
-    def attn_mixed():
-        pcp.paged_extend_attn(g["q"], g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
-                              g["prefix_lens"], g["k_pool"], g["v_pool"], mb.page_size,
-                              mb.n_q_heads, mb.n_kv_heads, mb.head_dim, mb.window, mb.sm_scale,
-                              out=mout, lse=mlse, workspace=mws, dev_err=err,
-                              qo_indptr_host=mb.qo_indptr)
-    ms = time_calls(torch, attn_mixed, flush)
-    mflops = 4 * mb.head_dim * mb.n_q_heads * visible_pairs(mb.prefix_lens, mb.chunk_lens,
-                                                            mb.window)
-    tf = mflops / (ms * 1e-3) / 1e12
-    res["mixed_attn"] = {"workload": mb.name, "ms": ms, "TFLOP/s": tf,
-                         "frac_bf16": tf / peaks["bf16_tflops"]}
     if pcp.read_error(err) != 0:
         raise RuntimeError("device error in secondary measurements")
     return res
@@ -721,8 +763,8 @@ def cow_secondary(pcp, torch, dev, peaks, flush, n_copies=2048, page_size=16, hk
     perm = torch.randperm(num_pages, device=dev, generator=g).to(torch.int32)
     src, dst = perm[:n_copies].contiguous(), perm[n_copies:2 * n_copies].contiguous()
     nsl = torch.full((n_copies,), page_size, dtype=torch.int32, device=dev)
-    ms = time_calls(torch, lambda: pcp.copy_page_slots(kp, vp, page_size, src, dst, nsl,
-                                                        check=False), flush)
+    ms = time_calls(torch, lambda ev: pcp.copy_page_slots(kp, vp, page_size, src, dst, nsl,
+                                                           check=False), flush)
     nbytes = 2 * 2 * n_copies * page_size * hkv * d * 2
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": f"{n_copies} whole pages of {page_size} slots x {hkv} KV heads x D {d}",
@@ -730,70 +772,46 @@ def cow_secondary(pcp, torch, dev, peaks, flush, n_copies=2048, page_size=16, hk
 
 
 def masked_secondary(pcp, torch, W, dev, peaks, flush, err):
-    """Non-causal and 2-D-masked calls on the GQA chunked-prefill workload."""
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from helpers import to_device
+    """Non-causal and 2-D-masked calls on the GQA chunked-prefill workload;
+    effective FLOPs count the visible pairs only."""
     gb = W.gqa_prefill()
-    g = to_device(gb, dev)
-    loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
-                                    g["prefix_lens"], gb.page_size, gb.num_pages)
-    pcp.kv_append(g["k_new"], g["v_new"], loc, g["k_pool"], g["v_pool"], dev_err=err)
-    out = torch.empty_like(g["q"])
-    lse = torch.empty(gb.total_q, gb.n_q_heads, dtype=torch.float32, device=dev)
-    ws = torch.empty(pcp.workspace_size(gb.batch, gb.total_q, gb.n_q_heads, gb.n_kv_heads,
-                                        gb.head_dim), dtype=torch.uint8, device=dev)
     mask_np = W.random_mask(gb, "2d", seed=5, keep=0.5)
-    mask = torch.from_numpy(mask_np).to(dev)
-    res = {}
     P = gb.prefix_lens.astype(np.int64)
     C = gb.chunk_lens
-    L = P + C
-    for name, causal, m in (("non_causal_attn", False, None), ("masked_2d_attn", True, mask)):
-        def call():
-            pcp.paged_extend_attn(g["q"], g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
-                                  g["prefix_lens"], g["k_pool"], g["v_pool"], gb.page_size,
-                                  gb.n_q_heads, gb.n_kv_heads, gb.head_dim, 0, gb.sm_scale,
-                                  out=out, lse=lse, workspace=ws, dev_err=err,
-                                  qo_indptr_host=gb.qo_indptr, causal=causal, mask=m)
-        ms = time_calls(torch, call, flush, n=10, warm=3)
-        if m is None:
-            pairs = int((C * L).sum())
-        else:
-            keep = np.cumsum(mask_np, axis=1)   # kept keys among 0..j
-            pairs = 0
-            for b in range(gb.batch):
-                pos = P[b] + np.arange(C[b])
-                pairs += int(keep[b, pos].sum())
-        flops = 4 * gb.head_dim * gb.n_q_heads * pairs
-        tf = flops / (ms * 1e-3) / 1e12
-        res[name] = {"workload": gb.name + (", non-causal" if m is None else
-                                            ", causal + 2-D key mask keeping 1/2"),
-                     "ms": ms, "TFLOP/s": tf, "frac_bf16": tf / peaks["bf16_tflops"],
-                     "visible_pairs_per_head": pairs}
-    return res
+    keep = np.cumsum(mask_np, axis=1)   # kept keys among 0..j
+    masked_pairs = 0
+    for b in range(gb.batch):
+        masked_pairs += int(keep[b, P[b] + np.arange(C[b])].sum())
+    nc = attn_figures(pcp, torch, gb, dev, peaks, flush, err, n=10, warm=3, causal=False,
+                      pairs=int((C * (P + C)).sum()))
+    nc["workload"] += ", non-causal"
+    mk = attn_figures(pcp, torch, gb, dev, peaks, flush, err, n=10, warm=3, mask=mask_np,
+                      pairs=masked_pairs)
+    mk["workload"] += ", causal + 2-D key mask keeping 1/2"
+    return {"non_causal_attn": nc, "masked_2d_attn": mk}
 
 
-def time_calls(torch, fn, flush, n=20, warm=5, kernel=None, pcp=None):
-    """Median ms of fn() between CUDA events, L2 flushed before each call; with
-    `kernel` (pcp.TIMING_*) the events bracket that library kernel only."""
+def time_calls(torch, fn, flush, n=20, warm=5, events=False):
+    """Median ms of fn(ev) between CUDA events, L2 flushed before each call.
+    With events=False the events bracket the whole call (fn gets None); with
+    events=True fn gets the (before, after) pair to hand to the library, which
+    records it around one kernel."""
     stream = torch.cuda.current_stream()
     for _ in range(warm):
-        fn()
+        fn(None)
     torch.cuda.synchronize()
     ms = []
     for _ in range(n):
         flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if kernel is None:
+        if not events:
             a.record(stream)
-            fn()
+            fn(None)
             b.record(stream)
         else:
             a.record(stream)  # creates the events before the library records them
             b.record(stream)
-            pcp.set_timing_events(a, b, kernel)
-            fn()
-            pcp.set_timing_events(None, None, kernel)
+            fn((a, b))
         b.synchronize()
         ms.append(a.elapsed_time(b))
     return float(np.median(ms))

@@ -6,9 +6,9 @@
  *
  *   1. pcp_compute_out_cache_loc -- where each new token of a chunk goes in
  *      the page pool, continuing inside the last partly filled page
- *      (AReno PR #642 "chunked prefill must attend to cached prefix",
- *      "What does this PR do?", third bullet; AstrAI "scalar paged prefill
- *      fallback and decode causal fix", PagePool.bind_tasks, out_cache_loc).
+ *      (AReno PR #642, "What does this PR do?", third bullet; AstrAI
+ *      compare "scalar paged prefill fallback and decode causal fix",
+ *      PagePool.bind_tasks, out_cache_loc).
  *   2. pcp_kv_append -- the scatter of the chunk's K/V into the pool
  *      (AstrAI CudaBackend.fwd_prefill, the k_buffer[layer, out_cache_loc]
  *      write).
@@ -227,17 +227,21 @@ pcp_status pcp_paged_extend_attn_masked(
  * not call cudaMalloc -- and so cannot pass a workspace.  Arguments, layouts,
  * results and errors are those of pcp_paged_extend_attn; the work lists,
  * split-KV partials and counters go to a file-scope device array of
- * PCP_NOALLOC_SCRATCH_BYTES instead.  A call whose
- * pcp_extend_workspace_size(...) exceeds that returns PCP_ERR_WORKSPACE
- * before launching anything.  Nothing is allocated: no cudaMalloc, no
- * cudaFree, no allocating library call.
+ * PCP_NOALLOC_SCRATCH_BYTES instead.  The arguments are checked first, as
+ * pcp_paged_extend_attn checks them (a bad argument returns the same
+ * status); then a call whose pcp_extend_workspace_size(...) exceeds the
+ * array returns PCP_ERR_WORKSPACE before launching anything.  Nothing is
+ * allocated: no cudaMalloc, no cudaFree, no allocating library call.
  *
  * The first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream
- * capture.  All calls on a device share the one array and it keeps the last
- * call's contents; each call re-initialises what must start at zero, but
- * calls whose GPU work overlaps (different streams, or several host threads)
- * race on the array and must be ordered by the caller.
+ * capture.  The cached address belongs to the device's primary context: after
+ * cudaDeviceReset (or any other teardown of that context) it is stale, and
+ * this entry point must not be called again in the process.  All calls on a
+ * device share the one array and it keeps the last call's contents; each call
+ * re-initialises what must start at zero, but calls whose GPU work overlaps
+ * (different streams, or several host threads) race on the array and must be
+ * ordered by the caller.
  */
 pcp_status pcp_paged_extend_attn_noalloc(const void* q, const int32_t* qo_indptr,
                                          const int32_t* kv_indptr, const int32_t* kv_indices,
@@ -388,20 +392,50 @@ pcp_status pcp_copy_page_slots(void* k_pool, void* v_pool, int64_t num_pages, in
  */
 pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_err);
 
-/* Kernels pcp_set_timing_events can bracket. */
-#define PCP_TIMING_TC 0   /* the tensor-core extend kernel */
-#define PCP_TIMING_ROWS 1 /* the split-KV row kernel (decode-shaped rows) */
+/*
+ * Per-call instrumentation, for profiling and for tests of the device-side
+ * error paths.  The pages have no counterpart.  A zeroed struct (or a NULL
+ * pointer) means: no events, the default wait limit.
+ *   tc_event_before / tc_event_after: NULL, or cudaEvent_t values (as void*)
+ *     recorded on the call's stream right before and right after the launch
+ *     of the tensor-core kernel, so the caller can time that kernel alone
+ *     (recorded even when the call has no tensor-core work).  Both or
+ *     neither.  Recording them orders the kernel after its predecessor and
+ *     its successor after it: the call loses the launch overlap it has
+ *     without events.
+ *   rows_event_before / rows_event_after: the same around the split-KV row
+ *     kernel (recorded only when the call launches it).
+ *   wait_limit_ns: 0 for the default (2 s), else the limit of every pipeline
+ *     wait of the tensor-core and row kernels (producer/consumer mbarrier
+ *     waits).  A wait that runs out records PCP_ERR_TIMEOUT in *dev_err, and
+ *     its CTA lets its in-flight copies and MMAs complete (those drain waits
+ *     keep the 2 s limit), frees its tensor memory and exits; the other
+ *     CTAs finish their work.  The results of such a call are undefined; the
+ *     device, the stream and the library stay usable.  A tiny limit (a few
+ *     ns) makes a call time out on purpose; tests use it to run that path.
+ * The library keeps nothing of it after the call returns.
+ */
+typedef struct pcp_call_options {
+    void* tc_event_before;
+    void* tc_event_after;
+    void* rows_event_before;
+    void* rows_event_after;
+    uint64_t wait_limit_ns;
+} pcp_call_options;
 
 /*
- * Profiling hook.  When both events (cudaEvent_t passed as void*) are
- * non-NULL, every later pcp_paged_extend_attn call that launches `kernel`
- * (PCP_TIMING_TC or PCP_TIMING_ROWS) records `before` on its stream right
- * before that kernel is launched and `after` right after it, so a caller can
- * time that kernel alone.  Pass NULLs to turn it off.  Process-wide; not for
- * concurrent use from several threads.  An unknown `kernel` or only one NULL
- * event returns PCP_ERR_INVALID_ARG.
+ * pcp_paged_extend_attn_masked with per-call options (NULL: none).  Events
+ * given one without the other return PCP_ERR_INVALID_ARG before anything is
+ * launched.
  */
-pcp_status pcp_set_timing_events(int kernel, void* before, void* after);
+pcp_status pcp_paged_extend_attn_ex(
+    const void* q, const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+    const int32_t* prefix_lens, const int32_t* qo_indptr_host, int batch, int64_t total_q,
+    const void* k_pool, const void* v_pool, int64_t num_pages, int page_size, int n_q_heads,
+    int n_kv_heads, int head_dim, int window, float sm_scale, int causal, const uint8_t* mask,
+    int64_t mask_b_stride, int64_t mask_h_stride, int64_t mask_q_stride, int32_t mask_q_len,
+    int32_t mask_kv_len, void* out, float* lse, void* workspace, size_t workspace_bytes,
+    int32_t* dev_err, void* stream, const pcp_call_options* options);
 
 #ifdef __cplusplus
 }

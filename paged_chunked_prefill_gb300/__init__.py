@@ -27,14 +27,10 @@ from ._binding import (  # noqa: F401
     library_path,
     paged_extend_attn,
     read_error,
-    set_timing_events,
-    TIMING_ROWS,
-    TIMING_TC,
     workspace_size,
 )
 
 __all__ = [
     "Pager", "PCPError", "Status", "compute_out_cache_loc", "copy_page_slots", "kv_append",
-    "lib", "library_path", "paged_extend_attn", "read_error", "set_timing_events", "TIMING_ROWS", "TIMING_TC",
-    "workspace_size",
+    "lib", "library_path", "paged_extend_attn", "read_error", "workspace_size",
 ]

@@ -30,6 +30,14 @@ class Status(enum.IntEnum):
     TIMEOUT = 6
 
 
+class CallOptions(ctypes.Structure):
+    """``pcp_call_options``: per-call events around the tensor-core and row
+    kernels, and the limit of the kernels' pipeline waits."""
+    _fields_ = [("tc_event_before", ctypes.c_void_p), ("tc_event_after", ctypes.c_void_p),
+                ("rows_event_before", ctypes.c_void_p), ("rows_event_after", ctypes.c_void_p),
+                ("wait_limit_ns", ctypes.c_uint64)]
+
+
 class PCPError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = int(status)
@@ -72,6 +80,11 @@ def lib():
                                                    i32, i32, i32, i32, f32, i32, P, i64, i64,
                                                    i64, i32, i32, P, P, P, sz, P, P]
         L.pcp_paged_extend_attn_masked.restype = i32
+        L.pcp_paged_extend_attn_ex.argtypes = [P, P, P, P, P, P, i32, i64, P, P, i64, i32,
+                                               i32, i32, i32, i32, f32, i32, P, i64, i64, i64,
+                                               i32, i32, P, P, P, sz, P, P,
+                                               ctypes.POINTER(CallOptions)]
+        L.pcp_paged_extend_attn_ex.restype = i32
         L.pcp_pager_create.argtypes = [i64, i32]
         L.pcp_pager_create.restype = P
         L.pcp_pager_destroy.argtypes = [P]
@@ -99,8 +112,6 @@ def lib():
         L.pcp_copy_page_slots.restype = i32
         L.pcp_read_error.argtypes = [P, P, P]
         L.pcp_read_error.restype = i32
-        L.pcp_set_timing_events.argtypes = [i32, P, P]
-        L.pcp_set_timing_events.restype = i32
         _lib = L
         return L
 
@@ -265,6 +276,7 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
                       dev_err: Optional[torch.Tensor] = None,
                       qo_indptr_host=None, causal: bool = True,
                       mask: Optional[torch.Tensor] = None,
+                      tc_events=None, rows_events=None, wait_limit_ns: int = 0,
                       check: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
     """Extend attention of every query row over its cached prefix and own
     chunk (bottom-right causal, GQA, optional window).  Returns (out, lse):
@@ -276,7 +288,10 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
     causal=False: every row sees all keys of its sequence (no window).
     mask: optional bool tensor (True = keep) of shape [B, kv] or
     [B, 1|Hq, 1|q, kv], indexed by the row inside the chunk and the key
-    position, applied on top of the causal rule."""
+    position, applied on top of the causal rule.
+    tc_events / rows_events: optional (before, after) torch.cuda.Event pairs
+    recorded around the tensor-core / row kernel of this call.
+    wait_limit_ns: limit of the kernels' pipeline waits (0: the default)."""
     dev = q.device
     _need(q, "q", torch.bfloat16, dev)
     _need(k_pool, "k_pool", torch.bfloat16, dev)
@@ -302,7 +317,20 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
     if own:
         dev_err = _dev_err(dev)
     host_ptr, host_keep = _host_i32(qo_indptr_host, batch + 1, "qo_indptr_host")
-    if causal and mask is None:
+    if tc_events is not None or rows_events is not None or wait_limit_ns:
+        ev = lambda e: ctypes.c_void_p(e.cuda_event) if e is not None else ctypes.c_void_p(0)
+        tb, ta = tc_events if tc_events is not None else (None, None)
+        rb, ra = rows_events if rows_events is not None else (None, None)
+        opts = CallOptions(ev(tb), ev(ta), ev(rb), ev(ra), int(wait_limit_ns))
+        mkeep, mptr, sb, sh, sq, mq, mkv = _mask_args(mask, batch, n_q_heads, dev)
+        _check(lib().pcp_paged_extend_attn_ex(
+            _ptr(q), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(prefix_lens),
+            host_ptr, batch, total_q, _ptr(k_pool), _ptr(v_pool), num_pages, page_size,
+            n_q_heads, n_kv_heads, head_dim, window, float(sm_scale), int(bool(causal)), mptr,
+            sb, sh, sq, mq, mkv, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+            _ptr(dev_err), _stream(dev), ctypes.byref(opts)), "pcp_paged_extend_attn_ex")
+        del mkeep
+    elif causal and mask is None:
         _check(lib().pcp_paged_extend_attn(
             _ptr(q), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(prefix_lens),
             host_ptr, batch, total_q, _ptr(k_pool), _ptr(v_pool), num_pages, page_size,
@@ -321,10 +349,6 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
     del host_keep
     _finish(dev_err, own, check, "pcp_paged_extend_attn")
     return out, lse
-
-
-TIMING_TC = 0    # the tensor-core extend kernel
-TIMING_ROWS = 1  # the split-KV row kernel
 
 
 def copy_page_slots(k_pool: torch.Tensor, v_pool: torch.Tensor, page_size: int,
@@ -348,14 +372,6 @@ def copy_page_slots(k_pool: torch.Tensor, v_pool: torch.Tensor, page_size: int,
                                      src_pages.numel(), _ptr(dev_err), _stream(dev)),
            "pcp_copy_page_slots")
     _finish(dev_err, own, check, "pcp_copy_page_slots")
-
-
-def set_timing_events(before, after, kernel: int = TIMING_TC) -> None:
-    """Record `before`/`after` (torch.cuda.Event, or None) around `kernel`
-    (TIMING_TC or TIMING_ROWS) in every later paged_extend_attn call."""
-    b = ctypes.c_void_p(before.cuda_event) if before is not None else ctypes.c_void_p(0)
-    a = ctypes.c_void_p(after.cuda_event) if after is not None else ctypes.c_void_p(0)
-    _check(lib().pcp_set_timing_events(kernel, b, a), "pcp_set_timing_events")
 
 
 class Pager:

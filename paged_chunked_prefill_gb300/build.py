@@ -54,8 +54,6 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                     "-I" + INCLUDE, "-I" + CSRC, "--expt-relaxed-constexpr"]
     if ptxas_info:
         flags += ["-Xptxas", "-v"]
-    # extra nvcc flags (e.g. -D overrides of tuning constants for a sweep)
-    flags += os.environ.get("PCP_EXTRA_NVCC_FLAGS", "").split()
     procs = []
     objs = []
     for src in _sources():

@@ -11,9 +11,6 @@
 #include "pcp.h"
 #include "pcp_internal.h"
 
-#ifndef PCP_TMA_MIN_ROWS
-#define PCP_TMA_MIN_ROWS 8
-#endif
 
 namespace pcp {
 
@@ -60,8 +57,6 @@ using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, voi
                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeFn g_encode = nullptr;
-// profiling events per kernel kind (PCP_TIMING_TC, PCP_TIMING_ROWS)
-cudaEvent_t g_ev_before[2] = {nullptr, nullptr}, g_ev_after[2] = {nullptr, nullptr};
 
 // SM count of the current device, cached per device.
 pcp_status sm_count(int* out) {
@@ -121,6 +116,213 @@ int gcd_int(int a, int b) {
 }
 
 }  // namespace
+
+pcp_status check_extend_args(const ExtendArgs& a, WsLayout* lay) {
+    if (a.batch < 0 || a.total_q < 0 || a.total_q >= (int64_t(1) << 31) || a.n_q_heads < 1 ||
+        a.n_kv_heads < 1 || a.page_size < 1 || a.window < 0 || a.num_pages < 0 ||
+        a.dev_err == nullptr)
+        return PCP_ERR_INVALID_ARG;
+    if ((a.causal != 0 && a.causal != 1) || (!a.causal && a.window > 0))
+        return PCP_ERR_INVALID_ARG;
+    const MaskParams& m = a.mask;
+    if (m.data != nullptr &&
+        (m.b_stride < 0 || m.h_stride < 0 || m.q_stride < 0 || m.q_len < 0 || m.kv_len < 0 ||
+         !aligned(m.data, 16) || m.b_stride % 16 != 0 || m.h_stride % 16 != 0 ||
+         m.q_stride % 16 != 0))
+        return PCP_ERR_INVALID_ARG;
+    if (a.batch == 0 && a.total_q != 0) return PCP_ERR_INVALID_ARG;
+    if (a.n_q_heads % a.n_kv_heads != 0) return PCP_ERR_INVALID_ARG;
+    if (a.head_dim != 64 && a.head_dim != 128) return PCP_ERR_UNSUPPORTED;
+    if (a.n_q_heads / a.n_kv_heads > kTileM) return PCP_ERR_UNSUPPORTED;
+    if (!std::isfinite(a.sm_scale)) return PCP_ERR_INVALID_ARG;
+    if (a.num_pages * (int64_t)a.page_size >= (int64_t(1) << 31)) return PCP_ERR_UNSUPPORTED;
+    if (!ws_layout(a.batch, a.total_q, a.n_q_heads, a.n_kv_heads, a.head_dim, lay))
+        return PCP_ERR_INVALID_ARG;
+    if (a.total_q == 0) return PCP_OK;
+    if (!a.q || !a.qo_indptr || !a.kv_indptr || !a.kv_indices || !a.prefix_lens || !a.k_pool ||
+        !a.v_pool || !a.out)
+        return PCP_ERR_INVALID_ARG;
+    if (a.num_pages < 1) return PCP_ERR_INVALID_ARG;
+    if (!aligned(a.q, 16) || !aligned(a.out, 16) || !aligned(a.k_pool, 16) ||
+        !aligned(a.v_pool, 16))
+        return PCP_ERR_INVALID_ARG;
+    if (a.qo_indptr_host != nullptr) {
+        const int32_t* h = a.qo_indptr_host;
+        if (h[0] != 0 || h[a.batch] != a.total_q) return PCP_ERR_INVALID_ARG;
+        for (int b = 0; b < a.batch; ++b)
+            if (h[b + 1] < h[b]) return PCP_ERR_INVALID_ARG;
+    }
+    return PCP_OK;
+}
+
+pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
+    // ---- host-visible checks, before anything is launched
+    WsLayout lay;
+    pcp_status st = check_extend_args(a, &lay);
+    if (st != PCP_OK) return st;
+    pcp_call_options o = {};
+    if (opts != nullptr) o = *opts;
+    if ((o.tc_event_before == nullptr) != (o.tc_event_after == nullptr) ||
+        (o.rows_event_before == nullptr) != (o.rows_event_after == nullptr))
+        return PCP_ERR_INVALID_ARG;
+    if (a.total_q == 0) return PCP_OK;
+    if (a.workspace == nullptr || a.workspace_bytes < lay.total || !aligned(a.workspace, 256))
+        return PCP_ERR_WORKSPACE;
+    const int group = a.n_q_heads / a.n_kv_heads;
+    const int head_dim = a.head_dim;
+    const int page_size = a.page_size;
+    // With the host copy of qo_indptr the call launches only the kernels that
+    // have work: the tensor-core kernel for chunks of more than
+    // row_path_max_chunk(G) rows, the row kernel and combine for the others.
+    const int rmax = row_path_max_chunk(group);
+    bool run_tc = true, run_rows = rmax > 0;
+    if (a.qo_indptr_host != nullptr) {
+        bool any_tc = false, any_row = false;
+        for (int b = 0; b < a.batch; ++b) {
+            const int64_t c = (int64_t)a.qo_indptr_host[b + 1] - a.qo_indptr_host[b];
+            if (c > rmax) any_tc = true;
+            else if (c > 0) any_row = true;
+        }
+        run_tc = any_tc;
+        run_rows = run_rows && any_row;
+    }
+
+    int sms = 0;
+    st = sm_count(&sms);
+    if (st != PCP_OK) return st;
+    EncodeFn enc = nullptr;
+    st = get_encoder(&enc);
+    if (st != PCP_OK) return st;
+
+    const float scale = a.sm_scale > 0.f ? a.sm_scale : 1.0f / std::sqrt((float)head_dim);
+    const float scale_log2 = scale * 1.4426950408889634f;
+    const uint64_t wait_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : kSpinLimitNs;
+    cudaStream_t s = static_cast<cudaStream_t>(a.stream);
+    unsigned char* ws = static_cast<unsigned char*>(a.workspace);
+    const int qpos = q_positions_per_tile(group);
+    const int num_slots = (int)(a.num_pages * page_size);
+    // TMA boxes for page runs of >= kTmaMinRows keys; smaller pages go to
+    // the cp.async gather warps
+    const int g128 = gcd_int(page_size, kTileN);
+    const int box_rows = g128 >= kTmaMinRows ? g128 : 0;
+    const int page_shift =
+        (page_size & (page_size - 1)) == 0 ? __builtin_ctz((unsigned)page_size) : -1;
+
+    // ---- tensor maps: Q boxes of (64 dims, G heads, qpos positions); K/V
+    // boxes of (64 dims, one KV head, one page run)
+    CUtensorMap tq, tk, tv;
+    if ((st = encode_3d(enc, &tq, a.q, head_dim, a.n_q_heads, a.total_q, 64, group, qpos)) !=
+        PCP_OK)
+        return st;
+    const uint32_t kv_box = box_rows > 0 ? box_rows : 8;
+    if ((st = encode_3d(enc, &tk, a.k_pool, head_dim, a.n_kv_heads, num_slots, 64, 1, kv_box)) !=
+        PCP_OK)
+        return st;
+    if ((st = encode_3d(enc, &tv, a.v_pool, head_dim, a.n_kv_heads, num_slots, 64, 1, kv_box)) !=
+        PCP_OK)
+        return st;
+
+    // ---- 1. plan
+    PlanParams pp;
+    pp.qo_indptr = a.qo_indptr;
+    pp.kv_indptr = a.kv_indptr;
+    pp.prefix_lens = a.prefix_lens;
+    pp.batch = a.batch;
+    pp.total_q = a.total_q;
+    pp.n_kv_heads = a.n_kv_heads;
+    pp.group = group;
+    pp.page_size = page_size;
+    pp.window = a.window;
+    pp.causal = a.causal;
+    pp.tc_work = run_tc ? 1 : 0;
+    pp.sm_count = sms;
+    pp.ws = ws;
+    pp.lay = lay;
+    pp.dev_err = a.dev_err;
+    if (failed(launch_plan(s, pp))) return PCP_ERR_CUDA;
+
+    // ---- 2. tensor-core extend kernel (persistent, one CTA per SM)
+    TcParams tp;
+    tp.qo_indptr = a.qo_indptr;
+    tp.kv_indptr = a.kv_indptr;
+    tp.kv_indices = a.kv_indices;
+    tp.prefix_lens = a.prefix_lens;
+    tp.ws = ws;
+    tp.lay = lay;
+    tp.k_pool = static_cast<const uint16_t*>(a.k_pool);
+    tp.v_pool = static_cast<const uint16_t*>(a.v_pool);
+    tp.out = static_cast<uint16_t*>(a.out);
+    tp.lse = a.lse;
+    tp.n_q_heads = a.n_q_heads;
+    tp.n_kv_heads = a.n_kv_heads;
+    tp.group = group;
+    tp.qpos = qpos;
+    tp.page_size = page_size;
+    tp.box_rows = box_rows;
+    tp.page_shift = page_shift;
+    tp.num_pages = a.num_pages;
+    tp.num_slots = num_slots;
+    tp.window = a.window;
+    tp.causal = a.causal;
+    tp.mask = a.mask;
+    tp.scale_log2 = scale_log2;
+    tp.wait_ns = wait_ns;
+    tp.dev_err = a.dev_err;
+    cudaEvent_t evb = static_cast<cudaEvent_t>(o.tc_event_before);
+    cudaEvent_t eva = static_cast<cudaEvent_t>(o.tc_event_after);
+    if (evb && failed(cudaEventRecord(evb, s))) return PCP_ERR_CUDA;
+    if (run_tc && failed(launch_extend_tc(head_dim, sms, s, tp, tq, tk, tv))) return PCP_ERR_CUDA;
+    if (eva && failed(cudaEventRecord(eva, s))) return PCP_ERR_CUDA;
+
+    // ---- 3. decode-shaped rows (split-KV on CUDA cores, equal tiles per CTA)
+    if (run_rows) {
+        RowParams rp;
+        rp.q = static_cast<const uint16_t*>(a.q);
+        rp.qo_indptr = a.qo_indptr;
+        rp.kv_indptr = a.kv_indptr;
+        rp.kv_indices = a.kv_indices;
+        rp.prefix_lens = a.prefix_lens;
+        rp.ws = ws;
+        rp.lay = lay;
+        rp.k_pool = static_cast<const uint16_t*>(a.k_pool);
+        rp.v_pool = static_cast<const uint16_t*>(a.v_pool);
+        rp.out = static_cast<uint16_t*>(a.out);
+        rp.lse = a.lse;
+        rp.n_q_heads = a.n_q_heads;
+        rp.n_kv_heads = a.n_kv_heads;
+        rp.group = group;
+        rp.page_size = page_size;
+        rp.box_rows = box_rows;
+        rp.box_shift = box_rows > 0 ? __builtin_ctz((unsigned)box_rows) : 0;
+        rp.page_shift = page_shift;
+        rp.num_pages = a.num_pages;
+        rp.num_slots = num_slots;
+        rp.window = a.window;
+        rp.causal = a.causal;
+        rp.mask = a.mask;
+        rp.scale_log2 = scale_log2;
+        rp.wait_ns = wait_ns;
+        rp.dev_err = a.dev_err;
+        cudaEvent_t erb = static_cast<cudaEvent_t>(o.rows_event_before);
+        cudaEvent_t era = static_cast<cudaEvent_t>(o.rows_event_after);
+        if (erb && failed(cudaEventRecord(erb, s))) return PCP_ERR_CUDA;
+        if (failed(launch_rows(head_dim, row_grid(sms), s, rp, tk, tv))) return PCP_ERR_CUDA;
+        if (era && failed(cudaEventRecord(era, s))) return PCP_ERR_CUDA;
+        // ---- 4. merge split-KV partials (one CTA per split group)
+        CombineParams cp;
+        cp.ws = ws;
+        cp.lay = lay;
+        cp.out = static_cast<uint16_t*>(a.out);
+        cp.lse = a.lse;
+        cp.n_q_heads = a.n_q_heads;
+        cp.n_kv_heads = a.n_kv_heads;
+        cp.group = group;
+        cp.n_groups = a.batch * a.n_kv_heads;
+        if (failed(launch_combine(head_dim, s, cp))) return PCP_ERR_CUDA;
+    }
+    return PCP_OK;
+}
+
 }  // namespace pcp
 
 using namespace pcp;
@@ -140,7 +342,7 @@ const char* pcp_status_string(int status) {
     }
 }
 
-int pcp_abi_version(void) { return 2; }
+int pcp_abi_version(void) { return 3; }
 
 const char* pcp_last_cuda_error(void) {
     return t_last_cuda == cudaSuccess ? "no error" : cudaGetErrorString(t_last_cuda);
@@ -212,6 +414,48 @@ size_t pcp_extend_workspace_size(int batch, int64_t total_q, int n_q_heads, int 
     return L.total;
 }
 
+pcp_status pcp_paged_extend_attn_ex(
+    const void* q, const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+    const int32_t* prefix_lens, const int32_t* qo_indptr_host, int batch, int64_t total_q,
+    const void* k_pool, const void* v_pool, int64_t num_pages, int page_size, int n_q_heads,
+    int n_kv_heads, int head_dim, int window, float sm_scale, int causal, const uint8_t* mask,
+    int64_t mask_b_stride, int64_t mask_h_stride, int64_t mask_q_stride, int32_t mask_q_len,
+    int32_t mask_kv_len, void* out, float* lse, void* workspace, size_t workspace_bytes,
+    int32_t* dev_err, void* stream, const pcp_call_options* options) {
+    ExtendArgs a;
+    a.q = q;
+    a.qo_indptr = qo_indptr;
+    a.kv_indptr = kv_indptr;
+    a.kv_indices = kv_indices;
+    a.prefix_lens = prefix_lens;
+    a.qo_indptr_host = qo_indptr_host;
+    a.batch = batch;
+    a.total_q = total_q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.num_pages = num_pages;
+    a.page_size = page_size;
+    a.n_q_heads = n_q_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.window = window;
+    a.sm_scale = sm_scale;
+    a.causal = causal;
+    a.mask.data = mask;
+    a.mask.b_stride = mask_b_stride;
+    a.mask.h_stride = mask_h_stride;
+    a.mask.q_stride = mask_q_stride;
+    a.mask.q_len = mask_q_len;
+    a.mask.kv_len = mask_kv_len;
+    a.out = out;
+    a.lse = lse;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.dev_err = dev_err;
+    a.stream = stream;
+    return run_extend(a, options);
+}
+
 pcp_status pcp_paged_extend_attn_masked(
     const void* q, const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
     const int32_t* prefix_lens, const int32_t* qo_indptr_host, int batch, int64_t total_q,
@@ -220,194 +464,12 @@ pcp_status pcp_paged_extend_attn_masked(
     int64_t mask_b_stride, int64_t mask_h_stride, int64_t mask_q_stride, int32_t mask_q_len,
     int32_t mask_kv_len, void* out, float* lse, void* workspace, size_t workspace_bytes,
     int32_t* dev_err, void* stream) {
-    // ---- host-visible argument checks, before anything is launched
-    if (batch < 0 || total_q < 0 || total_q >= (int64_t(1) << 31) || n_q_heads < 1 ||
-        n_kv_heads < 1 || page_size < 1 || window < 0 || num_pages < 0 || dev_err == nullptr)
-        return PCP_ERR_INVALID_ARG;
-    if ((causal != 0 && causal != 1) || (!causal && window > 0)) return PCP_ERR_INVALID_ARG;
-    if (mask != nullptr &&
-        (mask_b_stride < 0 || mask_h_stride < 0 || mask_q_stride < 0 || mask_q_len < 0 ||
-         mask_kv_len < 0 || !aligned(mask, 16) || mask_b_stride % 16 != 0 ||
-         mask_h_stride % 16 != 0 || mask_q_stride % 16 != 0))
-        return PCP_ERR_INVALID_ARG;
-    if (batch == 0 && total_q != 0) return PCP_ERR_INVALID_ARG;
-    if (n_q_heads % n_kv_heads != 0) return PCP_ERR_INVALID_ARG;
-    if (head_dim != 64 && head_dim != 128) return PCP_ERR_UNSUPPORTED;
-    const int group = n_q_heads / n_kv_heads;
-    if (group > kTileM) return PCP_ERR_UNSUPPORTED;
-    if (!std::isfinite(sm_scale)) return PCP_ERR_INVALID_ARG;
-    if (num_pages * (int64_t)page_size >= (int64_t(1) << 31)) return PCP_ERR_UNSUPPORTED;
-    WsLayout lay;
-    if (!ws_layout(batch, total_q, n_q_heads, n_kv_heads, head_dim, &lay))
-        return PCP_ERR_INVALID_ARG;
-    if (total_q == 0) return PCP_OK;
-    if (!q || !qo_indptr || !kv_indptr || !kv_indices || !prefix_lens || !k_pool || !v_pool ||
-        !out)
-        return PCP_ERR_INVALID_ARG;
-    if (num_pages < 1) return PCP_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16))
-        return PCP_ERR_INVALID_ARG;
-    if (workspace == nullptr || workspace_bytes < lay.total || !aligned(workspace, 256))
-        return PCP_ERR_WORKSPACE;
-    // With the host copy of qo_indptr the call launches only the kernels that
-    // have work: the tensor-core kernel for chunks of more than
-    // row_path_max_chunk(G) rows, the row kernel and combine for the others.
-    const int rmax = row_path_max_chunk(group);
-    bool run_tc = true, run_rows = rmax > 0;
-    if (qo_indptr_host != nullptr) {
-        if (qo_indptr_host[0] != 0 || qo_indptr_host[batch] != total_q)
-            return PCP_ERR_INVALID_ARG;
-        bool any_tc = false, any_row = false;
-        for (int b = 0; b < batch; ++b) {
-            const int64_t c = (int64_t)qo_indptr_host[b + 1] - qo_indptr_host[b];
-            if (c < 0) return PCP_ERR_INVALID_ARG;
-            if (c > rmax) any_tc = true;
-            else if (c > 0) any_row = true;
-        }
-        run_tc = any_tc;
-        run_rows = run_rows && any_row;
-    }
-
-    int sms = 0;
-    pcp_status st = sm_count(&sms);
-    if (st != PCP_OK) return st;
-    EncodeFn enc = nullptr;
-    st = get_encoder(&enc);
-    if (st != PCP_OK) return st;
-
-    const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)head_dim);
-    const float scale_log2 = scale * 1.4426950408889634f;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
-    const int qpos = q_positions_per_tile(group);
-    const int num_slots = (int)(num_pages * page_size);
-    // TMA boxes for page runs of >= PCP_TMA_MIN_ROWS keys; smaller pages go to
-    // the cp.async gather warps (below 8 rows the TMA unit's per-box cost
-    // dominates; above, TMA out-runs two gather warps)
-    const int g128 = gcd_int(page_size, kTileN);
-    const int box_rows = g128 >= PCP_TMA_MIN_ROWS ? g128 : 0;
-
-    // ---- tensor maps: Q boxes of (64 dims, G heads, qpos positions); K/V
-    // boxes of (64 dims, one KV head, one page run)
-    CUtensorMap tq, tk, tv;
-    if ((st = encode_3d(enc, &tq, q, head_dim, n_q_heads, total_q, 64, group, qpos)) != PCP_OK)
-        return st;
-    const uint32_t kv_box = box_rows > 0 ? box_rows : 8;
-    if ((st = encode_3d(enc, &tk, k_pool, head_dim, n_kv_heads, num_slots, 64, 1, kv_box)) !=
-        PCP_OK)
-        return st;
-    if ((st = encode_3d(enc, &tv, v_pool, head_dim, n_kv_heads, num_slots, 64, 1, kv_box)) !=
-        PCP_OK)
-        return st;
-
-    // ---- 1. plan
-    PlanParams pp;
-    pp.qo_indptr = qo_indptr;
-    pp.kv_indptr = kv_indptr;
-    pp.prefix_lens = prefix_lens;
-    pp.batch = batch;
-    pp.total_q = total_q;
-    pp.n_kv_heads = n_kv_heads;
-    pp.group = group;
-    pp.page_size = page_size;
-    pp.window = window;
-    pp.causal = causal;
-    pp.tc_work = run_tc ? 1 : 0;
-    pp.sm_count = sms;
-    pp.ws = ws;
-    pp.lay = lay;
-    pp.dev_err = dev_err;
-    if (failed(launch_plan(s, pp))) return PCP_ERR_CUDA;
-
-    // ---- 2. tensor-core extend kernel (persistent, one CTA per SM)
-    TcParams tp;
-    tp.qo_indptr = qo_indptr;
-    tp.kv_indptr = kv_indptr;
-    tp.kv_indices = kv_indices;
-    tp.prefix_lens = prefix_lens;
-    tp.ws = ws;
-    tp.lay = lay;
-    tp.k_pool = static_cast<const uint16_t*>(k_pool);
-    tp.v_pool = static_cast<const uint16_t*>(v_pool);
-    tp.out = static_cast<uint16_t*>(out);
-    tp.lse = lse;
-    tp.n_q_heads = n_q_heads;
-    tp.n_kv_heads = n_kv_heads;
-    tp.group = group;
-    tp.qpos = qpos;
-    tp.page_size = page_size;
-    tp.box_rows = box_rows;
-    tp.page_shift = (page_size & (page_size - 1)) == 0 ? __builtin_ctz((unsigned)page_size) : -1;
-    tp.num_pages = num_pages;
-    MaskParams mp;
-    mp.data = mask;
-    mp.b_stride = mask_b_stride;
-    mp.h_stride = mask_h_stride;
-    mp.q_stride = mask_q_stride;
-    mp.q_len = mask_q_len;
-    mp.kv_len = mask_kv_len;
-    tp.num_slots = num_slots;
-    tp.window = window;
-    tp.causal = causal;
-    tp.mask = mp;
-    tp.scale_log2 = scale_log2;
-    tp.dev_err = dev_err;
-    cudaEvent_t evb = nullptr, eva = nullptr, evrb = nullptr, evra = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        evb = g_ev_before[PCP_TIMING_TC];
-        eva = g_ev_after[PCP_TIMING_TC];
-        evrb = g_ev_before[PCP_TIMING_ROWS];
-        evra = g_ev_after[PCP_TIMING_ROWS];
-    }
-    if (evb && failed(cudaEventRecord(evb, s))) return PCP_ERR_CUDA;
-    if (run_tc && failed(launch_extend_tc(head_dim, sms, s, tp, tq, tk, tv))) return PCP_ERR_CUDA;
-    if (eva && failed(cudaEventRecord(eva, s))) return PCP_ERR_CUDA;
-
-    // ---- 3. decode-shaped rows (split-KV on CUDA cores, equal tiles per CTA)
-    if (run_rows) {
-        RowParams rp;
-        rp.q = static_cast<const uint16_t*>(q);
-        rp.qo_indptr = qo_indptr;
-        rp.kv_indptr = kv_indptr;
-        rp.kv_indices = kv_indices;
-        rp.prefix_lens = prefix_lens;
-        rp.ws = ws;
-        rp.lay = lay;
-        rp.k_pool = static_cast<const uint16_t*>(k_pool);
-        rp.v_pool = static_cast<const uint16_t*>(v_pool);
-        rp.out = static_cast<uint16_t*>(out);
-        rp.lse = lse;
-        rp.n_q_heads = n_q_heads;
-        rp.n_kv_heads = n_kv_heads;
-        rp.group = group;
-        rp.page_size = page_size;
-        rp.box_rows = box_rows;
-        rp.box_shift = box_rows > 0 ? __builtin_ctz((unsigned)box_rows) : 0;
-        rp.page_shift = tp.page_shift;
-        rp.num_pages = num_pages;
-        rp.num_slots = num_slots;
-        rp.window = window;
-        rp.causal = causal;
-        rp.mask = mp;
-        rp.scale_log2 = scale_log2;
-        rp.dev_err = dev_err;
-        if (evrb && failed(cudaEventRecord(evrb, s))) return PCP_ERR_CUDA;
-        if (failed(launch_rows(head_dim, row_grid(sms), s, rp, tk, tv))) return PCP_ERR_CUDA;
-        if (evra && failed(cudaEventRecord(evra, s))) return PCP_ERR_CUDA;
-        // ---- 4. merge split-KV partials (one CTA per split group)
-        CombineParams cp;
-        cp.ws = ws;
-        cp.lay = lay;
-        cp.out = static_cast<uint16_t*>(out);
-        cp.lse = lse;
-        cp.n_q_heads = n_q_heads;
-        cp.n_kv_heads = n_kv_heads;
-        cp.group = group;
-        cp.n_groups = batch * n_kv_heads;
-        if (failed(launch_combine(head_dim, s, cp))) return PCP_ERR_CUDA;
-    }
-    return PCP_OK;
+    return pcp_paged_extend_attn_ex(q, qo_indptr, kv_indptr, kv_indices, prefix_lens,
+                                    qo_indptr_host, batch, total_q, k_pool, v_pool, num_pages,
+                                    page_size, n_q_heads, n_kv_heads, head_dim, window, sm_scale,
+                                    causal, mask, mask_b_stride, mask_h_stride, mask_q_stride,
+                                    mask_q_len, mask_kv_len, out, lse, workspace,
+                                    workspace_bytes, dev_err, stream, nullptr);
 }
 
 pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
@@ -418,11 +480,11 @@ pcp_status pcp_paged_extend_attn(const void* q, const int32_t* qo_indptr,
                                  int n_q_heads, int n_kv_heads, int head_dim, int window,
                                  float sm_scale, void* out, float* lse, void* workspace,
                                  size_t workspace_bytes, int32_t* dev_err, void* stream) {
-    return pcp_paged_extend_attn_masked(q, qo_indptr, kv_indptr, kv_indices, prefix_lens,
-                                        qo_indptr_host, batch, total_q, k_pool, v_pool,
-                                        num_pages, page_size, n_q_heads, n_kv_heads, head_dim,
-                                        window, sm_scale, 1, nullptr, 0, 0, 0, 0, 0, out, lse,
-                                        workspace, workspace_bytes, dev_err, stream);
+    return pcp_paged_extend_attn_ex(q, qo_indptr, kv_indptr, kv_indices, prefix_lens,
+                                    qo_indptr_host, batch, total_q, k_pool, v_pool, num_pages,
+                                    page_size, n_q_heads, n_kv_heads, head_dim, window, sm_scale,
+                                    1, nullptr, 0, 0, 0, 0, 0, out, lse, workspace,
+                                    workspace_bytes, dev_err, stream, nullptr);
 }
 
 pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_err) {
@@ -431,15 +493,6 @@ pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_er
     if (failed(cudaMemcpyAsync(host_err, dev_err, sizeof(int32_t), cudaMemcpyDeviceToHost, s)))
         return PCP_ERR_CUDA;
     if (failed(cudaStreamSynchronize(s))) return PCP_ERR_CUDA;
-    return PCP_OK;
-}
-
-pcp_status pcp_set_timing_events(int kernel, void* before, void* after) {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if ((before == nullptr) != (after == nullptr)) return PCP_ERR_INVALID_ARG;
-    if (kernel != PCP_TIMING_TC && kernel != PCP_TIMING_ROWS) return PCP_ERR_INVALID_ARG;
-    g_ev_before[kernel] = static_cast<cudaEvent_t>(before);
-    g_ev_after[kernel] = static_cast<cudaEvent_t>(after);
     return PCP_OK;
 }
 

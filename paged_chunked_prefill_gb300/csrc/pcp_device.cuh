@@ -74,10 +74,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // `limit_ns` nanoseconds (recording PCP_ERR_TIMEOUT and raising the CTA's
 // abort flag) or as soon as another thread of the CTA raised the abort flag.
 // Returns false when it gave up.
-#ifndef PCP_MBAR_CLOCK_EVERY
-#define PCP_MBAR_CLOCK_EVERY 1
-#endif
-constexpr uint32_t kMbarClockEvery = PCP_MBAR_CLOCK_EVERY;
+constexpr uint32_t kMbarClockEvery = 1;
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int* abort_flag, int32_t* dev_err,

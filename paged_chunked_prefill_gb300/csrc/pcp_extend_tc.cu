@@ -55,7 +55,7 @@ struct TcCfg {
     static constexpr uint32_t kOffV = kOffQ + kQTiles * kQBytes;
     static constexpr uint32_t kOffK = kOffV + kStagesV * kTileBytes;
     static constexpr uint32_t kOffBar = kOffK + kStagesK * kTileBytes;
-    static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 6 + 1;
+    static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 6 + 2;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;
     static_assert(kOffBar % 8 == 0 && kOffMisc % 4 == 0, "smem alignment");
@@ -71,6 +71,7 @@ struct TcCfg {
     static constexpr int bPFull = bSFull + 2;
     static constexpr int bODone = bSFull + 4;
     static constexpr int bDrain = bSFull + 6;
+    static constexpr int bGatherDrain = bSFull + 7;
 };
 
 struct Geo {
@@ -323,6 +324,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(bar(C::bODone + u), 1);
         }
         mbar_init(bar(C::bDrain), 1);
+        mbar_init(bar(C::bGatherDrain), 32u * kGatherWarps);
         fence_mbarrier_init();
         misc[2] = 0;
         prefetch_tensormap(&tm_q);
@@ -388,17 +390,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // the next tile's page ids are in flight while this one waits
                     const int z_next =
                         i + 1 < ntiles ? fetch_box_slot<D>(p, geo, pages, t + 1, lane) : z_cur;
+                    // every wait is decided for the whole warp: the box issue
+                    // below has warp-collective steps
                     if (is_k) {
                         const int sk = cur % SK;
-                        if (!mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u, abort_flag,
-                                       p.dev_err, kSpinLimitNs))
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u,
+                                                  abort_flag, p.dev_err, p.wait_ns)))
                             break;
                         tma_kv_tile<D>(p, geo, t, z_cur, &tm_k, p.k_pool,
                                        sK + sk * C::kTileBytes, bar(C::bKFull + sk), false, lane);
                     } else {
                         const int sv = cur % SV;
-                        if (!mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u, abort_flag,
-                                       p.dev_err, kSpinLimitNs))
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u,
+                                                  abort_flag, p.dev_err, p.wait_ns)))
                             break;
                         tma_kv_tile<D>(p, geo, t, z_cur, &tm_v, p.v_pool,
                                        sV + sv * C::kTileBytes, bar(C::bVFull + sv), true, lane);
@@ -447,13 +453,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             prefetch_l1(pages + (p.page_shift >= 0 ? key >> p.page_shift
                                                                    : key / p.page_size));
                     }
-                    if (!mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u, abort_flag,
-                                   p.dev_err, kSpinLimitNs))
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u,
+                                              abort_flag, p.dev_err, p.wait_ns)))
                         break;
                     gather_kv_rows<D>(p, geo, slot, p.k_pool, sK + sk * C::kTileBytes, gw, lane);
                     cp_async_mbar_arrive_noinc(bar(C::bKFull + sk));
-                    if (!mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u, abort_flag,
-                                   p.dev_err, kSpinLimitNs))
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u,
+                                              abort_flag, p.dev_err, p.wait_ns)))
                         break;
                     gather_kv_rows<D>(p, geo, slot, p.v_pool, sV + sv * C::kTileBytes, gw, lane);
                     cp_async_mbar_arrive_noinc(bar(C::bVFull + sv));
@@ -490,13 +498,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 (acc || kk > 0) ? 1u : 0u);
                 };
                 bool ok = mbar_wait(bar(C::bQFull), n_done & 1u, abort_flag, p.dev_err,
-                                    kSpinLimitNs);
+                                    p.wait_ns);
                 uint32_t aidx0 = act0, aidx1 = act1;
                 if (ok) {
                     tc_fence_after();
                     const uint32_t c0 = kv_iter;
                     ok = mbar_wait(bar(C::bKFull + c0 % SK), (c0 / SK) & 1u, abort_flag,
-                                   p.dev_err, kSpinLimitNs);
+                                   p.dev_err, p.wait_ns);
                     if (ok) {
                         if (p.box_rows == 0) fence_proxy_async_smem();
                         if (tile_active(geo, 0, geo.t_begin)) {
@@ -515,7 +523,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t cur = kv_iter + i;
                     const int st = cur % SV;
                     if (!mbar_wait(bar(C::bVFull + st), (cur / SV) & 1u, abort_flag, p.dev_err,
-                                   kSpinLimitNs)) {
+                                   p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -532,7 +540,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     auto step_u = [&](const int u, uint32_t& ai, const int first_u) -> bool {
                         if (tile_active(geo, u, t)) {
                             if (!mbar_wait(bar(C::bPFull + u), ai & 1u, abort_flag, p.dev_err,
-                                           kSpinLimitNs))
+                                           p.wait_ns))
                                 return false;
                             tc_fence_after();
                             issue_pv(u, st, t != first_u);
@@ -542,7 +550,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (has_next && tile_active(geo, u, t + 1)) {
                             if (!k_next) {
                                 if (!mbar_wait(bar(C::bKFull + nst), ((cur + 1) / SK) & 1u,
-                                               abort_flag, p.dev_err, kSpinLimitNs))
+                                               abort_flag, p.dev_err, p.wait_ns))
                                     return false;
                                 if (p.box_rows == 0) fence_proxy_async_smem();
                                 k_next = true;
@@ -586,7 +594,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // waits decide per warp (tcgen05.ld/st and the P arrival are
                     // warp-collective)
                     if (!__all_sync(0xffffffffu, mbar_wait(bar(C::bSFull + u), a & 1u, abort_flag,
-                                                           p.dev_err, kSpinLimitNs))) {
+                                                           p.dev_err, p.wait_ns))) {
                         ok = false;
                         break;
                     }
@@ -688,7 +696,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (t > first_u) {
                         if (!__all_sync(0xffffffffu,
                                         mbar_wait(bar(C::bODone + u), (a - 1u) & 1u, abort_flag,
-                                                  p.dev_err, kSpinLimitNs))) {
+                                                  p.dev_err, p.wait_ns))) {
                             tmem_st_wait();
                             ok = false;
                             break;
@@ -719,7 +727,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (ok) {
                     const uint32_t a_last = act_u + (uint32_t)(last_u - first_u);
                     ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bODone + u), a_last & 1u,
-                                                           abort_flag, p.dev_err, kSpinLimitNs));
+                                                           abort_flag, p.dev_err, p.wait_ns));
                 }
                 if (ok) {
                     tc_fence_after();
@@ -765,6 +773,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool aborted = *abort_flag != 0;
     if (warp == kWarpTma || warp >= kWarpGather0) {
         cp_async_wait_all();
+        if (aborted && warp >= kWarpGather0) {
+            // the mbarrier arrivals the gathers' cp.async copies trigger have
+            // been made once this one, triggered after all of them, lands
+            cp_async_mbar_arrive_noinc(bar(C::bGatherDrain));
+            volatile int dummy = 0;
+            if (warp == kWarpGather0 && lane == 0)
+                mbar_wait(bar(C::bGatherDrain), 0u, &dummy, p.dev_err, kSpinLimitNs);
+            __syncwarp();
+        }
         if (aborted && lane == 0) {
             // let every TMA load this warp issued land before the CTA exits
             volatile int dummy = 0;

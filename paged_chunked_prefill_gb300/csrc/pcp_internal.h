@@ -18,6 +18,10 @@ constexpr int kWarpTma = 8;       // Q (and the K page boxes) by TMA
 constexpr int kWarpMma = 9;       // one thread issues tcgen05.mma
 constexpr int kWarpGather0 = 10;  // warps 10, 11: cp.async page gathers of K/V
 constexpr int kGatherWarps = 2;
+// Pages whose runs inside a 128-key tile hold at least this many keys are
+// loaded by TMA boxes; smaller ones by the cp.async gather warps (below 8
+// rows the TMA unit's per-box cost dominates; above, TMA out-runs them).
+constexpr int kTmaMinRows = 8;
 
 // ---- CUDA-core row kernel (decode-shaped rows, split-KV)
 constexpr int kRowMaxRows = 16;   // query rows (positions x heads) per row item
@@ -25,7 +29,9 @@ constexpr int kRowTile = 128;     // keys per row-kernel tile
 constexpr int kRowThreads = 160;      // 4 consumer warps + 1 load warp
 constexpr int kRowMaxCtas = 512;       // row-kernel CTAs at most (one per SM below that)
 
-// Spin-wait limit of every bounded wait (nanoseconds).
+// Default limit of the kernels' bounded pipeline waits, and the fixed limit of
+// the waits that drain a CTA's in-flight copies and MMAs before it exits
+// (nanoseconds).
 constexpr uint64_t kSpinLimitNs = 2000000000ull;
 
 // A sequence's chunk goes to the row kernel when its rows (chunk_len * G)
@@ -179,6 +185,7 @@ struct TcParams {
     int causal;
     MaskParams mask;
     float scale_log2;  // sm_scale * log2(e)
+    uint64_t wait_ns;  // limit of the pipeline waits
     int32_t* dev_err;
 };
 
@@ -220,7 +227,45 @@ struct RowParams {
     int causal;
     MaskParams mask;
     float scale_log2;
+    uint64_t wait_ns;  // limit of the pipeline waits
     int32_t* dev_err;
 };
+
+// ---- one extend-attention call as the entry points receive it
+struct ExtendArgs {
+    const void* q;
+    const int32_t* qo_indptr;
+    const int32_t* kv_indptr;
+    const int32_t* kv_indices;
+    const int32_t* prefix_lens;
+    const int32_t* qo_indptr_host;
+    int batch;
+    int64_t total_q;
+    const void* k_pool;
+    const void* v_pool;
+    int64_t num_pages;
+    int page_size;
+    int n_q_heads;
+    int n_kv_heads;
+    int head_dim;
+    int window;
+    float sm_scale;
+    int causal;
+    MaskParams mask;
+    void* out;
+    float* lse;
+    void* workspace;
+    size_t workspace_bytes;
+    int32_t* dev_err;
+    void* stream;
+};
+
+// Host-side checks of an extend-attention call, everything but the
+// workspace: PCP_OK or the status the call returns before launching anything.
+// On PCP_OK *lay is the call's workspace layout.
+pcp_status check_extend_args(const ExtendArgs& a, WsLayout* lay);
+
+// The whole call (checks, workspace, launches); opts may be null.
+pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts);
 
 }  // namespace pcp

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "pcp.h"
+#include "pcp_internal.h"
 
 namespace {
 
@@ -51,23 +52,38 @@ extern "C" pcp_status pcp_paged_extend_attn_noalloc(
     const void* k_pool, const void* v_pool, int64_t num_pages, int page_size, int n_q_heads,
     int n_kv_heads, int head_dim, int window, float sm_scale, void* out, float* lse,
     int32_t* dev_err, void* stream) {
-    const size_t need =
-        pcp_extend_workspace_size(batch, total_q, n_q_heads, n_kv_heads, head_dim);
-    if (need == 0 || total_q == 0) {
-        // an unsupported shape or an empty call: the regular entry point
-        // gives the answer without touching any workspace
-        return pcp_paged_extend_attn(q, qo_indptr, kv_indptr, kv_indices, prefix_lens,
-                                     qo_indptr_host, batch, total_q, k_pool, v_pool, num_pages,
-                                     page_size, n_q_heads, n_kv_heads, head_dim, window,
-                                     sm_scale, out, lse, nullptr, 0, dev_err, stream);
-    }
-    if (need > (size_t)PCP_NOALLOC_SCRATCH_BYTES) return PCP_ERR_WORKSPACE;
+    pcp::ExtendArgs a = {};
+    a.q = q;
+    a.qo_indptr = qo_indptr;
+    a.kv_indptr = kv_indptr;
+    a.kv_indices = kv_indices;
+    a.prefix_lens = prefix_lens;
+    a.qo_indptr_host = qo_indptr_host;
+    a.batch = batch;
+    a.total_q = total_q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.num_pages = num_pages;
+    a.page_size = page_size;
+    a.n_q_heads = n_q_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.window = window;
+    a.sm_scale = sm_scale;
+    a.causal = 1;
+    a.out = out;
+    a.lse = lse;
+    a.dev_err = dev_err;
+    a.stream = stream;
+    // the same argument checks as the workspace entry point, first
+    pcp::WsLayout lay;
+    const pcp_status chk = pcp::check_extend_args(a, &lay);
+    if (chk != PCP_OK || total_q == 0) return chk;
+    if (lay.total > (size_t)PCP_NOALLOC_SCRATCH_BYTES) return PCP_ERR_WORKSPACE;
     void* scratch = nullptr;
     const pcp_status st = scratch_for_current_device(&scratch);
     if (st != PCP_OK) return st;
-    return pcp_paged_extend_attn(q, qo_indptr, kv_indptr, kv_indices, prefix_lens,
-                                 qo_indptr_host, batch, total_q, k_pool, v_pool, num_pages,
-                                 page_size, n_q_heads, n_kv_heads, head_dim, window, sm_scale,
-                                 out, lse, scratch, (size_t)PCP_NOALLOC_SCRATCH_BYTES, dev_err,
-                                 stream);
+    a.workspace = scratch;
+    a.workspace_bytes = (size_t)PCP_NOALLOC_SCRATCH_BYTES;
+    return pcp::run_extend(a, nullptr);
 }

@@ -97,6 +97,8 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     float* l_s = m_s + 4 * kRowMaxRows;
     int4* s_desc = reinterpret_cast<int4*>(sm + C::kOffDesc);  // published by mbarrier
     __shared__ int s_abort;
+    // consumer warps' posts at their joint decision points
+    __shared__ int s_post[4], s_fail[4];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
@@ -200,6 +202,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
         };
         uint32_t it = 0;  // ring position
         int last_issued = -1;
+        int last_item = -1;  // last item (or end marker) handed to the consumers
         int kg = reinterpret_cast<const int*>(p.ws + p.lay.row_first)[blockIdx.x];
         int4 gA = rg[3 * kg], gB = rg[3 * kg + 1], gC = rg[3 * kg + 2];
         int4 n0, n1, n2;
@@ -209,7 +212,9 @@ __global__ void __launch_bounds__(kRowThreads, 1)
         bool have = true;  // n0..n2 hold an item
         for (int k = 0;; ++k) {
             const int qs = k % NI;
-            const bool valid = have && !*abort_flag;
+            // every decision of this warp is taken for all its lanes (the
+            // abort flag is read once per warp)
+            const bool valid = have && !__any_sync(0xffffffffu, *abort_flag != 0);
             const int4 d0 = n0, d1 = n1, d2 = n2;
             int cur_sl[4];
 #pragma unroll
@@ -223,8 +228,8 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 gC = rg[3 * kg + 2];
             }
             // hand the item (or the end marker) and its Q rows to the consumers
-            if (!mbar_wait(item_empty(qs), ((uint32_t)(k / NI) & 1u) ^ 1u, abort_flag, p.dev_err,
-                           kSpinLimitNs))
+            if (!__all_sync(0xffffffffu, mbar_wait(item_empty(qs), ((uint32_t)(k / NI) & 1u) ^ 1u,
+                                                   abort_flag, p.dev_err, p.wait_ns)))
                 break;
             const int g = d0.y;
             if (valid) {
@@ -246,6 +251,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 s_desc[qs * 3 + 2] = d2;
                 mbar_arrive(item_full(qs));
             }
+            last_item = k;
             if (!valid) break;
             const int kb = d1.x, ke = d1.y, L = d2.w;
             const int32_t* pages = p.kv_indices + d2.z;
@@ -257,8 +263,8 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 const int st = itp % S;
                 int nsl[4];
                 if (i + 1 < ntiles) fetch(pages, L, t + 1, nsl);
-                if (!mbar_wait(empty_bar(st), ((itp / S) & 1u) ^ 1u, abort_flag, p.dev_err,
-                               kSpinLimitNs))
+                if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(st), ((itp / S) & 1u) ^ 1u,
+                                                       abort_flag, p.dev_err, p.wait_ns)))
                     break;
                 const uint32_t kd = sStage + st * 2 * C::kTileBytes;
                 const uint32_t vd = kd + C::kTileBytes;
@@ -321,32 +327,48 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 for (int j = 0; j < 4; ++j)
                     if (i + 1 < ntiles) cur_sl[j] = nsl[j];
             }
-            if (*abort_flag) break;
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             it += (uint32_t)ntiles;
             have = next_valid;
         }
         // nothing may still be landing in shared memory when the CTA exits
         cp_async_wait_all();
         if (*abort_flag && lane == 0) {
+            // the copies of the last tiles and of the last item's Q rows (and
+            // the mbarrier arrivals they trigger) land before the CTA exits
             volatile int dummy = 0;
             for (int j = last_issued - S + 1; j <= last_issued; ++j)
                 if (j >= 0)
                     mbar_wait(full_bar(j % S), ((uint32_t)j / S) & 1u, &dummy, p.dev_err,
                               kSpinLimitNs);
+            if (last_item >= 0)
+                mbar_wait(item_full(last_item % NI), ((uint32_t)(last_item / NI)) & 1u, &dummy,
+                          p.dev_err, kSpinLimitNs);
         }
         return;
     }
 
     // ======================================================== consumer warps
+    // The four consumer warps meet at named barriers, so they leave the item
+    // loop together: each warp posts its state at a decision point and all of
+    // them read every post after the barrier.  (A wait gives up for the whole
+    // warp at once.)
     uint32_t it = 0;
+    bool failed = false;  // this warp gave up a wait
     for (int k = 0;; ++k) {
         const int qs = k % NI;
-        if (!mbar_wait(item_full(qs), (uint32_t)(k / NI) & 1u, abort_flag, p.dev_err, kSpinLimitNs))
-            break;
+        // 0: an item, 1: the end marker, 2: the wait gave up
+        int post = 2;
+        if (!failed &&
+            __all_sync(0xffffffffu, mbar_wait(item_full(qs), (uint32_t)(k / NI) & 1u, abort_flag,
+                                              p.dev_err, p.wait_ns)))
+            post = s_desc[qs * 3 + 0].x < 0 ? 1 : 0;
+        if (lane == 0) s_post[warp] = post;
+        consumer_sync();
+        if (s_post[0] | s_post[1] | s_post[2] | s_post[3]) break;
         const int4 d0 = s_desc[qs * 3 + 0];
         const int4 d1 = s_desc[qs * 3 + 1];
         const int4 d2 = s_desc[qs * 3 + 2];
-        if (d0.x < 0) break;
         const int g = d0.y, split = d0.z, nsplit = d0.w;
         const int kb = d1.x, ke = d1.y, first_item = d1.z, q0 = d1.w;
         const int P = d2.y;
@@ -393,14 +415,13 @@ __global__ void __launch_bounds__(kRowThreads, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) o[dn][j] = 0.f;
 
-        int last_st = 0;
-        bool ok = true;
         for (int i = 0; i < ntiles; ++i) {
             const int t = t_first + i;
             const uint32_t itp = it + i;
             const int st = itp % S;
-            if (!mbar_wait(full_bar(st), (itp / S) & 1u, abort_flag, p.dev_err, kSpinLimitNs)) {
-                ok = false;
+            if (!__all_sync(0xffffffffu, mbar_wait(full_bar(st), (itp / S) & 1u, abort_flag,
+                                                   p.dev_err, p.wait_ns))) {
+                failed = true;
                 break;
             }
                 const uint32_t kbase = sStage + st * 2 * C::kTileBytes;
@@ -526,17 +547,17 @@ __global__ void __launch_bounds__(kRowThreads, 1)
             if (i + 1 < ntiles) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(st));
-            } else {
-                last_st = st;
             }
         }
-        if (!ok) break;
         it += (uint32_t)ntiles;
+        const int last_st = (int)((it - 1u) % S);
+        if (lane == 0) s_fail[warp] = failed ? 1 : 0;
 
         // merge the four warps' states through shared memory: the stage of
         // this item's last tile, whose release waits until the merge is done
         float* wo = reinterpret_cast<float*>(sm + C::kOffStage + last_st * 2 * C::kTileBytes);
         consumer_sync();
+        if (s_fail[0] | s_fail[1] | s_fail[2] | s_fail[3]) break;
         {
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);

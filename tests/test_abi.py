@@ -41,7 +41,7 @@ def test_status_strings(lib):
         s = lib.pcp_status_string(code).decode()
         assert s.startswith("PCP_")
     assert lib.pcp_status_string(99).decode() == "PCP_ERR_UNKNOWN"
-    assert lib.pcp_abi_version() == 2
+    assert lib.pcp_abi_version() == 3
     lib.pcp_last_cuda_error.restype = ctypes.c_char_p
     assert lib.pcp_last_cuda_error().decode() == "no error"
 
@@ -95,10 +95,31 @@ def test_host_validation_without_device(lib):
     assert masked(1, 0, P(0x1008), 64, 0, 0) == 1    # mask not 16-byte aligned
     assert masked(1, 0, one, 40, 0, 0) == 1          # stride not a multiple of 16
     assert masked(1, 0, one, 64, 0, -16) == 1        # negative stride
-    # the profiling hook takes a known kernel and both events or neither
-    assert lib.pcp_set_timing_events(7, P(0), P(0)) == 1
-    assert lib.pcp_set_timing_events(0, one, P(0)) == 1
-    assert lib.pcp_set_timing_events(1, P(0), P(0)) == 0
+    # per-call options: each kernel's events come both or not at all
+    from paged_chunked_prefill_gb300._binding import CallOptions
+    lib.pcp_paged_extend_attn_ex.restype = ctypes.c_int
+    def ex(opts):
+        return lib.pcp_paged_extend_attn_ex(
+            one, one, one, one, one, P(0), 1, 10, one, one, 4, 16, 8, 8, 128, 0,
+            ctypes.c_float(0.0), 1, P(0), ctypes.c_int64(0), ctypes.c_int64(0),
+            ctypes.c_int64(0), 0, 0, one, one, one, ctypes.c_size_t(1 << 30), err, P(0),
+            ctypes.byref(opts) if opts is not None else P(0))
+    assert ex(CallOptions(one, P(0), P(0), P(0), 0)) == 1
+    assert ex(CallOptions(P(0), P(0), P(0), one, 0)) == 1
+    # the argument checks come before the options are looked at
+    assert lib.pcp_paged_extend_attn_ex(
+        one, one, one, one, one, P(0), 1, 10, one, one, 4, 16, 30, 8, 128, 0,
+        ctypes.c_float(0.0), 1, P(0), ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0),
+        0, 0, one, one, one, ctypes.c_size_t(1 << 30), err, P(0),
+        ctypes.byref(CallOptions(one, P(0), P(0), P(0), 0))) == 1
+    # the entry point without a workspace checks its arguments first, then
+    # refuses calls larger than its fixed scratch (no device access either way)
+    g = lib.pcp_paged_extend_attn_noalloc
+    def noalloc(hq):
+        return g(one, one, one, one, one, P(0), 4096, ctypes.c_int64(65536), one, one,
+                 ctypes.c_int64(1), 16, hq, 8, 128, 0, ctypes.c_float(0.0), one, one, err, P(0))
+    assert noalloc(32) == 4
+    assert noalloc(30) == 1
     # empty work returns OK without touching the device
     assert lib.pcp_paged_extend_attn(P(0), P(0), P(0), P(0), P(0), P(0), 0, 0, P(0), P(0), 0, 16, 8,
                                      8, 128, 0, 0.0, P(0), P(0), P(0), 0, err, P(0)) == 0

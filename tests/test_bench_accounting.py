@@ -49,3 +49,41 @@ def test_row_samples_sum_to_the_whole():
     tok = np.arange(b.total_q)
     assert bench.rows_pairs(b, tok, np.zeros_like(tok)) == \
         bench.visible_pairs(b.prefix_lens, b.chunk_lens, b.window)
+
+
+def test_split_work_divides_the_mixed_batch():
+    """The mixed batch's 2048-token chunks go to the tensor cores (2,098,176 +
+    6,292,480 pairs); its 1-token chunk and the 31 decode rows (chunk_len * G
+    = 4 <= 16 rows) go to the row kernel, which reads every visible key's K
+    and V once per KV head."""
+    b = W.mixed_batch()
+    tc_pairs, row_bytes = bench.split_work(b)
+    assert tc_pairs == 2_098_176 + 6_292_480
+    c = b.chunk_lens
+    rows = c == 1
+    L = (b.prefix_lens + c)[rows].astype(np.int64)
+    D, Hkv, Hq = b.head_dim, b.n_kv_heads, b.n_q_heads
+    pages = sum(-(-int(l) // b.page_size) for l in L)
+    expect = int(L.sum()) * Hkv * D * 4 + int(rows.sum()) * Hq * (4 * D + 4) + 4 * pages
+    assert row_bytes == expect
+
+
+@pytest.mark.parametrize("window", [0, 5, 300])
+def test_split_work_matches_brute_force(window):
+    """Tensor-core pairs by brute force over the chunks longer than the row
+    path takes; row bytes from each row's visible keys counted one by one."""
+    b = W.make_batch([0, 37, 300, 5, 900, 17], [5, 40, 1, 64, 2, 3], 8, 2, 64, 16, seed=7,
+                     window=window)
+    rmax = bench.row_max_chunk(b)
+    assert rmax == 4
+    c, P = b.chunk_lens, b.prefix_lens
+    tc = c > rmax
+    tc_pairs, row_bytes = bench.split_work(b)
+    assert tc_pairs == brute_pairs(P[tc], c[tc], window)
+    keys = 0
+    for Pb, cb in zip(P[~tc], c[~tc]):
+        first = max(0, Pb - window + 1) if window > 0 else 0
+        keys += len(range(first, Pb + cb))
+    pages = sum(-(-int(Pb + cb) // 16) for Pb, cb in zip(P[~tc], c[~tc]))
+    n_rows = int(c[~tc].sum())
+    assert row_bytes == keys * 2 * 64 * 4 + n_rows * 8 * (4 * 64 + 4) + 4 * pages

@@ -8,19 +8,21 @@ device array inside the library instead.  The test calls it through the C ABI
 twice in a row, on two different batches (both with split-KV decode rows, so
 the shared scratch's counters and partials from the first call are still
 there when the second one runs), and compares each result with the regular
-entry point, which gets a workspace from PyTorch.  It also checks that a call
-needing more than the fixed scratch is refused before anything runs.
+entry point, which gets a workspace from PyTorch.  Both run the same
+deterministic kernels on the same inputs, so the results must be identical
+bit for bit.  It also checks that a call needing more than the fixed scratch
+is refused before anything runs, after the same argument checks as the
+regular entry point.
 
 This file is collected last on purpose, so a run that stops at the first
 failure has run every other test before it.
 """
 import ctypes
 
-import numpy as np
 import pytest
 
 import workloads as W
-from helpers import assert_close, bf16_tensor_to_f64, to_device
+from helpers import to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -62,9 +64,9 @@ def _run_both(batch):
     assert st == 0, pcp.lib().pcp_status_string(st)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert_close(bf16_tensor_to_f64(out), lse.cpu().numpy().astype(np.float64),
-                 bf16_tensor_to_f64(ref_out), ref_lse.cpu().numpy().astype(np.float64),
-                 "no-alloc vs workspace entry point")
+    # same kernels, same inputs: bit-identical results
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
 
 
 def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
@@ -80,6 +82,12 @@ def test_noalloc_refuses_oversized_calls():
     need = pcp.workspace_size(4096, 65536, 32, 8, 128)
     assert need > 16 * 1024 * 1024
     P = ctypes.c_void_p
-    st = _noalloc_fn()(P(0), P(0), P(0), P(0), P(0), P(0), 4096, 65536, P(0), P(0), 1, 16, 32, 8,
-                       128, 0, 0.0, P(0), P(0), P(0), P(0))
+    one = P(0x1000)  # never dereferenced: both calls return before any launch
+    err = P(0x2000)
+    st = _noalloc_fn()(one, one, one, one, one, P(0), 4096, 65536, one, one, 1, 16, 32, 8,
+                       128, 0, 0.0, one, one, err, P(0))
     assert st == pcp.Status.WORKSPACE
+    # a bad argument is reported as such, also on an oversized call
+    st = _noalloc_fn()(one, one, one, one, one, P(0), 4096, 65536, one, one, 1, 16, 30, 8,
+                       128, 0, 0.0, one, one, err, P(0))
+    assert st == pcp.Status.INVALID_ARG
