@@ -405,14 +405,17 @@ pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_er
  *     without events.
  *   rows_event_before / rows_event_after: the same around the split-KV row
  *     kernel (recorded only when the call launches it).
- *   wait_limit_ns: 0 for the default (2 s), else the limit of every pipeline
- *     wait of the tensor-core and row kernels (producer/consumer mbarrier
- *     waits).  A wait that runs out records PCP_ERR_TIMEOUT in *dev_err, and
- *     its CTA lets its in-flight copies and MMAs complete (those drain waits
- *     keep the 2 s limit), frees its tensor memory and exits; the other
- *     CTAs finish their work.  The results of such a call are undefined; the
- *     device, the stream and the library stay usable.  A tiny limit (a few
- *     ns) makes a call time out on purpose; tests use it to run that path.
+ *   test_stall_ns: 0, or a test of the kernels' timeout path: in every CTA
+ *     of the tensor-core and row kernels the call launches, one pipeline
+ *     wait (the tensor-core MMA issuer's first one; the row kernel's
+ *     consumers' first one) is made on an mbarrier that nothing arrives on,
+ *     with this limit instead of the default 2 s.  It runs out, as any wait
+ *     of the kernels does after 2 s when the GPU stops making progress:
+ *     PCP_ERR_TIMEOUT goes to *dev_err, the CTA's other warps give up their
+ *     waits, its in-flight copies and MMAs complete (those drain waits keep
+ *     the 2 s limit), its tensor memory is freed and it exits.  The call's
+ *     results are then undefined; the device, the stream and the library
+ *     stay usable.
  * The library keeps nothing of it after the call returns.
  */
 typedef struct pcp_call_options {
@@ -420,7 +423,7 @@ typedef struct pcp_call_options {
     void* tc_event_after;
     void* rows_event_before;
     void* rows_event_after;
-    uint64_t wait_limit_ns;
+    uint64_t test_stall_ns;
 } pcp_call_options;
 
 /*

@@ -32,10 +32,10 @@ class Status(enum.IntEnum):
 
 class CallOptions(ctypes.Structure):
     """``pcp_call_options``: per-call events around the tensor-core and row
-    kernels, and the limit of the kernels' pipeline waits."""
+    kernels, and the stall that tests the kernels' timeout path."""
     _fields_ = [("tc_event_before", ctypes.c_void_p), ("tc_event_after", ctypes.c_void_p),
                 ("rows_event_before", ctypes.c_void_p), ("rows_event_after", ctypes.c_void_p),
-                ("wait_limit_ns", ctypes.c_uint64)]
+                ("test_stall_ns", ctypes.c_uint64)]
 
 
 class PCPError(RuntimeError):
@@ -276,7 +276,7 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
                       dev_err: Optional[torch.Tensor] = None,
                       qo_indptr_host=None, causal: bool = True,
                       mask: Optional[torch.Tensor] = None,
-                      tc_events=None, rows_events=None, wait_limit_ns: int = 0,
+                      tc_events=None, rows_events=None, test_stall_ns: int = 0,
                       check: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
     """Extend attention of every query row over its cached prefix and own
     chunk (bottom-right causal, GQA, optional window).  Returns (out, lse):
@@ -291,7 +291,9 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
     position, applied on top of the causal rule.
     tc_events / rows_events: optional (before, after) torch.cuda.Event pairs
     recorded around the tensor-core / row kernel of this call.
-    wait_limit_ns: limit of the kernels' pipeline waits (0: the default)."""
+    test_stall_ns: 0, or the limit of a wait that nothing ends, made by every
+    CTA of the kernels the call launches (a test of their timeout path: the
+    call then reports PCP_ERR_TIMEOUT)."""
     dev = q.device
     _need(q, "q", torch.bfloat16, dev)
     _need(k_pool, "k_pool", torch.bfloat16, dev)
@@ -317,11 +319,11 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
     if own:
         dev_err = _dev_err(dev)
     host_ptr, host_keep = _host_i32(qo_indptr_host, batch + 1, "qo_indptr_host")
-    if tc_events is not None or rows_events is not None or wait_limit_ns:
+    if tc_events is not None or rows_events is not None or test_stall_ns:
         ev = lambda e: ctypes.c_void_p(e.cuda_event) if e is not None else ctypes.c_void_p(0)
         tb, ta = tc_events if tc_events is not None else (None, None)
         rb, ra = rows_events if rows_events is not None else (None, None)
-        opts = CallOptions(ev(tb), ev(ta), ev(rb), ev(ra), int(wait_limit_ns))
+        opts = CallOptions(ev(tb), ev(ta), ev(rb), ev(ra), int(test_stall_ns))
         mkeep, mptr, sb, sh, sq, mq, mkv = _mask_args(mask, batch, n_q_heads, dev)
         _check(lib().pcp_paged_extend_attn_ex(
             _ptr(q), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(prefix_lens),

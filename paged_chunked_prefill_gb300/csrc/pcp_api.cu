@@ -196,7 +196,6 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
 
     const float scale = a.sm_scale > 0.f ? a.sm_scale : 1.0f / std::sqrt((float)head_dim);
     const float scale_log2 = scale * 1.4426950408889634f;
-    const uint64_t wait_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : kSpinLimitNs;
     cudaStream_t s = static_cast<cudaStream_t>(a.stream);
     unsigned char* ws = static_cast<unsigned char*>(a.workspace);
     const int qpos = q_positions_per_tile(group);
@@ -266,7 +265,7 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     tp.causal = a.causal;
     tp.mask = a.mask;
     tp.scale_log2 = scale_log2;
-    tp.wait_ns = wait_ns;
+    tp.stall_ns = o.test_stall_ns;
     tp.dev_err = a.dev_err;
     cudaEvent_t evb = static_cast<cudaEvent_t>(o.tc_event_before);
     cudaEvent_t eva = static_cast<cudaEvent_t>(o.tc_event_after);
@@ -301,7 +300,7 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
         rp.causal = a.causal;
         rp.mask = a.mask;
         rp.scale_log2 = scale_log2;
-        rp.wait_ns = wait_ns;
+        rp.stall_ns = o.test_stall_ns;
         rp.dev_err = a.dev_err;
         cudaEvent_t erb = static_cast<cudaEvent_t>(o.rows_event_before);
         cudaEvent_t era = static_cast<cudaEvent_t>(o.rows_event_after);

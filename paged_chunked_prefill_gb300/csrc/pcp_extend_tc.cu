@@ -55,7 +55,7 @@ struct TcCfg {
     static constexpr uint32_t kOffV = kOffQ + kQTiles * kQBytes;
     static constexpr uint32_t kOffK = kOffV + kStagesV * kTileBytes;
     static constexpr uint32_t kOffBar = kOffK + kStagesK * kTileBytes;
-    static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 6 + 2;
+    static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 6 + 3;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;
     static_assert(kOffBar % 8 == 0 && kOffMisc % 4 == 0, "smem alignment");
@@ -72,6 +72,7 @@ struct TcCfg {
     static constexpr int bODone = bSFull + 4;
     static constexpr int bDrain = bSFull + 6;
     static constexpr int bGatherDrain = bSFull + 7;
+    static constexpr int bStall = bSFull + 8;  // nothing arrives on it (timeout test)
 };
 
 struct Geo {
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t sV = base + C::kOffV;
     const uint32_t sBar = base + C::kOffBar;
     volatile int* misc = reinterpret_cast<volatile int*>(gbase + C::kOffMisc);
-    // misc[0] TMEM base, misc[1] current item, misc[2] abort flag
+    // misc[0] TMEM base, misc[1] current item, misc[2] abort flag, misc[3] 0
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -325,8 +326,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mbar_init(bar(C::bDrain), 1);
         mbar_init(bar(C::bGatherDrain), 32u * kGatherWarps);
+        mbar_init(bar(C::bStall), 1);
         fence_mbarrier_init();
         misc[2] = 0;
+        misc[3] = 0;
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
@@ -396,7 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const int sk = cur % SK;
                         if (!__all_sync(0xffffffffu,
                                         mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u,
-                                                  abort_flag, p.dev_err, p.wait_ns)))
+                                                  abort_flag, p.dev_err, kSpinLimitNs)))
                             break;
                         tma_kv_tile<D>(p, geo, t, z_cur, &tm_k, p.k_pool,
                                        sK + sk * C::kTileBytes, bar(C::bKFull + sk), false, lane);
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const int sv = cur % SV;
                         if (!__all_sync(0xffffffffu,
                                         mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u,
-                                                  abort_flag, p.dev_err, p.wait_ns)))
+                                                  abort_flag, p.dev_err, kSpinLimitNs)))
                             break;
                         tma_kv_tile<D>(p, geo, t, z_cur, &tm_v, p.v_pool,
                                        sV + sv * C::kTileBytes, bar(C::bVFull + sv), true, lane);
@@ -455,13 +458,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     if (!__all_sync(0xffffffffu,
                                     mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u,
-                                              abort_flag, p.dev_err, p.wait_ns)))
+                                              abort_flag, p.dev_err, kSpinLimitNs)))
                         break;
                     gather_kv_rows<D>(p, geo, slot, p.k_pool, sK + sk * C::kTileBytes, gw, lane);
                     cp_async_mbar_arrive_noinc(bar(C::bKFull + sk));
                     if (!__all_sync(0xffffffffu,
                                     mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u,
-                                              abort_flag, p.dev_err, p.wait_ns)))
+                                              abort_flag, p.dev_err, kSpinLimitNs)))
                         break;
                     gather_kv_rows<D>(p, geo, slot, p.v_pool, sV + sv * C::kTileBytes, gw, lane);
                     cp_async_mbar_arrive_noinc(bar(C::bVFull + sv));
@@ -497,14 +500,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         umma_ts(d, a + kk * 8, b0 + (uint32_t)kk * (2048u >> 4), idesc_pv,
                                 (acc || kk > 0) ? 1u : 0u);
                 };
-                bool ok = mbar_wait(bar(C::bQFull), n_done & 1u, abort_flag, p.dev_err,
-                                    p.wait_ns);
+                // the timeout test: the CTA's first wait is one nothing ends
+                bool ok = p.stall_ns == 0 || n_done > 0 ||
+                          mbar_wait(bar(C::bStall), 0u, abort_flag, p.dev_err, p.stall_ns);
+                ok = ok && mbar_wait(bar(C::bQFull), n_done & 1u, abort_flag, p.dev_err,
+                                     kSpinLimitNs);
                 uint32_t aidx0 = act0, aidx1 = act1;
                 if (ok) {
                     tc_fence_after();
                     const uint32_t c0 = kv_iter;
                     ok = mbar_wait(bar(C::bKFull + c0 % SK), (c0 / SK) & 1u, abort_flag,
-                                   p.dev_err, p.wait_ns);
+                                   p.dev_err, kSpinLimitNs);
                     if (ok) {
                         if (p.box_rows == 0) fence_proxy_async_smem();
                         if (tile_active(geo, 0, geo.t_begin)) {
@@ -523,7 +529,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t cur = kv_iter + i;
                     const int st = cur % SV;
                     if (!mbar_wait(bar(C::bVFull + st), (cur / SV) & 1u, abort_flag, p.dev_err,
-                                   p.wait_ns)) {
+                                   kSpinLimitNs)) {
                         ok = false;
                         break;
                     }
@@ -540,7 +546,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     auto step_u = [&](const int u, uint32_t& ai, const int first_u) -> bool {
                         if (tile_active(geo, u, t)) {
                             if (!mbar_wait(bar(C::bPFull + u), ai & 1u, abort_flag, p.dev_err,
-                                           p.wait_ns))
+                                           kSpinLimitNs))
                                 return false;
                             tc_fence_after();
                             issue_pv(u, st, t != first_u);
@@ -550,7 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (has_next && tile_active(geo, u, t + 1)) {
                             if (!k_next) {
                                 if (!mbar_wait(bar(C::bKFull + nst), ((cur + 1) / SK) & 1u,
-                                               abort_flag, p.dev_err, p.wait_ns))
+                                               abort_flag, p.dev_err, kSpinLimitNs))
                                     return false;
                                 if (p.box_rows == 0) fence_proxy_async_smem();
                                 k_next = true;
@@ -594,7 +600,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // waits decide per warp (tcgen05.ld/st and the P arrival are
                     // warp-collective)
                     if (!__all_sync(0xffffffffu, mbar_wait(bar(C::bSFull + u), a & 1u, abort_flag,
-                                                           p.dev_err, p.wait_ns))) {
+                                                           p.dev_err, kSpinLimitNs))) {
                         ok = false;
                         break;
                     }
@@ -696,7 +702,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (t > first_u) {
                         if (!__all_sync(0xffffffffu,
                                         mbar_wait(bar(C::bODone + u), (a - 1u) & 1u, abort_flag,
-                                                  p.dev_err, p.wait_ns))) {
+                                                  p.dev_err, kSpinLimitNs))) {
                             tmem_st_wait();
                             ok = false;
                             break;
@@ -727,7 +733,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (ok) {
                     const uint32_t a_last = act_u + (uint32_t)(last_u - first_u);
                     ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bODone + u), a_last & 1u,
-                                                           abort_flag, p.dev_err, p.wait_ns));
+                                                           abort_flag, p.dev_err, kSpinLimitNs));
                 }
                 if (ok) {
                     tc_fence_after();
@@ -771,38 +777,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // no work left here: the next kernel on the stream may start launching
     pdl_launch_dependents();
     const bool aborted = *abort_flag != 0;
+    // drain waits are never cut short by the abort flag: they watch misc[3],
+    // which stays 0, and run to their own limit
+    volatile int* no_abort = &misc[3];
     if (warp == kWarpTma || warp >= kWarpGather0) {
         cp_async_wait_all();
         if (aborted && warp >= kWarpGather0) {
             // the mbarrier arrivals the gathers' cp.async copies trigger have
             // been made once this one, triggered after all of them, lands
             cp_async_mbar_arrive_noinc(bar(C::bGatherDrain));
-            volatile int dummy = 0;
             if (warp == kWarpGather0 && lane == 0)
-                mbar_wait(bar(C::bGatherDrain), 0u, &dummy, p.dev_err, kSpinLimitNs);
+                mbar_wait(bar(C::bGatherDrain), 0u, no_abort, p.dev_err, kSpinLimitNs);
             __syncwarp();
         }
         if (aborted && lane == 0) {
             // let every TMA load this warp issued land before the CTA exits
-            volatile int dummy = 0;
             if (warp == kWarpTma && n_done > 0)
-                mbar_wait(bar(C::bQFull), (n_done - 1) & 1u, &dummy, p.dev_err, kSpinLimitNs);
+                mbar_wait(bar(C::bQFull), (n_done - 1) & 1u, no_abort, p.dev_err, kSpinLimitNs);
             if (warp == kWarpTma)
                 for (int it = last_issued - SK + 1; it <= last_issued; ++it)
                     if (it >= 0)
-                        mbar_wait(bar(C::bKFull + it % SK), ((uint32_t)it / SK) & 1u, &dummy,
+                        mbar_wait(bar(C::bKFull + it % SK), ((uint32_t)it / SK) & 1u, no_abort,
                                   p.dev_err, kSpinLimitNs);
             if (warp == kWarpGather0)
                 for (int it = last_issued - SV + 1; it <= last_issued; ++it)
                     if (it >= 0)
-                        mbar_wait(bar(C::bVFull + it % SV), ((uint32_t)it / SV) & 1u, &dummy,
+                        mbar_wait(bar(C::bVFull + it % SV), ((uint32_t)it / SV) & 1u, no_abort,
                                   p.dev_err, kSpinLimitNs);
         }
     } else if (warp == kWarpMma && lane == 0) {
         // every MMA (and its mbarrier arrivals) completes before TMEM is freed
-        volatile int dummy = 0;
         umma_commit(bar(C::bDrain));
-        mbar_wait(bar(C::bDrain), 0u, &dummy, p.dev_err, kSpinLimitNs);
+        mbar_wait(bar(C::bDrain), 0u, no_abort, p.dev_err, kSpinLimitNs);
     }
     tc_fence_before();
     __syncthreads();

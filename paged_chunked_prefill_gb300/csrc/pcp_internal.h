@@ -185,7 +185,7 @@ struct TcParams {
     int causal;
     MaskParams mask;
     float scale_log2;  // sm_scale * log2(e)
-    uint64_t wait_ns;  // limit of the pipeline waits
+    uint64_t stall_ns; // test hook (0: off): see pcp_call_options.test_stall_ns
     int32_t* dev_err;
 };
 
@@ -227,7 +227,7 @@ struct RowParams {
     int causal;
     MaskParams mask;
     float scale_log2;
-    uint64_t wait_ns;  // limit of the pipeline waits
+    uint64_t stall_ns; // test hook (0: off): see pcp_call_options.test_stall_ns
     int32_t* dev_err;
 };
 

@@ -96,9 +96,10 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     float* m_s = reinterpret_cast<float*>(sm + C::kOffM);
     float* l_s = m_s + 4 * kRowMaxRows;
     int4* s_desc = reinterpret_cast<int4*>(sm + C::kOffDesc);  // published by mbarrier
-    __shared__ int s_abort;
+    __shared__ int s_abort, s_zero;
     // consumer warps' posts at their joint decision points
     __shared__ int s_post[4], s_fail[4];
+    __shared__ __align__(8) uint64_t s_stall;  // nothing arrives on it (timeout test)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
@@ -144,8 +145,10 @@ __global__ void __launch_bounds__(kRowThreads, 1)
             mbar_init(item_full(s), 33);  // 32 lanes' Q copies + the descriptor
             mbar_init(item_empty(s), 4);
         }
+        mbar_init(smem_addr(&s_stall), 1);
         fence_mbarrier_init();
         s_abort = 0;
+        s_zero = 0;
     }
     __syncthreads();
 
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
             }
             // hand the item (or the end marker) and its Q rows to the consumers
             if (!__all_sync(0xffffffffu, mbar_wait(item_empty(qs), ((uint32_t)(k / NI) & 1u) ^ 1u,
-                                                   abort_flag, p.dev_err, p.wait_ns)))
+                                                   abort_flag, p.dev_err, kSpinLimitNs)))
                 break;
             const int g = d0.y;
             if (valid) {
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 int nsl[4];
                 if (i + 1 < ntiles) fetch(pages, L, t + 1, nsl);
                 if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(st), ((itp / S) & 1u) ^ 1u,
-                                                       abort_flag, p.dev_err, p.wait_ns)))
+                                                       abort_flag, p.dev_err, kSpinLimitNs)))
                     break;
                 const uint32_t kd = sStage + st * 2 * C::kTileBytes;
                 const uint32_t vd = kd + C::kTileBytes;
@@ -335,14 +338,15 @@ __global__ void __launch_bounds__(kRowThreads, 1)
         cp_async_wait_all();
         if (*abort_flag && lane == 0) {
             // the copies of the last tiles and of the last item's Q rows (and
-            // the mbarrier arrivals they trigger) land before the CTA exits
-            volatile int dummy = 0;
+            // the mbarrier arrivals they trigger) land before the CTA exits;
+            // these waits watch s_zero, never raised, and run to their limit
+            volatile int* no_abort = &s_zero;
             for (int j = last_issued - S + 1; j <= last_issued; ++j)
                 if (j >= 0)
-                    mbar_wait(full_bar(j % S), ((uint32_t)j / S) & 1u, &dummy, p.dev_err,
+                    mbar_wait(full_bar(j % S), ((uint32_t)j / S) & 1u, no_abort, p.dev_err,
                               kSpinLimitNs);
             if (last_item >= 0)
-                mbar_wait(item_full(last_item % NI), ((uint32_t)(last_item / NI)) & 1u, &dummy,
+                mbar_wait(item_full(last_item % NI), ((uint32_t)(last_item / NI)) & 1u, no_abort,
                           p.dev_err, kSpinLimitNs);
         }
         return;
@@ -359,9 +363,14 @@ __global__ void __launch_bounds__(kRowThreads, 1)
         const int qs = k % NI;
         // 0: an item, 1: the end marker, 2: the wait gave up
         int post = 2;
+        // the timeout test: the consumers' first wait is one nothing ends
+        if (k == 0 && p.stall_ns != 0 &&
+            !__all_sync(0xffffffffu,
+                        mbar_wait(smem_addr(&s_stall), 0u, abort_flag, p.dev_err, p.stall_ns)))
+            failed = true;
         if (!failed &&
             __all_sync(0xffffffffu, mbar_wait(item_full(qs), (uint32_t)(k / NI) & 1u, abort_flag,
-                                              p.dev_err, p.wait_ns)))
+                                              p.dev_err, kSpinLimitNs)))
             post = s_desc[qs * 3 + 0].x < 0 ? 1 : 0;
         if (lane == 0) s_post[warp] = post;
         consumer_sync();
@@ -420,7 +429,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
             const uint32_t itp = it + i;
             const int st = itp % S;
             if (!__all_sync(0xffffffffu, mbar_wait(full_bar(st), (itp / S) & 1u, abort_flag,
-                                                   p.dev_err, p.wait_ns))) {
+                                                   p.dev_err, kSpinLimitNs))) {
                 failed = true;
                 break;
             }

@@ -1,13 +1,15 @@
 """The bounded waits of the tensor-core and row kernels, made to run out.
 
-Every producer/consumer wait of the two kernels gives up after a limit (2 s
-by default).  A wait that gives up records PCP_ERR_TIMEOUT in the error word,
-and its CTA lets the copies and MMAs it has in flight complete, frees its
-tensor memory and exits.  Here a call runs with a limit of one nanosecond,
-so its first wait that is not already satisfied gives up: the call must
-report PCP_ERR_TIMEOUT, and an ordinary call on the same stream right after
-it must match the FP64 oracle.  Nothing here faults or hangs a GPU: the
-waits that drain a giving-up CTA keep their 2 s limit.
+Every producer/consumer wait of the two kernels gives up after 2 s.  A wait
+that gives up records PCP_ERR_TIMEOUT in the error word, the CTA's other
+warps give up their waits, and the CTA lets the copies and MMAs it has in
+flight complete, frees its tensor memory and exits.  Here a call runs with the
+test stall of the per-call options: every CTA's first pipeline wait is made
+on an mbarrier that nothing arrives on, with a limit of 0.2 ms, while its
+load warps have copies in flight.  The call must report PCP_ERR_TIMEOUT, and
+an ordinary call on the same stream right after it must match the FP64
+oracle.  Nothing here faults or hangs a GPU: every wait has a limit, and the
+waits that drain a giving-up CTA keep theirs at 2 s.
 
 The cases cover the tensor-core kernel with TMA page boxes (page size 64)
 and with cp.async page gathers (page size 1), and the split-KV row kernel
@@ -31,13 +33,13 @@ def _append(batch, d):
     pcp.kv_append(d["k_new"], d["v_new"], loc, d["k_pool"], d["v_pool"])
 
 
-def _attend(batch, d, err, wait_limit_ns=0):
+def _attend(batch, d, err, test_stall_ns=0):
     import paged_chunked_prefill_gb300 as pcp
     return pcp.paged_extend_attn(d["q"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
                                  d["prefix_lens"], d["k_pool"], d["v_pool"], batch.page_size,
                                  batch.n_q_heads, batch.n_kv_heads, batch.head_dim,
                                  batch.window, batch.sm_scale, dev_err=err,
-                                 qo_indptr_host=batch.qo_indptr, wait_limit_ns=wait_limit_ns)
+                                 qo_indptr_host=batch.qo_indptr, test_stall_ns=test_stall_ns)
 
 
 CASES = {
@@ -59,7 +61,7 @@ def test_wait_timeout_is_reported_and_the_next_call_is_correct(case):
     d = to_device(batch)
     _append(batch, d)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    _attend(batch, d, err, wait_limit_ns=1)
+    _attend(batch, d, err, test_stall_ns=200_000)
     assert pcp.read_error(err) == pcp.Status.TIMEOUT
     # the same stream goes on: an ordinary call matches the oracle
     err.zero_()
