@@ -1,7 +1,8 @@
 """Benchmark of the paged chunked-prefill hot path on GB300.
 
-One step = slot mapping + KV append + paged extend attention (device work
-planning, the tensor-core kernel and the split-KV row kernel) over one batch
+One step = slot mapping and KV append (one fused kernel) + paged extend
+attention (device work planning, the tensor-core kernel and the split-KV row
+kernel) over one batch
 of the GQA chunked-prefill workload (Qwen3-8B-like attention: B=8, 32 query /
 8 KV heads, head_dim 128, page_size 16, chunk 512, prefix ~U[0, 8192],
 scattered pages), inputs resident in HBM.  The metric is effective TFLOP/s:
@@ -146,7 +147,7 @@ def launches_per_step(batch) -> int:
     G = batch.n_q_heads // batch.n_kv_heads
     rmax = 16 // G if G <= 16 else 0
     c = np.diff(batch.qo_indptr)
-    return 3 + int((c > rmax).any()) + 2 * int(((c > 0) & (c <= rmax)).any())
+    return 2 + int((c > rmax).any()) + 2 * int(((c > 0) & (c <= rmax)).any())
 
 
 def load_peaks():
@@ -371,16 +372,14 @@ def main():
                                         batch.n_kv_heads, batch.head_dim),
                      dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    loc = torch.empty(batch.total_q, dtype=torch.int64, device=dev)
     out = torch.empty_like(d["q"])
     lse = torch.empty(batch.total_q, batch.n_q_heads, dtype=torch.float32, device=dev)
     flush = L2Flush(torch, dev)
 
     def step(tc_events=None):
-        pcp.compute_out_cache_loc(d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
-                                  d["prefix_lens"], batch.page_size, batch.num_pages,
-                                  total_q=batch.total_q, out=loc, dev_err=err)
-        pcp.kv_append(d["k_new"], d["v_new"], loc, d["k_pool"], d["v_pool"], dev_err=err)
+        pcp.kv_append_paged(d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["prefix_lens"],
+                            batch.page_size, d["k_new"], d["v_new"], d["k_pool"], d["v_pool"],
+                            dev_err=err)
         pcp.paged_extend_attn(d["q"], d["qo_indptr"], d["kv_indptr"],
                               d["kv_indices"], d["prefix_lens"], d["k_pool"], d["v_pool"],
                               batch.page_size, batch.n_q_heads, batch.n_kv_heads,
@@ -458,9 +457,9 @@ def main():
         "config": config_dict(batch, world),
         "roofline": roofline,
         "e2e": e2e,
-        # out_cache_loc, kv_append, plan, then the tensor-core kernel and/or the
-        # row kernel + combine (the host copy of qo_indptr skips a kernel
-        # without work), in each of the two timed loops
+        # the fused slot mapping + append, plan, then the tensor-core kernel
+        # and/or the row kernel + combine (the host copy of qo_indptr skips a
+        # kernel without work), in each of the two timed loops
         "gpu_launches": 2 * args.steps * launches_per_step(batch),
         "clocks": clocks.summary(),
     }
@@ -534,7 +533,6 @@ def end_to_end(args, torch, pcp, batch, d, out_ref, flush, stream, flops, world)
         S["h_out"], S["h_lse"] = views(S["h_res"], out_offs, out_like)
         S["k_pool"] = d["k_pool"].clone()
         S["v_pool"] = d["v_pool"].clone()
-        S["loc"] = torch.empty(batch.total_q, dtype=torch.int64, device=dev)
         S["ws"] = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         sets.append(S)
     d2h = out_bytes
@@ -543,10 +541,9 @@ def end_to_end(args, torch, pcp, batch, d, out_ref, flush, stream, flops, world)
         S["in"].copy_(h_in, non_blocking=True)
 
     def kernels(S):
-        pcp.compute_out_cache_loc(S["qo_indptr"], S["kv_indptr"], S["kv_indices"],
-                                  S["prefix_lens"], batch.page_size, batch.num_pages,
-                                  total_q=batch.total_q, out=S["loc"], dev_err=err)
-        pcp.kv_append(S["k_new"], S["v_new"], S["loc"], S["k_pool"], S["v_pool"], dev_err=err)
+        pcp.kv_append_paged(S["qo_indptr"], S["kv_indptr"], S["kv_indices"], S["prefix_lens"],
+                            batch.page_size, S["k_new"], S["v_new"], S["k_pool"], S["v_pool"],
+                            dev_err=err)
         pcp.paged_extend_attn(S["q"], S["qo_indptr"], S["kv_indptr"], S["kv_indices"],
                               S["prefix_lens"], S["k_pool"], S["v_pool"], batch.page_size,
                               batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.window,
@@ -689,19 +686,30 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
                                      traffic=ncu_traffic("decode_rows",
                                                          f"row_attn_kernel<{db.head_dim}>"))
 
-    # the KV append of the GQA chunk (4096 tokens) and of the long-context chunk
+    # the KV append of the GQA chunk (4096 tokens) and of the long-context
+    # chunk (32768 tokens): the fused slot mapping + append the step runs, and
+    # the append alone from a precomputed out_cache_loc
     for key, b in (("kv_append", W.gqa_prefill()), ("kv_append_long", W.long_context())):
         g = to_device(b, dev)
         loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
                                         g["prefix_lens"], b.page_size, b.num_pages)
+        kv_bytes = 2 * 2 * b.total_q * b.n_kv_heads * b.head_dim * 2
+        what = f"{b.total_q} tokens x {b.n_kv_heads} KV heads x D {b.head_dim}"
+        ms = time_calls(torch, lambda ev: pcp.kv_append_paged(
+            g["qo_indptr"], g["kv_indptr"], g["kv_indices"], g["prefix_lens"], b.page_size,
+            g["k_new"], g["v_new"], g["k_pool"], g["v_pool"], dev_err=err), flush)
+        gbs = kv_bytes / (ms * 1e-3) / 1e9
+        res[key] = {"workload": what, "ms": ms, "GB/s": gbs,
+                    "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": kv_bytes,
+                    "what": "pcp_kv_append_paged: slot mapping and append in one kernel"}
         ms = time_calls(torch, lambda ev: pcp.kv_append(g["k_new"], g["v_new"], loc,
                                                         g["k_pool"], g["v_pool"], dev_err=err),
                         flush)
-        nbytes = 2 * 2 * b.total_q * b.n_kv_heads * b.head_dim * 2 + 8 * b.total_q
+        nbytes = kv_bytes + 8 * b.total_q
         gbs = nbytes / (ms * 1e-3) / 1e9
-        res[key] = {"workload": f"{b.total_q} tokens x {b.n_kv_heads} KV heads x D "
-                                f"{b.head_dim}", "ms": ms, "GB/s": gbs,
-                    "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes}
+        res[key + "_from_loc"] = {"workload": what, "ms": ms, "GB/s": gbs,
+                                  "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes,
+                                  "what": "pcp_kv_append from a precomputed out_cache_loc"}
         del g, loc
 
     # the long-context batch, the mixed scheduler batch (prompt chunks on the

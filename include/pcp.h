@@ -129,6 +129,30 @@ pcp_status pcp_kv_append(const void* k, const void* v, const int64_t* out_cache_
                          void* v_pool, int64_t pool_slots, int32_t* dev_err, void* stream);
 
 /*
+ * Slot mapping and KV append in one kernel (integer and copy, bit-exact):
+ * for every new token t of sequence b (qo_indptr[b] <= t < qo_indptr[b+1]),
+ * its slot s = kv_indices[kv_indptr[b] + p / page_size] * page_size
+ * + p % page_size with p = prefix_lens[b] + (t - qo_indptr[b]) (as
+ * pcp_compute_out_cache_loc), then k_pool[s] = k[t] and v_pool[s] = v[t] (as
+ * pcp_kv_append).  The same two steps of a serving step (AReno PR #642,
+ * "What does this PR do?", third bullet: prefill continues inside the last
+ * allocated page; AstrAI CudaBackend.fwd_prefill, the k_buffer write at
+ * out_cache_loc) without the round trip through an out_cache_loc array.
+ * k, v: [total_q, n_kv_heads, head_dim] bf16; the pools hold num_pages *
+ * page_size slots.  out_cache_loc: NULL, or device int64 [total_q] that
+ * receives the slots (-1 for a token whose page id is bad).  A page id
+ * outside [0, num_pages) sets *dev_err = PCP_ERR_BAD_INDEX and that token is
+ * not written.  head_dim * 2 bytes must be a multiple of 16; k, v and the
+ * pools must be 16-byte aligned.
+ */
+pcp_status pcp_kv_append_paged(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                               const int32_t* kv_indices, const int32_t* prefix_lens, int batch,
+                               int64_t total_q, int page_size, int64_t num_pages, const void* k,
+                               const void* v, int n_kv_heads, int head_dim, void* k_pool,
+                               void* v_pool, int64_t* out_cache_loc, int32_t* dev_err,
+                               void* stream);
+
+/*
  * Bytes of device workspace pcp_paged_extend_attn needs for a call with at
  * most `batch` sequences and `total_q` query rows (work lists, split-KV
  * partials and counters).  Pure host arithmetic; 0 for an unsupported shape.
@@ -160,7 +184,12 @@ size_t pcp_extend_workspace_size(int batch, int64_t total_q, int n_q_heads, int 
  * anything is launched.  Results are bit-identical with and without it.
  *
  * The K/V of the chunk itself must already be in the pool (pcp_kv_append
- * first, as a serving step does).  Supported: head_dim in {64, 128},
+ * first, as a serving step does).  The call starts reading qo_indptr,
+ * kv_indptr and prefix_lens while the kernel before it on the stream is
+ * still running (a programmatic dependent launch): a kernel of the caller's
+ * that writes them right before this call must not trigger programmatic
+ * dependents before those writes (a kernel that does not use that feature
+ * is always fine).  Supported: head_dim in {64, 128},
  * n_q_heads % n_kv_heads == 0, n_q_heads / n_kv_heads <= 128, page_size >= 1,
  * window >= 0, num_pages * page_size < 2^31.  q, out, the pools and the
  * workspace must be 16-byte aligned (256-byte aligned workspace).

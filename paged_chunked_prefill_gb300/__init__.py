@@ -11,6 +11,7 @@ Functions (same names as the C entry points, without the ``pcp_`` prefix):
 
 * ``compute_out_cache_loc`` -- slots of a step's new tokens (int64)
 * ``kv_append``             -- scatter the chunk's K/V into the page pools
+* ``kv_append_paged``       -- slot mapping and KV append in one kernel
 * ``copy_page_slots``       -- copy-on-write of shared pages
 * ``paged_extend_attn``     -- extend attention, returns ``(out, lse)``
 * ``workspace_size``        -- bytes of scratch a call needs
@@ -23,6 +24,7 @@ from ._binding import (  # noqa: F401
     compute_out_cache_loc,
     copy_page_slots,
     kv_append,
+    kv_append_paged,
     lib,
     library_path,
     paged_extend_attn,
@@ -32,5 +34,5 @@ from ._binding import (  # noqa: F401
 
 __all__ = [
     "Pager", "PCPError", "Status", "compute_out_cache_loc", "copy_page_slots", "kv_append",
-    "lib", "library_path", "paged_extend_attn", "read_error", "workspace_size",
+    "kv_append_paged", "lib", "library_path", "paged_extend_attn", "read_error", "workspace_size",
 ]

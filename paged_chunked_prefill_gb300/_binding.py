@@ -71,6 +71,9 @@ def lib():
         L.pcp_compute_out_cache_loc.restype = i32
         L.pcp_kv_append.argtypes = [P, P, P, i64, i32, i32, P, P, i64, P, P]
         L.pcp_kv_append.restype = i32
+        L.pcp_kv_append_paged.argtypes = [P, P, P, P, i32, i64, i32, i64, P, P, i32, i32, P, P,
+                                          P, P, P]
+        L.pcp_kv_append_paged.restype = i32
         L.pcp_extend_workspace_size.argtypes = [i32, i64, i32, i32, i32]
         L.pcp_extend_workspace_size.restype = sz
         L.pcp_paged_extend_attn.argtypes = [P, P, P, P, P, P, i32, i64, P, P, i64, i32, i32,
@@ -241,6 +244,38 @@ def kv_append(k: torch.Tensor, v: torch.Tensor, out_cache_loc: torch.Tensor,
                                k.shape[2], _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
                                _ptr(dev_err), _stream(dev)), "pcp_kv_append")
     _finish(dev_err, own, check, "pcp_kv_append")
+
+
+def kv_append_paged(qo_indptr: torch.Tensor, kv_indptr: torch.Tensor,
+                    kv_indices: torch.Tensor, prefix_lens: torch.Tensor, page_size: int,
+                    k: torch.Tensor, v: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                    out_cache_loc: Optional[torch.Tensor] = None,
+                    dev_err: Optional[torch.Tensor] = None, check: bool = True) -> None:
+    """Slot mapping and KV append in one kernel: each new token's slot from
+    the page table, then k_pool[slot] = k[t], v_pool[slot] = v[t] (in place).
+    out_cache_loc (int64 [total_q], optional) receives the slots."""
+    dev = k.device
+    for n, t in (("k", k), ("v", v), ("k_pool", k_pool), ("v_pool", v_pool)):
+        _need(t, n, torch.bfloat16, dev)
+    for n, t in (("qo_indptr", qo_indptr), ("kv_indptr", kv_indptr),
+                 ("kv_indices", kv_indices), ("prefix_lens", prefix_lens)):
+        _need(t, n, torch.int32, dev)
+    if out_cache_loc is not None:
+        _need(out_cache_loc, "out_cache_loc", torch.int64, dev)
+    if k.dim() != 3 or v.shape != k.shape or k_pool.shape != v_pool.shape:
+        raise ValueError("k, v must be [n, Hkv, D] and the pools [slots, Hkv, D]")
+    if tuple(k_pool.shape[1:]) != tuple(k.shape[1:]) or k_pool.shape[0] % page_size:
+        raise ValueError("pool rows must match k rows and hold whole pages")
+    own = dev_err is None
+    if own:
+        dev_err = _dev_err(dev)
+    _check(lib().pcp_kv_append_paged(_ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices),
+                                     _ptr(prefix_lens), qo_indptr.numel() - 1, k.shape[0],
+                                     page_size, k_pool.shape[0] // page_size, _ptr(k), _ptr(v),
+                                     k.shape[1], k.shape[2], _ptr(k_pool), _ptr(v_pool),
+                                     _ptr(out_cache_loc), _ptr(dev_err), _stream(dev)),
+           "pcp_kv_append_paged")
+    _finish(dev_err, own, check, "pcp_kv_append_paged")
 
 
 def _mask_args(mask: Optional[torch.Tensor], batch: int, n_q_heads: int, device):

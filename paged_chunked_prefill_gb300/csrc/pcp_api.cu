@@ -34,6 +34,12 @@ cudaError_t launch_copy_page_slots(const int32_t* src, const int32_t* dst,
                                    const int32_t* n_slots, int n_copies, int64_t num_pages,
                                    int page_size, int chunks_per_slot, void* k_pool,
                                    void* v_pool, int32_t* dev_err, cudaStream_t stream);
+cudaError_t launch_kv_append_paged(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                   const int32_t* kv_indices, const int32_t* prefix_lens,
+                                   int batch, int64_t total_q, int page_size, int64_t num_pages,
+                                   const void* k, const void* v, int chunks_per_token,
+                                   void* k_pool, void* v_pool, int64_t* loc, int32_t* dev_err,
+                                   int sm_count, cudaStream_t stream);
 cudaError_t launch_kv_append(const void* k, const void* v, const int64_t* loc, int64_t n_tokens,
                              int chunks_per_token, void* k_pool, void* v_pool, int64_t pool_slots,
                              int32_t* dev_err, int sm_count, cudaStream_t stream);
@@ -221,6 +227,10 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
         PCP_OK)
         return st;
 
+    // A decode-only call of at most kRowSelfPlanMaxSeqs sequences is planned
+    // by the row kernel itself; everything else by the planner kernel.
+    const bool self_plan = !run_tc && run_rows && a.batch <= kRowSelfPlanMaxSeqs;
+
     // ---- 1. plan
     PlanParams pp;
     pp.qo_indptr = a.qo_indptr;
@@ -238,7 +248,7 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     pp.ws = ws;
     pp.lay = lay;
     pp.dev_err = a.dev_err;
-    if (failed(launch_plan(s, pp))) return PCP_ERR_CUDA;
+    if (!self_plan && failed(launch_plan(s, pp))) return PCP_ERR_CUDA;
 
     // ---- 2. tensor-core extend kernel (persistent, one CTA per SM)
     TcParams tp;
@@ -276,6 +286,9 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     // ---- 3. decode-shaped rows (split-KV on CUDA cores, equal tiles per CTA)
     if (run_rows) {
         RowParams rp;
+        rp.self_plan = self_plan ? 1 : 0;
+        rp.batch = a.batch;
+        rp.total_q = a.total_q;
         rp.q = static_cast<const uint16_t*>(a.q);
         rp.qo_indptr = a.qo_indptr;
         rp.kv_indptr = a.kv_indptr;
@@ -383,6 +396,34 @@ pcp_status pcp_kv_append(const void* k, const void* v, const int64_t* out_cache_
     const int chunks = n_kv_heads * head_dim * 2 / 16;
     cudaError_t e = launch_kv_append(k, v, out_cache_loc, n_tokens, chunks, k_pool, v_pool,
                                      pool_slots, dev_err, sms, static_cast<cudaStream_t>(stream));
+    return failed(e) ? PCP_ERR_CUDA : PCP_OK;
+}
+
+pcp_status pcp_kv_append_paged(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                               const int32_t* kv_indices, const int32_t* prefix_lens, int batch,
+                               int64_t total_q, int page_size, int64_t num_pages, const void* k,
+                               const void* v, int n_kv_heads, int head_dim, void* k_pool,
+                               void* v_pool, int64_t* out_cache_loc, int32_t* dev_err,
+                               void* stream) {
+    if (batch < 0 || total_q < 0 || page_size < 1 || num_pages < 0 || n_kv_heads < 1 ||
+        head_dim < 1 || dev_err == nullptr)
+        return PCP_ERR_INVALID_ARG;
+    if ((head_dim * 2) % 16 != 0) return PCP_ERR_UNSUPPORTED;
+    if (batch == 0 && total_q != 0) return PCP_ERR_INVALID_ARG;
+    if (total_q == 0) return PCP_OK;
+    if (!qo_indptr || !kv_indptr || !kv_indices || !prefix_lens || !k || !v || !k_pool ||
+        !v_pool)
+        return PCP_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16))
+        return PCP_ERR_INVALID_ARG;
+    int sms = 0;
+    pcp_status st = sm_count(&sms);
+    if (st != PCP_OK) return st;
+    const int chunks = n_kv_heads * head_dim * 2 / 16;
+    cudaError_t e = launch_kv_append_paged(qo_indptr, kv_indptr, kv_indices, prefix_lens, batch,
+                                           total_q, page_size, num_pages, k, v, chunks, k_pool,
+                                           v_pool, out_cache_loc, dev_err, sms,
+                                           static_cast<cudaStream_t>(stream));
     return failed(e) ? PCP_ERR_CUDA : PCP_OK;
 }
 

@@ -32,9 +32,13 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 // Every kernel of the library is launched as a programmatic dependent of the
 // kernel before it on the stream, so its launch and prologue may overlap the
 // end of that kernel.  pdl_wait() returns once the previous kernel has
-// completed and its memory is visible; every kernel calls it on every path
-// before its first global memory access, which keeps the ordering transitive
-// along the whole stream.  Without the launch attribute both are no-ops.
+// completed and its memory is visible.  Every kernel calls it on every path
+// before it completes, so a kernel past its pdl_wait() knows that everything
+// before it on the stream has completed.  Each kernel calls it before it
+// writes global memory and before it reads anything but the call's metadata
+// (qo_indptr, kv_indptr, prefix_lens: inputs of the call, not outputs of the
+// kernels before it); only the planner reads those before its wait.  Without
+// the launch attribute both are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -28,6 +28,10 @@ constexpr int kRowMaxRows = 16;   // query rows (positions x heads) per row item
 constexpr int kRowTile = 128;     // keys per row-kernel tile
 constexpr int kRowThreads = 160;      // 4 consumer warps + 1 load warp
 constexpr int kRowMaxCtas = 512;       // row-kernel CTAs at most (one per SM below that)
+// A call whose chunks are all decode-shaped (known from the host copy of
+// qo_indptr) and that has at most this many sequences is planned inside the
+// row kernel: every CTA builds the split in shared memory, no planner launch.
+constexpr int kRowSelfPlanMaxSeqs = 512;
 
 // Default limit of the kernels' bounded pipeline waits, and the fixed limit of
 // the waits that drain a CTA's in-flight copies and MMAs before it exits
@@ -203,6 +207,9 @@ struct CombineParams {
 
 // ---- parameters of the row (split-KV) kernel
 struct RowParams {
+    int self_plan;     // 1: plan in the kernel (batch <= kRowSelfPlanMaxSeqs, no planner run)
+    int batch;
+    int64_t total_q;
     const uint16_t* q;
     const int32_t* qo_indptr;
     const int32_t* kv_indptr;

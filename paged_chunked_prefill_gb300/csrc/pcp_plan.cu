@@ -8,7 +8,13 @@
 //    kQTiles * (128 / G) positions of one chunk for one KV head (all G query
 //    heads of that KV head packed into the MMA rows).  Items are ordered by
 //    cost (number of KV tiles) descending -- longest-processing-time first
-//    for the persistent kernel's dynamic scheduler -- with a counting sort.
+//    for the persistent kernel's dynamic scheduler -- with a counting sort
+//    over cost buckets (exact below 64 tiles, 16 tiles wide above).  Inside
+//    a bucket every warp places the items of one (sequence, KV head) next to
+//    each other, so the CTAs running at the same time stream few sequences'
+//    K/V and each tile is read from DRAM about once (with one item per
+//    bucket slot in any order, a long prefix is re-read by every item from
+//    DRAM once the groups' K/V together exceed the L2).
 //  * row groups for decode-shaped chunks (chunk_len * G <= 16 rows), one per
 //    (sequence, KV head): their 128-key tiles are laid end to end and the
 //    row kernel's CTA i of n takes tiles [i*T/n, (i+1)*T/n), so every SM
@@ -47,6 +53,12 @@ __device__ __forceinline__ SeqInfo seq_info(const PlanParams& p, int b) {
 // First visible key of absolute position `pos`.
 __device__ __forceinline__ int first_key(int pos, int window) {
     return window > 0 ? max(0, pos - window + 1) : 0;
+}
+
+// Bucket of a tensor-core item's cost in the longest-first counting sort:
+// the cost itself below 64 KV tiles, 16-tile buckets above.
+__device__ __forceinline__ int cost_bucket(int cost) {
+    return cost < 64 ? cost : min(1023, 64 + ((cost - 64) >> 4));
 }
 
 // KV tiles of tensor-core item k of a chunk: up to the item's last row
@@ -172,13 +184,16 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     const int H = p.n_kv_heads;
     const int n_ctas = row_grid(p.sm_count);
 
-    pdl_wait();
+    // The call's metadata are not the previous kernel's output, so they are
+    // read and the tensor-core histogram built while that kernel finishes;
+    // the wait for it comes before the first write to global memory (the
+    // workspace may still be read by the previous call's kernels).
     pdl_launch_dependents();
     hist[tid] = 0;
-    for (int64_t i = tid; i < (int64_t)p.batch * H; i += 1024) gdesc[i] = make_int4(0, 0, 0, 0);
     if (tid == 0) s_row_tiles = 0;
+    bool bad_meta = false;  // this thread saw contradictory metadata
 
-    // metadata of sequence chunk0 + tid (kept in s_seq); reports bad sequences once
+    // metadata of sequence chunk0 + tid (kept in s_seq); notes bad sequences
     auto load_chunk = [&](int chunk0, bool report) {
         const int b = chunk0 + tid;
         int4 v = make_int4(0, 0, 0, 0);
@@ -188,7 +203,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
             off = make_int2(q.q0, q.kvb);
             // qo_indptr[batch] must be total_q (the last sequence's end)
             if (report && (!q.ok || (b == p.batch - 1 && q.q0 + q.c != p.total_q)))
-                report_error(p.dev_err, PCP_ERR_INVALID_ARG);
+                bad_meta = true;
             const int tiles = (q.ok && q.c > 0 && q.c <= rmax)
                                   ? (q.L - 1) / kRowTile - first_key(q.P, p.window) / kRowTile + 1
                                   : 0;
@@ -218,14 +233,19 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
                 const int sl = segment_of(s_a, 1024, f);
                 const int4 v = s_seq[sl];
                 const int cost = tc_cost(v.y, v.x, f - s_a[sl], item_pos, p.window, p.causal);
-                warp_agg_add(hist, min(cost, 1023), H);
+                warp_agg_add(hist, cost_bucket(cost), H);
             }
         }
     }
     __syncthreads();
     const int n_tc = p.tc_work ? desc_offsets(hist, warp_sums) : 0;
     const unsigned long long row_tiles_all = s_row_tiles;
+
+    // ---- from here on global memory is written: the previous kernel is done
+    pdl_wait();
+    if (bad_meta) report_error(p.dev_err, PCP_ERR_INVALID_ARG);
     if (tid == 0 && row_tiles_all >= (1ull << 31)) report_error(p.dev_err, PCP_ERR_UNSUPPORTED);
+    for (int64_t i = tid; i < (int64_t)p.batch * H; i += 1024) gdesc[i] = make_int4(0, 0, 0, 0);
     const int T = (int)min(row_tiles_all, (unsigned long long)INT32_MAX);
     // the split uses min(n, T) CTAs, so every one of them holds at least one
     // tile and every partial slot of a group is written
@@ -241,7 +261,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     for (int chunk0 = 0; chunk0 < p.batch; chunk0 += 1024) {
         __syncthreads();
         if (!one_chunk) load_chunk(chunk0, false);
-        s_a[tid] = n_tc_of(s_seq[tid]);
+        s_a[tid] = n_tc_of(s_seq[tid]) * H;  // items flattened as (sequence, KV head, item)
         s_b[tid] = s_seq[tid].w > 0 ? H : 0;
         s_c[tid] = s_seq[tid].w;
         __syncthreads();
@@ -251,16 +271,17 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
         for (int f = tid; f < total_a; f += 1024) {
             const int sl = segment_of(s_a, 1024, f);
             const int4 v = s_seq[sl];
-            const int k = f - s_a[sl];
+            const int n = n_tc_of(v);
+            const int g = (f - s_a[sl]) / n;
+            const int k = (f - s_a[sl]) - g * n;
             const int cost = tc_cost(v.y, v.x, k, item_pos, p.window, p.causal);
-            const int slot = warp_agg_add(hist, min(cost, 1023), H);
-            for (int g = 0; g < H; ++g) {
-                if (slot + g >= p.lay.cap_tc) {
-                    report_error(p.dev_err, PCP_ERR_WORKSPACE);
-                    break;
-                }
-                tc[slot + g] = make_int4(chunk0 + sl, g, k * item_pos, cost);
+            // lanes with one bucket get consecutive slots in lane order
+            const int slot = warp_agg_add(hist, cost_bucket(cost), 1);
+            if (slot >= p.lay.cap_tc) {
+                report_error(p.dev_err, PCP_ERR_WORKSPACE);
+                continue;
             }
+            tc[slot] = make_int4(chunk0 + sl, g, k * item_pos, cost);
         }
         for (int f = tid; f < total_b; f += 1024) {
             const int sl = segment_of(s_b, 1024, f);

@@ -100,10 +100,86 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     // consumer warps' posts at their joint decision points
     __shared__ int s_post[4], s_fail[4];
     __shared__ __align__(8) uint64_t s_stall;  // nothing arrives on it (timeout test)
+    // self-planned calls: per sequence {chunk_len, prefix_len, kv_indptr[b],
+    // qo_indptr[b]}, and exclusive prefix sums over the sequences of their
+    // row tiles and of their row-group counts (1 for a decode-shaped chunk)
+    __shared__ int4 s_sp_seq[kRowSelfPlanMaxSeqs];
+    __shared__ int s_sp_ts[kRowSelfPlanMaxSeqs + 1], s_sp_gs[kRowSelfPlanMaxSeqs + 1];
+    __shared__ long long s_sp_wsum[2][kRowThreads / 32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
-    pdl_wait();  // the work list is the planner's output
+    const int H = p.n_kv_heads;
+    const int rmax = row_path_max_chunk(p.group);
+    // ---- self-planned call: the split of the row tiles, from the metadata
+    // alone (read before the wait below; they are inputs of the call)
+    long long sp_total = 0;  // row tiles of one KV head, all sequences
+    bool sp_bad = false;     // this thread saw contradictory metadata
+    if (p.self_plan) {
+        // thread i takes sequences 4i .. 4i + 3
+        long long t_run = 0, g_run = 0;
+        int tl[4], rw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b = 4 * tid + j;
+            tl[j] = rw[j] = 0;
+            if (b < p.batch) {
+                const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
+                const int kvb = p.kv_indptr[b], pages = p.kv_indptr[b + 1] - kvb;
+                const int P = p.prefix_lens[b], c = q1 - q0;
+                const bool ok = q0 >= 0 && c >= 0 && q1 <= p.total_q && P >= 0 && pages >= 0 &&
+                                (int64_t)pages * p.page_size >= (int64_t)P + c;
+                sp_bad = sp_bad || !ok || (b == p.batch - 1 && q1 != p.total_q);
+                if (ok && c > 0 && c <= rmax) {
+                    const int lo = p.window > 0 ? max(0, P - p.window + 1) : 0;
+                    tl[j] = (P + c - 1) / kRowTile - lo / kRowTile + 1;
+                    rw[j] = 1;
+                }
+                s_sp_seq[b] = make_int4(c, P, kvb, q0);
+            }
+            t_run += tl[j];
+            g_run += rw[j];
+        }
+        // exclusive scans over the threads: warp shuffles, then the warps
+        long long ti = t_run, gi = g_run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long a = __shfl_up_sync(0xffffffffu, ti, o);
+            const long long c = __shfl_up_sync(0xffffffffu, gi, o);
+            if (lane >= o) {
+                ti += a;
+                gi += c;
+            }
+        }
+        if (lane == 31) {
+            s_sp_wsum[0][warp] = ti;
+            s_sp_wsum[1][warp] = gi;
+        }
+        __syncthreads();
+        long long tb = 0, gb = 0;
+        for (int w = 0; w < kRowThreads / 32; ++w) {
+            if (w < warp) {
+                tb += s_sp_wsum[0][w];
+                gb += s_sp_wsum[1][w];
+            }
+            sp_total += s_sp_wsum[0][w];
+        }
+        tb += ti - t_run;
+        gb += gi - g_run;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b = 4 * tid + j;
+            if (b <= p.batch) {  // entry `batch` holds the totals
+                s_sp_ts[b] = (int)min(tb, (long long)INT32_MAX);
+                s_sp_gs[b] = (int)gb;
+            }
+            tb += tl[j];
+            gb += rw[j];
+        }
+        __syncthreads();
+    }
+    pdl_wait();  // the work list is the planner's output (or, self-planned,
+                 // the workspace may still be read by the kernel before)
     pdl_launch_dependents();
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(p.ws + p.lay.header);
     const int4* rg = reinterpret_cast<const int4*>(p.ws + p.lay.row_groups);
@@ -126,12 +202,45 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     // laid end to end: the same amount of K/V for every CTA.  Each row group
     // it meets (from row_first[blockIdx.x] on) is one item; the load warp
     // resolves the next item and reads its first page ids during this one.
-    const int T = hdr->row_tiles;
-    if (hdr->row_ctas != (int)gridDim.x) {  // the plan was made for another grid
-        if (tid == 0 && T > 0) report_error(p.dev_err, PCP_ERR_INVALID_ARG);
-        return;
+    int T;
+    if (p.self_plan) {
+        if (sp_bad) report_error(p.dev_err, PCP_ERR_INVALID_ARG);
+        if (sp_total * H >= (1ll << 31)) {
+            if (tid == 0 && blockIdx.x == 0) report_error(p.dev_err, PCP_ERR_UNSUPPORTED);
+            return;
+        }
+        T = (int)(sp_total * H);
+    } else {
+        T = hdr->row_tiles;
+        if (hdr->row_ctas != (int)gridDim.x) {  // the plan was made for another grid
+            if (tid == 0 && T > 0) report_error(p.dev_err, PCP_ERR_INVALID_ARG);
+            return;
+        }
     }
     const int n_use = row_ctas_used(gridDim.x, T);
+    // the row-kernel CTA holding tile x: the last i with i*T/n_use <= x
+    auto cta_of = [&](int x) { return (int)((((int64_t)x + 1) * n_use + T - 1) / T) - 1; };
+    if (p.self_plan) {
+        // the combine kernel's descriptor of every (sequence, KV head) group,
+        // {first partial slot, splits, qo_indptr[b], chunk_len}, zeros for a
+        // sequence without decode-shaped rows: the entries are spread over
+        // all CTAs of the grid
+        int4* gdesc = reinterpret_cast<int4*>(p.ws + p.lay.group_desc);
+        for (int64_t e = (int64_t)blockIdx.x * kRowThreads + tid; e < (int64_t)p.batch * H;
+             e += (int64_t)gridDim.x * kRowThreads) {
+            const int b = (int)(e / H), g = (int)(e - (int64_t)b * H);
+            const int tiles = s_sp_ts[b + 1] - s_sp_ts[b];
+            int4 gd = make_int4(0, 0, 0, 0);
+            if (tiles > 0) {
+                const int4 sq = s_sp_seq[b];
+                const int k = H * s_sp_gs[b] + g;
+                const int S0 = H * s_sp_ts[b] + g * tiles;
+                const int i0 = cta_of(S0), i1 = cta_of(S0 + tiles - 1);
+                gd = make_int4(k + i0, i1 - i0 + 1, sq.w, sq.x);
+            }
+            gdesc[e] = gd;
+        }
+    }
     if ((int)blockIdx.x >= n_use) return;
     const int x0 = row_tile_begin(blockIdx.x, n_use, T);
     const int x1 = row_tile_begin(blockIdx.x + 1, n_use, T);
@@ -195,6 +304,46 @@ __global__ void __launch_bounds__(kRowThreads, 1)
         // row item {b, g, split, n_splits}, {kv_begin, kv_end, first partial
         // slot, q0}, {chunk_len, prefix_len, kv_indptr[b], kv_len}; its split
         // index is blockIdx.x - (first CTA of the group) = blockIdx.x + kg - slot
+        // row group kg's descriptor (planner layout): {b, g, S_k, tiles_k},
+        // {first key, qo_indptr[b], first partial slot, n_splits},
+        // {chunk_len, prefix_len, kv_indptr[b], kv_len}; self-planned calls
+        // build it from the shared-memory sums
+        auto group = [&](int kg, int4& A, int4& B, int4& Cg) {
+            if (!p.self_plan) {
+                A = rg[3 * kg];
+                B = rg[3 * kg + 1];
+                Cg = rg[3 * kg + 2];
+                return;
+            }
+            const int j = kg / H, g = kg - j * H;
+            int lo = 0, hi = p.batch;  // the sequence of row group j: last b with gs[b] <= j
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_sp_gs[mid] <= j) lo = mid;
+                else hi = mid;
+            }
+            const int b = lo;
+            const int4 sq = s_sp_seq[b];
+            const int tiles = s_sp_ts[b + 1] - s_sp_ts[b];
+            const int S0 = H * s_sp_ts[b] + g * tiles;
+            const int i0 = cta_of(S0), i1 = cta_of(S0 + tiles - 1);
+            A = make_int4(b, g, S0, tiles);
+            B = make_int4(p.window > 0 ? max(0, sq.y - p.window + 1) : 0, sq.w, kg + i0,
+                          i1 - i0 + 1);
+            Cg = make_int4(sq.x, sq.y, sq.z, sq.x + sq.y);
+        };
+        // the row group holding tile x (self-planned calls)
+        auto group_at = [&](int x) {
+            const int y = x / H;
+            int lo = 0, hi = p.batch;  // last b with ts[b] <= x / H
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_sp_ts[mid] <= y) lo = mid;
+                else hi = mid;
+            }
+            const int tiles = s_sp_ts[lo + 1] - s_sp_ts[lo];
+            return H * s_sp_gs[lo] + (x - H * s_sp_ts[lo]) / tiles;
+        };
         auto resolve = [&](int kg, int4 A, int4 B, int4 Cg, int4& e0, int4& e1, int4& e2) {
             const int a = max(x0, A.z) - A.z, e = min(x1, A.z + A.w) - A.z;
             const int t0 = B.x / kRowTile;
@@ -206,8 +355,10 @@ __global__ void __launch_bounds__(kRowThreads, 1)
         uint32_t it = 0;  // ring position
         int last_issued = -1;
         int last_item = -1;  // last item (or end marker) handed to the consumers
-        int kg = reinterpret_cast<const int*>(p.ws + p.lay.row_first)[blockIdx.x];
-        int4 gA = rg[3 * kg], gB = rg[3 * kg + 1], gC = rg[3 * kg + 2];
+        int kg = p.self_plan ? group_at(x0)
+                             : reinterpret_cast<const int*>(p.ws + p.lay.row_first)[blockIdx.x];
+        int4 gA, gB, gC;
+        group(kg, gA, gB, gC);
         int4 n0, n1, n2;
         resolve(kg, gA, gB, gC, n0, n1, n2);
         int next_sl[4];
@@ -226,9 +377,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
             const bool next_valid = valid && gA.z + gA.w < x1;
             if (next_valid) {  // loads in flight during this item
                 ++kg;
-                gA = rg[3 * kg];
-                gB = rg[3 * kg + 1];
-                gC = rg[3 * kg + 2];
+                group(kg, gA, gB, gC);
             }
             // hand the item (or the end marker) and its Q rows to the consumers
             if (!__all_sync(0xffffffffu, mbar_wait(item_empty(qs), ((uint32_t)(k / NI) & 1u) ^ 1u,

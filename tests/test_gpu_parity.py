@@ -140,6 +140,29 @@ def test_host_hint_is_bit_identical(case):
     full_parity(b, f"hinted {case}")
 
 
+@pytest.mark.parametrize("n,ps,window", [(1, 64, 0), (31, 16, 0), (300, 1, 0), (512, 64, 700),
+                                          (513, 16, 0)])
+def test_self_planned_decode_is_bit_identical(n, ps, window):
+    """A decode-only call with the host copy of qo_indptr and at most 512
+    sequences is planned inside the row kernel (no planner launch); without
+    the copy the planner kernel plans it.  Both give identical bits, also
+    with zero-length chunks, two-row chunks and a window (513 sequences:
+    the planner both times)."""
+    rng = np.random.default_rng(n + ps)
+    P = rng.integers(1, 5000 if n < 100 else 1500, size=n)
+    C = rng.choice([0, 1, 1, 1, 2], size=n)
+    C[0] = 1  # at least one row
+    hq, hkv, d = (16, 4, 128) if n < 100 else (8, 2, 64)
+    b = W.make_batch(P, C, hq, hkv, d, ps, seed=60 + n, window=window)
+    res = []
+    for hint in (True, False):
+        _, _, out, lse = run_gpu(b, host_hint=hint)
+        res.append((bf16_tensor_bits(out), lse.cpu().numpy()))
+    np.testing.assert_array_equal(res[0][0], res[1][0])
+    np.testing.assert_array_equal(res[0][1], res[1][1])
+    sampled_parity(b, n_random=128, what=f"self-planned decode n={n} ps={ps} W={window}")
+
+
 def test_decode_rows_many_splits():
     """A few very long decode rows and many short ones: the long groups span
     many row-kernel CTAs (many partial slots), the short ones share a CTA."""
@@ -265,6 +288,73 @@ def test_chunk_partition_invariance_gpu():
         results.append((np.concatenate(outs), np.concatenate(lses)))
     for o, l in results[1:]:
         assert_close(o, l, results[0][0], results[0][1], "partition")
+
+
+# ------------------------------------------------- fused slot mapping + append
+@pytest.mark.parametrize("name", ["tiny", "mixed", "stress_ps1_w0", "stress_ps16_w4096",
+                                  "gqa_prefill"])
+def test_fused_append_bit_exact(name):
+    """pcp_kv_append_paged: the slots and the appended pools equal the
+    oracle's slot mapping and scatter bit for bit; slots no token names keep
+    their contents."""
+    import torch
+    import paged_chunked_prefill_gb300 as pcp
+    batch = W.config_by_name(name)
+    d = to_device(batch)
+    loc = torch.full((batch.total_q,), -7, dtype=torch.int64, device="cuda")
+    pcp.kv_append_paged(d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["prefix_lens"],
+                        batch.page_size, d["k_new"], d["v_new"], d["k_pool"], d["v_pool"],
+                        out_cache_loc=loc)
+    loc_ref = oracle.out_cache_loc(batch.qo_indptr, batch.kv_indptr, batch.kv_indices,
+                                   batch.prefix_lens, batch.page_size, batch.num_pages)
+    kp_ref, vp_ref = batch.k_pool.copy(), batch.v_pool.copy()
+    oracle.kv_append(batch.k_new, batch.v_new, loc_ref, kp_ref, vp_ref)
+    np.testing.assert_array_equal(loc.cpu().numpy(), loc_ref)
+    np.testing.assert_array_equal(bf16_tensor_bits(d["k_pool"]), kp_ref)
+    np.testing.assert_array_equal(bf16_tensor_bits(d["v_pool"]), vp_ref)
+
+
+def test_fused_append_without_loc_then_attention():
+    """The fused append with no out_cache_loc array, followed by attention:
+    the same results as the separate slot mapping and append."""
+    import torch
+    import paged_chunked_prefill_gb300 as pcp
+    batch = W.mixed_batch(prompt=700, chunk=300, n_decode=9, decode_max=3000)
+    d = to_device(batch)
+    pcp.kv_append_paged(d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["prefix_lens"],
+                        batch.page_size, d["k_new"], d["v_new"], d["k_pool"], d["v_pool"])
+    out, lse = pcp.paged_extend_attn(d["q"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                                     d["prefix_lens"], d["k_pool"], d["v_pool"],
+                                     batch.page_size, batch.n_q_heads, batch.n_kv_heads,
+                                     batch.head_dim, batch.window, batch.sm_scale)
+    _, _, out2, lse2 = run_gpu(batch)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+
+
+def test_fused_append_reports_bad_page():
+    """A bad page id among a chunk's pages: PCP_ERR_BAD_INDEX, slot -1, that
+    token not written, every other token appended."""
+    import torch
+    import paged_chunked_prefill_gb300 as pcp
+    b = W.make_batch([10], [50], 8, 2, 64, 16, seed=41)
+    bad = b.kv_indices.copy()
+    bad[3] = -1          # keys 48..63: tokens 38..49 of the chunk
+    b2 = W.Batch(**{**b.__dict__, "kv_indices": bad})
+    d = to_device(b2)
+    loc = torch.zeros(b.total_q, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pcp.kv_append_paged(d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["prefix_lens"], 16,
+                        d["k_new"], d["v_new"], d["k_pool"], d["v_pool"], out_cache_loc=loc,
+                        dev_err=err)
+    assert pcp.read_error(err) == pcp.Status.BAD_INDEX
+    l = loc.cpu().numpy()
+    pos = 10 + np.arange(50)
+    assert (l[pos // 16 == 3] == -1).all()
+    good = pos // 16 != 3
+    np.testing.assert_array_equal(l[good], b.kv_indices[pos[good] // 16] * 16 + pos[good] % 16)
+    kp = bf16_tensor_bits(d["k_pool"])
+    np.testing.assert_array_equal(kp[l[good]], b.k_new[good])
 
 
 # ------------------------------------------------------------------- errors
