@@ -259,9 +259,10 @@ struct GatherShape {
     static constexpr int kInsts = kRows / kRowsPerInst;       // instructions per tile
 };
 
+// sa / sb: the slots of the warp's rows `lane` and `lane + 32` (-1: none);
+// the copy lanes of a row take its slot by shuffle.
 template <int D>
-__device__ __forceinline__ void gather_kv_rows(const TcParams& p, const Geo& geo,
-                                               const int (&slot)[GatherShape<D>::kInsts],
+__device__ __forceinline__ void gather_kv_rows(const TcParams& p, const Geo& geo, int sa, int sb,
                                                const uint16_t* pool, uint32_t dst, int gw,
                                                int lane) {
     using C = TcCfg<D>;
@@ -270,10 +271,12 @@ __device__ __forceinline__ void gather_kv_rows(const TcParams& p, const Geo& geo
     const int rsub = lane / GS::kChunks;
 #pragma unroll
     for (int j = 0; j < GS::kInsts; ++j) {
-        const int row = gw * GS::kRows + j * GS::kRowsPerInst + rsub;
-        const bool ok = slot[j] >= 0;
+        const int rw = j * GS::kRowsPerInst + rsub;  // row among the warp's 64
+        const int slot = __shfl_sync(0xffffffffu, j * GS::kRowsPerInst < 32 ? sa : sb, rw & 31);
+        const int row = gw * GS::kRows + rw;
+        const bool ok = slot >= 0;
         const uint16_t* src =
-            ok ? pool + ((int64_t)slot[j] * p.n_kv_heads + geo.g) * D + c * 8 : pool;
+            ok ? pool + ((int64_t)slot * p.n_kv_heads + geo.g) * D + c * 8 : pool;
         cp_async_16(dst + (c >> 3) * C::kHalfBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4),
                     src, ok ? 16u : 0u);
     }
@@ -422,51 +425,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // tile (two warps issuing cp.async in parallel)
             if (p.box_rows == 0) {
                 using GS = GatherShape<D>;
+                static_assert(GS::kRows == 64, "two 32-row halves per gather warp and tile");
                 const int gw = warp - kWarpGather0;
                 const int32_t* pages = p.kv_indices + p.kv_indptr[geo.b];
-                const int rsub = lane / GS::kChunks;
-                // slots of this lane's rows of tile t (shared by K and V)
-                auto fetch_slots = [&](int t, int (&slot)[GS::kInsts]) {
-#pragma unroll
-                    for (int j = 0; j < GS::kInsts; ++j) {
-                        const int key = t * kTileN + gw * GS::kRows + j * GS::kRowsPerInst + rsub;
-                        slot[j] = -1;
-                        if (key < geo.L) {
-                            const int entry =
-                                p.page_shift >= 0 ? key >> p.page_shift : key / p.page_size;
-                            const int page = pages[entry];
-                            if (page >= 0 && page < p.num_pages)
-                                slot[j] = page * p.page_size + (key - entry * p.page_size);
-                            else
-                                report_error(p.dev_err, PCP_ERR_BAD_INDEX);
-                        }
+                // Slot of key `key` (-1 past the sequence end or for a bad page).
+                auto slot_of = [&](int key) {
+                    int slot = -1;
+                    if (key < geo.L) {
+                        const int entry = p.page_shift >= 0 ? key >> p.page_shift
+                                                            : key / p.page_size;
+                        const int page = pages[entry];
+                        if (page >= 0 && page < p.num_pages)
+                            slot = page * p.page_size + (key - entry * p.page_size);
+                        else
+                            report_error(p.dev_err, PCP_ERR_BAD_INDEX);
                     }
+                    return slot;
                 };
+                // The warp's 64 rows of tile t: lane l looks up rows l and
+                // l + 32 (consecutive page-table entries, one coalesced load
+                // each), one tile ahead of their use; a row's copy lanes take
+                // its slot by shuffle.
+                const int row0 = gw * GS::kRows;
+                int sa = slot_of(geo.t_begin * kTileN + row0 + lane);
+                int sb = slot_of(geo.t_begin * kTileN + row0 + 32 + lane);
                 for (int i = 0; i < ntiles; ++i) {
                     const int t = geo.t_begin + i;
                     const uint32_t cur = kv_iter + i;
                     const int sk = cur % SK, sv = cur % SV;
-                    int slot[GS::kInsts];
-                    fetch_slots(t, slot);
-                    // the next tile's page-table lines go to L1 while this one
-                    // is waited for and issued
-                    if (i + 1 < ntiles) {
-                        const int key = (t + 1) * kTileN + gw * GS::kRows + 2 * lane;
-                        if (key < geo.L)
-                            prefetch_l1(pages + (p.page_shift >= 0 ? key >> p.page_shift
-                                                                   : key / p.page_size));
+                    const int ca = sa, cb = sb;
+                    if (i + 1 < ntiles) {  // the next tile's lookups are in flight meanwhile
+                        sa = slot_of((t + 1) * kTileN + row0 + lane);
+                        sb = slot_of((t + 1) * kTileN + row0 + 32 + lane);
                     }
                     if (!__all_sync(0xffffffffu,
                                     mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u,
                                               abort_flag, p.dev_err, kSpinLimitNs)))
                         break;
-                    gather_kv_rows<D>(p, geo, slot, p.k_pool, sK + sk * C::kTileBytes, gw, lane);
+                    gather_kv_rows<D>(p, geo, ca, cb, p.k_pool, sK + sk * C::kTileBytes, gw, lane);
                     cp_async_mbar_arrive_noinc(bar(C::bKFull + sk));
                     if (!__all_sync(0xffffffffu,
                                     mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u,
                                               abort_flag, p.dev_err, kSpinLimitNs)))
                         break;
-                    gather_kv_rows<D>(p, geo, slot, p.v_pool, sV + sv * C::kTileBytes, gw, lane);
+                    gather_kv_rows<D>(p, geo, ca, cb, p.v_pool, sV + sv * C::kTileBytes, gw, lane);
                     cp_async_mbar_arrive_noinc(bar(C::bVFull + sv));
                 }
             }
