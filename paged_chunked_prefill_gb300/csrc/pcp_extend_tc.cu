@@ -599,14 +599,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 bool ok = true;
                 for (int t = first_u; t <= last_u; ++t) {
                     const uint32_t a = act_u + (uint32_t)(t - first_u);
-                    // waits decide per warp (tcgen05.ld/st and the P arrival are
-                    // warp-collective)
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar(C::bSFull + u), a & 1u, abort_flag,
-                                                           p.dev_err, kSpinLimitNs))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
                     const int key0 = t * kTileN;
                     constexpr bool has_mask = kMask;
                     // causal: the diagonal and window-edge tiles; otherwise the
@@ -618,7 +610,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                   : key0 + kTileN > geo.L);
                     // keep-bits of this row's keys in the tile (bit j of mb[j / 32]):
                     // the boolean mask's entries, and'ed with the causal / length
-                    // range, so each key costs one bit test
+                    // range, so each key costs one bit test.  They do not depend
+                    // on S: their loads are issued before the wait for S, so the
+                    // load latency overlaps the QK^T MMA.
                     uint32_t mb[4] = {~0u, ~0u, ~0u, ~0u};
                     if constexpr (has_mask) {
                         if (p.mask.h_stride == 0 && p.mask.q_stride == 0) {
@@ -643,6 +637,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                         for (int w = 0; w < 4; ++w) mb[w] &= range_bits(lo - 32 * w, hi - 32 * w);
                     }
+                    // waits decide per warp (tcgen05.ld/st and the P arrival are
+                    // warp-collective)
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar(C::bSFull + u), a & 1u, abort_flag,
+                                                           p.dev_err, kSpinLimitNs))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     // the whole S row of this thread: one TMEM load
                     uint32_t v[128];
                     tmem_ld128(tS, v);
