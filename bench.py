@@ -65,12 +65,24 @@ def rows_pairs(batch, tok, head) -> int:
 # again.
 NCU_TRAFFIC = {
     ("gqa_prefill", "extend_tc_kernel<128>"): {
-        "bytes": 203.634176e6 + 17.143808e6,
-        "csrc_sha256": "3243b7b826445c18422d22c25f4e0db7",
+        "bytes": 199.122688e6 + 17.033216e6,
+        "csrc_sha256": "07eb6976004c67d480c38874e8afb85e",
     },
     ("decode_rows", "row_attn_kernel<128>"): {
-        "bytes": 275.753472e6 + 3.334656e6,
-        "csrc_sha256": "3243b7b826445c18422d22c25f4e0db7",
+        "bytes": 275.753984e6 + 3.887616e6,
+        "csrc_sha256": "07eb6976004c67d480c38874e8afb85e",
+    },
+    ("long_context", "extend_tc_kernel<128>"): {
+        "bytes": 4139.245312e6 + 532.051712e6,
+        "csrc_sha256": "07eb6976004c67d480c38874e8afb85e",
+    },
+    ("mixed", "extend_tc_kernel<128>"): {
+        "bytes": 25.268480e6 + 0.000256e6,
+        "csrc_sha256": "07eb6976004c67d480c38874e8afb85e",
+    },
+    ("mixed", "row_attn_kernel<128>"): {
+        "bytes": 284.228608e6 + 0.230400e6,
+        "csrc_sha256": "07eb6976004c67d480c38874e8afb85e",
     },
 }
 
@@ -618,7 +630,7 @@ def end_to_end(args, torch, pcp, batch, d, out_ref, flush, stream, flops, world)
 
 
 def attn_figures(pcp, torch, batch, dev, peaks, flush, err, n=20, warm=5, causal=True,
-                 mask=None, pairs=None):
+                 mask=None, pairs=None, key=None):
     """One attention call on `batch` (its chunk's K/V appended first), L2
     flushed before each timed call: the whole call, and the tensor-core and
     row kernels alone between per-call events.  Effective FLOPs count the
@@ -657,13 +669,15 @@ def attn_figures(pcp, torch, batch, dev, peaks, flush, err, n=20, warm=5, causal
         r["tc_kernel"] = {"bound": "tensor", "kernel": f"extend_tc_kernel<{D}>",
                           "kernel_ms": kms, "achieved": tf, "peak": peaks["bf16_tflops"],
                           "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
-                          "visible_pairs_per_head": int(tc_pairs)}
+                          "visible_pairs_per_head": int(tc_pairs),
+                          "traffic": ncu_traffic(key, f"extend_tc_kernel<{D}>") if key else None}
     if row_bytes > 0 and pairs is None:
         kms = time_calls(torch, lambda ev: call(row_ev=ev), flush, n=n, warm=warm, events=True)
         gbs = row_bytes / (kms * 1e-3) / 1e9
         r["row_kernel"] = {"bound": "hbm", "kernel": f"row_attn_kernel<{D}>", "kernel_ms": kms,
                            "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                           "frac": gbs / peaks["hbm_gbs"], "bytes": int(row_bytes)}
+                           "frac": gbs / peaks["hbm_gbs"], "bytes": int(row_bytes),
+                           "traffic": ncu_traffic(key, f"row_attn_kernel<{D}>") if key else None}
     return r
 
 
@@ -676,15 +690,39 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
 
     # decode rows: the 31 decode rows of the mixed batch as a decode-only call
     db = W.decode_rows()
-    r = attn_figures(pcp, torch, db, dev, peaks, flush, err)
+    r = attn_figures(pcp, torch, db, dev, peaks, flush, err, key="decode_rows")
     _, nbytes = split_work(db)
     gbs = nbytes / (r["ms"] * 1e-3) / 1e9
     res["decode_rows"] = {"workload": db.name, "ms": r["ms"], "GB/s": gbs,
                           "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes,
                           "what": "whole call: planner, row kernel, split-KV combine"}
-    res["decode_rows_kernel"] = dict(r["row_kernel"],
-                                     traffic=ncu_traffic("decode_rows",
-                                                         f"row_attn_kernel<{db.head_dim}>"))
+    res["decode_rows_kernel"] = r["row_kernel"]
+
+    # the same 31 rows as a serving decode step: the fused append of their
+    # new tokens, then the attention call (whose row kernel plans the call
+    # while the append runs)
+    g = to_device(db, dev)
+    dout = torch.empty_like(g["q"])
+    dlse = torch.empty(db.total_q, db.n_q_heads, dtype=torch.float32, device=dev)
+    dws = torch.empty(pcp.workspace_size(db.batch, db.total_q, db.n_q_heads, db.n_kv_heads,
+                                         db.head_dim), dtype=torch.uint8, device=dev)
+
+    def dstep(ev):
+        pcp.kv_append_paged(g["qo_indptr"], g["kv_indptr"], g["kv_indices"], g["prefix_lens"],
+                            db.page_size, g["k_new"], g["v_new"], g["k_pool"], g["v_pool"],
+                            dev_err=err)
+        pcp.paged_extend_attn(g["q"], g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
+                              g["prefix_lens"], g["k_pool"], g["v_pool"], db.page_size,
+                              db.n_q_heads, db.n_kv_heads, db.head_dim, db.window, db.sm_scale,
+                              out=dout, lse=dlse, workspace=dws, dev_err=err,
+                              qo_indptr_host=db.qo_indptr)
+    ms = time_calls(torch, dstep, flush)
+    sbytes = nbytes + 2 * 2 * db.total_q * db.n_kv_heads * db.head_dim * 2
+    gbs = sbytes / (ms * 1e-3) / 1e9
+    res["decode_step"] = {"workload": db.name, "ms": ms, "GB/s": gbs,
+                          "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": sbytes,
+                          "what": "fused append of the rows' new tokens, then the attention call"}
+    del g, dout, dlse, dws
 
     # the KV append of the GQA chunk (4096 tokens) and of the long-context
     # chunk (32768 tokens): the fused slot mapping + append the step runs, and
@@ -717,8 +755,9 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
     # flat one-slot-per-token pool (page size 1), and the page-boundary and
     # window stress batches
     res["long_context_attn"] = attn_figures(pcp, torch, W.long_context(), dev, peaks, flush,
-                                            err, n=5, warm=2)
-    res["mixed_attn"] = attn_figures(pcp, torch, W.mixed_batch(), dev, peaks, flush, err)
+                                            err, n=5, warm=2, key="long_context")
+    res["mixed_attn"] = attn_figures(pcp, torch, W.mixed_batch(), dev, peaks, flush, err,
+                                     key="mixed")
     res["gqa_prefill_ps1"] = attn_figures(pcp, torch, W.gqa_prefill(page_size=1), dev, peaks,
                                           flush, err, n=10, warm=3)
     for name in ("stress_ps1_w4096", "stress_ps1_w0", "stress_ps16_w4096", "stress_ps16_w0"):
