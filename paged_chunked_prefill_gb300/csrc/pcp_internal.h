@@ -46,6 +46,14 @@ __host__ __device__ inline int row_path_max_chunk(int group) {
 
 __host__ __device__ inline int q_positions_per_tile(int group) { return kTileM / group; }
 
+// The row-tile split charges every row group's start as this many extra
+// tiles: a CTA's time grows with the group pieces it takes (their Q loads,
+// boundary tiles and four-warp merges cost about two tiles' streaming time
+// each), so a CTA that starts more groups takes fewer real tiles.  The
+// groups' tiles are laid end to end as [kRowGroupStartTiles virtual tiles,
+// then the real ones].
+constexpr int kRowGroupStartTiles = 2;
+
 // CTAs of the row kernel: one per SM.  The planner splits the row work for
 // exactly this many.
 __host__ __device__ inline int row_grid(int sm_count) {
@@ -68,7 +76,7 @@ struct WsHeader {
     int n_tc_items;
     int n_row_groups;  // (sequence, KV head) groups on the row path
     int tc_next;       // dynamic scheduler counter of the tensor-core kernel
-    int row_tiles;     // T: 128-key tiles of all row groups
+    int row_tiles;     // T: 128-key tiles of all row groups, with each group's virtual start tiles
     int row_ctas;      // n: row-kernel CTAs the split was made for
     int pad[59];       // 256 bytes
 };
@@ -90,7 +98,7 @@ struct WsLayout {
     size_t header;        // offset of WsHeader
     size_t tc_items;      // int4 [cap_tc]
     size_t row_groups;    // int4 [3 * cap_groups]: row group descriptors
-    size_t row_first;     // int [kRowMaxCtas]: first row group of each row-kernel CTA
+    size_t row_first;     // int [kRowMaxCtas]: first row group of each row-kernel CTA (-1: none)
     size_t group_desc;    // int4 [cap_groups]: {first partial slot, n_splits, q0, chunk_len}
     size_t partial_o;     // float [cap_row * kRowMaxRows * head_dim]
     size_t partial_ml;    // float2 [cap_row * kRowMaxRows]

@@ -222,7 +222,9 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
         __syncthreads();
         load_chunk(chunk0, true);
         s_a[tid] = n_tc_of(s_seq[tid]);
-        unsigned long long rt = (unsigned long long)s_seq[tid].w * H;
+        // each row group adds its virtual start tiles to the split
+        unsigned long long rt =
+            s_seq[tid].w > 0 ? (unsigned long long)(s_seq[tid].w + kRowGroupStartTiles) * H : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) rt += __shfl_xor_sync(0xffffffffu, rt, o);
         if (lane == 0 && rt) atomicAdd(&s_row_tiles, rt);
@@ -246,6 +248,8 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     if (bad_meta) report_error(p.dev_err, PCP_ERR_INVALID_ARG);
     if (tid == 0 && row_tiles_all >= (1ull << 31)) report_error(p.dev_err, PCP_ERR_UNSUPPORTED);
     for (int64_t i = tid; i < (int64_t)p.batch * H; i += 1024) gdesc[i] = make_int4(0, 0, 0, 0);
+    // a CTA whose tiles are all virtual has no row group
+    if (tid < kRowMaxCtas) row_first[tid] = -1;
     const int T = (int)min(row_tiles_all, (unsigned long long)INT32_MAX);
     // the split uses min(n, T) CTAs, so every one of them holds at least one
     // tile and every partial slot of a group is written
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
         if (!one_chunk) load_chunk(chunk0, false);
         s_a[tid] = n_tc_of(s_seq[tid]) * H;  // items flattened as (sequence, KV head, item)
         s_b[tid] = s_seq[tid].w > 0 ? H : 0;
-        s_c[tid] = s_seq[tid].w;
+        s_c[tid] = s_seq[tid].w > 0 ? s_seq[tid].w + kRowGroupStartTiles : 0;
         __syncthreads();
         const int total_a = p.tc_work ? excl_scan(s_a, warp_sums) : 0;
         const int total_b = excl_scan(s_b, warp_sums);
@@ -290,7 +294,10 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
             const int k = grp_base + f;
             const int4 v = s_seq[sl];
             const int tiles = v.w;
-            const int S = tile_base + s_c[sl] * H + g * tiles;
+            // the group's span on the tile line starts with its virtual tiles;
+            // its pieces are the CTAs' shares of its real tiles [S, S + tiles)
+            const int S0 = tile_base + s_c[sl] * H + g * (tiles + kRowGroupStartTiles);
+            const int S = S0 + kRowGroupStartTiles;
             const int i_first = cta_of(S), i_last = cta_of(S + tiles - 1);
             const int ns = i_last - i_first + 1;
             const int base = k + i_first;
@@ -304,9 +311,9 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
             rg[3 * k + 1] = make_int4(first_key(P, p.window), q0, base, ns);
             rg[3 * k + 2] = make_int4(v.x, P, s_off[sl].y, L);
             gdesc[(int64_t)b * H + g] = make_int4(base, ns, q0, v.x);
-            // CTAs whose first tile lies in this group start with it
+            // CTAs whose range starts in this group's span start with it
             for (int i = i_first; i <= i_last; ++i)
-                if (row_tile_begin(i, n_use, T) >= S) row_first[i] = k;
+                if (row_tile_begin(i, n_use, T) >= S0) row_first[i] = k;
         }
         grp_base += total_b;
         tile_base += total_c * H;

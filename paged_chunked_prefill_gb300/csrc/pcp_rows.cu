@@ -43,8 +43,16 @@ struct RowCfg {
     static constexpr int kOffDesc = kOffQ + kItemSlots * kRowMaxRows * kQStride;  // int4 [slot][3]
     static constexpr int kOffBar = kOffDesc + kItemSlots * 48;
     static constexpr int kOffM = kOffBar + (2 * kStages + 2 * kItemSlots) * 8;  // float [4][16] m, l
-    static constexpr int kSmemBytes = kOffM + 2 * 4 * kRowMaxRows * 4 + 64 + 1024;
-    static_assert(kOffDesc % 16 == 0 && kOffBar % 8 == 0 && kOffStage % 1024 == 0,
+    // merge buffer of an item's four warp states, four rows at a time:
+    // [4 warps][4 rows][D + 8] fp32 (the padding puts the rows of one float2
+    // store on different banks)
+    static constexpr int kMergeRows = 4;
+    static constexpr int kMergeStride = D + 8;
+    static constexpr int kOffMerge = kOffM + 2 * 4 * kRowMaxRows * 4;
+    static constexpr int kSmemBytes =
+        kOffMerge + 4 * kMergeRows * kMergeStride * 4 + 64 + 1024;
+    static_assert(kOffDesc % 16 == 0 && kOffBar % 8 == 0 && kOffStage % 1024 == 0 &&
+                      kOffMerge % 16 == 0,
                   "smem alignment");
 };
 
@@ -113,7 +121,8 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     const int rmax = row_path_max_chunk(p.group);
     // ---- self-planned call: the split of the row tiles, from the metadata
     // alone (read before the wait below; they are inputs of the call)
-    long long sp_total = 0;  // row tiles of one KV head, all sequences
+    long long sp_total = 0;   // row tiles of one KV head, all sequences
+    long long sp_groups = 0;  // row sequences (row groups of one KV head)
     bool sp_bad = false;     // this thread saw contradictory metadata
     if (p.self_plan) {
         // thread i takes sequences 4i .. 4i + 3
@@ -163,6 +172,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                 gb += s_sp_wsum[1][w];
             }
             sp_total += s_sp_wsum[0][w];
+            sp_groups += s_sp_wsum[1][w];
         }
         tb += ti - t_run;
         gb += gi - g_run;
@@ -205,11 +215,13 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     int T;
     if (p.self_plan) {
         if (sp_bad) report_error(p.dev_err, PCP_ERR_INVALID_ARG);
-        if (sp_total * H >= (1ll << 31)) {
+        // the tile line holds every group's virtual start tiles too
+        const long long t_all = (sp_total + (long long)kRowGroupStartTiles * sp_groups) * H;
+        if (t_all >= (1ll << 31)) {
             if (tid == 0 && blockIdx.x == 0) report_error(p.dev_err, PCP_ERR_UNSUPPORTED);
             return;
         }
-        T = (int)(sp_total * H);
+        T = (int)t_all;
     } else {
         T = hdr->row_tiles;
         if (hdr->row_ctas != (int)gridDim.x) {  // the plan was made for another grid
@@ -220,6 +232,9 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     const int n_use = row_ctas_used(gridDim.x, T);
     // the row-kernel CTA holding tile x: the last i with i*T/n_use <= x
     auto cta_of = [&](int x) { return (int)((((int64_t)x + 1) * n_use + T - 1) / T) - 1; };
+    // self-planned calls: where sequence b's groups start on the tile line
+    // (each group: kRowGroupStartTiles virtual tiles, then its real ones)
+    auto sp_line = [&](int b) { return H * (s_sp_ts[b] + kRowGroupStartTiles * s_sp_gs[b]); };
     if (p.self_plan) {
         // the combine kernel's descriptor of every (sequence, KV head) group,
         // {first partial slot, splits, qo_indptr[b], chunk_len}, zeros for a
@@ -234,8 +249,8 @@ __global__ void __launch_bounds__(kRowThreads, 1)
             if (tiles > 0) {
                 const int4 sq = s_sp_seq[b];
                 const int k = H * s_sp_gs[b] + g;
-                const int S0 = H * s_sp_ts[b] + g * tiles;
-                const int i0 = cta_of(S0), i1 = cta_of(S0 + tiles - 1);
+                const int R0 = sp_line(b) + g * (tiles + kRowGroupStartTiles) + kRowGroupStartTiles;
+                const int i0 = cta_of(R0), i1 = cta_of(R0 + tiles - 1);
                 gd = make_int4(k + i0, i1 - i0 + 1, sq.w, sq.x);
             }
             gdesc[e] = gd;
@@ -325,24 +340,28 @@ __global__ void __launch_bounds__(kRowThreads, 1)
             const int b = lo;
             const int4 sq = s_sp_seq[b];
             const int tiles = s_sp_ts[b + 1] - s_sp_ts[b];
-            const int S0 = H * s_sp_ts[b] + g * tiles;
-            const int i0 = cta_of(S0), i1 = cta_of(S0 + tiles - 1);
-            A = make_int4(b, g, S0, tiles);
+            const int R0 = sp_line(b) + g * (tiles + kRowGroupStartTiles) + kRowGroupStartTiles;
+            const int i0 = cta_of(R0), i1 = cta_of(R0 + tiles - 1);
+            A = make_int4(b, g, R0, tiles);
             B = make_int4(p.window > 0 ? max(0, sq.y - p.window + 1) : 0, sq.w, kg + i0,
                           i1 - i0 + 1);
             Cg = make_int4(sq.x, sq.y, sq.z, sq.x + sq.y);
         };
-        // the row group holding tile x (self-planned calls)
+        // the first row group with real tiles in [x, x1) (self-planned
+        // calls): the group whose span holds tile x, unless x lies among its
+        // virtual tiles and its real ones start at or past x1 (-1: none)
         auto group_at = [&](int x) {
-            const int y = x / H;
-            int lo = 0, hi = p.batch;  // last b with ts[b] <= x / H
+            int lo = 0, hi = p.batch;  // last b with sp_line(b) <= x
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
-                if (s_sp_ts[mid] <= y) lo = mid;
+                if (sp_line(mid) <= x) lo = mid;
                 else hi = mid;
             }
-            const int tiles = s_sp_ts[lo + 1] - s_sp_ts[lo];
-            return H * s_sp_gs[lo] + (x - H * s_sp_ts[lo]) / tiles;
+            const int span = s_sp_ts[lo + 1] - s_sp_ts[lo] + kRowGroupStartTiles;
+            const int g = (x - sp_line(lo)) / span;
+            const int real0 = sp_line(lo) + g * span + kRowGroupStartTiles;
+            if (x < real0 && real0 >= x1) return -1;
+            return H * s_sp_gs[lo] + g;
         };
         auto resolve = [&](int kg, int4 A, int4 B, int4 Cg, int4& e0, int4& e1, int4& e2) {
             const int a = max(x0, A.z) - A.z, e = min(x1, A.z + A.w) - A.z;
@@ -357,13 +376,15 @@ __global__ void __launch_bounds__(kRowThreads, 1)
         int last_item = -1;  // last item (or end marker) handed to the consumers
         int kg = p.self_plan ? group_at(x0)
                              : reinterpret_cast<const int*>(p.ws + p.lay.row_first)[blockIdx.x];
-        int4 gA, gB, gC;
-        group(kg, gA, gB, gC);
-        int4 n0, n1, n2;
-        resolve(kg, gA, gB, gC, n0, n1, n2);
-        int next_sl[4];
-        fetch(p.kv_indices + n2.z, n2.w, n1.x / kRowTile, next_sl);
-        bool have = true;  // n0..n2 hold an item
+        bool have = kg >= 0;  // n0..n2 hold an item (a CTA of virtual tiles only has none)
+        int4 gA = make_int4(0, 0, 0, 0), gB = gA, gC = gA;
+        int4 n0 = gA, n1 = gA, n2 = gA;
+        int next_sl[4] = {-1, -1, -1, -1};
+        if (have) {
+            group(kg, gA, gB, gC);
+            resolve(kg, gA, gB, gC, n0, n1, n2);
+            fetch(p.kv_indices + n2.z, n2.w, n1.x / kRowTile, next_sl);
+        }
         for (int k = 0;; ++k) {
             const int qs = k % NI;
             // every decision of this warp is taken for all its lanes (the
@@ -374,7 +395,8 @@ __global__ void __launch_bounds__(kRowThreads, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) cur_sl[j] = next_sl[j];
             // the range goes on past this group: the next group follows
-            const bool next_valid = valid && gA.z + gA.w < x1;
+            // the next group's real tiles start after its virtual ones
+            const bool next_valid = valid && gA.z + gA.w + kRowGroupStartTiles < x1;
             if (next_valid) {  // loads in flight during this item
                 ++kg;
                 group(kg, gA, gB, gC);
@@ -702,21 +724,20 @@ __global__ void __launch_bounds__(kRowThreads, 1)
                         mma_16816(o[2 * dn2], pa[bl], v0, v1);
                         mma_16816(o[2 * dn2 + 1], pa[bl], v2, v3);
                     }
-            if (i + 1 < ntiles) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(st));
-            }
+            // every tile's stage goes back to the load warp as soon as its
+            // PV is done (the merge below does not use the stages)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(st));
         }
         it += (uint32_t)ntiles;
-        const int last_st = (int)((it - 1u) % S);
         if (lane == 0) s_fail[warp] = failed ? 1 : 0;
 
-        // merge the four warps' states through shared memory: the stage of
-        // this item's last tile, whose release waits until the merge is done
-        float* wo = reinterpret_cast<float*>(sm + C::kOffStage + last_st * 2 * C::kTileBytes);
-        consumer_sync();
-        if (s_fail[0] | s_fail[1] | s_fail[2] | s_fail[3]) break;
-        {
+        // Merge the four warps' states (each holds its 32 keys of every tile):
+        // (m, l) per row through m_s / l_s, then, four rows at a time, every
+        // warp leaves its O rows in its slice of the merge buffer and the
+        // threads sum the four slices element by element (warps in a fixed
+        // order, so the rounding does not depend on timing).  All stages are
+        // back with the load warp, which keeps streaming the next item.
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
         l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
@@ -727,45 +748,56 @@ __global__ void __launch_bounds__(kRowThreads, 1)
             l_s[warp * kRowMaxRows + row_lo] = l_lo;
             l_s[warp * kRowMaxRows + row_hi] = l_hi;
         }
-#pragma unroll
-        for (int dn = 0; dn < D / 8; ++dn) {
-            const int d = dn * 8 + tig * 2;
-            *reinterpret_cast<float2*>(&wo[(warp * kRowMaxRows + row_lo) * D + d]) =
-                make_float2(o[dn][0], o[dn][1]);
-            *reinterpret_cast<float2*>(&wo[(warp * kRowMaxRows + row_hi) * D + d]) =
-                make_float2(o[dn][2], o[dn][3]);
-        }
-        }
         consumer_sync();
-        for (int idx = tid; idx < R * D; idx += kConsumerThreads) {
-            const int r = idx / D, d = idx % D;
-            float M = -INFINITY;
+        if (s_fail[0] | s_fail[1] | s_fail[2] | s_fail[3]) break;
+        float* mbuf = reinterpret_cast<float*>(sm + C::kOffMerge);
+        constexpr int MR = C::kMergeRows;
+        for (int r0 = 0; r0 < R; r0 += MR) {
+            if (row_lo >= r0 && row_lo < r0 + MR) {
+                float* dst = mbuf + (warp * MR + row_lo - r0) * C::kMergeStride + tig * 2;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w * kRowMaxRows + r]);
-            float acc = 0.f, lsum = 0.f;
-            if (M != -INFINITY) {
+                for (int dn = 0; dn < D / 8; ++dn)
+                    *reinterpret_cast<float2*>(dst + dn * 8) = make_float2(o[dn][0], o[dn][1]);
+            }
+            if (row_hi >= r0 && row_hi < r0 + MR) {
+                float* dst = mbuf + (warp * MR + row_hi - r0) * C::kMergeStride + tig * 2;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float e = fast_exp2(m_s[w * kRowMaxRows + r] - M);
-                    acc += e * wo[(w * kRowMaxRows + r) * D + d];
-                    lsum += e * l_s[w * kRowMaxRows + r];
+                for (int dn = 0; dn < D / 8; ++dn)
+                    *reinterpret_cast<float2*>(dst + dn * 8) = make_float2(o[dn][2], o[dn][3]);
+            }
+            consumer_sync();
+            for (int idx = tid; idx < MR * D; idx += kConsumerThreads) {
+                const int r = r0 + idx / D, d = idx % D;
+                if (r >= R) continue;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) M = fmaxf(M, m_s[w * kRowMaxRows + r]);
+                float acc = 0.f, lsum = 0.f;
+                if (M != -INFINITY) {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float mw = m_s[w * kRowMaxRows + r];
+                        const float e = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+                        acc += e * mbuf[(w * MR + r - r0) * C::kMergeStride + d];
+                        lsum += e * l_s[w * kRowMaxRows + r];
+                    }
+                }
+                const int64_t orow = (int64_t)(q0 + r / G) * p.n_q_heads + g * G + r % G;
+                if (nsplit == 1) {
+                    const float v = lsum > 0.f ? acc / lsum : 0.f;
+                    p.out[orow * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                    if (d == 0 && p.lse != nullptr)
+                        p.lse[orow] = lsum > 0.f ? (M + __log2f(lsum)) * 0.69314718055994531f
+                                                 : -INFINITY;
+                } else {
+                    part_o[((int64_t)(first_item + split) * kRowMaxRows + r) * D + d] = acc;
+                    if (d == 0)
+                        part_ml[(int64_t)(first_item + split) * kRowMaxRows + r] =
+                            make_float2(M, lsum);
                 }
             }
-            const int64_t orow = (int64_t)(q0 + r / G) * p.n_q_heads + g * G + r % G;
-            if (nsplit == 1) {
-                const float v = lsum > 0.f ? acc / lsum : 0.f;
-                p.out[orow * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-                if (d == 0 && p.lse != nullptr)
-                    p.lse[orow] = lsum > 0.f ? (M + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
-            } else {
-                part_o[((int64_t)(first_item + split) * kRowMaxRows + r) * D + d] = acc;
-                if (d == 0)
-                    part_ml[(int64_t)(first_item + split) * kRowMaxRows + r] = make_float2(M, lsum);
-            }
+            consumer_sync();  // the buffer is free for the next rows (or item)
         }
-        consumer_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(last_st));
     }
 }
 
