@@ -804,13 +804,13 @@ __global__ void __launch_bounds__(kRowThreads, 1)
 // Merge the split-KV partials of one (sequence, KV head) group: one CTA per
 // group, out[row, h, :] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s and
 // lse = (M + log2 L) ln 2, with M the largest split maximum (log2 units).
-// Every phase issues its loads independently (one (split, row) pair or one
-// output element per thread), so the kernel costs a few memory latencies.
+// Each thread computes whole output elements: after the group descriptor it
+// issues the loads of all its elements' partials ((m, l) and o of every
+// split, eight splits at a time with a running maximum) at once, so the
+// kernel costs two dependent memory round trips and no block barrier.
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams p) {
-    constexpr int kMaxSplits = 64;  // more splits are folded over several passes
-    __shared__ float2 ml_s[kMaxSplits][kRowMaxRows];
-    __shared__ float M_s[kRowMaxRows], L_s[kRowMaxRows];
+    constexpr int kBatch = 8;  // splits whose loads are in flight together
     pdl_wait();
     pdl_launch_dependents();
     const int4 gd = reinterpret_cast<const int4*>(p.ws + p.lay.group_desc)[blockIdx.x];
@@ -821,48 +821,34 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
     const int R = gd.w * G;
     const float* part_o = reinterpret_cast<const float*>(p.ws + p.lay.partial_o);
     const float2* part_ml = reinterpret_cast<const float2*>(p.ws + p.lay.partial_ml);
-    const int tid = threadIdx.x;
-    if (tid < kRowMaxRows) {
-        M_s[tid] = -INFINITY;
-        L_s[tid] = 0.f;
-    }
-    for (int s0 = 0; s0 < ns; s0 += kMaxSplits) {
-        const int nb = min(kMaxSplits, ns - s0);
-        __syncthreads();
-        for (int idx = tid; idx < nb * kRowMaxRows; idx += blockDim.x) {
-            const int sp = idx / kRowMaxRows, r = idx % kRowMaxRows;
-            ml_s[sp][r] = r < R ? part_ml[(int64_t)(base + s0 + sp) * kRowMaxRows + r]
-                                : make_float2(-INFINITY, 0.f);
-        }
-        __syncthreads();
-        if (tid < R) {  // running max and normaliser over the splits so far
-            float M = M_s[tid];
-            for (int sp = 0; sp < nb; ++sp) M = fmaxf(M, ml_s[sp][tid].x);
-            float L = M == -INFINITY ? 0.f : L_s[tid] * fast_exp2(M_s[tid] - M);
-            for (int sp = 0; sp < nb; ++sp)
-                if (M != -INFINITY) L += fast_exp2(ml_s[sp][tid].x - M) * ml_s[sp][tid].y;
-            M_s[tid] = M;
-            L_s[tid] = L;
-        }
-    }
-    __syncthreads();
-    for (int idx = tid; idx < R * D; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < R * D; idx += blockDim.x) {
         const int r = idx / D, d = idx % D;
-        const float M = M_s[r];
-        float acc = 0.f;
-        for (int s0 = 0; s0 < ns; s0 += 8) {
-            float v[8], e[8];
+        float M = -INFINITY, L = 0.f, acc = 0.f;
+        for (int s0 = 0; s0 < ns; s0 += kBatch) {
+            float2 ml[kBatch];
+            float v[kBatch];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < kBatch; ++j) {
                 const int sp = s0 + j;
-                v[j] = sp < ns ? part_o[((int64_t)(base + sp) * kRowMaxRows + r) * D + d] : 0.f;
-                const float m = sp < ns ? part_ml[(int64_t)(base + sp) * kRowMaxRows + r].x : -INFINITY;
-                e[j] = (M == -INFINITY || m == -INFINITY) ? 0.f : fast_exp2(m - M);
+                const int64_t slot = (int64_t)(base + sp) * kRowMaxRows + r;
+                ml[j] = sp < ns ? part_ml[slot] : make_float2(-INFINITY, 0.f);
+                v[j] = sp < ns ? part_o[slot * D + d] : 0.f;
             }
+            float Mb = M;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc += e[j] * v[j];
+            for (int j = 0; j < kBatch; ++j) Mb = fmaxf(Mb, ml[j].x);
+            if (Mb == -INFINITY) continue;
+            const float a = M == -INFINITY ? 0.f : fast_exp2(M - Mb);
+            L *= a;
+            acc *= a;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const float e = ml[j].x == -INFINITY ? 0.f : fast_exp2(ml[j].x - Mb);
+                L += e * ml[j].y;
+                acc += e * v[j];
+            }
+            M = Mb;
         }
-        const float L = L_s[r];
         const int64_t orow = (int64_t)(q0 + r / G) * p.n_q_heads + g * G + r % G;
         p.out[orow * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? acc / L : 0.f));
         if (d == 0 && p.lse != nullptr)
