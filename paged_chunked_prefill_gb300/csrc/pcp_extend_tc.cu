@@ -21,10 +21,11 @@
 //                  per page run and 64-column block);
 //      warp 9      one thread issues tcgen05.mma: S_u = Q_u K^T into TMEM,
 //                  then O_u += P_u V with P_u read from TMEM;
-//      warps 10-11 page gathers of K/V for pages below 8 keys: 16 lanes cover
-//                  one 256-byte row with 16-byte cp.async (fully coalesced),
-//                  rows past the sequence end zero-filled.  (The TMA unit takes
-//                  about one box per ~100 cycles, so one-key boxes are hopeless.)
+//      warps 10-11 page gathers of K/V for pages below 8 keys, with the TMA
+//                  warp as a third gatherer: 16 lanes cover one 256-byte row
+//                  with 16-byte cp.async (fully coalesced), rows past the
+//                  sequence end zero-filled.  (The TMA unit takes about one box
+//                  per ~100 cycles, so one-key boxes are hopeless.)
 //    K and V land in 128-byte-swizzled shared-memory stages either way.
 //  * Ping-pong: while one softmax group works on its S tile, the tensor core
 //    runs the other group's QK^T or PV.
@@ -249,30 +250,34 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
     return below_hi & ~below_lo;
 }
 
-// One gather warp's share (rows gw*64 .. gw*64+63) of a K or V tile: lanes
-// split into groups covering one 256-byte (128-byte for D = 64) row each.
+// One gather warp's share (rows [gw * 43, min(128, gw * 43 + 43)) of the
+// three warps) of a K or V tile: lanes split into groups covering one 256-byte
+// (128-byte for D = 64) row each.
 template <int D>
 struct GatherShape {
     static constexpr int kChunks = D / 8;                     // 16-byte chunks per row
     static constexpr int kRowsPerInst = 32 / kChunks;         // rows per warp instruction
-    static constexpr int kRows = kTileN / kGatherWarps;       // rows per warp per tile
-    static constexpr int kInsts = kRows / kRowsPerInst;       // instructions per tile
+    static constexpr int kRows = (kTileN + kGatherWarps - 1) / kGatherWarps;  // 43 rows at most
+    static constexpr int kInsts = (kRows + kRowsPerInst - 1) / kRowsPerInst;  // instructions
+    static_assert(kRows > 32 && kRows <= 64, "two 32-row lookups per gather warp");
 };
 
-// sa / sb: the slots of the warp's rows `lane` and `lane + 32` (-1: none);
-// the copy lanes of a row take its slot by shuffle.
+// sa / sb: the slots of the warp's rows `lane` and `lane + 32` of its share
+// (-1: none); the copy lanes of a row take its slot by shuffle.  Rows past
+// the share (`nrows`) belong to the next warp and are skipped.
 template <int D>
 __device__ __forceinline__ void gather_kv_rows(const TcParams& p, const Geo& geo, int sa, int sb,
                                                const uint16_t* pool, uint32_t dst, int gw,
-                                               int lane) {
+                                               int nrows, int lane) {
     using C = TcCfg<D>;
     using GS = GatherShape<D>;
     const int c = lane % GS::kChunks;
     const int rsub = lane / GS::kChunks;
 #pragma unroll
     for (int j = 0; j < GS::kInsts; ++j) {
-        const int rw = j * GS::kRowsPerInst + rsub;  // row among the warp's 64
+        const int rw = j * GS::kRowsPerInst + rsub;  // row among the warp's share
         const int slot = __shfl_sync(0xffffffffu, j * GS::kRowsPerInst < 32 ? sa : sb, rw & 31);
+        if (rw >= nrows) continue;
         const int row = gw * GS::kRows + rw;
         const bool ok = slot >= 0;
         const uint16_t* src =
@@ -314,6 +319,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(bar(C::bQFull), 1);
         // TMA path: one arrive.expect_tx; gather path: one arrival per gather lane
         const uint32_t full_count = p.box_rows > 0 ? 1u : 32u * kGatherWarps;
+        // the warps that issue cp.async (or stand by for it) and drain it on
+        // the abort path: 10 and 11 with page boxes, 8, 10 and 11 gathering
+        const uint32_t drain_count = p.box_rows > 0 ? 64u : 32u * kGatherWarps;
         for (int s = 0; s < SK; ++s) {
             mbar_init(bar(C::bKFull + s), full_count);
             mbar_init(bar(C::bKEmpty + s), 1);
@@ -328,7 +336,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(bar(C::bODone + u), 1);
         }
         mbar_init(bar(C::bDrain), 1);
-        mbar_init(bar(C::bGatherDrain), 32u * kGatherWarps);
+        mbar_init(bar(C::bGatherDrain), drain_count);
         mbar_init(bar(C::bStall), 1);
         fence_mbarrier_init();
         misc[2] = 0;
@@ -374,12 +382,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the V tiles.  The TMA unit accepts a warp's boxes one lane after the
         // other (about 140 cycles per 2 KB box), so two issuing warps double
         // the rate at which small pages arrive.
-        const bool kv_tma_warp =
-            warp == kWarpTma || (p.box_rows > 0 && warp == kWarpGather0);
-        if (kv_tma_warp) {
-            // ------------------------------------------------ TMA: Q, K / V
-            const bool is_k = warp == kWarpTma;
-            if (is_k && lane == 0) {
+        if (warp == kWarpTma || warp >= kWarpGather0) {
+            if (warp == kWarpTma && lane == 0) {  // Q, by TMA on both paths
                 mbar_arrive_expect_tx(bar(C::bQFull),
                                       (uint32_t)(geo.nq * C::kHalves * G * p.qpos * 128));
                 for (int u = 0; u < geo.nq; ++u)
@@ -388,88 +392,97 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                     bar(C::bQFull), h * 64, geo.g * G, geo.q_row0 + u * p.qpos);
             }
             if (p.box_rows > 0) {
-                const int32_t* pages = p.kv_indices + p.kv_indptr[geo.b];
-                int z_cur = fetch_box_slot<D>(p, geo, pages, geo.t_begin, lane);
-                for (int i = 0; i < ntiles; ++i) {
-                    const int t = geo.t_begin + i;
-                    const uint32_t cur = kv_iter + i;
-                    // the next tile's page ids are in flight while this one waits
-                    const int z_next =
-                        i + 1 < ntiles ? fetch_box_slot<D>(p, geo, pages, t + 1, lane) : z_cur;
-                    // every wait is decided for the whole warp: the box issue
-                    // below has warp-collective steps
-                    if (is_k) {
-                        const int sk = cur % SK;
+                // ------------------------------------------------ TMA: K / V page boxes
+                const bool is_k = warp == kWarpTma;
+                if (warp == kWarpTma || warp == kWarpGather0) {
+                    const int32_t* pages = p.kv_indices + p.kv_indptr[geo.b];
+                    int z_cur = fetch_box_slot<D>(p, geo, pages, geo.t_begin, lane);
+                    for (int i = 0; i < ntiles; ++i) {
+                        const int t = geo.t_begin + i;
+                        const uint32_t cur = kv_iter + i;
+                        // the next tile's page ids are in flight while this one waits
+                        const int z_next =
+                            i + 1 < ntiles ? fetch_box_slot<D>(p, geo, pages, t + 1, lane) : z_cur;
+                        // every wait is decided for the whole warp: the box issue
+                        // below has warp-collective steps
+                        if (is_k) {
+                            const int sk = cur % SK;
+                            if (!__all_sync(0xffffffffu,
+                                            mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u,
+                                                      abort_flag, p.dev_err, kSpinLimitNs)))
+                                break;
+                            tma_kv_tile<D>(p, geo, t, z_cur, &tm_k, p.k_pool,
+                                           sK + sk * C::kTileBytes, bar(C::bKFull + sk), false,
+                                           lane);
+                        } else {
+                            const int sv = cur % SV;
+                            if (!__all_sync(0xffffffffu,
+                                            mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u,
+                                                      abort_flag, p.dev_err, kSpinLimitNs)))
+                                break;
+                            tma_kv_tile<D>(p, geo, t, z_cur, &tm_v, p.v_pool,
+                                           sV + sv * C::kTileBytes, bar(C::bVFull + sv), true,
+                                           lane);
+                        }
+                        last_issued = (int)cur;
+                        z_cur = z_next;
+                    }
+                }
+            } else {
+                // ------------------------------------------------ cp.async page gathers
+                // warps 10, 11 and 8 each copy a third of the rows of every K and
+                // V tile (three warps issuing cp.async in parallel)
+                {
+                    using GS = GatherShape<D>;
+                    const int gw = warp == kWarpTma ? 2 : warp - kWarpGather0;
+                    const int nrows = min(GS::kRows, kTileN - gw * GS::kRows);
+                    const int32_t* pages = p.kv_indices + p.kv_indptr[geo.b];
+                    // Slot of key `key` (-1 past the sequence end or for a bad page).
+                    auto slot_of = [&](int key) {
+                        int slot = -1;
+                        if (key < geo.L) {
+                            const int entry = p.page_shift >= 0 ? key >> p.page_shift
+                                                                : key / p.page_size;
+                            const int page = pages[entry];
+                            if (page >= 0 && page < p.num_pages)
+                                slot = page * p.page_size + (key - entry * p.page_size);
+                            else
+                                report_error(p.dev_err, PCP_ERR_BAD_INDEX);
+                        }
+                        return slot;
+                    };
+                    // The warp's rows of tile t: lane l looks up rows l and l + 32
+                    // of its share (consecutive page-table entries, one coalesced
+                    // load each), one tile ahead of their use; a row's copy lanes
+                    // take its slot by shuffle.
+                    const int row0 = gw * GS::kRows;
+                    const bool hi_ok = 32 + lane < nrows;
+                    int sa = slot_of(geo.t_begin * kTileN + row0 + lane);
+                    int sb = hi_ok ? slot_of(geo.t_begin * kTileN + row0 + 32 + lane) : -1;
+                    for (int i = 0; i < ntiles; ++i) {
+                        const int t = geo.t_begin + i;
+                        const uint32_t cur = kv_iter + i;
+                        const int sk = cur % SK, sv = cur % SV;
+                        const int ca = sa, cb = sb;
+                        if (i + 1 < ntiles) {  // the next tile's lookups are in flight meanwhile
+                            sa = slot_of((t + 1) * kTileN + row0 + lane);
+                            sb = hi_ok ? slot_of((t + 1) * kTileN + row0 + 32 + lane) : -1;
+                        }
                         if (!__all_sync(0xffffffffu,
                                         mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u,
                                                   abort_flag, p.dev_err, kSpinLimitNs)))
                             break;
-                        tma_kv_tile<D>(p, geo, t, z_cur, &tm_k, p.k_pool,
-                                       sK + sk * C::kTileBytes, bar(C::bKFull + sk), false, lane);
-                    } else {
-                        const int sv = cur % SV;
+                        gather_kv_rows<D>(p, geo, ca, cb, p.k_pool, sK + sk * C::kTileBytes, gw,
+                                          nrows, lane);
+                        cp_async_mbar_arrive_noinc(bar(C::bKFull + sk));
                         if (!__all_sync(0xffffffffu,
                                         mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u,
                                                   abort_flag, p.dev_err, kSpinLimitNs)))
                             break;
-                        tma_kv_tile<D>(p, geo, t, z_cur, &tm_v, p.v_pool,
-                                       sV + sv * C::kTileBytes, bar(C::bVFull + sv), true, lane);
+                        gather_kv_rows<D>(p, geo, ca, cb, p.v_pool, sV + sv * C::kTileBytes, gw,
+                                          nrows, lane);
+                        cp_async_mbar_arrive_noinc(bar(C::bVFull + sv));
                     }
-                    last_issued = (int)cur;
-                    z_cur = z_next;
-                }
-            }
-        } else if (warp >= kWarpGather0) {
-            // ------------------------------------------------ cp.async page gathers
-            // each gather warp copies rows gw*64 .. gw*64+63 of every K and V
-            // tile (two warps issuing cp.async in parallel)
-            if (p.box_rows == 0) {
-                using GS = GatherShape<D>;
-                static_assert(GS::kRows == 64, "two 32-row halves per gather warp and tile");
-                const int gw = warp - kWarpGather0;
-                const int32_t* pages = p.kv_indices + p.kv_indptr[geo.b];
-                // Slot of key `key` (-1 past the sequence end or for a bad page).
-                auto slot_of = [&](int key) {
-                    int slot = -1;
-                    if (key < geo.L) {
-                        const int entry = p.page_shift >= 0 ? key >> p.page_shift
-                                                            : key / p.page_size;
-                        const int page = pages[entry];
-                        if (page >= 0 && page < p.num_pages)
-                            slot = page * p.page_size + (key - entry * p.page_size);
-                        else
-                            report_error(p.dev_err, PCP_ERR_BAD_INDEX);
-                    }
-                    return slot;
-                };
-                // The warp's 64 rows of tile t: lane l looks up rows l and
-                // l + 32 (consecutive page-table entries, one coalesced load
-                // each), one tile ahead of their use; a row's copy lanes take
-                // its slot by shuffle.
-                const int row0 = gw * GS::kRows;
-                int sa = slot_of(geo.t_begin * kTileN + row0 + lane);
-                int sb = slot_of(geo.t_begin * kTileN + row0 + 32 + lane);
-                for (int i = 0; i < ntiles; ++i) {
-                    const int t = geo.t_begin + i;
-                    const uint32_t cur = kv_iter + i;
-                    const int sk = cur % SK, sv = cur % SV;
-                    const int ca = sa, cb = sb;
-                    if (i + 1 < ntiles) {  // the next tile's lookups are in flight meanwhile
-                        sa = slot_of((t + 1) * kTileN + row0 + lane);
-                        sb = slot_of((t + 1) * kTileN + row0 + 32 + lane);
-                    }
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait(bar(C::bKEmpty + sk), ((cur / SK) & 1u) ^ 1u,
-                                              abort_flag, p.dev_err, kSpinLimitNs)))
-                        break;
-                    gather_kv_rows<D>(p, geo, ca, cb, p.k_pool, sK + sk * C::kTileBytes, gw, lane);
-                    cp_async_mbar_arrive_noinc(bar(C::bKFull + sk));
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait(bar(C::bVEmpty + sv), ((cur / SV) & 1u) ^ 1u,
-                                              abort_flag, p.dev_err, kSpinLimitNs)))
-                        break;
-                    gather_kv_rows<D>(p, geo, ca, cb, p.v_pool, sV + sv * C::kTileBytes, gw, lane);
-                    cp_async_mbar_arrive_noinc(bar(C::bVFull + sv));
                 }
             }
         } else if (warp == kWarpMma) {
@@ -786,7 +799,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     volatile int* no_abort = &misc[3];
     if (warp == kWarpTma || warp >= kWarpGather0) {
         cp_async_wait_all();
-        if (aborted && warp >= kWarpGather0) {
+        if (aborted && (warp >= kWarpGather0 || p.box_rows == 0)) {
             // the mbarrier arrivals the gathers' cp.async copies trigger have
             // been made once this one, triggered after all of them, lands
             cp_async_mbar_arrive_noinc(bar(C::bGatherDrain));

@@ -16,8 +16,8 @@ constexpr int kQTiles = 2;        // Q tiles per work item (share each K/V tile)
 constexpr int kTcThreads = 384;   // 2 x 4 softmax warps, TMA warp, MMA warp, 2 gather warps
 constexpr int kWarpTma = 8;       // Q (and the K page boxes) by TMA
 constexpr int kWarpMma = 9;       // one thread issues tcgen05.mma
-constexpr int kWarpGather0 = 10;  // warps 10, 11: cp.async page gathers of K/V
-constexpr int kGatherWarps = 2;
+constexpr int kWarpGather0 = 10;  // warps 10, 11 (and the TMA warp): cp.async page gathers of K/V
+constexpr int kGatherWarps = 3;   // gathering warps on the cp.async path: 10, 11 and 8
 // Pages whose runs inside a 128-key tile hold at least this many keys are
 // loaded by TMA boxes; smaller ones by the cp.async gather warps (below 8
 // rows the TMA unit's per-box cost dominates; above, TMA out-runs them).
