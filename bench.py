@@ -630,11 +630,14 @@ def end_to_end(args, torch, pcp, batch, d, out_ref, flush, stream, flops, world)
 
 
 def attn_figures(pcp, torch, batch, dev, peaks, flush, err, n=20, warm=5, causal=True,
-                 mask=None, pairs=None, key=None):
+                 mask=None, pairs=None, key=None, computed_pairs=None):
     """One attention call on `batch` (its chunk's K/V appended first), L2
     flushed before each timed call: the whole call, and the tensor-core and
     row kernels alone between per-call events.  Effective FLOPs count the
-    visible pairs only (`pairs` per head when a mask hides more keys)."""
+    visible pairs only (`pairs` per head when a mask hides more keys).  With
+    a boolean mask the kernel still multiplies every pair its causal range
+    holds and drops the masked ones in the softmax: `computed_pairs` (per
+    head) gives that figure too, the rate at which the tensor cores work."""
     d = to_device(batch, dev)
     loc = pcp.compute_out_cache_loc(d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
                                     d["prefix_lens"], batch.page_size, batch.num_pages)
@@ -651,17 +654,29 @@ def attn_figures(pcp, torch, batch, dev, peaks, flush, err, n=20, warm=5, causal
                               d["prefix_lens"], d["k_pool"], d["v_pool"], batch.page_size,
                               batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.window,
                               batch.sm_scale, out=out, lse=lse, workspace=ws, dev_err=err,
-                              qo_indptr_host=batch.qo_indptr, causal=causal, mask=mask_t,
+                              qo_indptr_host=batch.qo_indptr,
+                              prefix_lens_host=batch.prefix_lens, causal=causal, mask=mask_t,
                               tc_events=tc_ev, rows_events=row_ev)
     tc_pairs, row_bytes = split_work(batch)
     all_pairs = visible_pairs(batch.prefix_lens, batch.chunk_lens, batch.window)
+    # the plan the call made (workspace header: n_tc_items, n_row_groups;
+    # written by the planner kernel, which a call with tensor-core work
+    # runs): decode-shaped chunks that joined the tensor-core queue count there
+    call()
+    n_tc_items, n_row_groups = (int(x) for x in ws[:8].view(torch.int32).cpu().tolist())
+    absorbed = tc_pairs > 0 and row_bytes > 0 and n_row_groups == 0
+    if absorbed:
+        tc_pairs, row_bytes = all_pairs, 0
     if pairs is not None:  # a mask or non-causal call: all its work is on the tensor cores
         all_pairs = tc_pairs = pairs
     D, Hq = batch.head_dim, batch.n_q_heads
     ms = time_calls(torch, lambda ev: call(), flush, n=n, warm=warm)
     r = {"workload": batch.name, "ms": ms,
          "TFLOP/s": 4 * D * Hq * all_pairs / (ms * 1e-3) / 1e12,
-         "what": "whole call (planner, kernels, combine), effective FLOPs of visible pairs"}
+         "what": "whole call (planner, kernels, combine), effective FLOPs of visible pairs",
+         **({"tc_items": n_tc_items, "row_groups": n_row_groups} if tc_pairs > 0 else {})}
+    if absorbed:
+        r["decode_rows_on_tensor_cores"] = True
     r["frac_bf16"] = r["TFLOP/s"] / peaks["bf16_tflops"]
     if tc_pairs > 0:
         kms = time_calls(torch, lambda ev: call(tc_ev=ev), flush, n=n, warm=warm, events=True)
@@ -671,6 +686,13 @@ def attn_figures(pcp, torch, batch, dev, peaks, flush, err, n=20, warm=5, causal
                           "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
                           "visible_pairs_per_head": int(tc_pairs),
                           "traffic": ncu_traffic(key, f"extend_tc_kernel<{D}>") if key else None}
+        if computed_pairs is not None:
+            ctf = 4 * D * Hq * computed_pairs / (kms * 1e-3) / 1e12
+            r["tc_kernel"].update({
+                "computed_pairs_per_head": int(computed_pairs), "computed_TFLOP/s": ctf,
+                "frac_computed": ctf / peaks["bf16_tflops"],
+                "what_computed": "every causal pair multiplied, masked ones included: the "
+                                 "tensor-core rate; frac counts the kept pairs only"})
     if row_bytes > 0 and pairs is None:
         kms = time_calls(torch, lambda ev: call(row_ev=ev), flush, n=n, warm=warm, events=True)
         gbs = row_bytes / (kms * 1e-3) / 1e9
@@ -695,7 +717,8 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
     gbs = nbytes / (r["ms"] * 1e-3) / 1e9
     res["decode_rows"] = {"workload": db.name, "ms": r["ms"], "GB/s": gbs,
                           "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes,
-                          "what": "whole call: planner, row kernel, split-KV combine"}
+                          "what": "whole call: row kernel (planning its own split), split-KV "
+                                  "combine"}
     res["decode_rows_kernel"] = r["row_kernel"]
 
     # the same 31 rows as a serving decode step: the fused append of their
@@ -833,7 +856,8 @@ def masked_secondary(pcp, torch, W, dev, peaks, flush, err):
                       pairs=int((C * (P + C)).sum()))
     nc["workload"] += ", non-causal"
     mk = attn_figures(pcp, torch, gb, dev, peaks, flush, err, n=10, warm=3, mask=mask_np,
-                      pairs=masked_pairs)
+                      pairs=masked_pairs,
+                      computed_pairs=visible_pairs(gb.prefix_lens, gb.chunk_lens, 0))
     mk["workload"] += ", causal + 2-D key mask keeping 1/2"
     return {"non_causal_attn": nc, "masked_2d_attn": mk}
 

@@ -422,9 +422,10 @@ pcp_status pcp_copy_page_slots(void* k_pool, void* v_pool, int64_t num_pages, in
 pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_err);
 
 /*
- * Per-call instrumentation, for profiling and for tests of the device-side
- * error paths.  The pages have no counterpart.  A zeroed struct (or a NULL
- * pointer) means: no events, the default wait limit.
+ * Per-call options: instrumentation for profiling and for tests of the
+ * device-side error paths (the pages have no counterpart), and a host copy
+ * of prefix_lens for the launch decision.  A zeroed struct (or a NULL
+ * pointer) means: no events, the default wait limit, no host copy.
  *   tc_event_before / tc_event_after: NULL, or cudaEvent_t values (as void*)
  *     recorded on the call's stream right before and right after the launch
  *     of the tensor-core kernel, so the caller can time that kernel alone
@@ -445,6 +446,18 @@ pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_er
  *     the 2 s limit), its tensor memory is freed and it exits.  The call's
  *     results are then undefined; the device, the stream and the library
  *     stay usable.
+ *   prefix_lens_host: NULL, or a HOST copy of prefix_lens ([batch] int32,
+ *     read during the call only), used together with qo_indptr_host.  A call
+ *     with tensor-core work takes its decode-shaped chunks onto the tensor
+ *     cores (one-Q-tile items in the longest-first queue) when the longest
+ *     of them, charged 4/5 of a two-Q-tile step per 128-key tile, stays
+ *     within 1.1 times the larger of the longest prompt item and the
+ *     average work per SM.  Without both host copies the planner kernel
+ *     decides this on the device, and the row kernel and the combine are
+ *     launched and find no work when it takes them on; with both, the host
+ *     makes the same decision and launches only the kernels that have work.
+ *     The decision moves work between kernels only: results are correct
+ *     either way (bit-identical whenever the decision is the same).
  * The library keeps nothing of it after the call returns.
  */
 typedef struct pcp_call_options {
@@ -453,6 +466,7 @@ typedef struct pcp_call_options {
     void* rows_event_before;
     void* rows_event_after;
     uint64_t test_stall_ns;
+    const int32_t* prefix_lens_host;
 } pcp_call_options;
 
 /*

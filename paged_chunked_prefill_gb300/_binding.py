@@ -32,10 +32,11 @@ class Status(enum.IntEnum):
 
 class CallOptions(ctypes.Structure):
     """``pcp_call_options``: per-call events around the tensor-core and row
-    kernels, and the stall that tests the kernels' timeout path."""
+    kernels, the stall that tests the kernels' timeout path, and the host
+    copy of prefix_lens."""
     _fields_ = [("tc_event_before", ctypes.c_void_p), ("tc_event_after", ctypes.c_void_p),
                 ("rows_event_before", ctypes.c_void_p), ("rows_event_after", ctypes.c_void_p),
-                ("test_stall_ns", ctypes.c_uint64)]
+                ("test_stall_ns", ctypes.c_uint64), ("prefix_lens_host", ctypes.c_void_p)]
 
 
 class PCPError(RuntimeError):
@@ -312,6 +313,7 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
                       qo_indptr_host=None, causal: bool = True,
                       mask: Optional[torch.Tensor] = None,
                       tc_events=None, rows_events=None, test_stall_ns: int = 0,
+                      prefix_lens_host=None,
                       check: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
     """Extend attention of every query row over its cached prefix and own
     chunk (bottom-right causal, GQA, optional window).  Returns (out, lse):
@@ -320,6 +322,11 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
     qo_indptr_host: optional host copy of qo_indptr (numpy int32 array or CPU
     int32 tensor); with it the call skips the launch of a kernel that would
     have no work.
+    prefix_lens_host: optional host copy of prefix_lens; with qo_indptr_host
+    the host decides whether the decode-shaped chunks of a call with
+    tensor-core work join the tensor-core queue (otherwise the planner
+    kernel decides it on the device), and skips the row kernel and the
+    combine when they do.
     causal=False: every row sees all keys of its sequence (no window).
     mask: optional bool tensor (True = keep) of shape [B, kv] or
     [B, 1|Hq, 1|q, kv], indexed by the row inside the chunk and the key
@@ -354,11 +361,13 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
     if own:
         dev_err = _dev_err(dev)
     host_ptr, host_keep = _host_i32(qo_indptr_host, batch + 1, "qo_indptr_host")
-    if tc_events is not None or rows_events is not None or test_stall_ns:
+    pl_ptr, pl_keep = _host_i32(prefix_lens_host, batch, "prefix_lens_host")
+    if (tc_events is not None or rows_events is not None or test_stall_ns or
+            prefix_lens_host is not None):
         ev = lambda e: ctypes.c_void_p(e.cuda_event) if e is not None else ctypes.c_void_p(0)
         tb, ta = tc_events if tc_events is not None else (None, None)
         rb, ra = rows_events if rows_events is not None else (None, None)
-        opts = CallOptions(ev(tb), ev(ta), ev(rb), ev(ra), int(test_stall_ns))
+        opts = CallOptions(ev(tb), ev(ta), ev(rb), ev(ra), int(test_stall_ns), pl_ptr)
         mkeep, mptr, sb, sh, sq, mq, mkv = _mask_args(mask, batch, n_q_heads, dev)
         _check(lib().pcp_paged_extend_attn_ex(
             _ptr(q), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(prefix_lens),
@@ -383,7 +392,7 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
             sb, sh, sq, mq, mkv, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
             _ptr(dev_err), _stream(dev)), "pcp_paged_extend_attn_masked")
         del mkeep
-    del host_keep
+    del host_keep, pl_keep
     _finish(dev_err, own, check, "pcp_paged_extend_attn")
     return out, lse
 

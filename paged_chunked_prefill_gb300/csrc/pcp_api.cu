@@ -196,6 +196,35 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     int sms = 0;
     st = sm_count(&sms);
     if (st != PCP_OK) return st;
+
+    // With host copies of qo_indptr and prefix_lens the host decides whether
+    // a call with both kinds of chunks takes its decode-shaped ones onto the
+    // tensor cores (the planner's rule, absorb_decode_rows, on the same
+    // figures) and then launches only the kernels that have work.
+    int absorb = -1;
+    if (run_tc && run_rows && a.qo_indptr_host != nullptr && o.prefix_lens_host != nullptr) {
+        const int item_pos = q_positions_per_tile(group) * kQTiles;
+        unsigned long long w_tc = 0, w_dec = 0;
+        int max_tc = 0, max_dec = 0;
+        for (int b = 0; b < a.batch; ++b) {
+            const int c = a.qo_indptr_host[b + 1] - a.qo_indptr_host[b];
+            const int P = o.prefix_lens_host[b];
+            if (c <= 0 || P < 0 || (int64_t)P + c >= INT32_MAX) continue;
+            if (c > rmax) {
+                for (int k = 0; k * item_pos < c; ++k) {
+                    const int t = tc_item_tiles(P, c, k, item_pos, a.window, a.causal);
+                    w_tc += (unsigned long long)t * a.n_kv_heads;
+                    max_tc = t > max_tc ? t : max_tc;
+                }
+            } else {
+                const int t = dec_weight(tc_item_tiles(P, c, 0, item_pos, a.window, a.causal));
+                w_dec += (unsigned long long)t * a.n_kv_heads;
+                max_dec = t > max_dec ? t : max_dec;
+            }
+        }
+        absorb = absorb_decode_rows(w_tc, max_tc, w_dec, max_dec, sms) ? 1 : 0;
+        if (absorb == 1) run_rows = false;
+    }
     EncodeFn enc = nullptr;
     st = get_encoder(&enc);
     if (st != PCP_OK) return st;
@@ -244,6 +273,7 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     pp.window = a.window;
     pp.causal = a.causal;
     pp.tc_work = run_tc ? 1 : 0;
+    pp.absorb = absorb;
     pp.sm_count = sms;
     pp.ws = ws;
     pp.lay = lay;
@@ -354,7 +384,7 @@ const char* pcp_status_string(int status) {
     }
 }
 
-int pcp_abi_version(void) { return 3; }
+int pcp_abi_version(void) { return 4; }
 
 const char* pcp_last_cuda_error(void) {
     return t_last_cuda == cudaSuccess ? "no error" : cudaGetErrorString(t_last_cuda);

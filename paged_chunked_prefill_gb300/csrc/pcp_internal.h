@@ -46,6 +46,37 @@ __host__ __device__ inline int row_path_max_chunk(int group) {
 
 __host__ __device__ inline int q_positions_per_tile(int group) { return kTileM / group; }
 
+// Whether a call with tensor-core work takes its decode-shaped chunks onto
+// the tensor cores as one-Q-tile items: the longest of them (w: 4/5 of its
+// KV tiles, rounded up, in two-Q-tile steps) within 1.1 times the larger of
+// the longest prompt item and the average work per SM.  w_tc / max_tc: the
+// prompt items' summed and largest cost in KV tiles; w_dec / max_dec: the
+// decode-shaped items' weighted ones (per KV head included in the sums).
+__host__ __device__ inline int dec_weight(int tiles) { return (4 * tiles + 4) / 5; }
+__host__ __device__ inline bool absorb_decode_rows(unsigned long long w_tc, int max_tc,
+                                                   unsigned long long w_dec, int max_dec,
+                                                   int sm_count) {
+    if (w_tc == 0 || w_dec == 0) return false;
+    // 10 * max_dec <= 11 * max(max_tc, (w_tc + w_dec) / sms), in integers
+    const unsigned long long sms = sm_count > 0 ? (unsigned long long)sm_count : 1ull;
+    const unsigned long long lhs = 10ull * (unsigned long long)max_dec * sms;
+    const unsigned long long a = 11ull * (unsigned long long)max_tc * sms;
+    const unsigned long long b = 11ull * (w_tc + w_dec);
+    return lhs <= (a > b ? a : b);
+}
+
+// KV tiles of tensor-core item k (positions [k * item_pos, ...)) of a chunk
+// of c rows after a prefix of P keys: from the first key its first row sees
+// to its last row (causal) or the sequence end.
+__host__ __device__ inline int tc_item_tiles(int P, int c, int k, int item_pos, int window,
+                                             int causal) {
+    const int first = P + k * item_pos;
+    const int end = (k + 1) * item_pos < c ? (k + 1) * item_pos : c;
+    const int last = causal ? P + end - 1 : P + c - 1;
+    const int lo = window > 0 ? (first - window + 1 > 0 ? first - window + 1 : 0) : 0;
+    return last / kTileN - lo / kTileN + 1;
+}
+
 // The row-tile split charges every row group's start as this many extra
 // tiles: a CTA's time grows with the group pieces it takes (their Q loads,
 // boundary tiles and four-warp merges cost about two tiles' streaming time
@@ -166,6 +197,8 @@ struct PlanParams {
     int window;
     int causal;
     int tc_work;       // 0: the host knows no chunk goes to the tensor cores
+    int absorb;        // decode-shaped chunks on the tensor cores: 1 / 0 as the host
+                       // decided, -1: the planner decides (absorb_decode_rows)
     int sm_count;
     unsigned char* ws;
     WsLayout lay;

@@ -23,6 +23,14 @@
 //    log-sum-exp combine.  This is the split-KV idea of the AstrAI paged
 //    decode kernel (splits from the SM count, partials merged by a combine
 //    step) with the split points chosen for equal work per SM.
+//  * a call that has tensor-core work takes its decode-shaped chunks onto the
+//    tensor cores as one-Q-tile items when the longest of them ends within
+//    the tensor-core schedule's expected length: the longest-first queue
+//    then fills the SMs that the prompt items leave idle, and the row kernel
+//    and the combine find no work.  A decode-shaped item costs about 0.8 of
+//    a two-Q-tile step per KV tile (its one Q tile alone: measured 1.66 us
+//    against 2.07 us on the GQA workload), so it is charged that in the
+//    longest-first order and in the test.
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
 #include "pcp_launch.h"
@@ -61,13 +69,11 @@ __device__ __forceinline__ int cost_bucket(int cost) {
     return cost < 64 ? cost : min(1023, 64 + ((cost - 64) >> 4));
 }
 
-// KV tiles of tensor-core item k of a chunk: up to the item's last row
-// (causal), or every key of the sequence (non-causal).
+
+// KV tiles of tensor-core item k of a chunk (tc_item_tiles).
 __device__ __forceinline__ int tc_cost(int P, int c, int k, int item_pos, int window,
                                        int causal) {
-    const int first = P + k * item_pos;
-    const int last = causal ? P + min((k + 1) * item_pos, c) - 1 : P + c - 1;
-    return last / kTileN - first_key(first, window) / kTileN + 1;
+    return tc_item_tiles(P, c, k, item_pos, window, causal);
 }
 
 // Turn a 1024-bucket histogram into descending exclusive offsets (bucket
@@ -165,7 +171,10 @@ __device__ __forceinline__ int warp_agg_add(int* base, int key, int inc) {
 // through prefix sums, so a long chunk does not serialise on one thread.
 __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanParams p) {
     __shared__ int hist[1024];
+    __shared__ int hist_dec[1024];  // decode-shaped chunks as tensor-core items
     __shared__ int warp_sums[64];
+    __shared__ unsigned long long s_w_tc, s_w_dec;  // summed costs (two-Q-tile steps)
+    __shared__ int s_max_tc, s_max_dec;             // longest item of each kind
     __shared__ int s_a[1025];       // per-sequence counts, then their exclusive prefix
     __shared__ int s_b[1025];
     __shared__ int s_c[1025];
@@ -190,7 +199,12 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     // workspace may still be read by the previous call's kernels).
     pdl_launch_dependents();
     hist[tid] = 0;
-    if (tid == 0) s_row_tiles = 0;
+    hist_dec[tid] = 0;
+    if (tid == 0) {
+        s_row_tiles = 0;
+        s_w_tc = s_w_dec = 0;
+        s_max_tc = s_max_dec = 0;
+    }
     bool bad_meta = false;  // this thread saw contradictory metadata
 
     // metadata of sequence chunk0 + tid (kept in s_seq); notes bad sequences
@@ -212,16 +226,29 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
         s_seq[tid] = v;
         s_off[tid] = off;
     };
-    auto n_tc_of = [&](int4 v) {  // tensor-core items of one KV head
-        return (v.z && v.x > rmax) ? (v.x + item_pos - 1) / item_pos : 0;
+    // tensor-core items of one KV head (decode-shaped chunks: one, when
+    // the call takes them onto the tensor cores)
+    auto n_tc_of = [&](int4 v, bool absorb) {
+        return (v.z && (v.x > rmax || (absorb && v.w > 0))) ? (v.x + item_pos - 1) / item_pos
+                                                            : 0;
     };
     const bool one_chunk = p.batch <= 1024;
 
-    // ---- sweep 1: tensor-core cost histogram, row tile total
+    // ---- sweep 1: tensor-core cost histogram, row tile total, and both
+    // kinds' total and longest cost
+    unsigned long long w_tc = 0, w_dec = 0;
+    int max_tc = 0, max_dec = 0;
     for (int chunk0 = 0; chunk0 < p.batch; chunk0 += 1024) {
         __syncthreads();
         load_chunk(chunk0, true);
-        s_a[tid] = n_tc_of(s_seq[tid]);
+        s_a[tid] = n_tc_of(s_seq[tid], false);
+        if (p.tc_work && s_seq[tid].w > 0) {
+            // a decode-shaped chunk: one item of its row tiles per KV head
+            const int wc = dec_weight(s_seq[tid].w);
+            w_dec += (unsigned long long)wc * H;
+            max_dec = max(max_dec, wc);
+            warp_agg_add(hist_dec, cost_bucket(wc), H);
+        }
         // each row group adds its virtual start tiles to the split
         unsigned long long rt =
             s_seq[tid].w > 0 ? (unsigned long long)(s_seq[tid].w + kRowGroupStartTiles) * H : 0;
@@ -235,13 +262,38 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
                 const int sl = segment_of(s_a, 1024, f);
                 const int4 v = s_seq[sl];
                 const int cost = tc_cost(v.y, v.x, f - s_a[sl], item_pos, p.window, p.causal);
+                w_tc += (unsigned long long)cost * H;
+                max_tc = max(max_tc, cost);
                 warp_agg_add(hist, cost_bucket(cost), H);
             }
         }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        w_tc += __shfl_xor_sync(0xffffffffu, w_tc, o);
+        w_dec += __shfl_xor_sync(0xffffffffu, w_dec, o);
+        max_tc = max(max_tc, __shfl_xor_sync(0xffffffffu, max_tc, o));
+        max_dec = max(max_dec, __shfl_xor_sync(0xffffffffu, max_dec, o));
+    }
+    if (lane == 0) {
+        if (w_tc) atomicAdd(&s_w_tc, w_tc);
+        if (w_dec) atomicAdd(&s_w_dec, w_dec);
+        atomicMax(&s_max_tc, max_tc);
+        atomicMax(&s_max_dec, max_dec);
+    }
+    __syncthreads();
+    // Decode-shaped chunks go to the tensor cores when the call has prompt
+    // items and the longest decode-shaped item stays within 1.1 times the
+    // schedule's expected length (its longest item or its average per SM);
+    // the host's decision, when it made one, stands.
+    const bool absorb =
+        p.tc_work && (p.absorb >= 0 ? p.absorb == 1
+                                    : absorb_decode_rows(s_w_tc, s_max_tc, s_w_dec, s_max_dec,
+                                                         p.sm_count));
+    if (absorb) hist[tid] += hist_dec[tid];
     __syncthreads();
     const int n_tc = p.tc_work ? desc_offsets(hist, warp_sums) : 0;
-    const unsigned long long row_tiles_all = s_row_tiles;
+    const unsigned long long row_tiles_all = absorb ? 0ull : s_row_tiles;
 
     // ---- from here on global memory is written: the previous kernel is done
     pdl_wait();
@@ -265,9 +317,10 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     for (int chunk0 = 0; chunk0 < p.batch; chunk0 += 1024) {
         __syncthreads();
         if (!one_chunk) load_chunk(chunk0, false);
-        s_a[tid] = n_tc_of(s_seq[tid]) * H;  // items flattened as (sequence, KV head, item)
-        s_b[tid] = s_seq[tid].w > 0 ? H : 0;
-        s_c[tid] = s_seq[tid].w > 0 ? s_seq[tid].w + kRowGroupStartTiles : 0;
+        // items flattened as (sequence, KV head, item)
+        s_a[tid] = n_tc_of(s_seq[tid], absorb) * H;
+        s_b[tid] = !absorb && s_seq[tid].w > 0 ? H : 0;
+        s_c[tid] = !absorb && s_seq[tid].w > 0 ? s_seq[tid].w + kRowGroupStartTiles : 0;
         __syncthreads();
         const int total_a = p.tc_work ? excl_scan(s_a, warp_sums) : 0;
         const int total_b = excl_scan(s_b, warp_sums);
@@ -275,12 +328,14 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
         for (int f = tid; f < total_a; f += 1024) {
             const int sl = segment_of(s_a, 1024, f);
             const int4 v = s_seq[sl];
-            const int n = n_tc_of(v);
+            const int n = n_tc_of(v, absorb);
             const int g = (f - s_a[sl]) / n;
             const int k = (f - s_a[sl]) - g * n;
             const int cost = tc_cost(v.y, v.x, k, item_pos, p.window, p.causal);
+            // a decode-shaped chunk's item is in the bucket of its weight
+            const int wc = v.x > rmax ? cost : dec_weight(v.w);
             // lanes with one bucket get consecutive slots in lane order
-            const int slot = warp_agg_add(hist, cost_bucket(cost), 1);
+            const int slot = warp_agg_add(hist, cost_bucket(wc), 1);
             if (slot >= p.lay.cap_tc) {
                 report_error(p.dev_err, PCP_ERR_WORKSPACE);
                 continue;

@@ -41,7 +41,7 @@ def test_status_strings(lib):
         s = lib.pcp_status_string(code).decode()
         assert s.startswith("PCP_")
     assert lib.pcp_status_string(99).decode() == "PCP_ERR_UNKNOWN"
-    assert lib.pcp_abi_version() == 3
+    assert lib.pcp_abi_version() == 4
     lib.pcp_last_cuda_error.restype = ctypes.c_char_p
     assert lib.pcp_last_cuda_error().decode() == "no error"
 
