@@ -154,12 +154,19 @@ def split_work(batch):
     return tc_pairs, row_bytes
 
 
-def launches_per_step(batch) -> int:
-    """Library kernels one step launches."""
+def launches_per_step(batch, rows_on_tensor_cores: bool = False) -> int:
+    """Library kernels one step launches (with host copies of qo_indptr and
+    prefix_lens): the fused append; the planner unless the row kernel plans
+    a decode-only call of at most 512 sequences itself; the tensor-core
+    kernel for chunks above the row path's size; the row kernel and the
+    combine for decode-shaped chunks unless they joined the tensor cores."""
     G = batch.n_q_heads // batch.n_kv_heads
     rmax = 16 // G if G <= 16 else 0
     c = np.diff(batch.qo_indptr)
-    return 2 + int((c > rmax).any()) + 2 * int(((c > 0) & (c <= rmax)).any())
+    tc = bool((c > rmax).any())
+    rows = bool(((c > 0) & (c <= rmax)).any()) and not rows_on_tensor_cores
+    plan = not (not tc and rows and batch.batch <= 512)
+    return 1 + int(plan) + int(tc) + 2 * int(rows)
 
 
 def load_peaks():
@@ -360,6 +367,9 @@ def main():
     ap.add_argument("--workload", default="gqa_prefill",
                     help="workloads.CONFIGS name (the headline line uses gqa_prefill)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", default=None, choices=SECONDARY_KEYS,
+                    help="run one secondary measurement alone and print it (no headline line; "
+                         "for profiling its kernels)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -375,6 +385,13 @@ def main():
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
     args.warmup = max(args.warmup, 3)
+    if args.only is not None:
+        peaks, peak_kind = load_peaks()
+        res = secondary(pcp, torch, W, dev, peaks, peak_kind, L2Flush(torch, dev),
+                        only=args.only)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "secondary": res}))
+        return
 
     batch = W.config_by_name(args.workload)
     d = to_device(batch, dev)
@@ -397,7 +414,7 @@ def main():
                               batch.page_size, batch.n_q_heads, batch.n_kv_heads,
                               batch.head_dim, batch.window, batch.sm_scale, out=out, lse=lse,
                               workspace=ws, dev_err=err, qo_indptr_host=batch.qo_indptr,
-                              tc_events=tc_events)
+                              prefix_lens_host=batch.prefix_lens, tc_events=tc_events)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -405,6 +422,11 @@ def main():
     torch.cuda.synchronize()
     if pcp.read_error(err) != 0:
         raise RuntimeError(f"device error {pcp.read_error(err)} during warm-up")
+    # where the decode-shaped chunks ran (the planner's header: n_row_groups)
+    c = np.diff(batch.qo_indptr)
+    rmax = row_max_chunk(batch)
+    rows_on_tc = bool((c > rmax).any() and ((c > 0) & (c <= rmax)).any() and
+                      int(ws[4:8].view(torch.int32).item()) == 0)
 
     # ---- timed region: L2 flushed before every step, events around each step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -472,7 +494,7 @@ def main():
         # the fused slot mapping + append, plan, then the tensor-core kernel
         # and/or the row kernel + combine (the host copy of qo_indptr skips a
         # kernel without work), in each of the two timed loops
-        "gpu_launches": 2 * args.steps * launches_per_step(batch),
+        "gpu_launches": 2 * args.steps * launches_per_step(batch, rows_on_tc),
         "clocks": clocks.summary(),
     }
 
@@ -560,7 +582,8 @@ def end_to_end(args, torch, pcp, batch, d, out_ref, flush, stream, flops, world)
                               S["prefix_lens"], S["k_pool"], S["v_pool"], batch.page_size,
                               batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.window,
                               batch.sm_scale, out=S["out"], lse=S["lse"], workspace=S["ws"],
-                              dev_err=err, qo_indptr_host=batch.qo_indptr)
+                              dev_err=err, qo_indptr_host=batch.qo_indptr,
+                              prefix_lens_host=batch.prefix_lens)
 
     def d2h_copies(S):
         S["h_res"].copy_(S["res"], non_blocking=True)
@@ -703,27 +726,17 @@ def attn_figures(pcp, torch, batch, dev, peaks, flush, err, n=20, warm=5, causal
     return r
 
 
-def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
-    """Per-kernel figures on every workload the benchmark does not time as
-    its headline, L2 flushed before each call."""
-    res = {"peak_source": f"{peak_kind} (MEASURED_PEAKS.json when present): bf16 dense "
-                          f"burst {peaks['bf16_tflops']} TFLOP/s, HBM copy {peaks['hbm_gbs']} GB/s"}
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
+SECONDARY_KEYS = ("decode_rows", "decode_step", "kv_append", "kv_append_long",
+                  "long_context_attn", "mixed_attn", "gqa_prefill_ps1", "stress_ps1_w4096",
+                  "stress_ps1_w0", "stress_ps16_w4096", "stress_ps16_w0", "masked",
+                  "chunk_planner", "cow_page_copy")
 
-    # decode rows: the 31 decode rows of the mixed batch as a decode-only call
-    db = W.decode_rows()
-    r = attn_figures(pcp, torch, db, dev, peaks, flush, err, key="decode_rows")
+
+def decode_step_secondary(pcp, torch, db, dev, peaks, flush, err, res):
+    """The decode rows as a serving decode step: the fused append of their new
+    tokens, then the attention call (whose row kernel plans the call while
+    the append runs)."""
     _, nbytes = split_work(db)
-    gbs = nbytes / (r["ms"] * 1e-3) / 1e9
-    res["decode_rows"] = {"workload": db.name, "ms": r["ms"], "GB/s": gbs,
-                          "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes,
-                          "what": "whole call: row kernel (planning its own split), split-KV "
-                                  "combine"}
-    res["decode_rows_kernel"] = r["row_kernel"]
-
-    # the same 31 rows as a serving decode step: the fused append of their
-    # new tokens, then the attention call (whose row kernel plans the call
-    # while the append runs)
     g = to_device(db, dev)
     dout = torch.empty_like(g["q"])
     dlse = torch.empty(db.total_q, db.n_q_heads, dtype=torch.float32, device=dev)
@@ -738,7 +751,7 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
                               g["prefix_lens"], g["k_pool"], g["v_pool"], db.page_size,
                               db.n_q_heads, db.n_kv_heads, db.head_dim, db.window, db.sm_scale,
                               out=dout, lse=dlse, workspace=dws, dev_err=err,
-                              qo_indptr_host=db.qo_indptr)
+                              qo_indptr_host=db.qo_indptr, prefix_lens_host=db.prefix_lens)
     ms = time_calls(torch, dstep, flush)
     sbytes = nbytes + 2 * 2 * db.total_q * db.n_kv_heads * db.head_dim * 2
     gbs = sbytes / (ms * 1e-3) / 1e9
@@ -747,10 +760,40 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
                           "what": "fused append of the rows' new tokens, then the attention call"}
     del g, dout, dlse, dws
 
+
+def secondary(pcp, torch, W, dev, peaks, peak_kind, flush, only=None):
+    """Per-kernel figures on every workload the benchmark does not time as
+    its headline, L2 flushed before each call (`only`: one of
+    SECONDARY_KEYS, e.g. to profile its kernels alone)."""
+    res = {"peak_source": f"{peak_kind} (MEASURED_PEAKS.json when present): bf16 dense "
+                          f"burst {peaks['bf16_tflops']} TFLOP/s, HBM copy {peaks['hbm_gbs']} GB/s"}
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def want(key):
+        return only is None or only == key
+
+    # decode rows: the 31 decode rows of the mixed batch as a decode-only call
+    db = W.decode_rows()
+    if want("decode_rows"):
+        r = attn_figures(pcp, torch, db, dev, peaks, flush, err, key="decode_rows")
+        _, nbytes = split_work(db)
+        gbs = nbytes / (r["ms"] * 1e-3) / 1e9
+        res["decode_rows"] = {"workload": db.name, "ms": r["ms"], "GB/s": gbs,
+                              "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes,
+                              "what": "whole call: row kernel (planning its own split), "
+                                      "split-KV combine"}
+        res["decode_rows_kernel"] = r["row_kernel"]
+    if want("decode_step"):
+        decode_step_secondary(pcp, torch, db, dev, peaks, flush, err, res)
+
+
     # the KV append of the GQA chunk (4096 tokens) and of the long-context
     # chunk (32768 tokens): the fused slot mapping + append the step runs, and
     # the append alone from a precomputed out_cache_loc
-    for key, b in (("kv_append", W.gqa_prefill()), ("kv_append_long", W.long_context())):
+    for key, bf in (("kv_append", W.gqa_prefill), ("kv_append_long", W.long_context)):
+        if not want(key):
+            continue
+        b = bf()
         g = to_device(b, dev)
         loc = pcp.compute_out_cache_loc(g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
                                         g["prefix_lens"], b.page_size, b.num_pages)
@@ -777,21 +820,28 @@ def secondary(pcp, torch, W, dev, peaks, peak_kind, flush):
     # tensor cores beside decode rows in one call), the GQA workload over the
     # flat one-slot-per-token pool (page size 1), and the page-boundary and
     # window stress batches
-    res["long_context_attn"] = attn_figures(pcp, torch, W.long_context(), dev, peaks, flush,
-                                            err, n=5, warm=2, key="long_context")
-    res["mixed_attn"] = attn_figures(pcp, torch, W.mixed_batch(), dev, peaks, flush, err,
-                                     key="mixed")
-    res["gqa_prefill_ps1"] = attn_figures(pcp, torch, W.gqa_prefill(page_size=1), dev, peaks,
-                                          flush, err, n=10, warm=3)
+    if want("long_context_attn"):
+        res["long_context_attn"] = attn_figures(pcp, torch, W.long_context(), dev, peaks, flush,
+                                                err, n=5, warm=2, key="long_context")
+    if want("mixed_attn"):
+        res["mixed_attn"] = attn_figures(pcp, torch, W.mixed_batch(), dev, peaks, flush, err,
+                                         key="mixed")
+    if want("gqa_prefill_ps1"):
+        res["gqa_prefill_ps1"] = attn_figures(pcp, torch, W.gqa_prefill(page_size=1), dev,
+                                              peaks, flush, err, n=10, warm=3)
     for name in ("stress_ps1_w4096", "stress_ps1_w0", "stress_ps16_w4096", "stress_ps16_w0"):
-        res[name] = attn_figures(pcp, torch, W.config_by_name(name), dev, peaks, flush, err,
-                                 n=10, warm=3)
+        if want(name):
+            res[name] = attn_figures(pcp, torch, W.config_by_name(name), dev, peaks, flush,
+                                     err, n=10, warm=3)
 
     # non-causal attention and a 2-D key mask (keep 1/2) on the GQA workload
-    res.update(masked_secondary(pcp, torch, W, dev, peaks, flush, err))
+    if want("masked"):
+        res.update(masked_secondary(pcp, torch, W, dev, peaks, flush, err))
 
-    res["chunk_planner"] = planner_secondary(pcp)
-    res["cow_page_copy"] = cow_secondary(pcp, torch, dev, peaks, flush)
+    if want("chunk_planner"):
+        res["chunk_planner"] = planner_secondary(pcp)
+    if want("cow_page_copy"):
+        res["cow_page_copy"] = cow_secondary(pcp, torch, dev, peaks, flush)
     if pcp.read_error(err) != 0:
         raise RuntimeError("device error in secondary measurements")
     return res

@@ -290,9 +290,14 @@ __device__ __forceinline__ void gather_kv_rows(const TcParams& p, const Geo& geo
 }  // namespace
 
 // kMask: the call passes a boolean mask; kCausal: bottom-right causal (else
-// every row sees all keys).  Separate instantiations, so the plain causal
-// path carries none of the other paths' instructions or registers.
-template <int D, bool kMask, bool kCausal>
+// every row sees all keys); kGather: the instantiation that holds the
+// cp.async gathers for pages below kTmaMinRows keys (it takes TMA page
+// boxes too when box_rows > 0; the host launches it only for box_rows 0).
+// Separate instantiations, so the plain causal path carries none of the
+// other paths' instructions or registers: the gather code alone, never run
+// with page boxes, cost the page-box kernel 1-3%, and a gathering
+// instantiation without the page-box code spilled and lost 8%.
+template <int D, bool kMask, bool kCausal, bool kGather>
 __global__ void __launch_bounds__(kTcThreads, 1)
     extend_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -318,10 +323,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(C::bQFull), 1);
         // TMA path: one arrive.expect_tx; gather path: one arrival per gather lane
-        const uint32_t full_count = p.box_rows > 0 ? 1u : 32u * kGatherWarps;
+        const uint32_t full_count = kGather && p.box_rows == 0 ? 32u * kGatherWarps : 1u;
         // the warps that issue cp.async (or stand by for it) and drain it on
         // the abort path: 10 and 11 with page boxes, 8, 10 and 11 gathering
-        const uint32_t drain_count = p.box_rows > 0 ? 64u : 32u * kGatherWarps;
+        const uint32_t drain_count = kGather && p.box_rows == 0 ? 32u * kGatherWarps : 64u;
         for (int s = 0; s < SK; ++s) {
             mbar_init(bar(C::bKFull + s), full_count);
             mbar_init(bar(C::bKEmpty + s), 1);
@@ -391,7 +396,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tma_load_3d(sQ + u * C::kQBytes + h * (kTileM * 128), &tm_q,
                                     bar(C::bQFull), h * 64, geo.g * G, geo.q_row0 + u * p.qpos);
             }
-            if (p.box_rows > 0) {
+            if (!kGather || p.box_rows > 0) {
                 // ------------------------------------------------ TMA: K / V page boxes
                 const bool is_k = warp == kWarpTma;
                 if (warp == kWarpTma || warp == kWarpGather0) {
@@ -527,7 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = mbar_wait(bar(C::bKFull + c0 % SK), (c0 / SK) & 1u, abort_flag,
                                    p.dev_err, kSpinLimitNs);
                     if (ok) {
-                        if (p.box_rows == 0) fence_proxy_async_smem();
+                        if (kGather && p.box_rows == 0) fence_proxy_async_smem();
                         if (tile_active(geo, 0, geo.t_begin)) {
                             issue_qk(0, c0 % SK);
                             umma_commit(bar(C::bSFull + 0));
@@ -550,7 +555,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     // cp.async wrote part of this V tile: small pages, or the page
                     // run that holds the sequence end (zero-filled past it)
-                    if (p.box_rows == 0 ||
+                    if ((kGather && p.box_rows == 0) ||
                         (geo.L > t * kTileN && geo.L < t * kTileN + kTileN &&
                          (geo.L - t * kTileN) % p.box_rows != 0))
                         fence_proxy_async_smem();
@@ -573,7 +578,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 if (!mbar_wait(bar(C::bKFull + nst), ((cur + 1) / SK) & 1u,
                                                abort_flag, p.dev_err, kSpinLimitNs))
                                     return false;
-                                if (p.box_rows == 0) fence_proxy_async_smem();
+                                if (kGather && p.box_rows == 0) fence_proxy_async_smem();
                                 k_next = true;
                             }
                             issue_qk(u, nst);
@@ -799,7 +804,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     volatile int* no_abort = &misc[3];
     if (warp == kWarpTma || warp >= kWarpGather0) {
         cp_async_wait_all();
-        if (aborted && (warp >= kWarpGather0 || p.box_rows == 0)) {
+        if (aborted && (warp >= kWarpGather0 || (kGather && p.box_rows == 0))) {
             // the mbarrier arrivals the gathers' cp.async copies trigger have
             // been made once this one, triggered after all of them, lands
             cp_async_mbar_arrive_noinc(bar(C::bGatherDrain));
@@ -837,16 +842,26 @@ size_t tc_smem_bytes(int head_dim) {
     return head_dim == 128 ? TcCfg<128>::kSmemBytes : TcCfg<64>::kSmemBytes;
 }
 
+template <int D, bool kMask, bool kCausal, bool kGather>
+cudaError_t launch_extend_tc_g(int grid, cudaStream_t stream, const TcParams& p,
+                               const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv) {
+    const size_t smem = TcCfg<D>::kSmemBytes;
+    auto* kern = extend_tc_kernel<D, kMask, kCausal, kGather>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(grid), dim3(kTcThreads), smem, stream, p, tq, tk, tv);
+}
+
+// pages below kTmaMinRows keys (box_rows 0) take the gathering instantiation
 template <int D, bool kMask, bool kCausal>
 cudaError_t launch_extend_tc_t(int grid, cudaStream_t stream, const TcParams& p,
                                const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv) {
-    const size_t smem = TcCfg<D>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<D, kMask, kCausal>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(extend_tc_kernel<D, kMask, kCausal>, dim3(grid), dim3(kTcThreads), smem,
-                      stream, p, tq, tk, tv);
+    return p.box_rows > 0
+               ? launch_extend_tc_g<D, kMask, kCausal, false>(grid, stream, p, tq, tk, tv)
+               : launch_extend_tc_g<D, kMask, kCausal, true>(grid, stream, p, tq, tk, tv);
 }
 
 template <int D>

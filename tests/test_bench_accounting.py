@@ -87,3 +87,18 @@ def test_split_work_matches_brute_force(window):
     pages = sum(-(-int(Pb + cb) // 16) for Pb, cb in zip(P[~tc], c[~tc]))
     n_rows = int(c[~tc].sum())
     assert row_bytes == keys * 2 * 64 * 4 + n_rows * 8 * (4 * 64 + 4) + 4 * pages
+
+
+def test_launches_per_step():
+    """Library kernels per step: the GQA step launches the fused append, the
+    planner and the tensor-core kernel; a decode-only step of 31 sequences
+    the append, the row kernel (which plans itself) and the combine; the
+    mixed step all five, or three when its decode rows joined the tensor
+    cores."""
+    assert bench.launches_per_step(W.gqa_prefill()) == 3
+    assert bench.launches_per_step(W.decode_rows()) == 3
+    assert bench.launches_per_step(W.mixed_batch()) == 5
+    assert bench.launches_per_step(W.mixed_batch(), rows_on_tensor_cores=True) == 3
+    # more than 512 decode-only sequences go through the planner kernel
+    b = W.make_batch([100] * 513, [1] * 513, 4, 4, 64, 16, seed=3)
+    assert bench.launches_per_step(b) == 4
