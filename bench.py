@@ -60,46 +60,43 @@ def rows_pairs(batch, tok, head) -> int:
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the dominant kernel, from an ncu capture of this bench on the named workload.
-# It is reported only while the library sources hash to the value the capture
-# ran with; after any change the key reads null until the counters are taken
-# again.
+# It is reported only while the sources that build, plan and launch that
+# kernel hash to the value the capture ran with; after a change there the key
+# reads null until the counters are taken again.
 NCU_TRAFFIC = {
     ("gqa_prefill", "extend_tc_kernel<128>"): {
-        "bytes": 199.122688e6 + 17.033216e6,
-        "csrc_sha256": "07eb6976004c67d480c38874e8afb85e",
-    },
-    ("decode_rows", "row_attn_kernel<128>"): {
-        "bytes": 275.753984e6 + 3.887616e6,
-        "csrc_sha256": "07eb6976004c67d480c38874e8afb85e",
+        "bytes": 198.278656e6 + 13.562880e6,
+        "sources_sha256": "ec8be3566ca6fc7e8e802588a12572ce",
     },
     ("long_context", "extend_tc_kernel<128>"): {
-        "bytes": 4139.245312e6 + 532.051712e6,
-        "csrc_sha256": "07eb6976004c67d480c38874e8afb85e",
+        "bytes": 4032.028160e6 + 531.460864e6,
+        "sources_sha256": "ec8be3566ca6fc7e8e802588a12572ce",
     },
     ("mixed", "extend_tc_kernel<128>"): {
-        "bytes": 25.268480e6 + 0.000256e6,
-        "csrc_sha256": "07eb6976004c67d480c38874e8afb85e",
+        "bytes": 307.243008e6 + 5.393920e6,
+        "sources_sha256": "ec8be3566ca6fc7e8e802588a12572ce",
     },
-    ("mixed", "row_attn_kernel<128>"): {
-        "bytes": 284.228608e6 + 0.230400e6,
-        "csrc_sha256": "07eb6976004c67d480c38874e8afb85e",
+    ("decode_rows", "row_attn_kernel<128>"): {
+        "bytes": 275.755776e6 + 0.327168e6,
+        "sources_sha256": "ba30d8e73a0a2217ecdba17a9d3d9e50",
     },
 }
 
+# The sources behind a kernel's counters: its own file, the planner (item
+# order and split), the host side that sets up its launch, and the shared
+# device headers.
+COMMON_SOURCES = ("pcp_api.cu", "pcp_plan.cu", "pcp_device.cuh", "pcp_internal.h",
+                  "pcp_launch.h")
+KERNEL_SOURCES = {"extend_tc_kernel": "pcp_extend_tc.cu", "row_attn_kernel": "pcp_rows.cu"}
 
-# Library sources that hold no device code and launch nothing (the host page
-# pool and chunk planner): a change there leaves the kernels' counters valid.
-HOST_ONLY_SOURCES = {"pcp_sched.cu"}
 
-
-def csrc_sha256() -> str:
-    """Hash of the library sources that build or launch the kernels."""
+def sources_sha256(kernel: str) -> str:
+    """Hash of the sources behind one kernel's counters (kernel named with or
+    without its template arguments)."""
     import hashlib
     d = os.path.join(ROOT, "paged_chunked_prefill_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
-        if name in HOST_ONLY_SOURCES:
-            continue
+    for name in sorted(COMMON_SOURCES + (KERNEL_SOURCES[kernel.split("<")[0]],)):
         h.update(name.encode())
         with open(os.path.join(d, name), "rb") as f:
             h.update(f.read())
@@ -108,7 +105,7 @@ def csrc_sha256() -> str:
 
 def ncu_traffic(workload: str, kernel: str):
     rec = NCU_TRAFFIC.get((workload, kernel))
-    if rec is None or rec["csrc_sha256"] != csrc_sha256():
+    if rec is None or rec["sources_sha256"] != sources_sha256(kernel):
         return None
     return rec["bytes"]
 
