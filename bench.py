@@ -415,6 +415,9 @@ def main():
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
+        # the flush too: its kernels load on first use, which must not fall
+        # inside the first timed step
+        flush()
         step()
     torch.cuda.synchronize()
     if pcp.read_error(err) != 0:
@@ -432,11 +435,15 @@ def main():
     for e in ev:  # materialise the events before handing them to the library
         for x in e:
             x.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     with ClockSampler(dev.index) as clocks:
+        # the GPU idled while the sampler started (0.3 s): one more untimed
+        # step brings its clocks back before the timed ones
+        flush()
+        step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         # (1) whole steps: nothing between the library's launches, so each
         # kernel's launch overlaps the end of the one before it
         for i in range(args.steps):
@@ -483,7 +490,8 @@ def main():
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_steps": [round(x, 4) for x in step_ms], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_dict(batch, world),
         "roofline": roofline,
@@ -916,6 +924,7 @@ def time_calls(torch, fn, flush, n=20, warm=5, events=False):
     records it around one kernel."""
     stream = torch.cuda.current_stream()
     for _ in range(warm):
+        flush()
         fn(None)
     torch.cuda.synchronize()
     ms = []
