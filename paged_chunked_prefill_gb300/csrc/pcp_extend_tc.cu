@@ -58,7 +58,7 @@ struct TcCfg {
     static constexpr uint32_t kOffBar = kOffK + kStagesK * kTileBytes;
     static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 6 + 3;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;
+    static constexpr uint32_t kSmemBytes = kOffMisc + 128 + 1024;
     static_assert(kOffBar % 8 == 0 && kOffMisc % 4 == 0, "smem alignment");
     static_assert(kOffQ % 1024 == 0 && kOffK % 1024 == 0 && kOffV % 1024 == 0,
                   "128-byte-swizzled operands need 1024-byte alignment");
@@ -83,15 +83,16 @@ struct Geo {
     int t_begin, t_end;
 };
 
+// Geometry of item `it` of sequence b = it.x, whose qo_indptr[b], [b + 1]
+// and prefix length are q0, q1 and P.
 template <bool kCausal>
-__device__ __forceinline__ Geo make_geo(const TcParams& p, int4 it) {
+__device__ __forceinline__ Geo make_geo(const TcParams& p, int4 it, int q0, int q1, int P) {
     Geo g;
     g.b = it.x;
     g.g = it.y;
     g.pos0 = it.z;
-    const int q0 = p.qo_indptr[g.b];
-    g.c = p.qo_indptr[g.b + 1] - q0;
-    g.P = p.prefix_lens[g.b];
+    g.c = q1 - q0;
+    g.P = P;
     g.L = g.P + g.c;
     g.q_row0 = q0 + g.pos0;
     g.nq = (g.pos0 + p.qpos < g.c) ? 2 : 1;
@@ -314,7 +315,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t sV = base + C::kOffV;
     const uint32_t sBar = base + C::kOffBar;
     volatile int* misc = reinterpret_cast<volatile int*>(gbase + C::kOffMisc);
-    // misc[0] TMEM base, misc[1] current item, misc[2] abort flag, misc[3] 0
+    // misc[0] TMEM base, misc[1] current item, misc[2] abort flag, misc[3] 0;
+    // page boxes: misc[4 + 8 s ..]: the next item, its record, its sequence's
+    // qo_indptr[b], qo_indptr[b + 1] and prefix length, in slot s = the
+    // item's parity (written during the item before, read at its start: the
+    // slot is not rewritten before every thread has passed the next start)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -376,11 +381,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int last_issued = -1;           // TMA-issuing warps: last KV iteration they loaded
 
     for (;;) {
-        if (threadIdx.x == 0) misc[1] = atomicAdd(&hdr->tc_next, 1);
-        __syncthreads();
-        const int item = misc[1];
-        if (item >= n_items || *abort_flag) break;
-        const Geo geo = make_geo<kCausal>(p, items[item]);
+        // With page boxes the TMA warp claims the next item and reads its
+        // record and metadata during this one (after its last K tile), so an
+        // item starts without the atomic and the dependent loads; the first
+        // item, and every item of the gathering instantiation, load them here.
+        int item, q0, q1, Pl;
+        int4 rec;
+        if (kGather || n_done == 0) {
+            if (threadIdx.x == 0) misc[1] = atomicAdd(&hdr->tc_next, 1);
+            __syncthreads();
+            item = misc[1];
+            if (item >= n_items || *abort_flag) break;
+            rec = items[item];
+            q0 = p.qo_indptr[rec.x];
+            q1 = p.qo_indptr[rec.x + 1];
+            Pl = p.prefix_lens[rec.x];
+        } else {
+            __syncthreads();
+            volatile int* nx = misc + 4 + 8 * (n_done & 1u);
+            item = nx[0];
+            if (item >= n_items || *abort_flag) break;
+            rec = make_int4(nx[1], nx[2], nx[3], nx[4]);
+            q0 = nx[5];
+            q1 = nx[6];
+            Pl = nx[7];
+        }
+        const Geo geo = make_geo<kCausal>(p, rec, q0, q1, Pl);
         const int ntiles = geo.t_end - geo.t_begin + 1;
 
         // Page boxes: the TMA warp issues the K tiles and the first gather warp
@@ -431,6 +457,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         last_issued = (int)cur;
                         z_cur = z_next;
+                    }
+                    // The next item, claimed once this item's last K tile is
+                    // issued: a few tile steps before this item ends, late
+                    // enough that the longest-first queue stays greedy (a claim
+                    // at the item's start cost items-poor launches 20%), early
+                    // enough that the claim and its loads are done by then.
+                    if constexpr (!kGather) {
+                        if (is_k && lane == 0) {
+                            volatile int* nx = misc + 4 + 8 * ((n_done + 1u) & 1u);
+                            const int ni = atomicAdd(&hdr->tc_next, 1);
+                            nx[0] = ni;
+                            if (ni < n_items) {
+                                const int4 r = items[ni];
+                                nx[1] = r.x;
+                                nx[2] = r.y;
+                                nx[3] = r.z;
+                                nx[4] = r.w;
+                                nx[5] = p.qo_indptr[r.x];
+                                nx[6] = p.qo_indptr[r.x + 1];
+                                nx[7] = p.prefix_lens[r.x];
+                            }
+                        }
                     }
                 }
             } else {
