@@ -65,16 +65,16 @@ def rows_pairs(batch, tok, head) -> int:
 # reads null until the counters are taken again.
 NCU_TRAFFIC = {
     ("gqa_prefill", "extend_tc_kernel<128>"): {
-        "bytes": 198.278656e6 + 13.562880e6,
-        "sources_sha256": "ec8be3566ca6fc7e8e802588a12572ce",
+        "bytes": 197.531648e6 + 13.459200e6,
+        "sources_sha256": "9ac96f9c74756e89589f38c656cbb03e",
     },
     ("long_context", "extend_tc_kernel<128>"): {
-        "bytes": 4032.028160e6 + 531.460864e6,
-        "sources_sha256": "ec8be3566ca6fc7e8e802588a12572ce",
+        "bytes": 4023.937280e6 + 531.719936e6,
+        "sources_sha256": "9ac96f9c74756e89589f38c656cbb03e",
     },
     ("mixed", "extend_tc_kernel<128>"): {
-        "bytes": 307.243008e6 + 5.393920e6,
-        "sources_sha256": "ec8be3566ca6fc7e8e802588a12572ce",
+        "bytes": 307.227904e6 + 5.302784e6,
+        "sources_sha256": "9ac96f9c74756e89589f38c656cbb03e",
     },
     ("decode_rows", "row_attn_kernel<128>"): {
         "bytes": 275.755776e6 + 0.327168e6,
