@@ -155,7 +155,9 @@ pcp_status pcp_kv_append_paged(const int32_t* qo_indptr, const int32_t* kv_indpt
 /*
  * Bytes of device workspace pcp_paged_extend_attn needs for a call with at
  * most `batch` sequences and `total_q` query rows (work lists, split-KV
- * partials and counters).  Pure host arithmetic; 0 for an unsupported shape.
+ * partials and counters, and at the end the partials of split tensor-core
+ * items).  Pure host arithmetic; 0 for an unsupported shape.  A call whose
+ * workspace holds everything but the split items' buffers runs, unsplit.
  */
 size_t pcp_extend_workspace_size(int batch, int64_t total_q, int n_q_heads, int n_kv_heads,
                                  int head_dim);
@@ -458,6 +460,15 @@ pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_er
  *     makes the same decision and launches only the kernels that have work.
  *     The decision moves work between kernels only: results are correct
  *     either way (bit-identical whenever the decision is the same).
+ *     With both host copies, an unmasked call whose longest tensor-core item
+ *     is more than 1.3 times the average work per SM also splits its longest
+ *     items in two along their 128-key tiles (the items above half that
+ *     average and above 16 tiles, longest first, at most 64).  The two
+ *     parts are separate items of the queue; the part that finishes second
+ *     merges the first one's partial output and (max, normaliser) into the
+ *     result.  A split changes only the rounding order of those rows.  It
+ *     needs the full pcp_extend_workspace_size: with a smaller workspace
+ *     the call runs unsplit.
  * The library keeps nothing of it after the call returns.
  */
 typedef struct pcp_call_options {

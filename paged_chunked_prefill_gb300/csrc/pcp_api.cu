@@ -172,7 +172,10 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
         (o.rows_event_before == nullptr) != (o.rows_event_after == nullptr))
         return PCP_ERR_INVALID_ARG;
     if (a.total_q == 0) return PCP_OK;
-    if (a.workspace == nullptr || a.workspace_bytes < lay.total || !aligned(a.workspace, 256))
+    // a call needs the workspace up to the split buffers; it splits items only
+    // when the whole layout fits
+    if (a.workspace == nullptr || a.workspace_bytes < lay.split_begin ||
+        !aligned(a.workspace, 256))
         return PCP_ERR_WORKSPACE;
     const int group = a.n_q_heads / a.n_kv_heads;
     const int head_dim = a.head_dim;
@@ -201,8 +204,13 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     // a call with both kinds of chunks takes its decode-shaped ones onto the
     // tensor cores (the planner's rule, absorb_decode_rows, on the same
     // figures) and then launches only the kernels that have work.
+    // With both host copies the host also decides whether the call splits its
+    // longest tensor-core items along their KV tiles (split_longest_items):
+    // not for masked calls, and only when the workspace holds the split
+    // buffers.
     int absorb = -1;
-    if (run_tc && run_rows && a.qo_indptr_host != nullptr && o.prefix_lens_host != nullptr) {
+    int split = 0;
+    if (run_tc && a.qo_indptr_host != nullptr && o.prefix_lens_host != nullptr) {
         const int item_pos = q_positions_per_tile(group) * kQTiles;
         unsigned long long w_tc = 0, w_dec = 0;
         int max_tc = 0, max_dec = 0;
@@ -222,8 +230,17 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
                 max_dec = t > max_dec ? t : max_dec;
             }
         }
-        absorb = absorb_decode_rows(w_tc, max_tc, w_dec, max_dec, sms) ? 1 : 0;
-        if (absorb == 1) run_rows = false;
+        if (run_rows) {
+            absorb = absorb_decode_rows(w_tc, max_tc, w_dec, max_dec, sms) ? 1 : 0;
+            if (absorb == 1) run_rows = false;
+        }
+        const bool dec_tc = absorb == 1;
+        const unsigned long long w_all = w_tc + (dec_tc ? w_dec : 0ull);
+        const int longest = dec_tc && max_dec > max_tc ? max_dec : max_tc;
+        split = a.mask.data == nullptr && a.workspace_bytes >= lay.total &&
+                        split_longest_items(w_all, longest, sms)
+                    ? 1
+                    : 0;
     }
     EncodeFn enc = nullptr;
     st = get_encoder(&enc);
@@ -274,6 +291,7 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     pp.causal = a.causal;
     pp.tc_work = run_tc ? 1 : 0;
     pp.absorb = absorb;
+    pp.split = split;
     pp.sm_count = sms;
     pp.ws = ws;
     pp.lay = lay;
@@ -307,6 +325,7 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     tp.scale_log2 = scale_log2;
     tp.stall_ns = o.test_stall_ns;
     tp.dev_err = a.dev_err;
+    tp.split = split;
     cudaEvent_t evb = static_cast<cudaEvent_t>(o.tc_event_before);
     cudaEvent_t eva = static_cast<cudaEvent_t>(o.tc_event_after);
     if (evb && failed(cudaEventRecord(evb, s))) return PCP_ERR_CUDA;

@@ -39,6 +39,16 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 // (qo_indptr, kv_indptr, prefix_lens: inputs of the call, not outputs of the
 // kernels before it); only the planner reads those before its wait.  Without
 // the launch attribute both are no-ops.
+// Flags between CTAs of one grid (a split item's two parts).
+__device__ __forceinline__ void st_release_gpu(int* ptr, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -85,7 +85,7 @@ struct Geo {
 
 // Geometry of item `it` of sequence b = it.x, whose qo_indptr[b], [b + 1]
 // and prefix length are q0, q1 and P.
-template <bool kCausal>
+template <bool kCausal, bool kSplit>
 __device__ __forceinline__ Geo make_geo(const TcParams& p, int4 it, int q0, int q1, int P) {
     Geo g;
     g.b = it.x;
@@ -110,6 +110,21 @@ __device__ __forceinline__ Geo make_geo(const TcParams& p, int4 it, int q0, int 
             g.pl[u] = g.ph[u] = 0;
             g.first[u] = 1;
             g.last[u] = 0;
+        }
+    }
+    // a part of a split item: its Q tiles' KV ranges end below the item's
+    // middle tile tm (part 0) or start at it (part 1).  Items are split only
+    // above 16 KV tiles, so tm lies at least 8 tiles inside the item and both
+    // Q tiles keep KV tiles in both parts (their ranges differ by at most one
+    // tile at either end).
+    if constexpr (kSplit) {
+        if (it.w & kSplitTag) {
+            const int tm = (it.w >> 12) & (kSplitMaxTile - 1);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (it.w & 1) g.first[u] = max(g.first[u], tm);
+                else g.last[u] = min(g.last[u], tm - 1);
+            }
         }
     }
     g.t_begin = g.first[0];
@@ -290,6 +305,104 @@ __device__ __forceinline__ void gather_kv_rows(const TcParams& p, const Geo& geo
 
 }  // namespace
 
+// Epilogue of Q tile u of a split item's part, one row per thread (row r of
+// the tile).  Each warp (32 rows) settles its rows with the warp holding the
+// same rows in the other part, through a ticket and a ready flag of its own,
+// so nothing waits on a warp of this CTA that might have given up (only
+// warp-level synchronisation).  The warp that takes ticket 0 writes its O
+// rows (fp32, unnormalised) and (m, l) in the log2 domain to the item's
+// partial buffer and then raises the flag; the other one waits for the flag
+// (its partner is past its ticket, so it is running and the wait ends;
+// bounded all the same) and writes
+//   out = (2^(m_0 - M) O_0 + 2^(m_1 - M) O_1) / (2^(m_0 - M) l_0 + 2^(m_1 - M) l_1),
+//   lse = (M + log2 L) ln 2,  M = max(m_0, m_1),
+// always with part 0's terms first (explicit fma/mul, no contraction left to
+// the compiler), so the result does not depend on which part finished first.
+template <int D>
+__device__ __forceinline__ void split_epilogue(const TcParams& p, int sp, int part, int u, int r,
+                                               uint32_t tO, float m_ref, float l_run,
+                                               bool row_valid, int64_t orow) {
+    const int lane = r & 31;
+    const int64_t pidx = ((int64_t)sp * kQTiles + u) * kTileM + r;
+    unsigned char* ws = const_cast<unsigned char*>(p.ws);
+    float* po = reinterpret_cast<float*>(ws + p.lay.tc_part_o) + pidx * D;
+    float2* pml = reinterpret_cast<float2*>(ws + p.lay.tc_part_ml) + pidx;
+    // {ticket, ready} of this warp's rows
+    int* sync = reinterpret_cast<int*>(ws + p.lay.tc_sync) +
+                (((int64_t)sp * kQTiles + u) * 4 + (r >> 5)) * 2;
+    int ticket = 0;
+    if (lane == 0) ticket = atomicAdd(sync, 1);
+    ticket = __shfl_sync(0xffffffffu, ticket, 0);
+    if (ticket == 0) {
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32u * i, o);
+            tmem_ld_wait();
+            float4* dst = reinterpret_cast<float4*>(po + i * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                __stcg(dst + j, make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
+                                            __uint_as_float(o[4 * j + 2]),
+                                            __uint_as_float(o[4 * j + 3])));
+        }
+        __stcg(pml, make_float2(m_ref, l_run));
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(sync + 1, 1);
+        return;
+    }
+    if (lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (ld_acquire_gpu(sync + 1) == 0) {
+            if (global_timer_ns() - t0 > kSpinLimitNs) {
+                report_error(p.dev_err, PCP_ERR_TIMEOUT);
+                break;
+            }
+        }
+    }
+    __syncwarp();
+    const float2 ot = __ldcg(pml);
+    const float M = fmaxf(m_ref, ot.x);
+    const float e_s = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - M);
+    const float e_o = ot.x == -INFINITY ? 0.f : fast_exp2(ot.x - M);
+    // part 0's (weight, normaliser) first
+    const float e0 = part == 0 ? e_s : e_o, e1 = part == 0 ? e_o : e_s;
+    const float l0 = part == 0 ? l_run : ot.y, l1 = part == 0 ? ot.y : l_run;
+    const float L = __fmaf_rn(l0, e0, __fmul_rn(l1, e1));
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const float a0 = __fmul_rn(e0, inv), a1 = __fmul_rn(e1, inv);
+    // O of part 0 and of part 1 from this part's TMEM row (s) and the partial (x)
+    auto mix = [&](float sv, float x) {
+        return part == 0 ? __fmaf_rn(sv, a0, __fmul_rn(x, a1)) : __fmaf_rn(x, a0, __fmul_rn(sv, a1));
+    };
+    uint16_t* op = p.out + orow * D;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32u * i, o);
+        tmem_ld_wait();
+        const float4* src = reinterpret_cast<const float4*>(po + i * 32);
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 x = __ldcg(src + j);
+            w[2 * j] = pack_bf16x2(mix(__uint_as_float(o[4 * j]), x.x),
+                                   mix(__uint_as_float(o[4 * j + 1]), x.y));
+            w[2 * j + 1] = pack_bf16x2(mix(__uint_as_float(o[4 * j + 2]), x.z),
+                                       mix(__uint_as_float(o[4 * j + 3]), x.w));
+        }
+        if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(op + i * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        }
+    }
+    if (row_valid && p.lse != nullptr)
+        p.lse[orow] = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+}
+
 // kMask: the call passes a boolean mask; kCausal: bottom-right causal (else
 // every row sees all keys); kGather: the instantiation that holds the
 // cp.async gathers for pages below kTmaMinRows keys (it takes TMA page
@@ -298,7 +411,7 @@ __device__ __forceinline__ void gather_kv_rows(const TcParams& p, const Geo& geo
 // other paths' instructions or registers: the gather code alone, never run
 // with page boxes, cost the page-box kernel 1-3%, and a gathering
 // instantiation without the page-box code spilled and lost 8%.
-template <int D, bool kMask, bool kCausal, bool kGather>
+template <int D, bool kMask, bool kCausal, bool kGather, bool kSplit>
 __global__ void __launch_bounds__(kTcThreads, 1)
     extend_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -406,7 +519,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             q1 = nx[6];
             Pl = nx[7];
         }
-        const Geo geo = make_geo<kCausal>(p, rec, q0, q1, Pl);
+        const Geo geo = make_geo<kCausal, kSplit>(p, rec, q0, q1, Pl);
         const int ntiles = geo.t_end - geo.t_begin + 1;
 
         // Page boxes: the TMA warp issues the K tiles and the first gather warp
@@ -805,7 +918,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bODone + u), a_last & 1u,
                                                            abort_flag, p.dev_err, kSpinLimitNs));
                 }
-                if (ok) {
+                // a part of a split item merges with the other part (its split
+                // state is read from the item again, not kept live through the
+                // tile loop)
+                int wsplit = 0;
+                if constexpr (kSplit) {
+                    wsplit = (!kGather && n_done > 0) ? misc[4 + 8 * (n_done & 1u) + 4]
+                                                      : items[misc[1]].w;
+                    if (!(wsplit & kSplitTag)) wsplit = 0;
+                }
+                if (ok && wsplit != 0) {
+                    tc_fence_after();
+                    split_epilogue<D>(p, (wsplit >> 1) & 0x7FF, wsplit & 1, u, r, tO,
+                                      m_run == -INFINITY ? -INFINITY : m_run * sl2, l_run,
+                                      row_valid,
+                                      (int64_t)(geo.q_row0 + pos_local) * p.n_q_heads + head);
+                } else if (ok) {
                     tc_fence_after();
                     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
                     const int64_t orow = (int64_t)(geo.q_row0 + pos_local) * p.n_q_heads + head;
@@ -890,16 +1018,29 @@ size_t tc_smem_bytes(int head_dim) {
     return head_dim == 128 ? TcCfg<128>::kSmemBytes : TcCfg<64>::kSmemBytes;
 }
 
-template <int D, bool kMask, bool kCausal, bool kGather>
-cudaError_t launch_extend_tc_g(int grid, cudaStream_t stream, const TcParams& p,
+template <int D, bool kMask, bool kCausal, bool kGather, bool kSplit>
+cudaError_t launch_extend_tc_s(int grid, cudaStream_t stream, const TcParams& p,
                                const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv) {
     const size_t smem = TcCfg<D>::kSmemBytes;
-    auto* kern = extend_tc_kernel<D, kMask, kCausal, kGather>;
+    auto* kern = extend_tc_kernel<D, kMask, kCausal, kGather, kSplit>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kTcThreads), smem, stream, p, tq, tk, tv);
+}
+
+// a plan with split items (never with a mask) takes the instantiation that merges them
+template <int D, bool kMask, bool kCausal, bool kGather>
+cudaError_t launch_extend_tc_g(int grid, cudaStream_t stream, const TcParams& p,
+                               const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv) {
+    if constexpr (!kMask) {
+        if (p.split)
+            return launch_extend_tc_s<D, kMask, kCausal, kGather, true>(grid, stream, p, tq, tk,
+                                                                       tv);
+    }
+    return launch_extend_tc_s<D, kMask, kCausal, kGather, false>(grid, stream, p, tq, tk, tv);
 }
 
 // pages below kTmaMinRows keys (box_rows 0) take the gathering instantiation

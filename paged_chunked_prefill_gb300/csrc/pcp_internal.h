@@ -65,6 +65,17 @@ __host__ __device__ inline bool absorb_decode_rows(unsigned long long w_tc, int 
     return lhs <= (a > b ? a : b);
 }
 
+// Whether a call splits its longest tensor-core items in two: its longest
+// item (in two-Q-tile steps, as absorb_decode_rows weighs them) above 1.3
+// times the average work per SM (w_all: the summed cost, per KV head
+// included).  The planner then splits the items above half that average
+// (and above 16 tiles), longest first, at most kTcMaxSplitItems.
+__host__ __device__ inline bool split_longest_items(unsigned long long w_all, int longest,
+                                                    int sm_count) {
+    const unsigned long long sms = sm_count > 0 ? (unsigned long long)sm_count : 1ull;
+    return w_all > 0 && 10ull * (unsigned long long)longest * sms > 13ull * w_all;
+}
+
 // KV tiles of tensor-core item k (positions [k * item_pos, ...)) of a chunk
 // of c rows after a prefix of P keys: from the first key its first row sees
 // to its last row (causal) or the sequence end.
@@ -112,7 +123,17 @@ struct WsHeader {
     int pad[59];       // 256 bytes
 };
 
-// Tensor-core work item: {b, kv head g, first chunk position, cost in KV tiles}
+// Tensor-core work item: {b, kv head g, first chunk position, w}: w is the
+// cost in KV tiles, or, for a part of an item split along its KV tiles,
+// kSplitTag | (first KV tile of part 1) << 12 | (split index) << 1 | part.
+//
+// A call whose longest item far exceeds the average work per SM splits its
+// longest items in two (at most kTcMaxSplitItems of them); each split item
+// keeps the partial result of its first-finishing part in the workspace.
+constexpr int kTcMaxSplitItems = 64;
+constexpr int kSplitTag = 1 << 30;
+constexpr int kSplitMaxTile = 1 << 18;  // a split tile index must fit its 18 bits
+
 //
 // Row path.  The row groups' tiles are laid end to end (group k covers tiles
 // [S_k, S_k + tiles_k)) and CTA i of n takes tiles [i*T/n, (i+1)*T/n), so
@@ -127,14 +148,19 @@ struct WsHeader {
 
 struct WsLayout {
     size_t header;        // offset of WsHeader
-    size_t tc_items;      // int4 [cap_tc]
+    size_t tc_items;      // int4 [cap_tc + cap_split]
     size_t row_groups;    // int4 [3 * cap_groups]: row group descriptors
     size_t row_first;     // int [kRowMaxCtas]: first row group of each row-kernel CTA (-1: none)
     size_t group_desc;    // int4 [cap_groups]: {first partial slot, n_splits, q0, chunk_len}
     size_t partial_o;     // float [cap_row * kRowMaxRows * head_dim]
     size_t partial_ml;    // float2 [cap_row * kRowMaxRows]
+    size_t split_begin;   // bytes a call without split items uses (the split buffers follow)
+    size_t tc_part_o;     // float [cap_split][2 Q tiles][128 rows][head_dim]: split partials
+    size_t tc_part_ml;    // float2 [cap_split][2][128]: their (max, normaliser), log2 domain
+    size_t tc_sync;       // int [cap_split][2 Q tiles][4 warps][2]: {ticket, partial ready}
     size_t total;
     int64_t cap_tc;
+    int64_t cap_split;
     int64_t cap_row;
     int64_t cap_groups;
 };
@@ -150,13 +176,14 @@ inline bool ws_layout(int batch, int64_t total_q, int n_q_heads, int n_kv_heads,
     if (group > kTileM) return false;
     const int64_t qpos = (int64_t)q_positions_per_tile(group) * kQTiles;
     L->cap_tc = (int64_t)n_kv_heads * ((total_q + qpos - 1) / qpos + batch);
+    L->cap_split = L->cap_tc < kTcMaxSplitItems ? L->cap_tc : kTcMaxSplitItems;
     L->cap_groups = (int64_t)n_kv_heads * batch;
     L->cap_row = L->cap_groups + kRowMaxCtas;  // partial slots: k + i < groups + CTAs
     size_t off = 0;
     L->header = off;
     off += sizeof(WsHeader);
     L->tc_items = off = align_up(off, 256);
-    off += (size_t)(L->cap_tc > 0 ? L->cap_tc : 1) * 16;
+    off += (size_t)(L->cap_tc + L->cap_split > 0 ? L->cap_tc + L->cap_split : 1) * 16;
     L->row_groups = off = align_up(off, 256);
     off += (size_t)(L->cap_groups > 0 ? L->cap_groups : 1) * 48;
     L->row_first = off = align_up(off, 256);
@@ -167,6 +194,13 @@ inline bool ws_layout(int batch, int64_t total_q, int n_q_heads, int n_kv_heads,
     off += (size_t)L->cap_row * kRowMaxRows * head_dim * 4;
     L->partial_ml = off = align_up(off, 256);
     off += (size_t)L->cap_row * kRowMaxRows * 8;
+    L->split_begin = off = align_up(off, 256);
+    L->tc_part_o = off;
+    off += (size_t)L->cap_split * kQTiles * kTileM * head_dim * 4;
+    L->tc_part_ml = off = align_up(off, 256);
+    off += (size_t)L->cap_split * kQTiles * kTileM * 8;
+    L->tc_sync = off = align_up(off, 256);
+    off += (size_t)(L->cap_split > 0 ? L->cap_split : 1) * kQTiles * 4 * 2 * 4;
     L->total = align_up(off, 256);
     return true;
 }
@@ -197,6 +231,7 @@ struct PlanParams {
     int window;
     int causal;
     int tc_work;       // 0: the host knows no chunk goes to the tensor cores
+    int split;         // 1: split the longest tensor-core items (the host's decision)
     int absorb;        // decode-shaped chunks on the tensor cores: 1 / 0 as the host
                        // decided, -1: the planner decides (absorb_decode_rows)
     int sm_count;
@@ -232,6 +267,7 @@ struct TcParams {
     float scale_log2;  // sm_scale * log2(e)
     uint64_t stall_ns; // test hook (0: off): see pcp_call_options.test_stall_ns
     int32_t* dev_err;
+    int split;         // host: the plan may hold split items (the instantiation that merges them)
 };
 
 // ---- parameters of the split-KV combine kernel

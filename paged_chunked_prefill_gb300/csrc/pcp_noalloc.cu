@@ -79,7 +79,9 @@ extern "C" pcp_status pcp_paged_extend_attn_noalloc(
     pcp::WsLayout lay;
     const pcp_status chk = pcp::check_extend_args(a, &lay);
     if (chk != PCP_OK || total_q == 0) return chk;
-    if (lay.total > (size_t)PCP_NOALLOC_SCRATCH_BYTES) return PCP_ERR_WORKSPACE;
+    // (this entry point never splits items: it needs the layout up to the
+    // split buffers)
+    if (lay.split_begin > (size_t)PCP_NOALLOC_SCRATCH_BYTES) return PCP_ERR_WORKSPACE;
     void* scratch = nullptr;
     const pcp_status st = scratch_for_current_device(&scratch);
     if (st != PCP_OK) return st;

@@ -31,6 +31,12 @@
 //    a two-Q-tile step per KV tile (its one Q tile alone: measured 1.66 us
 //    against 2.07 us on the GQA workload), so it is charged that in the
 //    longest-first order and in the test.
+//  * a call whose longest item far exceeds the average work per SM (the
+//    host's decision, split_longest_items) splits its longest items in two
+//    along their KV tiles: the items above half the average work per SM and
+//    above 16 tiles, longest first, at most kTcMaxSplitItems.  The two parts
+//    are items of their own in the longest-first order; the part that ends
+//    second merges the first one's partial result.
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
 #include "pcp_launch.h"
@@ -67,6 +73,11 @@ __device__ __forceinline__ int first_key(int pos, int window) {
 // the cost itself below 64 KV tiles, 16-tile buckets above.
 __device__ __forceinline__ int cost_bucket(int cost) {
     return cost < 64 ? cost : min(1023, 64 + ((cost - 64) >> 4));
+}
+
+// Lowest cost in a bucket of cost_bucket.
+__device__ __forceinline__ int bucket_min_cost(int bucket) {
+    return bucket < 64 ? bucket : 64 + ((bucket - 64) << 4);
 }
 
 
@@ -169,9 +180,14 @@ __device__ __forceinline__ int warp_agg_add(int* base, int key, int inc) {
 // Sequences are processed in chunks of 1024 (one per thread); within a chunk
 // the per-sequence items and row groups are flattened across all threads
 // through prefix sums, so a long chunk does not serialise on one thread.
+// kSplit: the call splits its longest tensor-core items (the host's decision);
+// the other instantiation carries none of that code.
+template <bool kSplit>
 __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanParams p) {
-    __shared__ int hist[1024];
+    __shared__ int hist[1025];      // cost buckets; entry 1024 takes no-op additions
     __shared__ int hist_dec[1024];  // decode-shaped chunks as tensor-core items
+    __shared__ int s_cut;           // lowest bucket whose items are split in two (1024: none)
+    __shared__ int s_nsplit;        // split items placed so far
     __shared__ int warp_sums[64];
     __shared__ unsigned long long s_w_tc, s_w_dec;  // summed costs (two-Q-tile steps)
     __shared__ int s_max_tc, s_max_dec;             // longest item of each kind
@@ -201,6 +217,9 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     hist[tid] = 0;
     hist_dec[tid] = 0;
     if (tid == 0) {
+        hist[1024] = 0;
+        s_cut = 1024;
+        s_nsplit = 0;
         s_row_tiles = 0;
         s_w_tc = s_w_dec = 0;
         s_max_tc = s_max_dec = 0;
@@ -292,14 +311,65 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
                                                          p.sm_count));
     if (absorb) hist[tid] += hist_dec[tid];
     __syncthreads();
-    const int n_tc = p.tc_work ? desc_offsets(hist, warp_sums) : 0;
+    int n_tc = p.tc_work ? desc_offsets(hist, warp_sums) : 0;
     const unsigned long long row_tiles_all = absorb ? 0ull : s_row_tiles;
+
+    // The item of KV-tile cost `tiles` and bucket `bk` is split when bk >= cut:
+    // part 0 takes its first (tiles + 1) / 2 tiles.  A part's weight: its
+    // tiles, or for a decode-shaped item dec_weight of them.
+    auto part_weight = [&](int tiles, bool dec) { return dec ? dec_weight(tiles) : tiles; };
+    if (kSplit && p.tc_work && p.lay.cap_split > 0) {
+        // hist[b] now counts the items in the buckets above b, so the items in
+        // buckets >= b number hist[b - 1]; the buckets to split are the top ones
+        const unsigned long long w_all = s_w_tc + (absorb ? s_w_dec : 0ull);
+        const unsigned long long theta =
+            max(w_all / (2ull * (unsigned long long)max(p.sm_count, 1)), 16ull);
+        const int above = tid > 0 ? hist[tid - 1] : n_tc;
+        if (above <= p.lay.cap_split && (unsigned long long)bucket_min_cost(tid) > theta)
+            atomicMin(&s_cut, tid);
+        __syncthreads();
+        if (s_cut < 1024) {
+            // ---- sweep 1b: the histogram again, with the parts' own costs
+            hist[tid] = 0;
+            if (tid == 0) hist[1024] = 0;
+            for (int chunk0 = 0; chunk0 < p.batch; chunk0 += 1024) {
+                __syncthreads();
+                if (!one_chunk) load_chunk(chunk0, false);
+                s_a[tid] = n_tc_of(s_seq[tid], absorb);
+                __syncthreads();
+                const int total = excl_scan(s_a, warp_sums);
+                for (int f = tid; f < total; f += 1024) {
+                    const int sl = segment_of(s_a, 1024, f);
+                    const int4 v = s_seq[sl];
+                    const int k = f - s_a[sl];
+                    const bool dec = v.x <= rmax;
+                    const int tiles = tc_cost(v.y, v.x, k, item_pos, p.window, p.causal);
+                    const int bk = cost_bucket(part_weight(tiles, dec));
+                    const int first =
+                        first_key(v.y + k * item_pos, p.window) / kTileN;
+                    const bool split = bk >= s_cut && first + tiles <= kSplitMaxTile;
+                    const int c0 = (tiles + 1) / 2;
+                    warp_agg_add(hist, split ? cost_bucket(part_weight(c0, dec)) : bk, H);
+                    warp_agg_add(hist, split ? cost_bucket(part_weight(tiles - c0, dec)) : 1024,
+                                 H);
+                }
+            }
+            __syncthreads();
+            n_tc = desc_offsets(hist, warp_sums);
+        }
+    }
+    const int cut = kSplit ? s_cut : 1024;
 
     // ---- from here on global memory is written: the previous kernel is done
     pdl_wait();
     if (bad_meta) report_error(p.dev_err, PCP_ERR_INVALID_ARG);
     if (tid == 0 && row_tiles_all >= (1ull << 31)) report_error(p.dev_err, PCP_ERR_UNSUPPORTED);
     for (int64_t i = tid; i < (int64_t)p.batch * H; i += 1024) gdesc[i] = make_int4(0, 0, 0, 0);
+    if (kSplit && cut < 1024) {  // split items' tickets and ready flags start at zero
+        int* tc_sync = reinterpret_cast<int*>(p.ws + p.lay.tc_sync);
+        for (int64_t i = tid; i < p.lay.cap_split * kQTiles * 4 * 2; i += 1024) tc_sync[i] = 0;
+    }
+    const int64_t cap_items = p.lay.cap_tc + p.lay.cap_split;
     // a CTA whose tiles are all virtual has no row group
     if (tid < kRowMaxCtas) row_first[tid] = -1;
     const int T = (int)min(row_tiles_all, (unsigned long long)INT32_MAX);
@@ -332,15 +402,47 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
             const int g = (f - s_a[sl]) / n;
             const int k = (f - s_a[sl]) - g * n;
             const int cost = tc_cost(v.y, v.x, k, item_pos, p.window, p.causal);
-            // a decode-shaped chunk's item is in the bucket of its weight
-            const int wc = v.x > rmax ? cost : dec_weight(v.w);
-            // lanes with one bucket get consecutive slots in lane order
-            const int slot = warp_agg_add(hist, cost_bucket(wc), 1);
-            if (slot >= p.lay.cap_tc) {
-                report_error(p.dev_err, PCP_ERR_WORKSPACE);
-                continue;
+            if constexpr (!kSplit) {
+                // a decode-shaped chunk's item is in the bucket of its weight
+                const int wc = v.x > rmax ? cost : dec_weight(v.w);
+                // lanes with one bucket get consecutive slots in lane order
+                const int slot = warp_agg_add(hist, cost_bucket(wc), 1);
+                if (slot >= p.lay.cap_tc) {
+                    report_error(p.dev_err, PCP_ERR_WORKSPACE);
+                    continue;
+                }
+                tc[slot] = make_int4(chunk0 + sl, g, k * item_pos, cost);
+            } else {
+                // a decode-shaped chunk's item is in the bucket of its weight
+                const bool dec = v.x <= rmax;
+                const int bk = cost_bucket(part_weight(cost, dec));
+                const int first = first_key(v.y + k * item_pos, p.window) / kTileN;
+                const bool split = bk >= cut && first + cost <= kSplitMaxTile;
+                const int c0 = (cost + 1) / 2;
+                // lanes with one bucket get consecutive slots in lane order; a split
+                // item places its second part too (the others add nothing to the
+                // spare entry)
+                const int slot =
+                    warp_agg_add(hist, split ? cost_bucket(part_weight(c0, dec)) : bk, 1);
+                // (cut is the same for the whole block, so every lane of a warp
+                // takes this branch or none)
+                const int slot1 =
+                    cut < 1024 ? warp_agg_add(
+                                     hist, split ? cost_bucket(part_weight(cost - c0, dec)) : 1024, 1)
+                               : 0;
+                int w0 = cost, w1 = 0;
+                if (split) {
+                    const int sp = atomicAdd(&s_nsplit, 1);  // < cap_split by the cut
+                    w0 = kSplitTag | ((first + c0) << 12) | (sp << 1);
+                    w1 = w0 | 1;
+                }
+                if (slot >= cap_items || (split && slot1 >= cap_items)) {
+                    report_error(p.dev_err, PCP_ERR_WORKSPACE);
+                    continue;
+                }
+                tc[slot] = make_int4(chunk0 + sl, g, k * item_pos, w0);
+                if (split) tc[slot1] = make_int4(chunk0 + sl, g, k * item_pos, w1);
             }
-            tc[slot] = make_int4(chunk0 + sl, g, k * item_pos, cost);
         }
         for (int f = tid; f < total_b; f += 1024) {
             const int sl = segment_of(s_b, 1024, f);
@@ -375,7 +477,7 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     }
     __syncthreads();
     if (tid == 0) {
-        hdr->n_tc_items = (int)min((int64_t)n_tc, p.lay.cap_tc);
+        hdr->n_tc_items = (int)min((int64_t)n_tc, cap_items);
         hdr->n_row_groups = (int)min((int64_t)grp_base, p.lay.cap_groups);
         hdr->tc_next = 0;
         hdr->row_tiles = T;
@@ -384,7 +486,8 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
 }
 
 cudaError_t launch_plan(cudaStream_t stream, const PlanParams& p) {
-    return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, p);
+    if (p.split) return launch_pdl(plan_kernel<true>, dim3(1), dim3(1024), 0, stream, p);
+    return launch_pdl(plan_kernel<false>, dim3(1), dim3(1024), 0, stream, p);
 }
 
 }  // namespace pcp
