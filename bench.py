@@ -152,8 +152,9 @@ def split_work(batch):
 
 
 def launches_per_step(batch, rows_on_tensor_cores: bool = False) -> int:
-    """Library kernels one step launches (with host copies of qo_indptr and
-    prefix_lens): the fused append; the planner unless the row kernel plans
+    """Library kernels one step (the attention call with the step's new K/V
+    rows and host copies of qo_indptr and prefix_lens) launches: the planner
+    with the append beside it, or the append alone when the row kernel plans
     a decode-only call of at most 512 sequences itself; the tensor-core
     kernel for chunks above the row path's size; the row kernel and the
     combine for decode-shaped chunks unless they joined the tensor cores."""
@@ -162,8 +163,7 @@ def launches_per_step(batch, rows_on_tensor_cores: bool = False) -> int:
     c = np.diff(batch.qo_indptr)
     tc = bool((c > rmax).any())
     rows = bool(((c > 0) & (c <= rmax)).any()) and not rows_on_tensor_cores
-    plan = not (not tc and rows and batch.batch <= 512)
-    return 1 + int(plan) + int(tc) + 2 * int(rows)
+    return 1 + int(tc) + 2 * int(rows)
 
 
 def load_peaks():
@@ -403,15 +403,15 @@ def main():
     flush = L2Flush(torch, dev)
 
     def step(tc_events=None):
-        pcp.kv_append_paged(d["qo_indptr"], d["kv_indptr"], d["kv_indices"], d["prefix_lens"],
-                            batch.page_size, d["k_new"], d["v_new"], d["k_pool"], d["v_pool"],
-                            dev_err=err)
+        # one call: the append of the step's new K/V rows (in the planner's
+        # launch) and the attention over the pools
         pcp.paged_extend_attn(d["q"], d["qo_indptr"], d["kv_indptr"],
                               d["kv_indices"], d["prefix_lens"], d["k_pool"], d["v_pool"],
                               batch.page_size, batch.n_q_heads, batch.n_kv_heads,
                               batch.head_dim, batch.window, batch.sm_scale, out=out, lse=lse,
                               workspace=ws, dev_err=err, qo_indptr_host=batch.qo_indptr,
-                              prefix_lens_host=batch.prefix_lens, tc_events=tc_events)
+                              prefix_lens_host=batch.prefix_lens, tc_events=tc_events,
+                              k_new=d["k_new"], v_new=d["v_new"])
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -590,15 +590,13 @@ def end_to_end(args, torch, pcp, batch, d, out_ref, flush, stream, flops, world)
         S["in"].copy_(h_in, non_blocking=True)
 
     def kernels(S):
-        pcp.kv_append_paged(S["qo_indptr"], S["kv_indptr"], S["kv_indices"], S["prefix_lens"],
-                            batch.page_size, S["k_new"], S["v_new"], S["k_pool"], S["v_pool"],
-                            dev_err=err)
         pcp.paged_extend_attn(S["q"], S["qo_indptr"], S["kv_indptr"], S["kv_indices"],
                               S["prefix_lens"], S["k_pool"], S["v_pool"], batch.page_size,
                               batch.n_q_heads, batch.n_kv_heads, batch.head_dim, batch.window,
                               batch.sm_scale, out=S["out"], lse=S["lse"], workspace=S["ws"],
                               dev_err=err, qo_indptr_host=batch.qo_indptr,
-                              prefix_lens_host=batch.prefix_lens)
+                              prefix_lens_host=batch.prefix_lens, k_new=S["k_new"],
+                              v_new=S["v_new"])
 
     def d2h_copies(S):
         S["h_res"].copy_(S["res"], non_blocking=True)
@@ -759,20 +757,18 @@ def decode_step_secondary(pcp, torch, db, dev, peaks, flush, err, res):
                                          db.head_dim), dtype=torch.uint8, device=dev)
 
     def dstep(ev):
-        pcp.kv_append_paged(g["qo_indptr"], g["kv_indptr"], g["kv_indices"], g["prefix_lens"],
-                            db.page_size, g["k_new"], g["v_new"], g["k_pool"], g["v_pool"],
-                            dev_err=err)
         pcp.paged_extend_attn(g["q"], g["qo_indptr"], g["kv_indptr"], g["kv_indices"],
                               g["prefix_lens"], g["k_pool"], g["v_pool"], db.page_size,
                               db.n_q_heads, db.n_kv_heads, db.head_dim, db.window, db.sm_scale,
                               out=dout, lse=dlse, workspace=dws, dev_err=err,
-                              qo_indptr_host=db.qo_indptr, prefix_lens_host=db.prefix_lens)
+                              qo_indptr_host=db.qo_indptr, prefix_lens_host=db.prefix_lens,
+                              k_new=g["k_new"], v_new=g["v_new"])
     ms = time_calls(torch, dstep, flush)
     sbytes = nbytes + 2 * 2 * db.total_q * db.n_kv_heads * db.head_dim * 2
     gbs = sbytes / (ms * 1e-3) / 1e9
     res["decode_step"] = {"workload": db.name, "ms": ms, "GB/s": gbs,
                           "frac_hbm": gbs / peaks["hbm_gbs"], "bytes": sbytes,
-                          "what": "fused append of the rows' new tokens, then the attention call"}
+                          "what": "the attention call with the rows' new tokens appended in it"}
     del g, dout, dlse, dws
 
 

@@ -425,9 +425,10 @@ pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_er
 
 /*
  * Per-call options: instrumentation for profiling and for tests of the
- * device-side error paths (the pages have no counterpart), and a host copy
- * of prefix_lens for the launch decision.  A zeroed struct (or a NULL
- * pointer) means: no events, the default wait limit, no host copy.
+ * device-side error paths (the pages have no counterpart), a host copy of
+ * prefix_lens for the launch decision, and the step's new K/V rows to append
+ * before attending.  A zeroed struct (or a NULL pointer) means: no events,
+ * the default wait limit, no host copy, no append.
  *   tc_event_before / tc_event_after: NULL, or cudaEvent_t values (as void*)
  *     recorded on the call's stream right before and right after the launch
  *     of the tensor-core kernel, so the caller can time that kernel alone
@@ -469,6 +470,20 @@ pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_er
  *     result.  A split changes only the rounding order of those rows.  It
  *     needs the full pcp_extend_workspace_size: with a smaller workspace
  *     the call runs unsplit.
+ *   k_new / v_new: NULL, or the step's new K and V rows, [total_q,
+ *     n_kv_heads, head_dim] bf16 on the device, 16-byte aligned; both or
+ *     neither.  The call first does what pcp_kv_append_paged does with them
+ *     (slot mapping from the page table, scatter into k_pool / v_pool; a bad
+ *     page id sets *dev_err = PCP_ERR_BAD_INDEX and that token is not
+ *     written), then attends over the pools it wrote (AReno PR #642, "What
+ *     does this PR do?": the chunk's own keys are in the cache when it
+ *     attends).  The pools and the results are bit-identical to
+ *     pcp_kv_append_paged followed by the same call without k_new / v_new;
+ *     the append runs in the planner's launch, beside the planning, instead
+ *     of in a kernel of its own ahead of it.  The pools are written while the
+ *     call runs: the caller orders other readers of the same slots.
+ *   out_cache_loc: NULL, or (with k_new / v_new) device int64 [total_q] that
+ *     receives each new token's slot (-1 for a token whose page id is bad).
  * The library keeps nothing of it after the call returns.
  */
 typedef struct pcp_call_options {
@@ -478,6 +493,9 @@ typedef struct pcp_call_options {
     void* rows_event_after;
     uint64_t test_stall_ns;
     const int32_t* prefix_lens_host;
+    const void* k_new;
+    const void* v_new;
+    int64_t* out_cache_loc;
 } pcp_call_options;
 
 /*

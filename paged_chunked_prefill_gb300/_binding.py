@@ -32,11 +32,13 @@ class Status(enum.IntEnum):
 
 class CallOptions(ctypes.Structure):
     """``pcp_call_options``: per-call events around the tensor-core and row
-    kernels, the stall that tests the kernels' timeout path, and the host
-    copy of prefix_lens."""
+    kernels, the stall that tests the kernels' timeout path, the host copy of
+    prefix_lens, and the step's new K/V rows to append before attending."""
     _fields_ = [("tc_event_before", ctypes.c_void_p), ("tc_event_after", ctypes.c_void_p),
                 ("rows_event_before", ctypes.c_void_p), ("rows_event_after", ctypes.c_void_p),
-                ("test_stall_ns", ctypes.c_uint64), ("prefix_lens_host", ctypes.c_void_p)]
+                ("test_stall_ns", ctypes.c_uint64), ("prefix_lens_host", ctypes.c_void_p),
+                ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("out_cache_loc", ctypes.c_void_p)]
 
 
 class PCPError(RuntimeError):
@@ -313,7 +315,9 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
                       qo_indptr_host=None, causal: bool = True,
                       mask: Optional[torch.Tensor] = None,
                       tc_events=None, rows_events=None, test_stall_ns: int = 0,
-                      prefix_lens_host=None,
+                      prefix_lens_host=None, k_new: Optional[torch.Tensor] = None,
+                      v_new: Optional[torch.Tensor] = None,
+                      out_cache_loc: Optional[torch.Tensor] = None,
                       check: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
     """Extend attention of every query row over its cached prefix and own
     chunk (bottom-right causal, GQA, optional window).  Returns (out, lse):
@@ -335,7 +339,11 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
     recorded around the tensor-core / row kernel of this call.
     test_stall_ns: 0, or the limit of a wait that nothing ends, made by every
     CTA of the kernels the call launches (a test of their timeout path: the
-    call then reports PCP_ERR_TIMEOUT)."""
+    call then reports PCP_ERR_TIMEOUT).
+    k_new, v_new: optional bf16 [total_q, Hkv, D] new K/V rows of the step;
+    the call first appends them into k_pool / v_pool (as kv_append_paged
+    does, in the planner's launch) and then attends.  out_cache_loc (int64
+    [total_q], optional, with k_new) receives the slots."""
     dev = q.device
     _need(q, "q", torch.bfloat16, dev)
     _need(k_pool, "k_pool", torch.bfloat16, dev)
@@ -362,12 +370,24 @@ def paged_extend_attn(q: torch.Tensor, qo_indptr: torch.Tensor, kv_indptr: torch
         dev_err = _dev_err(dev)
     host_ptr, host_keep = _host_i32(qo_indptr_host, batch + 1, "qo_indptr_host")
     pl_ptr, pl_keep = _host_i32(prefix_lens_host, batch, "prefix_lens_host")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        _need(k_new, "k_new", torch.bfloat16, dev)
+        _need(v_new, "v_new", torch.bfloat16, dev)
+        if tuple(k_new.shape) != (total_q, n_kv_heads, head_dim) or v_new.shape != k_new.shape:
+            raise ValueError("k_new, v_new must be [total_q, n_kv_heads, head_dim]")
+    if out_cache_loc is not None:
+        if k_new is None:
+            raise ValueError("out_cache_loc comes with k_new / v_new")
+        _need(out_cache_loc, "out_cache_loc", torch.int64, dev)
     if (tc_events is not None or rows_events is not None or test_stall_ns or
-            prefix_lens_host is not None):
+            prefix_lens_host is not None or k_new is not None):
         ev = lambda e: ctypes.c_void_p(e.cuda_event) if e is not None else ctypes.c_void_p(0)
         tb, ta = tc_events if tc_events is not None else (None, None)
         rb, ra = rows_events if rows_events is not None else (None, None)
-        opts = CallOptions(ev(tb), ev(ta), ev(rb), ev(ra), int(test_stall_ns), pl_ptr)
+        opts = CallOptions(ev(tb), ev(ta), ev(rb), ev(ra), int(test_stall_ns), pl_ptr,
+                           _ptr(k_new), _ptr(v_new), _ptr(out_cache_loc))
         mkeep, mptr, sb, sh, sq, mq, mkv = _mask_args(mask, batch, n_q_heads, dev)
         _check(lib().pcp_paged_extend_attn_ex(
             _ptr(q), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(prefix_lens),

@@ -20,6 +20,7 @@ bool pdl_enabled() {
 }
 
 cudaError_t launch_plan(cudaStream_t stream, const PlanParams& p);
+cudaError_t launch_plan_append(cudaStream_t stream, const PlanParams& p, const AppendParams& a);
 cudaError_t launch_extend_tc(int head_dim, int grid, cudaStream_t stream, const TcParams& p,
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv);
 cudaError_t launch_rows(int head_dim, int grid, cudaStream_t stream, const RowParams& p,
@@ -34,12 +35,7 @@ cudaError_t launch_copy_page_slots(const int32_t* src, const int32_t* dst,
                                    const int32_t* n_slots, int n_copies, int64_t num_pages,
                                    int page_size, int chunks_per_slot, void* k_pool,
                                    void* v_pool, int32_t* dev_err, cudaStream_t stream);
-cudaError_t launch_kv_append_paged(const int32_t* qo_indptr, const int32_t* kv_indptr,
-                                   const int32_t* kv_indices, const int32_t* prefix_lens,
-                                   int batch, int64_t total_q, int page_size, int64_t num_pages,
-                                   const void* k, const void* v, int chunks_per_token,
-                                   void* k_pool, void* v_pool, int64_t* loc, int32_t* dev_err,
-                                   int sm_count, cudaStream_t stream);
+cudaError_t launch_kv_append_paged(const AppendParams& a, cudaStream_t stream);
 cudaError_t launch_kv_append(const void* k, const void* v, const int64_t* loc, int64_t n_tokens,
                              int chunks_per_token, void* k_pool, void* v_pool, int64_t pool_slots,
                              int32_t* dev_err, int sm_count, cudaStream_t stream);
@@ -171,6 +167,12 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     if ((o.tc_event_before == nullptr) != (o.tc_event_after == nullptr) ||
         (o.rows_event_before == nullptr) != (o.rows_event_after == nullptr))
         return PCP_ERR_INVALID_ARG;
+    // the step's new K/V rows, appended before attending: both or neither
+    const bool append = o.k_new != nullptr || o.v_new != nullptr;
+    if (append && (o.k_new == nullptr || o.v_new == nullptr ||
+                   (a.total_q > 0 && (!aligned(o.k_new, 16) || !aligned(o.v_new, 16)))))
+        return PCP_ERR_INVALID_ARG;
+    if (o.out_cache_loc != nullptr && !append) return PCP_ERR_INVALID_ARG;
     if (a.total_q == 0) return PCP_OK;
     // a call needs the workspace up to the split buffers; it splits items only
     // when the whole layout fits
@@ -296,7 +298,35 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     pp.ws = ws;
     pp.lay = lay;
     pp.dev_err = a.dev_err;
-    if (!self_plan && failed(launch_plan(s, pp))) return PCP_ERR_CUDA;
+    // The append (slot mapping and scatter of the step's new K/V rows) runs in
+    // the planner's launch, in CTAs of its own beside the planning CTA: as a
+    // kernel of its own ahead of the planner it filled every SM's register
+    // file, so the planner could start only once the append drained.  A
+    // self-planned call launches the append kernel ahead of the row kernel.
+    AppendParams ap;
+    if (append) {
+        ap.qo_indptr = a.qo_indptr;
+        ap.kv_indptr = a.kv_indptr;
+        ap.kv_indices = a.kv_indices;
+        ap.prefix_lens = a.prefix_lens;
+        ap.batch = a.batch;
+        ap.total_q = a.total_q;
+        ap.page_size = page_size;
+        ap.num_pages = a.num_pages;
+        ap.k = o.k_new;
+        ap.v = o.v_new;
+        ap.chunks_per_token = a.n_kv_heads * head_dim * 2 / 16;
+        ap.k_pool = const_cast<void*>(a.k_pool);
+        ap.v_pool = const_cast<void*>(a.v_pool);
+        ap.loc = o.out_cache_loc;
+        ap.dev_err = a.dev_err;
+    }
+    if (!self_plan) {
+        if (failed(append ? launch_plan_append(s, pp, ap) : launch_plan(s, pp)))
+            return PCP_ERR_CUDA;
+    } else if (append && failed(launch_kv_append_paged(ap, s))) {
+        return PCP_ERR_CUDA;
+    }
 
     // ---- 2. tensor-core extend kernel (persistent, one CTA per SM)
     TcParams tp;
@@ -403,7 +433,7 @@ const char* pcp_status_string(int status) {
     }
 }
 
-int pcp_abi_version(void) { return 4; }
+int pcp_abi_version(void) { return 5; }
 
 const char* pcp_last_cuda_error(void) {
     return t_last_cuda == cudaSuccess ? "no error" : cudaGetErrorString(t_last_cuda);
@@ -465,14 +495,23 @@ pcp_status pcp_kv_append_paged(const int32_t* qo_indptr, const int32_t* kv_indpt
         return PCP_ERR_INVALID_ARG;
     if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16))
         return PCP_ERR_INVALID_ARG;
-    int sms = 0;
-    pcp_status st = sm_count(&sms);
-    if (st != PCP_OK) return st;
-    const int chunks = n_kv_heads * head_dim * 2 / 16;
-    cudaError_t e = launch_kv_append_paged(qo_indptr, kv_indptr, kv_indices, prefix_lens, batch,
-                                           total_q, page_size, num_pages, k, v, chunks, k_pool,
-                                           v_pool, out_cache_loc, dev_err, sms,
-                                           static_cast<cudaStream_t>(stream));
+    AppendParams ap;
+    ap.qo_indptr = qo_indptr;
+    ap.kv_indptr = kv_indptr;
+    ap.kv_indices = kv_indices;
+    ap.prefix_lens = prefix_lens;
+    ap.batch = batch;
+    ap.total_q = total_q;
+    ap.page_size = page_size;
+    ap.num_pages = num_pages;
+    ap.k = k;
+    ap.v = v;
+    ap.chunks_per_token = n_kv_heads * head_dim * 2 / 16;
+    ap.k_pool = k_pool;
+    ap.v_pool = v_pool;
+    ap.loc = out_cache_loc;
+    ap.dev_err = dev_err;
+    cudaError_t e = launch_kv_append_paged(ap, static_cast<cudaStream_t>(stream));
     return failed(e) ? PCP_ERR_CUDA : PCP_OK;
 }
 

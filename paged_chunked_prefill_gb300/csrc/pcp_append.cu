@@ -7,6 +7,7 @@
 // k_buffer[layer, out_cache_loc] = k before attending; here both are kernels.
 #include <algorithm>
 
+#include "pcp_append_body.cuh"
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
 #include "pcp_launch.h"
@@ -63,32 +64,7 @@ __global__ void out_cache_loc_kernel(const int32_t* __restrict__ qo_indptr,
 // thread per token, into shared memory), then the stores go out.  One wave
 // of such blocks keeps 32 KB in flight per block.
 constexpr int kAppendThreads = 256;
-constexpr int kAppendUnroll = 4;
 constexpr int kAppendSpan = kAppendThreads * kAppendUnroll;
-
-// Slot of new token t from the page table (the arithmetic of
-// out_cache_loc_kernel); qo is qo_indptr (staged or global).  -1 when the
-// page id is bad or the metadata do not place t.
-__device__ __forceinline__ int64_t slot_of_token(const int32_t* qo, int batch, int64_t t,
-                                                 const int32_t* __restrict__ kv_indptr,
-                                                 const int32_t* __restrict__ kv_indices,
-                                                 const int32_t* __restrict__ prefix_lens,
-                                                 int page_size, int64_t num_pages) {
-    int lo = 0, hi = batch;  // sequence of row t: the last b with qo[b] <= t
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (qo[mid] <= t) lo = mid;
-        else hi = mid;
-    }
-    const int b = lo;
-    if (!(t >= qo[b] && t < qo[b + 1])) return -1;
-    const int64_t pos = (int64_t)__ldg(prefix_lens + b) + (t - qo[b]);
-    const int kb = __ldg(kv_indptr + b);
-    const int64_t entry = pos / page_size;
-    if (pos < 0 || entry >= (int64_t)__ldg(kv_indptr + b + 1) - kb) return -1;
-    const int64_t page = __ldg(kv_indices + kb + entry);
-    return (page >= 0 && page < num_pages) ? page * page_size + pos % page_size : -1;
-}
 
 // KV append from precomputed slots: k_pool[loc[t]] = k[t], v_pool[loc[t]] = v[t].
 __global__ void __launch_bounds__(kAppendThreads, 4)
@@ -133,80 +109,21 @@ __global__ void __launch_bounds__(kAppendThreads, 4)
     }
 }
 
-// Slot mapping and KV append in one pass: the slots of the span's tokens
-// come from the page table (qo_indptr staged in shared memory, then
-// prefix_lens, kv_indptr and the page id) while the span's K/V loads are in
-// flight, so no out_cache_loc array is read back.  The block holding a
-// token's first chunk writes loc[t] when asked.
+// Slot mapping and KV append in one pass (append_paged_span): the slots of
+// the span's tokens come from the page table while the span's K/V loads are
+// in flight, so no out_cache_loc array is read back.
 __global__ void __launch_bounds__(kAppendThreads, 4)
-    kv_append_paged_kernel(const int32_t* __restrict__ qo_indptr,
-                           const int32_t* __restrict__ kv_indptr,
-                           const int32_t* __restrict__ kv_indices,
-                           const int32_t* __restrict__ prefix_lens, int batch, int64_t total_q,
-                           int page_size, int64_t num_pages, const uint4* __restrict__ k,
-                           const uint4* __restrict__ v, int chunks_per_token,
-                           uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
-                           int64_t* __restrict__ loc, int32_t* dev_err) {
-    constexpr int kStagedSeqs = 2048;
-    __shared__ int s_qo[kStagedSeqs + 1];
-    __shared__ int64_t s_slot[kAppendSpan + 1];
+    kv_append_paged_kernel(const __grid_constant__ AppendParams a) {
+    __shared__ AppendSmem<kAppendThreads> S;
     pdl_wait();
     pdl_launch_dependents();
-    const int64_t total = total_q * chunks_per_token;
-    const int64_t c0 = (int64_t)blockIdx.x * kAppendSpan;
-    uint4 kr[kAppendUnroll], vr[kAppendUnroll];
-#pragma unroll
-    for (int j = 0; j < kAppendUnroll; ++j) {
-        const int64_t idx = c0 + j * kAppendThreads + threadIdx.x;
-        if (idx < total) {
-            kr[j] = __ldcs(k + idx);
-            vr[j] = __ldcs(v + idx);
-        }
-    }
-    const bool staged = batch <= kStagedSeqs;
-    if (staged) {
-        for (int i = threadIdx.x; i <= batch; i += kAppendThreads) s_qo[i] = qo_indptr[i];
-        __syncthreads();
-    }
-    const int32_t* qo = staged ? s_qo : qo_indptr;
-    const int64_t t0 = c0 / chunks_per_token;
-    const int64_t t1 = (min(total, c0 + kAppendSpan) - 1) / chunks_per_token;
-    for (int64_t t = t0 + threadIdx.x; t <= t1; t += kAppendThreads) {
-        const int64_t s = slot_of_token(qo, batch, t, kv_indptr, kv_indices, prefix_lens,
-                                        page_size, num_pages);
-        if (t * chunks_per_token >= c0) {
-            if (s < 0) report_error(dev_err, PCP_ERR_BAD_INDEX);
-            if (loc != nullptr) loc[t] = s;
-        }
-        s_slot[t - t0] = s;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < kAppendUnroll; ++j) {
-        const int64_t idx = c0 + j * kAppendThreads + threadIdx.x;
-        if (idx >= total) continue;
-        const int64_t t = idx / chunks_per_token;
-        const int64_t s = s_slot[t - t0];
-        if (s < 0) continue;
-        const int64_t ch = idx - t * chunks_per_token;
-        __stcs(k_pool + s * chunks_per_token + ch, kr[j]);
-        __stcs(v_pool + s * chunks_per_token + ch, vr[j]);
-    }
+    append_paged_span<kAppendThreads>(a, S, blockIdx.x);
 }
 
-cudaError_t launch_kv_append_paged(const int32_t* qo_indptr, const int32_t* kv_indptr,
-                                   const int32_t* kv_indices, const int32_t* prefix_lens,
-                                   int batch, int64_t total_q, int page_size, int64_t num_pages,
-                                   const void* k, const void* v, int chunks_per_token,
-                                   void* k_pool, void* v_pool, int64_t* loc, int32_t* dev_err,
-                                   int sm_count, cudaStream_t stream) {
-    (void)sm_count;
-    const int64_t blocks = (total_q * chunks_per_token + kAppendSpan - 1) / kAppendSpan;
+cudaError_t launch_kv_append_paged(const AppendParams& a, cudaStream_t stream) {
+    const int64_t blocks = (a.total_q * a.chunks_per_token + kAppendSpan - 1) / kAppendSpan;
     return launch_pdl(kv_append_paged_kernel, dim3((unsigned)blocks), dim3(kAppendThreads), 0,
-                      stream, qo_indptr, kv_indptr, kv_indices, prefix_lens, batch, total_q,
-                      page_size, num_pages, static_cast<const uint4*>(k),
-                      static_cast<const uint4*>(v), chunks_per_token,
-                      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), loc, dev_err);
+                      stream, a);
 }
 
 // Copy-on-write of shared pages: for copy c, slots [0, n_slots[c]) of page

@@ -240,6 +240,26 @@ struct PlanParams {
     int32_t* dev_err;
 };
 
+// ---- the fused slot mapping and KV append (pcp_kv_append_paged, and the
+// append a call runs beside its planner)
+struct AppendParams {
+    const int32_t* qo_indptr;
+    const int32_t* kv_indptr;
+    const int32_t* kv_indices;
+    const int32_t* prefix_lens;
+    int batch;
+    int64_t total_q;
+    int page_size;
+    int64_t num_pages;
+    const void* k;           // [total_q, n_kv_heads, head_dim] bf16
+    const void* v;
+    int chunks_per_token;    // n_kv_heads * head_dim * 2 / 16
+    void* k_pool;
+    void* v_pool;
+    int64_t* loc;            // nullptr, or out_cache_loc [total_q]
+    int32_t* dev_err;
+};
+
 // ---- parameters of the tensor-core extend kernel
 struct TcParams {
     const int32_t* qo_indptr;

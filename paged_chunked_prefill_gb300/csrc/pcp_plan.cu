@@ -37,6 +37,7 @@
 //    above 16 tiles, longest first, at most kTcMaxSplitItems.  The two parts
 //    are items of their own in the longest-first order; the part that ends
 //    second merges the first one's partial result.
+#include "pcp_append_body.cuh"
 #include "pcp_device.cuh"
 #include "pcp_internal.h"
 #include "pcp_launch.h"
@@ -182,21 +183,40 @@ __device__ __forceinline__ int warp_agg_add(int* base, int key, int inc) {
 // through prefix sums, so a long chunk does not serialise on one thread.
 // kSplit: the call splits its longest tensor-core items (the host's decision);
 // the other instantiation carries none of that code.
+// The planner's shared memory (the planning CTA's, in both kernels below).
+struct PlanSmem {
+    int hist[1025];      // cost buckets; entry 1024 takes no-op additions
+    int hist_dec[1024];  // decode-shaped chunks as tensor-core items
+    int s_cut;           // lowest bucket whose items are split in two (1024: none)
+    int s_nsplit;        // split items placed so far
+    int warp_sums[64];
+    unsigned long long s_w_tc, s_w_dec;  // summed costs (two-Q-tile steps)
+    int s_max_tc, s_max_dec;             // longest item of each kind
+    int s_a[1025];       // per-sequence counts, then their exclusive prefix
+    int s_b[1025];
+    int s_c[1025];
+    int4 s_seq[1024];    // {c, P, ok, row tiles}
+    int2 s_off[1024];    // {qo_indptr[b], kv_indptr[b]}
+    unsigned long long s_row_tiles;
+};
+
 template <bool kSplit>
-__global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanParams p) {
-    __shared__ int hist[1025];      // cost buckets; entry 1024 takes no-op additions
-    __shared__ int hist_dec[1024];  // decode-shaped chunks as tensor-core items
-    __shared__ int s_cut;           // lowest bucket whose items are split in two (1024: none)
-    __shared__ int s_nsplit;        // split items placed so far
-    __shared__ int warp_sums[64];
-    __shared__ unsigned long long s_w_tc, s_w_dec;  // summed costs (two-Q-tile steps)
-    __shared__ int s_max_tc, s_max_dec;             // longest item of each kind
-    __shared__ int s_a[1025];       // per-sequence counts, then their exclusive prefix
-    __shared__ int s_b[1025];
-    __shared__ int s_c[1025];
-    __shared__ int4 s_seq[1024];    // {c, P, ok, row tiles}
-    __shared__ int2 s_off[1024];    // {qo_indptr[b], kv_indptr[b]}
-    __shared__ unsigned long long s_row_tiles;
+__device__ __forceinline__ void plan_body(const PlanParams& p, PlanSmem& S) {
+    auto& hist = S.hist;
+    auto& hist_dec = S.hist_dec;
+    auto& s_cut = S.s_cut;
+    auto& s_nsplit = S.s_nsplit;
+    auto& warp_sums = S.warp_sums;
+    auto& s_w_tc = S.s_w_tc;
+    auto& s_w_dec = S.s_w_dec;
+    auto& s_max_tc = S.s_max_tc;
+    auto& s_max_dec = S.s_max_dec;
+    auto& s_a = S.s_a;
+    auto& s_b = S.s_b;
+    auto& s_c = S.s_c;
+    auto& s_seq = S.s_seq;
+    auto& s_off = S.s_off;
+    auto& s_row_tiles = S.s_row_tiles;
 
     WsHeader* hdr = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
     int4* tc = reinterpret_cast<int4*>(p.ws + p.lay.tc_items);
@@ -485,9 +505,51 @@ __global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ P
     }
 }
 
+template <bool kSplit>
+__global__ void __launch_bounds__(1024, 1) plan_kernel(const __grid_constant__ PlanParams p) {
+    __shared__ PlanSmem S;
+    plan_body<kSplit>(p, S);
+}
+
+// The planner in CTA 0 and the append of the call's new K/V rows in the other
+// CTAs (a span of 4096 chunks each), in one launch: both run at once, one
+// CTA per SM, instead of the planner waiting for an SM that the append has
+// left.
+constexpr int kPlanAppendThreads = 1024;
+constexpr size_t kPlanAppendSmem = sizeof(PlanSmem) > sizeof(AppendSmem<kPlanAppendThreads>)
+                                       ? sizeof(PlanSmem)
+                                       : sizeof(AppendSmem<kPlanAppendThreads>);
+
+template <bool kSplit>
+__global__ void __launch_bounds__(kPlanAppendThreads, 1)
+    plan_append_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ AppendParams a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    if (blockIdx.x == 0) {
+        plan_body<kSplit>(p, *reinterpret_cast<PlanSmem*>(smem));
+    } else {
+        // the new K/V rows may be the previous kernel's output, and the pools
+        // may still be read by it
+        pdl_wait();
+        pdl_launch_dependents();
+        append_paged_span<kPlanAppendThreads>(
+            a, *reinterpret_cast<AppendSmem<kPlanAppendThreads>*>(smem), blockIdx.x - 1);
+    }
+}
+
 cudaError_t launch_plan(cudaStream_t stream, const PlanParams& p) {
     if (p.split) return launch_pdl(plan_kernel<true>, dim3(1), dim3(1024), 0, stream, p);
     return launch_pdl(plan_kernel<false>, dim3(1), dim3(1024), 0, stream, p);
+}
+
+cudaError_t launch_plan_append(cudaStream_t stream, const PlanParams& p, const AppendParams& a) {
+    constexpr int64_t span = (int64_t)kPlanAppendThreads * kAppendUnroll;
+    const int64_t spans = (a.total_q * a.chunks_per_token + span - 1) / span;
+    const dim3 grid((unsigned)(1 + spans));
+    if (p.split)
+        return launch_pdl(plan_append_kernel<true>, grid, dim3(kPlanAppendThreads),
+                          kPlanAppendSmem, stream, p, a);
+    return launch_pdl(plan_append_kernel<false>, grid, dim3(kPlanAppendThreads),
+                      kPlanAppendSmem, stream, p, a);
 }
 
 }  // namespace pcp

@@ -41,7 +41,7 @@ def test_status_strings(lib):
         s = lib.pcp_status_string(code).decode()
         assert s.startswith("PCP_")
     assert lib.pcp_status_string(99).decode() == "PCP_ERR_UNKNOWN"
-    assert lib.pcp_abi_version() == 4
+    assert lib.pcp_abi_version() == 5
     lib.pcp_last_cuda_error.restype = ctypes.c_char_p
     assert lib.pcp_last_cuda_error().decode() == "no error"
 
@@ -106,6 +106,13 @@ def test_host_validation_without_device(lib):
             ctypes.byref(opts) if opts is not None else P(0))
     assert ex(CallOptions(one, P(0), P(0), P(0), 0)) == 1
     assert ex(CallOptions(P(0), P(0), P(0), one, 0)) == 1
+    # the appended rows: k_new and v_new both or neither, 16-byte aligned;
+    # out_cache_loc only with them
+    none = P(0)
+    assert ex(CallOptions(none, none, none, none, 0, none, one, none, none)) == 1
+    assert ex(CallOptions(none, none, none, none, 0, none, none, one, none)) == 1
+    assert ex(CallOptions(none, none, none, none, 0, none, P(0x1008), one, none)) == 1
+    assert ex(CallOptions(none, none, none, none, 0, none, none, none, one)) == 1
     # the argument checks come before the options are looked at
     assert lib.pcp_paged_extend_attn_ex(
         one, one, one, one, one, P(0), 1, 10, one, one, 4, 16, 30, 8, 128, 0,

@@ -90,15 +90,16 @@ def test_split_work_matches_brute_force(window):
 
 
 def test_launches_per_step():
-    """Library kernels per step: the GQA step launches the fused append, the
-    planner and the tensor-core kernel; a decode-only step of 31 sequences
-    the append, the row kernel (which plans itself) and the combine; the
-    mixed step all five, or three when its decode rows joined the tensor
-    cores."""
-    assert bench.launches_per_step(W.gqa_prefill()) == 3
+    """Library kernels per step (one call with the new K/V rows): the GQA
+    step launches the planner with the append beside it and the tensor-core
+    kernel; a decode-only step of 31 sequences the append, the row kernel
+    (which plans itself) and the combine; the mixed step four, or two when
+    its decode rows joined the tensor cores."""
+    assert bench.launches_per_step(W.gqa_prefill()) == 2
     assert bench.launches_per_step(W.decode_rows()) == 3
-    assert bench.launches_per_step(W.mixed_batch()) == 5
-    assert bench.launches_per_step(W.mixed_batch(), rows_on_tensor_cores=True) == 3
-    # more than 512 decode-only sequences go through the planner kernel
+    assert bench.launches_per_step(W.mixed_batch()) == 4
+    assert bench.launches_per_step(W.mixed_batch(), rows_on_tensor_cores=True) == 2
+    # more than 512 decode-only sequences: the planner (with the append
+    # beside it), the row kernel and the combine
     b = W.make_batch([100] * 513, [1] * 513, 4, 4, 64, 16, seed=3)
-    assert bench.launches_per_step(b) == 4
+    assert bench.launches_per_step(b) == 3
