@@ -65,20 +65,20 @@ def rows_pairs(batch, tok, head) -> int:
 # reads null until the counters are taken again.
 NCU_TRAFFIC = {
     ("gqa_prefill", "extend_tc_kernel<128>"): {
-        "bytes": 201.301504e6 + 13.922560e6,
-        "sources_sha256": "97fe8ba8a3515568d30797afbad966e6",
+        "bytes": 200.965376e6 + 13.591808e6,
+        "sources_sha256": "87fdfea9e31a088cca7a7a4d0d9b30d0",
     },
     ("long_context", "extend_tc_kernel<128>"): {
-        "bytes": 3990.420992e6 + 530.932480e6,
-        "sources_sha256": "97fe8ba8a3515568d30797afbad966e6",
+        "bytes": 4107.955712e6 + 531.129600e6,
+        "sources_sha256": "87fdfea9e31a088cca7a7a4d0d9b30d0",
     },
     ("mixed", "extend_tc_kernel<128>"): {
-        "bytes": 307.293184e6 + 5.312512e6,
-        "sources_sha256": "97fe8ba8a3515568d30797afbad966e6",
+        "bytes": 307.084032e6 + 5.412096e6,
+        "sources_sha256": "87fdfea9e31a088cca7a7a4d0d9b30d0",
     },
     ("decode_rows", "row_attn_kernel<128>"): {
-        "bytes": 275.751680e6 + 0.592128e6,
-        "sources_sha256": "476fc3909cd411890c06771684dcf18d",
+        "bytes": 275.768320e6 + 0.715520e6,
+        "sources_sha256": "a32e78d758e16b74fa854bc7f3581d9a",
     },
 }
 

@@ -478,9 +478,12 @@ pcp_status pcp_read_error(const int32_t* dev_err, void* stream, int32_t* host_er
  *     written), then attends over the pools it wrote (AReno PR #642, "What
  *     does this PR do?": the chunk's own keys are in the cache when it
  *     attends).  The pools and the results are bit-identical to
- *     pcp_kv_append_paged followed by the same call without k_new / v_new;
- *     the append runs in the planner's launch, beside the planning, instead
- *     of in a kernel of its own ahead of it.  The pools are written while the
+ *     pcp_kv_append_paged followed by the same call without k_new / v_new.
+ *     The append runs in the planner's launch, beside the planning, when it
+ *     fits in one wave of that launch's CTAs (one per SM, 4096 16-byte
+ *     chunks of K and as many of V each); a longer one, and the append of a
+ *     decode-only call planned inside the row kernel, runs as the kernel of
+ *     pcp_kv_append_paged ahead of the rest.  The pools are written while the
  *     call runs: the caller orders other readers of the same slots.
  *   out_cache_loc: NULL, or (with k_new / v_new) device int64 [total_q] that
  *     receives each new token's slot (-1 for a token whose page id is bad).

@@ -21,6 +21,7 @@ bool pdl_enabled() {
 
 cudaError_t launch_plan(cudaStream_t stream, const PlanParams& p);
 cudaError_t launch_plan_append(cudaStream_t stream, const PlanParams& p, const AppendParams& a);
+int64_t plan_append_spans(const AppendParams& a);
 cudaError_t launch_extend_tc(int head_dim, int grid, cudaStream_t stream, const TcParams& p,
                              const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv);
 cudaError_t launch_rows(int head_dim, int grid, cudaStream_t stream, const RowParams& p,
@@ -321,12 +322,16 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
         ap.loc = o.out_cache_loc;
         ap.dev_err = a.dev_err;
     }
-    if (!self_plan) {
-        if (failed(append ? launch_plan_append(s, pp, ap) : launch_plan(s, pp)))
-            return PCP_ERR_CUDA;
-    } else if (append && failed(launch_kv_append_paged(ap, s))) {
+    // Beside the planner only while the append fits in one wave of its
+    // 1024-thread CTAs (one per SM): a longer append runs faster as a kernel
+    // of its own, whose four 256-thread blocks per SM overlap one another's
+    // load and store phases (32,768 tokens: 43.5 us against 56-60 us), and
+    // the planner after it is then a small part of the step.
+    const bool beside = append && !self_plan && plan_append_spans(ap) <= sms - 1;
+    if (append && !beside && failed(launch_kv_append_paged(ap, s))) return PCP_ERR_CUDA;
+    if (!self_plan &&
+        failed(beside ? launch_plan_append(s, pp, ap) : launch_plan(s, pp)))
         return PCP_ERR_CUDA;
-    }
 
     // ---- 2. tensor-core extend kernel (persistent, one CTA per SM)
     TcParams tp;

@@ -541,10 +541,14 @@ cudaError_t launch_plan(cudaStream_t stream, const PlanParams& p) {
     return launch_pdl(plan_kernel<false>, dim3(1), dim3(1024), 0, stream, p);
 }
 
-cudaError_t launch_plan_append(cudaStream_t stream, const PlanParams& p, const AppendParams& a) {
+// Append CTAs of plan_append_kernel for the call (one span each).
+int64_t plan_append_spans(const AppendParams& a) {
     constexpr int64_t span = (int64_t)kPlanAppendThreads * kAppendUnroll;
-    const int64_t spans = (a.total_q * a.chunks_per_token + span - 1) / span;
-    const dim3 grid((unsigned)(1 + spans));
+    return (a.total_q * a.chunks_per_token + span - 1) / span;
+}
+
+cudaError_t launch_plan_append(cudaStream_t stream, const PlanParams& p, const AppendParams& a) {
+    const dim3 grid((unsigned)(1 + plan_append_spans(a)));
     if (p.split)
         return launch_pdl(plan_append_kernel<true>, grid, dim3(kPlanAppendThreads),
                           kPlanAppendSmem, stream, p, a);

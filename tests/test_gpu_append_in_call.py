@@ -2,7 +2,8 @@
 
 With k_new / v_new in the call options the call does what pcp_kv_append_paged
 does (slot mapping from the page table, scatter into the pools), in the
-planner's launch beside the planning CTA, or ahead of a self-planned row
+planner's launch beside the planning CTA (when it fits in one wave there),
+or as a kernel of its own ahead of the planner or of a self-planned row
 kernel, and then attends.  Pools, slots, out, lse and the error code equal
 those of pcp_kv_append_paged followed by the same call, bit for bit; one case
 is also compared with the FP64 oracle.
@@ -59,6 +60,9 @@ CASES = {
     "stress_ps1": lambda: W.stress_case(1, 0, batch=24, max_prefix=3000),
     "stress_ps16_w4096": lambda: W.stress_case(16, 4096, batch=24, max_prefix=6000),
     "gqa_d64": lambda: W.gqa_prefill(batch=3, head_dim=64, chunk=200, max_prefix=2000),
+    # 5120 new tokens of 8 KV heads at D=128: 160 spans of 4096 chunks, more
+    # than one wave beside the planner, so the append runs as its own kernel
+    "gqa_long_append": lambda: W.gqa_prefill(batch=10, chunk=512, max_prefix=1000),
     # decode-shaped rows only: self-planned by the row kernel with the hints,
     # planned by the planner kernel without them
     "decode_only": lambda: W.decode_rows(n_decode=12, decode_max=3000),
