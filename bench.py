@@ -506,9 +506,10 @@ def main():
         "config": config_dict(batch, world),
         "roofline": roofline,
         "e2e": e2e,
-        # the fused slot mapping + append, plan, then the tensor-core kernel
-        # and/or the row kernel + combine (the host copy of qo_indptr skips a
-        # kernel without work), in each of the two timed loops
+        # the planner with the append beside it (or the append kernel), then
+        # the tensor-core kernel and/or the row kernel + combine (the host
+        # copy of qo_indptr skips a kernel without work), in each of the two
+        # timed loops
         "gpu_launches": 2 * args.steps * launches_per_step(batch, rows_on_tc),
         "clocks": clocks.summary(),
     }
@@ -746,9 +747,9 @@ SECONDARY_KEYS = ("decode_rows", "decode_step", "kv_append", "kv_append_long",
 
 
 def decode_step_secondary(pcp, torch, db, dev, peaks, flush, err, res):
-    """The decode rows as a serving decode step: the fused append of their new
-    tokens, then the attention call (whose row kernel plans the call while
-    the append runs)."""
+    """The decode rows as a serving decode step: one attention call with
+    their new tokens, appended by the append kernel ahead of the row kernel
+    (which plans the call while the append runs)."""
     _, nbytes = split_work(db)
     g = to_device(db, dev)
     dout = torch.empty_like(g["q"])
