@@ -19,6 +19,9 @@
  *      causal offset = KV length - query length), GQA, an optional sliding
  *      window, and split-KV with a log-sum-exp combine for decode-shaped rows
  *      (AstrAI paged decode split-KV kernel and its combine kernel).
+ *   1-3 in one call: pcp_paged_extend_attn_ex with the step's new K/V rows in
+ *      its pcp_call_options (k_new / v_new) maps their slots and appends them
+ *      beside the planner, then attends.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
