@@ -296,6 +296,7 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     pp.absorb = absorb;
     pp.split = split;
     pp.sm_count = sms;
+    pp.tc_gather = box_rows == 0 ? 1 : 0;
     pp.ws = ws;
     pp.lay = lay;
     pp.dev_err = a.dev_err;

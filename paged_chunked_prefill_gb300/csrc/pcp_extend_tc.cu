@@ -501,7 +501,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int item, q0, q1, Pl;
         int4 rec;
         if (kGather || n_done == 0) {
-            if (threadIdx.x == 0) misc[1] = atomicAdd(&hdr->tc_next, 1);
+            // gathering: the first item of CTA i is item i (the planner starts
+            // the counter at the grid size), later ones come from the counter
+            // (page boxes: every item from the counter; the same start there
+            // cost the page-box kernel 1.4% through its register allocation)
+            if (threadIdx.x == 0)
+                misc[1] = kGather && n_done == 0 ? (int)blockIdx.x
+                                                 : atomicAdd(&hdr->tc_next, 1);
             __syncthreads();
             item = misc[1];
             if (item >= n_items || *abort_flag) break;

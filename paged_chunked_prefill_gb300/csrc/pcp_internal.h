@@ -235,6 +235,7 @@ struct PlanParams {
     int absorb;        // decode-shaped chunks on the tensor cores: 1 / 0 as the host
                        // decided, -1: the planner decides (absorb_decode_rows)
     int sm_count;
+    int tc_gather;     // 1: the tensor-core kernel gathers pages below kTmaMinRows keys
     unsigned char* ws;
     WsLayout lay;
     int32_t* dev_err;

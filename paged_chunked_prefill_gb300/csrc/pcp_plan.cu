@@ -499,7 +499,9 @@ __device__ __forceinline__ void plan_body(const PlanParams& p, PlanSmem& S) {
     if (tid == 0) {
         hdr->n_tc_items = (int)min((int64_t)n_tc, cap_items);
         hdr->n_row_groups = (int)min((int64_t)grp_base, p.lay.cap_groups);
-        hdr->tc_next = 0;
+        // with cp.async page gathers, the tensor-core kernel's CTA i (one per
+        // SM) starts with item i and the counter hands out the rest
+        hdr->tc_next = p.tc_gather ? p.sm_count : 0;
         hdr->row_tiles = T;
         hdr->row_ctas = n_ctas;
     }
