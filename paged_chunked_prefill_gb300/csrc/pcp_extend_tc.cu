@@ -494,20 +494,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int last_issued = -1;           // TMA-issuing warps: last KV iteration they loaded
 
     for (;;) {
-        // With page boxes the TMA warp claims the next item and reads its
-        // record and metadata during this one (after its last K tile), so an
-        // item starts without the atomic and the dependent loads; the first
-        // item, and every item of the gathering instantiation, load them here.
+        // The TMA warp claims the next item and reads its record and metadata
+        // during this one (after the item's last K tile, or its last gathered
+        // tile), so an item starts without the atomic and the dependent
+        // loads; the first item loads them here.
         int item, q0, q1, Pl;
         int4 rec;
-        if (kGather || n_done == 0) {
+        if (n_done == 0) {
             // gathering: the first item of CTA i is item i (the planner starts
-            // the counter at the grid size), later ones come from the counter
-            // (page boxes: every item from the counter; the same start there
-            // cost the page-box kernel 1.4% through its register allocation)
-            if (threadIdx.x == 0)
-                misc[1] = kGather && n_done == 0 ? (int)blockIdx.x
-                                                 : atomicAdd(&hdr->tc_next, 1);
+            // the counter at the grid size); page boxes: the first item from
+            // the counter too (item i there moved the page-box kernel's
+            // registers and cost it 1.4%)
+            if (threadIdx.x == 0) misc[1] = kGather ? (int)blockIdx.x : atomicAdd(&hdr->tc_next, 1);
             __syncthreads();
             item = misc[1];
             if (item >= n_items || *abort_flag) break;
@@ -654,6 +652,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         gather_kv_rows<D>(p, geo, ca, cb, p.v_pool, sV + sv * C::kTileBytes, gw,
                                           nrows, lane);
                         cp_async_mbar_arrive_noinc(bar(C::bVFull + sv));
+                    }
+                    // the next item claimed once this one's last tile is issued,
+                    // as on the page-box path
+                    if (warp == kWarpTma && lane == 0) {
+                        volatile int* nx = misc + 4 + 8 * ((n_done + 1u) & 1u);
+                        const int ni = atomicAdd(&hdr->tc_next, 1);
+                        nx[0] = ni;
+                        if (ni < n_items) {
+                            const int4 r = items[ni];
+                            nx[1] = r.x;
+                            nx[2] = r.y;
+                            nx[3] = r.z;
+                            nx[4] = r.w;
+                            nx[5] = p.qo_indptr[r.x];
+                            nx[6] = p.qo_indptr[r.x + 1];
+                            nx[7] = p.prefix_lens[r.x];
+                        }
                     }
                 }
             }
@@ -929,8 +944,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // tile loop)
                 int wsplit = 0;
                 if constexpr (kSplit) {
-                    wsplit = (!kGather && n_done > 0) ? misc[4 + 8 * (n_done & 1u) + 4]
-                                                      : items[misc[1]].w;
+                    wsplit = n_done > 0 ? misc[4 + 8 * (n_done & 1u) + 4] : items[misc[1]].w;
                     if (!(wsplit & kSplitTag)) wsplit = 0;
                 }
                 if (ok && wsplit != 0) {
