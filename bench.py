@@ -65,20 +65,20 @@ def rows_pairs(batch, tok, head) -> int:
 # reads null until the counters are taken again.
 NCU_TRAFFIC = {
     ("gqa_prefill", "extend_tc_kernel<128>"): {
-        "bytes": 200.965376e6 + 13.591808e6,
-        "sources_sha256": "87fdfea9e31a088cca7a7a4d0d9b30d0",
+        "bytes": 198.296320e6 + 13.732608e6,
+        "sources_sha256": "5c3cbc664519668f6b4918da9f794288",
     },
     ("long_context", "extend_tc_kernel<128>"): {
-        "bytes": 4107.955712e6 + 531.129600e6,
-        "sources_sha256": "87fdfea9e31a088cca7a7a4d0d9b30d0",
+        "bytes": 3990.802176e6 + 531.118592e6,
+        "sources_sha256": "5c3cbc664519668f6b4918da9f794288",
     },
     ("mixed", "extend_tc_kernel<128>"): {
-        "bytes": 307.084032e6 + 5.412096e6,
-        "sources_sha256": "87fdfea9e31a088cca7a7a4d0d9b30d0",
+        "bytes": 307.325696e6 + 5.396480e6,
+        "sources_sha256": "5c3cbc664519668f6b4918da9f794288",
     },
     ("decode_rows", "row_attn_kernel<128>"): {
-        "bytes": 275.768320e6 + 0.715520e6,
-        "sources_sha256": "a32e78d758e16b74fa854bc7f3581d9a",
+        "bytes": 275.757312e6 + 0.425984e6,
+        "sources_sha256": "a7d0fe28d690d0632941dde152837994",
     },
 }
 
