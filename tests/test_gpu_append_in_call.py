@@ -63,6 +63,9 @@ CASES = {
     # 5120 new tokens of 8 KV heads at D=128: 160 spans of 4096 chunks, more
     # than one wave beside the planner, so the append runs as its own kernel
     "gqa_long_append": lambda: W.gqa_prefill(batch=10, chunk=512, max_prefix=1000),
+    # empty chunks among the others, a chunk starting mid-page, one at prefix 0
+    "empty_chunks": lambda: W.make_batch([0, 37, 500, 9, 1200], [0, 70, 0, 1, 300], 16, 4, 128,
+                                         16, seed=12, window=600),
     # decode-shaped rows only: self-planned by the row kernel with the hints,
     # planned by the planner kernel without them
     "decode_only": lambda: W.decode_rows(n_decode=12, decode_max=3000),
@@ -74,6 +77,25 @@ CASES = {
 def test_append_in_call_is_bit_identical(case, hints):
     b = _assert_same(CASES[case](), hints)
     assert b[5] == 0
+
+
+def test_append_in_call_without_new_rows():
+    """A call with no query rows at all: nothing to append, nothing launched,
+    the pools untouched."""
+    import torch
+    import paged_chunked_prefill_gb300 as pcp
+    b = W.make_batch([40, 7], [0, 0], 8, 2, 64, 16, seed=13)
+    d = to_device(b)
+    before = d["k_pool"].clone()
+    empty = torch.empty(0, b.n_kv_heads, b.head_dim, dtype=torch.bfloat16, device="cuda")
+    out, lse = pcp.paged_extend_attn(d["q"], d["qo_indptr"], d["kv_indptr"], d["kv_indices"],
+                                     d["prefix_lens"], d["k_pool"], d["v_pool"], b.page_size,
+                                     b.n_q_heads, b.n_kv_heads, b.head_dim,
+                                     qo_indptr_host=b.qo_indptr, prefix_lens_host=b.prefix_lens,
+                                     k_new=empty, v_new=empty)
+    torch.cuda.synchronize()
+    assert out.numel() == 0 and lse.numel() == 0
+    assert torch.equal(d["k_pool"].view(torch.int16), before.view(torch.int16))
 
 
 def test_append_in_call_with_mask():
