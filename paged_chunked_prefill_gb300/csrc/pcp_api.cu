@@ -362,6 +362,22 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     tp.stall_ns = o.test_stall_ns;
     tp.dev_err = a.dev_err;
     tp.split = split;
+    // One-Q-tile items (decode-shaped chunks that join the tensor cores, and
+    // a chunk's last item when it holds at most one Q tile of positions) take
+    // the instantiation that alternates their S/P buffers; with the host copy
+    // of qo_indptr the host knows whether the call has any.  Calls without
+    // them keep the instantiation that carries none of that code.
+    int ping = 0;
+    if (run_tc && a.causal && a.mask.data == nullptr && !split && a.qo_indptr_host != nullptr) {
+        const int item_pos = qpos * kQTiles;
+        for (int b = 0; b < a.batch && !ping; ++b) {
+            const int c = a.qo_indptr_host[b + 1] - a.qo_indptr_host[b];
+            if (c <= 0) continue;
+            if (c <= rmax) ping = 1;  // decode-shaped: a one-Q-tile item if it joins
+            else if (((c - 1) / item_pos) * item_pos + qpos >= c) ping = 1;
+        }
+    }
+    tp.ping = ping;
     cudaEvent_t evb = static_cast<cudaEvent_t>(o.tc_event_before);
     cudaEvent_t eva = static_cast<cudaEvent_t>(o.tc_event_after);
     if (evb && failed(cudaEventRecord(evb, s))) return PCP_ERR_CUDA;

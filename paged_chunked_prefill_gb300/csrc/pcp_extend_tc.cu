@@ -411,7 +411,7 @@ __device__ __forceinline__ void split_epilogue(const TcParams& p, int sp, int pa
 // other paths' instructions or registers: the gather code alone, never run
 // with page boxes, cost the page-box kernel 1-3%, and a gathering
 // instantiation without the page-box code spilled and lost 8%.
-template <int D, bool kMask, bool kCausal, bool kGather, bool kSplit>
+template <int D, bool kMask, bool kCausal, bool kGather, bool kSplit, bool kPing>
 __global__ void __launch_bounds__(kTcThreads, 1)
     extend_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -490,6 +490,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     uint32_t kv_iter = 0;          // KV tiles handled so far by this CTA
     uint32_t act0 = 0u, act1 = 0u;  // active (Q tile, KV tile) pairs so far, per Q tile
+    // kPing: S/P rounds per buffer (act0/act1) and O rounds per accumulator
+    // (oct0/oct1) differ once a one-Q-tile item alternated its S buffers
+    uint32_t oct0 = 0u, oct1 = 0u;
     uint32_t n_done = 0;            // items finished (q_full phase)
     int last_issued = -1;           // TMA-issuing warps: last KV iteration they loaded
 
@@ -708,7 +711,90 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ok = ok && mbar_wait(bar(C::bQFull), n_done & 1u, abort_flag, p.dev_err,
                                      kSpinLimitNs);
                 uint32_t aidx0 = act0, aidx1 = act1;
-                if (ok) {
+                bool pp = false;  // a one-Q-tile item alternating its S/P buffers
+                if constexpr (kPing) pp = geo.nq == 1;
+                if constexpr (kPing) {
+                    if (pp) {
+                        // Q tile 0 only: the QK^T of KV tile i goes to S buffer i % 2,
+                        // two tiles ahead of its PV, so the softmax of tile i + 1 finds
+                        // its S ready while PV(i) runs
+                        auto qk_to = [&](int sbuf, int st) {
+                            const uint64_t b0 = dk + ((uint32_t)st * C::kTileBytes >> 4);
+                            const uint32_t d = tmem + (uint32_t)sbuf * 128u;
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                constexpr uint32_t kHalf16 = (kTileM * 128) >> 4;
+                                const uint32_t off =
+                                    (uint32_t)(kk >> 2) * kHalf16 + (uint32_t)(kk & 3) * 2u;
+                                umma_ss(d, dq + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
+                            }
+                        };
+                        auto pv_from = [&](int sbuf, int st, bool acc) {
+                            const uint64_t b0 = dv + ((uint32_t)st * C::kTileBytes >> 4);
+                            const uint32_t d = tmem + 256u;
+                            const uint32_t a = tmem + (uint32_t)sbuf * 128u;
+#pragma unroll
+                            for (int kk = 0; kk < kTileN / 16; ++kk)
+                                umma_ts(d, a + kk * 8, b0 + (uint32_t)kk * (2048u >> 4), idesc_pv,
+                                        (acc || kk > 0) ? 1u : 0u);
+                        };
+                        if (ok) {
+                            tc_fence_after();
+                            const int npro = ntiles < 2 ? ntiles : 2;
+                            for (int i = 0; ok && i < npro; ++i) {
+                                const uint32_t c = kv_iter + (uint32_t)i;
+                                ok = mbar_wait(bar(C::bKFull + c % SK), (c / SK) & 1u, abort_flag,
+                                               p.dev_err, kSpinLimitNs);
+                                if (ok) {
+                                    if (kGather && p.box_rows == 0) fence_proxy_async_smem();
+                                    qk_to(i, c % SK);
+                                    umma_commit(bar(C::bSFull + i));
+                                    umma_commit(bar(C::bKEmpty + c % SK));
+                                }
+                            }
+                        }
+                        for (int i = 0; ok && i < ntiles; ++i) {
+                            const int t = geo.t_begin + i;
+                            const uint32_t cur = kv_iter + (uint32_t)i;
+                            const int st = cur % SV;
+                            if (!mbar_wait(bar(C::bVFull + st), (cur / SV) & 1u, abort_flag,
+                                           p.dev_err, kSpinLimitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            if ((kGather && p.box_rows == 0) ||
+                                (geo.L > t * kTileN && geo.L < t * kTileN + kTileN &&
+                                 (geo.L - t * kTileN) % p.box_rows != 0))
+                                fence_proxy_async_smem();
+                            const int sbuf = i & 1;
+                            const uint32_t pr = sbuf ? aidx1 : aidx0;
+                            if (!mbar_wait(bar(C::bPFull + sbuf), pr & 1u, abort_flag, p.dev_err,
+                                           kSpinLimitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            if (sbuf) ++aidx1;
+                            else ++aidx0;
+                            tc_fence_after();
+                            pv_from(sbuf, st, i > 0);
+                            umma_commit(bar(C::bODone + 0));
+                            umma_commit(bar(C::bVEmpty + st));
+                            if (i + 2 < ntiles) {
+                                const uint32_t c = cur + 2u;
+                                if (!mbar_wait(bar(C::bKFull + c % SK), (c / SK) & 1u, abort_flag,
+                                               p.dev_err, kSpinLimitNs)) {
+                                    ok = false;
+                                    break;
+                                }
+                                if (kGather && p.box_rows == 0) fence_proxy_async_smem();
+                                qk_to(sbuf, c % SK);
+                                umma_commit(bar(C::bSFull + sbuf));
+                                umma_commit(bar(C::bKEmpty + c % SK));
+                            }
+                        }
+                    }
+                }
+                if (ok && !pp) {
                     tc_fence_after();
                     const uint32_t c0 = kv_iter;
                     ok = mbar_wait(bar(C::bKFull + c0 % SK), (c0 / SK) & 1u, abort_flag,
@@ -726,7 +812,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         umma_commit(bar(C::bKEmpty + c0 % SK));
                     }
                 }
-                for (int i = 0; ok && i < ntiles; ++i) {
+                for (int i = 0; ok && !pp && i < ntiles; ++i) {
                     const int t = geo.t_begin + i;
                     const uint32_t cur = kv_iter + i;
                     const int st = cur % SV;
@@ -791,6 +877,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int pl_u = u == 0 ? geo.pl[0] : geo.pl[1];
                 const int ph_u = u == 0 ? geo.ph[0] : geo.ph[1];
                 const uint32_t act_u = u == 0 ? act0 : act1;
+                // kPing: O rounds of this Q tile's accumulator, and whether the
+                // item alternates S/P buffers 0 and 1 over its KV tiles
+                const uint32_t oct_u = kPing ? (u == 0 ? oct0 : oct1) : act_u;
+                bool pp = false;
+                if constexpr (kPing) pp = geo.nq == 1;
                 const int pos_local = u * p.qpos + r / G;
                 const bool row_valid = r < p.qpos * G && geo.pos0 + pos_local < geo.c;
                 const int pabs = geo.P + geo.pos0 + pos_local;
@@ -799,6 +890,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 bool ok = true;
                 for (int t = first_u; t <= last_u; ++t) {
                     const uint32_t a = act_u + (uint32_t)(t - first_u);
+                    // S/P buffer, its round, this tile's O round, its S columns
+                    uint32_t sb = (uint32_t)u, sa = a, oa = a, tSi = tS;
+                    if constexpr (kPing) {
+                        const uint32_t i = (uint32_t)(t - first_u);
+                        oa = oct_u + i;
+                        if (pp) {
+                            sb = i & 1u;
+                            sa = (sb ? act1 : act0) + (i >> 1);
+                            tSi = tmem + lane_off + sb * 128u;
+                        }
+                    }
                     const int key0 = t * kTileN;
                     constexpr bool has_mask = kMask;
                     // causal: the diagonal and window-edge tiles; otherwise the
@@ -839,7 +941,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     // waits decide per warp (tcgen05.ld/st and the P arrival are
                     // warp-collective)
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar(C::bSFull + u), a & 1u, abort_flag,
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar(C::bSFull + sb), sa & 1u, abort_flag,
                                                            p.dev_err, kSpinLimitNs))) {
                         ok = false;
                         break;
@@ -847,7 +949,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_fence_after();
                     // the whole S row of this thread: one TMEM load
                     uint32_t v[128];
-                    tmem_ld128(tS, v);
+                    tmem_ld128(tSi, v);
                     tmem_ld_wait();
                     if (need_mask) {
                         // keys this row does not see become -inf: tile columns
@@ -901,11 +1003,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         acc2[c & 3] = add_f2(acc2[c & 3], e);
                         pk[c] = pack_bf16x2(f2_lo(e), f2_hi(e));
                         // P goes to TMEM in 16-column pieces while the rest is computed
-                        if ((c & 15) == 15) tmem_st16(tS + (uint32_t)(c - 15), &pk[c - 15]);
+                        if ((c & 15) == 15) tmem_st16(tSi + (uint32_t)(c - 15), &pk[c - 15]);
                     }
                     if (t > first_u) {
                         if (!__all_sync(0xffffffffu,
-                                        mbar_wait(bar(C::bODone + u), (a - 1u) & 1u, abort_flag,
+                                        mbar_wait(bar(C::bODone + u), (oa - 1u) & 1u, abort_flag,
                                                   p.dev_err, kSpinLimitNs))) {
                             tmem_st_wait();
                             ok = false;
@@ -929,13 +1031,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_fence_before();
                     // one arrival per warp once all its lanes' P is in TMEM
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(C::bPFull + u));
+                    if (lane == 0) mbar_arrive(bar(C::bPFull + sb));
                     // the row sum is off the MMA's critical path
                     const uint64_t acc = add_f2(add_f2(acc2[0], acc2[1]), add_f2(acc2[2], acc2[3]));
                     l_run = l_run * alpha + (f2_lo(acc) + f2_hi(acc));
                 }
                 if (ok) {
-                    const uint32_t a_last = act_u + (uint32_t)(last_u - first_u);
+                    const uint32_t a_last = oct_u + (uint32_t)(last_u - first_u);
                     ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bODone + u), a_last & 1u,
                                                            abort_flag, p.dev_err, kSpinLimitNs));
                 }
@@ -983,8 +1085,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
         kv_iter += (uint32_t)ntiles;
-        act0 += (uint32_t)(geo.last[0] - geo.first[0] + 1);
-        if (geo.nq == 2) act1 += (uint32_t)(geo.last[1] - geo.first[1] + 1);
+        if constexpr (kPing) {
+            const uint32_t n0 = (uint32_t)(geo.last[0] - geo.first[0] + 1);
+            if (geo.nq == 1) {  // S/P buffers alternated; every PV went to O0
+                act0 += (n0 + 1u) / 2u;
+                act1 += n0 / 2u;
+                oct0 += n0;
+            } else {
+                const uint32_t n1 = (uint32_t)(geo.last[1] - geo.first[1] + 1);
+                act0 += n0;
+                oct0 += n0;
+                act1 += n1;
+                oct1 += n1;
+            }
+        } else {
+            act0 += (uint32_t)(geo.last[0] - geo.first[0] + 1);
+            if (geo.nq == 2) act1 += (uint32_t)(geo.last[1] - geo.first[1] + 1);
+        }
         ++n_done;
         tc_fence_before();
         __syncthreads();
@@ -1038,29 +1155,37 @@ size_t tc_smem_bytes(int head_dim) {
     return head_dim == 128 ? TcCfg<128>::kSmemBytes : TcCfg<64>::kSmemBytes;
 }
 
-template <int D, bool kMask, bool kCausal, bool kGather, bool kSplit>
+template <int D, bool kMask, bool kCausal, bool kGather, bool kSplit, bool kPing>
 cudaError_t launch_extend_tc_s(int grid, cudaStream_t stream, const TcParams& p,
                                const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv) {
     const size_t smem = TcCfg<D>::kSmemBytes;
-    auto* kern = extend_tc_kernel<D, kMask, kCausal, kGather, kSplit>;
+    auto* kern = extend_tc_kernel<D, kMask, kCausal, kGather, kSplit, kPing>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kTcThreads), smem, stream, p, tq, tk, tv);
 }
 
-// a plan with split items (never with a mask) takes the instantiation that merges them
+// a plan with split items (never with a mask) takes the instantiation that
+// merges them; a causal unmasked call with one-Q-tile items (the host's
+// decision, p.ping) the one that alternates their S/P buffers
 template <int D, bool kMask, bool kCausal, bool kGather>
 cudaError_t launch_extend_tc_g(int grid, cudaStream_t stream, const TcParams& p,
                                const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv) {
     if constexpr (!kMask) {
         if (p.split)
-            return launch_extend_tc_s<D, kMask, kCausal, kGather, true>(grid, stream, p, tq, tk,
-                                                                       tv);
+            return launch_extend_tc_s<D, kMask, kCausal, kGather, true, false>(grid, stream, p,
+                                                                              tq, tk, tv);
+        if constexpr (kCausal) {
+            if (p.ping)
+                return launch_extend_tc_s<D, kMask, kCausal, kGather, false, true>(grid, stream, p,
+                                                                                  tq, tk, tv);
+        }
     }
-    return launch_extend_tc_s<D, kMask, kCausal, kGather, false>(grid, stream, p, tq, tk, tv);
+    return launch_extend_tc_s<D, kMask, kCausal, kGather, false, false>(grid, stream, p, tq, tk,
+                                                                        tv);
 }
 
 // pages below kTmaMinRows keys (box_rows 0) take the gathering instantiation
