@@ -65,20 +65,20 @@ def rows_pairs(batch, tok, head) -> int:
 # reads null until the counters are taken again.
 NCU_TRAFFIC = {
     ("gqa_prefill", "extend_tc_kernel<128>"): {
-        "bytes": 198.296320e6 + 13.732608e6,
-        "sources_sha256": "5c3cbc664519668f6b4918da9f794288",
+        "bytes": 197.476864e6 + 13.643520e6,
+        "sources_sha256": "fcfb533a8c17f20d5a98b53a7e3c34b4",
     },
     ("long_context", "extend_tc_kernel<128>"): {
-        "bytes": 3990.802176e6 + 531.118592e6,
-        "sources_sha256": "5c3cbc664519668f6b4918da9f794288",
+        "bytes": 4026.660864e6 + 531.701248e6,
+        "sources_sha256": "fcfb533a8c17f20d5a98b53a7e3c34b4",
     },
     ("mixed", "extend_tc_kernel<128>"): {
-        "bytes": 307.325696e6 + 5.396480e6,
-        "sources_sha256": "5c3cbc664519668f6b4918da9f794288",
+        "bytes": 307.322368e6 + 3.708928e6,
+        "sources_sha256": "fcfb533a8c17f20d5a98b53a7e3c34b4",
     },
     ("decode_rows", "row_attn_kernel<128>"): {
-        "bytes": 275.757312e6 + 0.425984e6,
-        "sources_sha256": "a7d0fe28d690d0632941dde152837994",
+        "bytes": 275.765760e6 + 0.491776e6,
+        "sources_sha256": "0837b5eb6e76c2e21300c9242af97c7f",
     },
 }
 
