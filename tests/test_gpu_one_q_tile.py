@@ -3,7 +3,11 @@
 An item holds two Q tiles of one (sequence, KV head) unless the chunk's last
 item has at most 128 / G positions left; such an item runs on one softmax
 warpgroup, over 1 to 25 KV tiles here.  Decode-shaped chunks beside them may
-join the tensor-core queue as one-Q-tile items too.  Every row is compared
+join the tensor-core queue as one-Q-tile items too.  With the host copy of
+qo_indptr a causal unmasked call with such items takes the instantiation in
+which they alternate S/P buffers 0 and 1 over their KV tiles (odd and even
+tile counts here); without it, or with a mask, the one in which each KV tile
+runs QK^T, softmax and PV in turn.  Every row is compared
 with the FP64 oracle, with and without the host copy of qo_indptr, on both
 head sizes, windows, a boolean mask and page sizes that take TMA page boxes
 and the cp.async gathers.
