@@ -364,11 +364,12 @@ pcp_status run_extend(const ExtendArgs& a, const pcp_call_options* opts) {
     tp.split = split;
     // One-Q-tile items (decode-shaped chunks that join the tensor cores, and
     // a chunk's last item when it holds at most one Q tile of positions) take
-    // the instantiation that alternates their S/P buffers; with the host copy
-    // of qo_indptr the host knows whether the call has any.  Calls without
+    // the instantiation that alternates their S/P buffers (with split items
+    // too, on the page-box path); with the host copy of qo_indptr the host
+    // knows whether the call has any.  Calls without
     // them keep the instantiation that carries none of that code.
     int ping = 0;
-    if (run_tc && a.causal && a.mask.data == nullptr && !split && a.qo_indptr_host != nullptr) {
+    if (run_tc && a.causal && a.mask.data == nullptr && a.qo_indptr_host != nullptr) {
         const int item_pos = qpos * kQTiles;
         for (int b = 0; b < a.batch && !ping; ++b) {
             const int c = a.qo_indptr_host[b + 1] - a.qo_indptr_host[b];

@@ -289,8 +289,8 @@ struct TcParams {
     uint64_t stall_ns; // test hook (0: off): see pcp_call_options.test_stall_ns
     int32_t* dev_err;
     int split;         // host: the plan may hold split items (the instantiation that merges them)
-    int ping;          // host: one-Q-tile items alternate their S/P buffers (causal, unmasked,
-                       // unsplit calls that have such items)
+    int ping;          // host: one-Q-tile items alternate their S/P buffers (causal, unmasked
+                       // calls that have such items)
 };
 
 // ---- parameters of the split-KV combine kernel
