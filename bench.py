@@ -65,20 +65,20 @@ def rows_pairs(batch, tok, head) -> int:
 # reads null until the counters are taken again.
 NCU_TRAFFIC = {
     ("gqa_prefill", "extend_tc_kernel<128>"): {
-        "bytes": 197.476864e6 + 13.643520e6,
-        "sources_sha256": "fcfb533a8c17f20d5a98b53a7e3c34b4",
+        "bytes": 197.944576e6 + 13.285120e6,
+        "sources_sha256": "65866cc5b44b23d79dfe5db669164ad2",
     },
     ("long_context", "extend_tc_kernel<128>"): {
-        "bytes": 4026.660864e6 + 531.701248e6,
-        "sources_sha256": "fcfb533a8c17f20d5a98b53a7e3c34b4",
+        "bytes": 4086.055936e6 + 532.024576e6,
+        "sources_sha256": "65866cc5b44b23d79dfe5db669164ad2",
     },
     ("mixed", "extend_tc_kernel<128>"): {
-        "bytes": 307.322368e6 + 3.708928e6,
-        "sources_sha256": "fcfb533a8c17f20d5a98b53a7e3c34b4",
+        "bytes": 307.345408e6 + 3.377408e6,
+        "sources_sha256": "65866cc5b44b23d79dfe5db669164ad2",
     },
     ("decode_rows", "row_attn_kernel<128>"): {
-        "bytes": 275.765760e6 + 0.491776e6,
-        "sources_sha256": "0837b5eb6e76c2e21300c9242af97c7f",
+        "bytes": 275.760384e6 + 0.564736e6,
+        "sources_sha256": "706c6fde763ecf2d3b22a9ec4691b98e",
     },
 }
 
